@@ -1,0 +1,165 @@
+"""CPU oracle for the MXFP4 MoE layer (test infrastructure only).
+
+Only the tests, the smoke check and the bench's CPU-baseline leg may import
+this package.  The product path (the CUDA library and its binding) never does.
+
+The arithmetic lives in moe_oracle.c (plain C, fp32, per-token loop); this
+module compiles it with gcc (-ffp-contract=off, so no fused multiply-add
+changes the rounding between x86 and Arm hosts) and wraps it with ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "libmoe_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+GCC_FLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-fopenmp"]
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *GCC_FLAGS, _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            vp, ci = ctypes.c_void_p, ctypes.c_int
+            lib.moe_ref_route.argtypes = [vp, ci, ci, ci, ci, ci, vp, vp]
+            lib.moe_ref_route.restype = ci
+            lib.moe_ref_permute.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, vp, vp]
+            lib.moe_ref_permute.restype = ci
+            lib.moe_ref_capacity.argtypes = [ci, ci, ci, ci]
+            lib.moe_ref_capacity.restype = ctypes.c_int64
+            lib.moe_ref_ffn.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, ci,
+                                        vp, vp, ci]
+            lib.moe_ref_ffn.restype = ci
+            lib.moe_ref_ffn_grouped.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci,
+                                                ci, vp]
+            lib.moe_ref_ffn_grouped.restype = ci
+            lib.moe_ref_mxfp4_value.argtypes = [ci, ci]
+            lib.moe_ref_mxfp4_value.restype = ctypes.c_double
+            lib.moe_ref_silu.argtypes = [ctypes.c_float]
+            lib.moe_ref_silu.restype = ctypes.c_float
+            lib.moe_ref_f32_to_bf16.argtypes = [ctypes.c_float]
+            lib.moe_ref_f32_to_bf16.restype = ctypes.c_uint16
+            lib.moe_ref_max_threads.argtypes = []
+            lib.moe_ref_max_threads.restype = ci
+            _lib = lib
+    return _lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _p(a):
+    if a is None:
+        return None
+    assert isinstance(a, np.ndarray) and a.flags["C_CONTIGUOUS"], "oracle wants C-contiguous numpy"
+    return a.ctypes.data
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise OracleError(f"{what} failed with status {rc}")
+
+
+def route(logits: np.ndarray, K: int, with_shared: bool, renormalize: bool = True):
+    """fp32 logits [T, E] -> (ids int32 [T, Kt], weights fp32 [T, Kt])."""
+    logits = np.ascontiguousarray(logits, np.float32)
+    T, E = logits.shape
+    Kt = K + (1 if with_shared else 0)
+    ids = np.empty((T, Kt), np.int32)
+    w = np.empty((T, Kt), np.float32)
+    _check(_load().moe_ref_route(_p(logits), T, E, K, int(with_shared), int(renormalize),
+                                 _p(ids), _p(w)), "route")
+    return ids, w
+
+
+def capacity(T: int, Kt: int, Et: int, tile_m: int) -> int:
+    return int(_load().moe_ref_capacity(T, Kt, Et, tile_m))
+
+
+def permute(ids: np.ndarray, Et: int, tile_m: int):
+    """Stable counting sort of pairs by expert with tile-aligned buckets.
+
+    Returns dict(sorted_pairs [cap], offsets [Et+1], inv [T*Kt],
+    tile_expert [cap // tile_m], num_tiles int)."""
+    ids = np.ascontiguousarray(ids, np.int32)
+    T, Kt = ids.shape
+    cap = capacity(T, Kt, Et, tile_m)
+    out = dict(sorted_pairs=np.empty(cap, np.int32), offsets=np.empty(Et + 1, np.int32),
+               inv=np.empty(T * Kt, np.int32), tile_expert=np.empty(cap // tile_m, np.int32))
+    nt = np.zeros(1, np.int32)
+    _check(_load().moe_ref_permute(_p(ids), T, Kt, Et, tile_m, _p(out["sorted_pairs"]),
+                                   _p(out["offsets"]), _p(out["inv"]), _p(out["tile_expert"]),
+                                   _p(nt)), "permute")
+    out["num_tiles"] = int(nt[0])
+    return out
+
+
+def ffn(x, w13, s13, w2, s2, ids, w, tokens=None, want_f32=False, n_threads=1):
+    """Per-token loop oracle.  x: bf16 bits uint16 [T, H]; returns bf16 bits
+    [n, H] for the requested tokens (all when tokens is None) and optionally
+    the fp32 accumulator before rounding."""
+    x = np.ascontiguousarray(x, np.uint16)
+    T, H = x.shape
+    Et, twoI, _ = w13.shape
+    I = twoI // 2
+    ids = np.ascontiguousarray(ids, np.int32)
+    w = np.ascontiguousarray(w, np.float32)
+    Kt = ids.shape[1]
+    tok = None if tokens is None else np.ascontiguousarray(tokens, np.int32)
+    n = T if tok is None else tok.size
+    out = np.empty((n, H), np.uint16)
+    of = np.empty((n, H), np.float32) if want_f32 else None
+    for a in (w13, s13, w2, s2):
+        assert a.dtype == np.uint8 and a.flags["C_CONTIGUOUS"]
+    _check(_load().moe_ref_ffn(_p(x), _p(w13), _p(s13), _p(w2), _p(s2), _p(ids), _p(w), T, H, I,
+                               Et, Kt, _p(tok), n, _p(out), _p(of), int(n_threads)), "ffn")
+    return (out, of) if want_f32 else out
+
+
+def ffn_grouped(x, w13, s13, w2, s2, w, perm):
+    x = np.ascontiguousarray(x, np.uint16)
+    T, H = x.shape
+    Et, twoI, _ = w13.shape
+    w = np.ascontiguousarray(w, np.float32)
+    Kt = w.shape[1]
+    out = np.empty((T, H), np.uint16)
+    _check(_load().moe_ref_ffn_grouped(_p(x), _p(w13), _p(s13), _p(w2), _p(s2), _p(w),
+                                       _p(perm["sorted_pairs"]), _p(perm["offsets"]), T, H,
+                                       twoI // 2, Et, Kt, _p(out)), "ffn_grouped")
+    return out
+
+
+def mxfp4_value(code: int, scale: int) -> float:
+    return float(_load().moe_ref_mxfp4_value(code, scale))
+
+
+def silu(g: float) -> float:
+    return float(_load().moe_ref_silu(g))
+
+
+def f32_to_bf16(f: float) -> int:
+    return int(_load().moe_ref_f32_to_bf16(f))
+
+
+def max_threads() -> int:
+    return int(_load().moe_ref_max_threads())
