@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark of the MXFP4 MoE layer (route -> permute -> gate_up -> down -> combine).
+
+One step = one pass of the whole layer over one batch of the workload's
+tokens, every kernel from libmoe.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode64]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Under torchrun every rank runs its own replica of the layer on its own batch
+(the layer is data parallel over tokens; no collective on the data path);
+the value is all ranks' tokens divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP4 MoE layer tokens/s; % of HBM roofline (decode) / tensor peak (prefill)"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="decode64")
+    p.add_argument("--tile-m", type=int, default=8)
+    p.add_argument("--path", default="auto", choices=["auto", "decode", "prefill"])
+    p.add_argument("--replicas", type=int, default=2,
+                   help="weight/input replicas rotated per step (keeps L2 cold)")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ env
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except Exception:
+        return None
+
+
+def _find_number(d, keys):
+    if isinstance(d, dict):
+        for k, v in d.items():
+            if k in keys and isinstance(v, (int, float)):
+                return float(v)
+        for v in d.values():
+            r = _find_number(v, keys)
+            if r is not None:
+                return r
+    return None
+
+
+def hbm_peak():
+    mp = measured_peaks()
+    if mp is not None:
+        v = _find_number(mp, ("hbm_gbs", "hbm_GBps", "copy_gbs"))
+        if v:
+            return v, "measured (MEASURED_PEAKS.json hbm_gbs)"
+    return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 copy measurement)"
+
+
+def traffic_from_profiles(kernel: str, workload: str, src_file: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (sha256 recorded in the summary)."""
+    sha = hashlib.sha256(open(src_file, "rb").read()).hexdigest()[:16]
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        txt = open(path).read()
+        for m in re.finditer(r"traffic_bytes_per_launch kernel=(\S+) workload=(\S+) "
+                             r"src_sha256=(\S+) bytes=(\d+)", txt):
+            if m.group(1) == kernel and m.group(2) == workload and m.group(3) == sha:
+                return int(m.group(4)), os.path.relpath(path, ROOT)
+    return None, None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.out = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+    try:
+        bus = torch.cuda.get_device_properties(device_index).pci_bus_id
+        if bus:
+            return str(bus)
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[device_index]
+    return str(device_index)
+
+
+# ------------------------------------------------------- algorithmic work
+
+def layer_work(w, ids_host):
+    """Algorithmic HBM bytes and flops of one step, from the actual routing."""
+    import numpy as np
+    from mxfp4_mixture_experts_softmax_gb300 import synth
+    touched = int(np.unique(ids_host).size)
+    H, I, T, P = w.H, w.I, w.T, w.pairs
+    w13_b = 2 * I * (H // 2 + H // 32)
+    w2_b = H * (I // 2 + I // 32)
+    gate_up = touched * w13_b + T * H * 2 + P * I * 2          # weights + x + h write
+    down = touched * w2_b + P * I * 2 + P * H * 4               # weights + h read + y write
+    layer = (touched * synth.weight_bytes_per_expert(w) + T * H * 4 + P * I * 4
+             + T * w.E * 4)                                     # + x, out, h, logits
+    flops = 2 * P * (2 * I * H + H * I)
+    return dict(touched=touched, gate_up_bytes=gate_up, down_bytes=down, layer_bytes=layer,
+                flops=flops, gate_up_flops=2 * P * 2 * I * H)
+
+
+# ------------------------------------------------------------ our arm
+
+def run_ours(args, ws, rank, local):
+    import numpy as np
+    import torch
+    from mxfp4_mixture_experts_softmax_gb300 import libmoe, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo",
+                                device_id=dev if torch.cuda.is_available() else None)
+    w = synth.WORKLOADS[args.workload]
+    path = {"auto": libmoe.MOE_PATH_AUTO, "decode": libmoe.MOE_PATH_DECODE,
+            "prefill": libmoe.MOE_PATH_PREFILL}[args.path]
+    tm = args.tile_m
+    host = synth.make_inputs(w)
+
+    def up(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t.to(dev)
+
+    R = max(1, args.replicas)
+    weights = [{k: up(host[k]) for k in ("w13", "s13", "w2", "s2")}]
+    for _ in range(R - 1):
+        weights.append({k: v.clone() for k, v in weights[0].items()})
+    logits = [up(host["logits"]) for _ in range(R)]
+    xs = [up(host["x"]) for _ in range(R)]
+    bufs = libmoe.alloc_layer(w.T, w.E, w.K, w.with_shared, w.H, w.I, w.Et, tm, dev)
+    h_buf, y_buf = libmoe.ffn_views(bufs["workspace"], w.T, w.H, w.I, w.Et, w.Kt, tm)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        r = i % R
+        W = weights[r]
+        if ev is not None:
+            ev[0].record(stream)
+        ids, tw = libmoe.moe_route(logits[r], w.K, w.with_shared, w.renormalize,
+                                   bufs["topk_ids"], bufs["topk_w"])
+        if ev is not None:
+            ev[1].record(stream)
+        perm = libmoe.moe_permute(ids, w.Et, tm, bufs["perm"])
+        if ev is not None:
+            ev[2].record(stream)
+        libmoe.moe_ffn_gate_up(xs[r], W["w13"], W["s13"], perm, h_buf, path)
+        if ev is not None:
+            ev[3].record(stream)
+        libmoe.moe_ffn_down(h_buf, W["w2"], W["s2"], tw, perm, y_buf, w.T, path)
+        if ev is not None:
+            ev[4].record(stream)
+        libmoe.moe_combine(y_buf, w.T, w.H, w.Kt, bufs["out"])
+        if ev is not None:
+            ev[5].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    ids_host = bufs["topk_ids"].cpu().numpy()
+    work = layer_work(w, ids_host)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id_for(local))
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(K):
+        step(i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    names = ["route", "permute", "gate_up", "down", "combine"]
+    per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+           for j, n in enumerate(names)}
+    if not np.isfinite(bufs["out"].float().cpu().numpy()).all():
+        raise RuntimeError("non-finite layer output")
+
+    # end to end: per step H2D of logits + x from pinned host memory, the layer,
+    # D2H of the output into pinned host memory
+    pin_logits = torch.from_numpy(host["logits"]).pin_memory()
+    pin_x = torch.from_numpy(host["x"]).view(torch.int16).view(torch.bfloat16).pin_memory()
+    pin_out = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        logits[0].copy_(pin_logits, non_blocking=True)
+        xs[0].copy_(pin_x, non_blocking=True)
+        libmoe.moe_layer(logits[0], xs[0], weights[0]["w13"], weights[0]["s13"],
+                         weights[0]["w2"], weights[0]["s2"], w.K, w.with_shared, w.renormalize,
+                         tile_m=tm, path=path, bufs=bufs)
+        pin_out.copy_(bufs["out"], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+
+    if ws > 1:
+        t = torch.tensor([total_ms, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+
+    result = None
+    if rank == 0:
+        peak, peak_src = hbm_peak()
+        gu_s = per["gate_up"] / 1e3
+        achieved = work["gate_up_bytes"] / gu_s / 1e9
+        traffic, traffic_src = traffic_from_profiles(
+            "decode_gate_up", args.workload,
+            os.path.join(ROOT, "mxfp4_mixture_experts_softmax_gb300", "csrc", "ffn_decode.cu"))
+        layer_s = sum(per.values()) / 1e3
+        tokens = w.T * K * ws
+        result = {
+            "metric": METRIC,
+            "value": tokens / (total_ms / 1e3),
+            "unit": "tokens/s",
+            "n_gpus": ws,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": total_ms / K,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded; random MXFP4 weights, N(0,1) activations and logits)",
+            "config": {
+                "workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K,
+                "shared_expert": w.with_shared, "Et": w.Et, "Kt": w.Kt, "tile_m": tm,
+                "path": args.path, "experts_touched": work["touched"],
+                "parallelism": f"replicas x{ws} (weak scaling, tokens per GPU fixed)",
+                "l2": f"inputs larger than L2: {work['layer_bytes'] / 1e9:.2f} GB touched per "
+                      f"step, {R} weight replicas rotated per step",
+            },
+            "roofline": {
+                "kernel": "decode_gate_up" if args.path != "prefill" else "prefill_gate_up",
+                "bound": "hbm",
+                "achieved": achieved,
+                "peak": peak,
+                "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": work["gate_up_bytes"],
+                "launch_us": per["gate_up"] * 1e3,
+                "peak_source": peak_src,
+                "traffic_source": traffic_src,
+            },
+            "layer_roofline": {
+                "bound": "hbm",
+                "algorithmic_bytes_per_step": work["layer_bytes"],
+                "achieved": work["layer_bytes"] / layer_s / 1e9,
+                "frac": work["layer_bytes"] / layer_s / 1e9 / peak,
+                "unit": "GB/s",
+                "flops_per_step": work["flops"],
+            },
+            "kernels_us": {n: v * 1e3 for n, v in per.items()},
+            "e2e": {"value": w.T * K * ws / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": int(host["logits"].nbytes + host["x"].nbytes),
+                    "d2h_bytes_per_step": int(w.T * w.H * 2),
+                    "ms_per_step": e2e_ms / K},
+            "gpu_launches": 5 * K,
+            "clocks": clocks,
+        }
+        if ws == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(w, host, ids_host, args.cpu_seconds)
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return result
+
+
+# ---------------------------------------------------------- the oracle
+
+def _oracle_sample(w, host, ids, wt, n_tokens, threads, offset=0):
+    import numpy as np
+    import oracle
+    toks = ((np.arange(n_tokens) + offset) % w.T).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.ffn(host["x"], host["w13"], host["s13"], host["w2"], host["s2"], ids, wt,
+               tokens=toks, n_threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, host, ids_unused, target_s):
+    """The CPU oracle as it stands, timed on this host's cores on a bounded
+    sample of the same workload (whole tokens: routing plus all Kt experts)."""
+    import oracle
+    from mxfp4_mixture_experts_softmax_gb300 import synth
+    threads = synth.cpu_threads()
+    t0 = time.perf_counter()
+    ids, wt = oracle.route(host["logits"], w.K, w.with_shared, w.renormalize)
+    route_s = time.perf_counter() - t0
+    n = threads
+    dt = _oracle_sample(w, host, ids, wt, n, threads)
+    total_tok, total_s = n, dt
+    while total_s < target_s and total_tok < 4 * w.T:
+        n2 = max(threads, int(n * (target_s - total_s) / max(dt, 1e-3)) // threads * threads)
+        n2 = min(n2, 4 * w.T - total_tok)
+        dt = _oracle_sample(w, host, ids, wt, n2, threads, offset=total_tok)
+        total_tok += n2
+        total_s += dt
+    per_tok_route = route_s / w.T
+    value = total_tok / (total_s + per_tok_route * total_tok)
+    return {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{total_tok} tokens of {w.name} (all {w.Kt} experts each, plus routing), "
+                      f"{total_s:.1f} s on {threads} threads"}
+
+
+def run_reference(args, ws, rank):
+    """The reference arm: the plain CPU oracle (there is no other implementation
+    of this layer to run), each step a bounded sample of the workload."""
+    if rank != 0:
+        return None
+    import oracle
+    from mxfp4_mixture_experts_softmax_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    host = synth.make_inputs(w)
+    threads = synth.cpu_threads()
+    n = threads  # tokens per step: one per thread
+
+    def step(i):
+        ids, wt = oracle.route(host["logits"], w.K, w.with_shared, w.renormalize)
+        _oracle_sample(w, host, ids, wt, n, threads, offset=i * n)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    sample = (f"{n} tokens of {w.name} per step (all {w.Kt} experts each) plus routing of the "
+              f"{w.T}-token batch, {threads} threads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K,
+                   "shared_expert": w.with_shared},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, ws, rank)
+    else:
+        res = run_ours(args, ws, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

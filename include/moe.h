@@ -1,0 +1,213 @@
+/*
+ * moe.h -- C ABI of libmoe, the GB300 (sm_103a) MXFP4 mixture-of-experts FFN
+ * layer with softmax top-K routing.
+ *
+ * The layer, in order (one call per step, all on one CUDA stream):
+ *   moe_route    softmax top-K routing of router logits; the shared expert is
+ *                appended as slot K (expert id E, weight 1)
+ *   moe_permute  stable counting sort of the (token, slot) pairs by expert,
+ *                each expert's bucket padded to a multiple of tile_m rows
+ *   moe_ffn      grouped gate_up GEMM with a SwiGLU epilogue, grouped down
+ *                GEMM scaled by the routing weight, slot-ordered combine
+ *
+ * Sources (web pages on the method):
+ *   [IX]  InferenceX, "MI355X Qwen3.5-397B SGLang" blog, section on the
+ *         optimisations: PR #21421 (softmax-scored fused top-K at E=512,
+ *         K=10) and PR #20736 (shared expert fused as routed expert top-K+1
+ *         when its width equals the routed width).
+ *   [VS]  VibeSys, "Qwen3.5-397B serving engine on 4x MI300A": section
+ *         "baseline" (fused MoE kernel dequantising MXFP4 in registers),
+ *         section "kernels and graph capture", section "cheaper prefill and
+ *         collectives" (32-row tiles in the MoE kernel).
+ *   [VL]  vLLM, "MiniMax M3 on MI355X": section "local shape and tiling"
+ *         (small-M vs large-M launcher regimes, grouped-MoE program order)
+ *         and section "shared expert fusion".
+ * The pages do not print the weight format; this library reads MXFP4 as E2M1
+ * codes, two per byte (low nibble = even k), with one E8M0 scale byte
+ * (2^(s-127)) per 32 consecutive k.
+ *
+ * Conventions for every call:
+ *   - Every pointer is a caller-owned DEVICE pointer (cudaMalloc or
+ *     equivalent) unless stated.  The library allocates nothing, keeps no
+ *     state between calls and never synchronises the host with the device.
+ *   - Work is enqueued on `stream` (0 = legacy default stream).  Calls are
+ *     asynchronous; read outputs only after the stream has completed.
+ *   - Arguments and shapes are checked on the host before any launch.  A
+ *     rejected call launches nothing and returns MOE_ERR_INVALID_ARG (NULL
+ *     pointer, negative size, misaligned pointer) or MOE_ERR_UNSUPPORTED_SHAPE
+ *     (a size outside the documented limits).  A failed launch returns
+ *     MOE_ERR_CUDA (the CUDA error is left for cudaGetLastError).
+ *   - Tensors are dense row-major.  bf16 tensors are passed as uint16_t bit
+ *     patterns.  Sizes are in elements unless stated.
+ */
+#ifndef LIBMOE_MOE_H
+#define LIBMOE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,
+    MOE_ERR_WORKSPACE_TOO_SMALL = 3,
+    MOE_ERR_CUDA = 4,
+    MOE_ERR_INTERNAL = 5
+} moe_status_t;
+
+/* Which moe_ffn kernels run: AUTO picks by the mean rows per expert. */
+typedef enum {
+    MOE_PATH_AUTO = 0,
+    MOE_PATH_DECODE = 1, /* small M: weights streamed through registers, mma.sync */
+    MOE_PATH_PREFILL = 2 /* large M: TMA + tcgen05 MMA with TMEM accumulators */
+} moe_path_t;
+
+/* Static string for a status code (never NULL). */
+const char* moe_status_string(moe_status_t status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int moe_version(void);
+
+/*
+ * moe_route -- softmax top-K routing [IX, PR #21421].
+ *
+ *   logits     fp32 [T, E] router logits.
+ *   topk_ids   int32 [T, Kt] out, Kt = K + (with_shared ? 1 : 0).
+ *   topk_w     fp32  [T, Kt] out.
+ * For each token: p = softmax over all E logits (fp32, expf); the K experts
+ * with the largest logits, in descending order, equal logits ordered by lower
+ * expert index (+0 and -0 compare equal); weights p[id] renormalised to sum
+ * to 1 over the K selected when `renormalize` is nonzero, else p[id].  With
+ * `with_shared` nonzero, slot K holds expert id E with weight 1 [IX, PR #20736].
+ * Limits: 1 <= K <= min(E, 32), 1 <= E <= 1024, T >= 0 (T = 0 is a no-op).
+ * Preconditions (not checked): no NaN logits and at least one finite logit
+ * per token; otherwise the outputs for that token are unspecified.
+ * Ids are bit-exact with the plain definition; weights agree with it to a few
+ * fp32 ulp (the summation order of the softmax denominator differs).
+ */
+moe_status_t moe_route(const float* logits, int T, int E, int K, int with_shared, int renormalize,
+                       int32_t* topk_ids, float* topk_w, cudaStream_t stream);
+
+/*
+ * moe_permute_capacity -- number of int32 entries of `sorted_pairs`:
+ *   cap = T*Kt + Et*(tile_m - 1); max_tiles = cap / tile_m entries of
+ *   `tile_expert`.  Returns 0 for invalid sizes.
+ */
+size_t moe_permute_capacity(int T, int Kt, int Et, int tile_m);
+size_t moe_permute_max_tiles(int T, int Kt, int Et, int tile_m);
+
+/*
+ * moe_permute -- group the T*Kt (token, slot) pairs by expert [VS, 32-row
+ * tiles in the MoE kernel].
+ *
+ *   topk_ids        int32 [T, Kt]; pair q = t*Kt + j names expert topk_ids[q].
+ *   sorted_pairs    int32 [cap] out: bucket e holds the pairs of expert e in
+ *                   increasing q, starting at expert_offsets[e]; every other
+ *                   position (bucket padding, tail) holds -1.
+ *   expert_offsets  int32 [Et+1] out: offsets[e] = sum over e' < e of
+ *                   count(e') rounded up to a multiple of tile_m;
+ *                   offsets[Et] = rows in use.
+ *   inv_pairs       int32 [T*Kt] out: position of pair q in sorted_pairs.
+ *   tile_expert     int32 [max_tiles] out: tile i (rows [i*tile_m,
+ *                   (i+1)*tile_m)) belongs to expert tile_expert[i]; tiles from
+ *                   num_tiles on hold -1.
+ *   num_tiles       int32 [1] out: offsets[Et] / tile_m (stays on the device).
+ * Limits: 1 <= Kt <= 33, 1 <= Et <= 1025, 1 <= tile_m <= 256, cap < 2^31.
+ * Output is bit-exact (a deterministic function of topk_ids).  Ids outside
+ * [0, Et) are a precondition violation: such pairs are dropped and their
+ * inv_pairs entry is -1.  One CTA does the whole sort.
+ */
+moe_status_t moe_permute(const int32_t* topk_ids, int T, int Kt, int Et, int tile_m,
+                         int32_t* sorted_pairs, int32_t* expert_offsets, int32_t* inv_pairs,
+                         int32_t* tile_expert, int32_t* num_tiles, cudaStream_t stream);
+
+/*
+ * moe_ffn_workspace_size -- bytes of device workspace moe_ffn needs:
+ * the bf16 SwiGLU intermediate [cap, I] and the weighted fp32 per-pair
+ * expert outputs [T*Kt, H], each 256-byte aligned.
+ */
+size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
+
+/*
+ * moe_ffn -- the expert FFN of every (token, slot) pair and the combine
+ * [VS, fused MXFP4 MoE kernel; IX/VL, shared expert in the same dispatch].
+ *
+ *   x        bf16 [T, H] activations.
+ *   w13      uint8 [Et, 2I, H/2] packed E2M1 codes of gate (rows 0..I-1) and
+ *            up (rows I..2I-1) projections; s13 uint8 [Et, 2I, H/32] E8M0.
+ *   w2       uint8 [Et, H, I/2] codes of the down projection; s2 [Et, H, I/32].
+ *   topk_w, sorted_pairs, expert_offsets, inv_pairs, tile_expert, num_tiles:
+ *            as produced by moe_route / moe_permute with the same T, Kt, Et
+ *            and tile_m.
+ *   out      bf16 [T, H] out.
+ *   workspace / ws_bytes: device scratch of at least moe_ffn_workspace_size().
+ * For each pair (t, j) with e = topk_ids[t, j]:
+ *   g = W_gate[e] x_t, u = W_up[e] x_t (fp32 accumulation of exact bf16
+ *   products), h = bf16(silu(g) * u), y = W2[e] h (fp32);
+ *   out_t = bf16(sum over j ascending of topk_w[t, j] * y_tj).
+ * Result tolerance against the plain fp32 definition: per element
+ * |out - ref| <= 1e-2 * (|ref| + rms(ref)) and relative L2 error <= 2e-3
+ * (the GEMM summation order differs; SwiGLU bf16 roundings may flip by 1 ulp).
+ * Weights are exact: every E2M1 value times its E8M0 scale is represented
+ * exactly in bf16 for scale bytes 7..247 (2^-120..2^120).
+ * Limits: H % 32 == 0, I % 32 == 0, H, I <= 65536, tile_m % 8 == 0 and
+ * tile_m <= 64 for the decode path; the prefill path needs tile_m in
+ * {32, 64, 128}.  Pointers 16-byte aligned.
+ */
+moe_status_t moe_ffn(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,
+                     const uint8_t* s2, const float* topk_w, const int32_t* sorted_pairs,
+                     const int32_t* expert_offsets, const int32_t* inv_pairs,
+                     const int32_t* tile_expert, const int32_t* num_tiles, int T, int H, int I,
+                     int Et, int Kt, int tile_m, uint16_t* out, void* workspace, size_t ws_bytes,
+                     cudaStream_t stream);
+
+/* moe_ffn with an explicit path choice (MOE_PATH_AUTO behaves like moe_ffn). */
+moe_status_t moe_ffn_path(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                          const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                          const int32_t* sorted_pairs, const int32_t* expert_offsets,
+                          const int32_t* inv_pairs, const int32_t* tile_expert,
+                          const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                          int tile_m, uint16_t* out, void* workspace, size_t ws_bytes,
+                          moe_path_t path, cudaStream_t stream);
+
+/*
+ * The three steps of moe_ffn as separate calls (moe_ffn runs exactly these,
+ * in this order, on its workspace: h at byte 0, y at
+ * moe_ffn_y_offset(T, I, Et, Kt, tile_m)).  `path` must resolve to the same
+ * path for both GEMM calls (AUTO always does for the same sizes).
+ *
+ * moe_ffn_gate_up: h[p, n] = bf16(silu(g) * u) for every sorted position p
+ *   that holds a pair (pads are not written); h is bf16 [cap, I].
+ * moe_ffn_down:    y[q, m] = topk_w[q] * (W2[e] h_p)[m] for every pair q at
+ *   position p; y is fp32 [T*Kt, H] (the routing-weighted expert outputs).
+ * moe_combine:     out[t, m] = bf16(sum over j = 0..Kt-1, ascending, of
+ *   y[t*Kt + j, m]); out is bf16 [T, H].
+ */
+moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                             const int32_t* sorted_pairs, const int32_t* tile_expert,
+                             const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                             int tile_m, uint16_t* h, moe_path_t path, cudaStream_t stream);
+moe_status_t moe_ffn_down(const uint16_t* h, const uint8_t* w2, const uint8_t* s2,
+                          const float* topk_w, const int32_t* sorted_pairs,
+                          const int32_t* tile_expert, const int32_t* num_tiles, int T, int H,
+                          int I, int Et, int Kt, int tile_m, float* y, moe_path_t path,
+                          cudaStream_t stream);
+moe_status_t moe_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t stream);
+
+/* Byte offset of y inside the moe_ffn workspace (h [cap, I] bf16 comes first). */
+size_t moe_ffn_y_offset(int T, int I, int Et, int Kt, int tile_m);
+
+/* The path MOE_PATH_AUTO picks for these sizes [VL, small-M vs large-M]. */
+moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBMOE_MOE_H */

@@ -1,0 +1,281 @@
+// moe_api.cu -- the extern "C" entry points of libmoe: argument checks on the
+// host, workspace layout, path choice and kernel launches.  Everything runs
+// on the caller's stream; nothing here allocates or synchronises.
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <initializer_list>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "moe_internal.h"
+
+namespace moe {
+
+
+cudaError_t ensure_dynamic_smem(const void* func, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    struct Entry {
+        const void* func;
+        int device;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static Entry seen[256];
+    static int n_seen = 0;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_seen; ++i)
+        if (seen[i].func == func && seen[i].device == dev && seen[i].bytes >= bytes) return cudaSuccess;
+    err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (err != cudaSuccess) return err;
+    if (n_seen < 256) seen[n_seen++] = Entry{func, dev, bytes};
+    return cudaSuccess;
+}
+
+static bool trace_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char* s = getenv("MOE_TRACE");
+        v = (s && s[0] && s[0] != '0') ? 1 : 0;
+    }
+    return v == 1;
+}
+
+static moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static int64_t capacity64(int T, int Kt, int Et, int tile_m) {
+    if (T < 0 || Kt < 1 || Et < 1 || tile_m < 1) return -1;
+    return (int64_t)T * Kt + (int64_t)Et * (tile_m - 1);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: null, negative or misaligned argument";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE: size outside the supported limits";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL: workspace smaller than moe_ffn_workspace_size()";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA launch failed (see cudaGetLastError)";
+        case MOE_ERR_INTERNAL: return "MOE_ERR_INTERNAL: internal error";
+    }
+    return "MOE_ERR_UNKNOWN: unknown status code";
+}
+
+int moe_version(void) { return 100; }
+
+moe_status_t moe_route(const float* logits, int T, int E, int K, int with_shared, int renormalize,
+                       int32_t* topk_ids, float* topk_w, cudaStream_t stream) {
+    if (T < 0 || E < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+    if (E > 1024 || K > 32 || K > E) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_route(logits, T, E, K, with_shared ? 1 : 0, renormalize ? 1 : 0,
+                                    topk_ids, topk_w, stream));
+}
+
+size_t moe_permute_capacity(int T, int Kt, int Et, int tile_m) {
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    return cap < 0 ? 0 : (size_t)cap;
+}
+
+size_t moe_permute_max_tiles(int T, int Kt, int Et, int tile_m) {
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    return cap < 0 ? 0 : (size_t)(cap / tile_m);
+}
+
+moe_status_t moe_permute(const int32_t* topk_ids, int T, int Kt, int Et, int tile_m,
+                         int32_t* sorted_pairs, int32_t* expert_offsets, int32_t* inv_pairs,
+                         int32_t* tile_expert, int32_t* num_tiles, cudaStream_t stream) {
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    if (cap < 0) return MOE_ERR_INVALID_ARG;
+    if (Kt > 33 || Et > 1025 || tile_m > 256 || cap >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!expert_offsets || !num_tiles) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_ids || !inv_pairs)) return MOE_ERR_INVALID_ARG;
+    if (cap > 0 && !sorted_pairs) return MOE_ERR_INVALID_ARG;
+    if (cap / tile_m > 0 && !tile_expert) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {topk_ids, sorted_pairs, expert_offsets, inv_pairs, tile_expert, num_tiles};
+    for (const void* p : ptrs)
+        if (p && !aligned(p, 4)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_permute(topk_ids, T, Kt, Et, tile_m, (int)cap, (int)(cap / tile_m),
+                                      sorted_pairs, expert_offsets, inv_pairs, tile_expert,
+                                      num_tiles, stream));
+}
+
+size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m) {
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    if (cap < 0 || H <= 0 || I <= 0) return 0;
+    return round_up((size_t)cap * I * sizeof(uint16_t), 256) +
+           round_up((size_t)T * Kt * H * sizeof(float), 256);
+}
+
+moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m) {
+    // mean rows per expert; the decode path wins while most experts see only
+    // a few rows, so the weight stream, not the MMA, bounds the time
+    const double rows_per_expert = Et > 0 ? (double)T * Kt / Et : 0.0;
+    if (rows_per_expert >= 16.0 && prefill_tile_supported(tile_m)) return MOE_PATH_PREFILL;
+    if (decode_tile_supported(tile_m)) return MOE_PATH_DECODE;
+    return prefill_tile_supported(tile_m) ? MOE_PATH_PREFILL : MOE_PATH_DECODE;
+}
+
+// Shape/path checks shared by the FFN calls.  Resolves AUTO (and the
+// MOE_FORCE_PATH environment override) to a concrete path.
+static moe_status_t check_ffn_shape(int T, int H, int I, int Et, int Kt, int tile_m,
+                                    moe_path_t* path) {
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    if (cap < 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+    if (H % 32 || I % 32 || H > 65536 || I > 65536 || Kt > 33 || Et > 1025 || tile_m > 256 ||
+        cap >= ((int64_t)1 << 31))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    moe_path_t p = *path;
+    if (p != MOE_PATH_AUTO && p != MOE_PATH_DECODE && p != MOE_PATH_PREFILL) return MOE_ERR_INVALID_ARG;
+    if (p == MOE_PATH_AUTO) {
+        const char* f = getenv("MOE_FORCE_PATH");
+        if (f && !strcmp(f, "decode")) p = MOE_PATH_DECODE;
+        else if (f && !strcmp(f, "prefill")) p = MOE_PATH_PREFILL;
+        else p = moe_ffn_auto_path(T, Kt, Et, tile_m);
+    }
+    if (p == MOE_PATH_DECODE && !decode_tile_supported(tile_m)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (p == MOE_PATH_PREFILL && (!prefill_tile_supported(tile_m) || !prefill_shape_supported(H, I)))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    *path = p;
+    return MOE_OK;
+}
+
+static bool ptrs_ok(std::initializer_list<const void*> ptrs, size_t align) {
+    for (const void* p : ptrs)
+        if (!p || !aligned(p, align)) return false;
+    return true;
+}
+
+static GroupedGemm base_gemm(const int32_t* sorted_pairs, const int32_t* tile_expert,
+                             const int32_t* num_tiles, int I, int Kt, int tile_m, int max_tiles) {
+    GroupedGemm g{};
+    g.sorted_pairs = sorted_pairs;
+    g.tile_expert = tile_expert;
+    g.num_tiles = num_tiles;
+    g.Kt = Kt;
+    g.tile_m = tile_m;
+    g.max_tiles = max_tiles;
+    g.I = I;
+    return g;
+}
+
+static void trace(const char* step, int T, int H, int I, int Et, int Kt, int tile_m, moe_path_t p) {
+    if (trace_enabled())
+        fprintf(stderr, "[libmoe] %s T=%d H=%d I=%d Et=%d Kt=%d tile_m=%d path=%s\n", step, T, H, I,
+                Et, Kt, tile_m, p == MOE_PATH_DECODE ? "decode" : "prefill");
+}
+
+size_t moe_ffn_y_offset(int T, int I, int Et, int Kt, int tile_m) {
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    if (cap < 0 || I <= 0) return 0;
+    return round_up((size_t)cap * I * sizeof(uint16_t), 256);
+}
+
+moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                             const int32_t* sorted_pairs, const int32_t* tile_expert,
+                             const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                             int tile_m, uint16_t* h, moe_path_t path, cudaStream_t stream) {
+    moe_status_t st = check_ffn_shape(T, H, I, Et, Kt, tile_m, &path);
+    if (st != MOE_OK || T == 0) return st;
+    if (!ptrs_ok({x, w13, h}, 16) || !ptrs_ok({s13, sorted_pairs, tile_expert, num_tiles}, 4))
+        return MOE_ERR_INVALID_ARG;
+    const int max_tiles = (int)(capacity64(T, Kt, Et, tile_m) / tile_m);
+    trace("moe_ffn_gate_up", T, H, I, Et, Kt, tile_m, path);
+    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, I, Kt, tile_m, max_tiles);
+    g.codes = w13;
+    g.scales = s13;
+    g.rows = 2 * I;
+    g.K = H;
+    g.act = x;
+    g.act_by_token = 1;
+    g.h_out = h;
+    cudaError_t err = path == MOE_PATH_DECODE ? launch_decode_gate_up(g, stream)
+                                               : launch_prefill_gate_up(g, stream);
+    return cuda_status(err);
+}
+
+moe_status_t moe_ffn_down(const uint16_t* h, const uint8_t* w2, const uint8_t* s2,
+                          const float* topk_w, const int32_t* sorted_pairs,
+                          const int32_t* tile_expert, const int32_t* num_tiles, int T, int H,
+                          int I, int Et, int Kt, int tile_m, float* y, moe_path_t path,
+                          cudaStream_t stream) {
+    moe_status_t st = check_ffn_shape(T, H, I, Et, Kt, tile_m, &path);
+    if (st != MOE_OK || T == 0) return st;
+    if (!ptrs_ok({h, w2, y}, 16) || !ptrs_ok({s2, topk_w, sorted_pairs, tile_expert, num_tiles}, 4))
+        return MOE_ERR_INVALID_ARG;
+    const int max_tiles = (int)(capacity64(T, Kt, Et, tile_m) / tile_m);
+    trace("moe_ffn_down", T, H, I, Et, Kt, tile_m, path);
+    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, I, Kt, tile_m, max_tiles);
+    g.codes = w2;
+    g.scales = s2;
+    g.rows = H;
+    g.K = I;
+    g.act = h;
+    g.act_by_token = 0;
+    g.y_out = y;
+    g.topk_w = topk_w;
+    cudaError_t err = path == MOE_PATH_DECODE ? launch_decode_down(g, stream)
+                                               : launch_prefill_down(g, stream);
+    return cuda_status(err);
+}
+
+moe_status_t moe_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t stream) {
+    if (T < 0 || H <= 0 || Kt < 1) return MOE_ERR_INVALID_ARG;
+    if (H % 4 || Kt > 33) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!ptrs_ok({y, out}, 16)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_combine(y, T, H, Kt, out, stream));
+}
+
+moe_status_t moe_ffn_path(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                          const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                          const int32_t* sorted_pairs, const int32_t* expert_offsets,
+                          const int32_t* inv_pairs, const int32_t* tile_expert,
+                          const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                          int tile_m, uint16_t* out, void* workspace, size_t ws_bytes,
+                          moe_path_t path, cudaStream_t stream) {
+    moe_status_t st = check_ffn_shape(T, H, I, Et, Kt, tile_m, &path);
+    if (st != MOE_OK || T == 0) return st;
+    if (!ptrs_ok({x, w13, w2, out, workspace}, 16) ||
+        !ptrs_ok({s13, s2, topk_w, sorted_pairs, expert_offsets, inv_pairs, tile_expert, num_tiles}, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_ffn_workspace_size(T, H, I, Et, Kt, tile_m)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    uint16_t* h = reinterpret_cast<uint16_t*>(workspace);
+    float* y = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) +
+                                        moe_ffn_y_offset(T, I, Et, Kt, tile_m));
+    st = moe_ffn_gate_up(x, w13, s13, sorted_pairs, tile_expert, num_tiles, T, H, I, Et, Kt, tile_m,
+                         h, path, stream);
+    if (st != MOE_OK) return st;
+    st = moe_ffn_down(h, w2, s2, topk_w, sorted_pairs, tile_expert, num_tiles, T, H, I, Et, Kt,
+                      tile_m, y, path, stream);
+    if (st != MOE_OK) return st;
+    return moe_combine(y, T, H, Kt, out, stream);
+}
+
+moe_status_t moe_ffn(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,
+                     const uint8_t* s2, const float* topk_w, const int32_t* sorted_pairs,
+                     const int32_t* expert_offsets, const int32_t* inv_pairs,
+                     const int32_t* tile_expert, const int32_t* num_tiles, int T, int H, int I,
+                     int Et, int Kt, int tile_m, uint16_t* out, void* workspace, size_t ws_bytes,
+                     cudaStream_t stream) {
+    return moe_ffn_path(x, w13, s13, w2, s2, topk_w, sorted_pairs, expert_offsets, inv_pairs,
+                        tile_expert, num_tiles, T, H, I, Et, Kt, tile_m, out, workspace, ws_bytes,
+                        MOE_PATH_AUTO, stream);
+}
+
+}  // extern "C"

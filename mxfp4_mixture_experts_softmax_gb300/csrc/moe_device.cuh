@@ -1,0 +1,121 @@
+// moe_device.cuh -- device helpers shared by the libmoe kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ----------------------------------------------------------------- loads
+
+// 16-byte streaming load of weight bytes: read once per launch, so keep them
+// out of L1 (they still pass through L2, where concurrent tiles of the same
+// expert can share them).
+__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ldg_stream_u16(const void* p) {
+    unsigned short r;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// ------------------------------------------------------------ MXFP4 decode
+
+// Eight E2M1 codes (one 32-bit word, code i in bits 4i..4i+3, i.e. element
+// 2b in the low nibble of byte b) to four bf16x2 values, each pair holding
+// codes (i, i+4): out[0] = (c0, c4), out[1] = (c1, c5), out[2] = (c2, c6),
+// out[3] = (c3, c7), low half first.
+//
+// Bit placement: a code s|e1 e0|m copied to bf16 bit 15 (sign) and bits 8..6
+// (e1 e0 m) is exactly the E2M1 value times 2^-126: e = 0 lands in the bf16
+// subnormals (m * 2^-1 * 2^-126), e > 0 in exponent field e with mantissa
+// bit m.  Masking two nibbles 16 bits apart and multiplying by
+// (2^6 + 2^12) places both copies without overlapping carries; the final
+// mask keeps the magnitude copy (<<6) and the sign copy (<<12).  The
+// multiply by `mult` = 2^(s-1) (bf16x2) then applies 2^126 and the E8M0
+// scale 2^(s-127) in one exact power-of-two product.
+__device__ __forceinline__ void mxfp4_word_to_bf16x2(uint32_t w, uint32_t mult, uint32_t out[4]) {
+    const uint32_t hi = w >> 8;
+    uint32_t t[4];
+    t[0] = ((w & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
+    t[1] = ((w & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
+    t[2] = ((hi & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
+    t[3] = ((hi & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&t[i]);
+        __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162*>(&mult);
+        __nv_bfloat162 r = __hmul2(a, m);
+        out[i] = *reinterpret_cast<uint32_t*>(&r);
+    }
+}
+
+// bf16x2 multiplier 2^(s-1) in both halves for E8M0 byte s <= 128
+// (exponent field s + 126).
+__device__ __forceinline__ uint32_t e8m0_mult_lo(uint32_t s) {
+    return (min(s, 128u) + 126u) * 0x00800080u;
+}
+
+// Second multiplier 2^(s-128) for scale bytes above 128 (exponent s - 1).
+__device__ __forceinline__ uint32_t e8m0_mult_hi(uint32_t s) {
+    return (max(s, 128u) - 1u) * 0x00800080u;
+}
+
+__device__ __forceinline__ void bf16x2_scale(uint32_t out[4], uint32_t mult) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&out[i]);
+        __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162*>(&mult);
+        __nv_bfloat162 r = __hmul2(a, m);
+        out[i] = *reinterpret_cast<uint32_t*>(&r);
+    }
+}
+
+// ----------------------------------------------------------- tensor cores
+
+// D = A * B + C, m16n8k16, bf16 inputs, fp32 accumulate (legacy warp MMA).
+__device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------- numerics
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+    __nv_bfloat16 b = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// Activation layout in shared memory: each group of 8 consecutive bf16
+// elements x0..x7 is stored as (x0,x4),(x1,x5),(x2,x6),(x3,x7), matching the
+// code pairing of mxfp4_word_to_bf16x2, so that one 16-byte load yields the
+// two B fragments of the two MMAs fed by one code word.
+__device__ __forceinline__ uint4 pair_interleave8(uint4 v) {
+    uint4 r;
+    r.x = __byte_perm(v.x, v.z, 0x5410);
+    r.y = __byte_perm(v.x, v.z, 0x7632);
+    r.z = __byte_perm(v.y, v.w, 0x5410);
+    r.w = __byte_perm(v.y, v.w, 0x7632);
+    return r;
+}
+
+}  // namespace moe

@@ -1,0 +1,55 @@
+// moe_internal.h -- launchers shared between the libmoe translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe_device.cuh"
+
+namespace moe {
+
+// Raises a kernel's dynamic shared memory limit once per device (idempotent;
+// the attribute is per function, so it stays set for later calls).
+cudaError_t ensure_dynamic_smem(const void* func, size_t bytes);
+
+cudaError_t launch_route(const float* logits, int T, int E, int K, int with_shared,
+                         int renormalize, int32_t* ids, float* w, cudaStream_t s);
+
+size_t permute_smem_bytes(int Et);
+cudaError_t launch_permute(const int32_t* ids, int T, int Kt, int Et, int tile_m, int cap,
+                           int max_tiles, int32_t* sorted_pairs, int32_t* offsets, int32_t* inv,
+                           int32_t* tile_expert, int32_t* num_tiles, cudaStream_t s);
+
+// Arguments of one grouped MXFP4 GEMM (swap-AB: weight rows are the MMA's M
+// side, the tile's token rows its N side).
+struct GroupedGemm {
+    const uint8_t* codes;        // [Et][rows][K/2]
+    const uint8_t* scales;       // [Et][rows][K/32]
+    int rows;                    // weight rows per expert (2I for gate_up, H for down)
+    int K;                       // reduction length (H for gate_up, I for down)
+    const uint16_t* act;         // bf16 B rows: x [T][H] (gate_up) or h [cap][I] (down)
+    int act_by_token;            // 1: B row = token q / Kt of the pair; 0: B row = sorted position
+    const int32_t* sorted_pairs;
+    const int32_t* tile_expert;
+    const int32_t* num_tiles;
+    int Kt;
+    int tile_m;
+    int max_tiles;
+    int I;                       // SwiGLU: gate rows [0, I), up rows [I, 2I)
+    uint16_t* h_out;             // SwiGLU output h [cap][I] (bf16)
+    float* y_out;                // weighted output [T*Kt][H] (fp32)
+    const float* topk_w;
+};
+
+bool decode_tile_supported(int tile_m);
+bool prefill_tile_supported(int tile_m);
+bool prefill_shape_supported(int H, int I);
+
+cudaError_t launch_decode_gate_up(const GroupedGemm& g, cudaStream_t s);
+cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s);
+cudaError_t launch_prefill_gate_up(const GroupedGemm& g, cudaStream_t s);
+cudaError_t launch_prefill_down(const GroupedGemm& g, cudaStream_t s);
+cudaError_t launch_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,148 @@
+// permute.cu -- stable counting sort of (token, slot) pairs by expert with
+// tile-aligned buckets, in one CTA.
+//
+// Tokens are grouped by expert in fixed-height row tiles so that the grouped
+// GEMMs see whole tiles of one expert (VibeSys Qwen3.5-397B on 4x MI300A,
+// section "cheaper prefill and collectives": 32-row MoE tiles).  The pages
+// report that parallelising the routing preparation gained nothing (section
+// "what did not help"), so one CTA of 1024 threads does all of it:
+//
+//  1. warp w counts the experts of its contiguous slice of pairs into its own
+//     shared-memory histogram row (32 rows x Et counters);
+//  2. per expert, an exclusive scan over the 32 warp rows gives each warp's
+//     starting rank inside the bucket; the bucket sizes rounded up to tile_m
+//     are scanned over experts to give the offsets;
+//  3. padding positions, the tile -> expert map and the tails are written;
+//  4. each warp walks its slice in order, 32 pairs at a time; lanes naming
+//     the same expert find each other with __match_any_sync and take
+//     consecutive positions in lane order.
+// Slices are contiguous and in warp order, so the result is the stable sort.
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    permute_kernel(const int32_t* __restrict__ ids, int P, int Et, int tile_m, int cap,
+                   int max_tiles, int32_t* __restrict__ sorted_pairs,
+                   int32_t* __restrict__ offsets_out, int32_t* __restrict__ inv,
+                   int32_t* __restrict__ tile_expert, int32_t* __restrict__ num_tiles) {
+    extern __shared__ int32_t smem[];
+    int32_t* hist = smem;                      // [kWarps][Et]: counts, then write cursors
+    int32_t* cnt = hist + kWarps * Et;         // [Et]
+    int32_t* off = cnt + Et;                   // [Et + 1]
+    int32_t* wsum = off + Et + 1;              // [kWarps]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < kWarps * Et; i += kThreads) hist[i] = 0;
+    __syncthreads();
+
+    const int chunk = (P + kWarps - 1) / kWarps;
+    const int q_begin = min(P, warp * chunk), q_end = min(P, q_begin + chunk);
+    int32_t* my_hist = hist + warp * Et;
+    for (int q = q_begin + lane; q < q_end; q += 32) {
+        const int e = __ldg(ids + q);
+        if ((unsigned)e < (unsigned)Et) atomicAdd(&my_hist[e], 1);
+    }
+    __syncthreads();
+
+    // per-expert exclusive scan over warps
+    for (int e = tid; e < Et; e += kThreads) {
+        int run = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            const int c = hist[w * Et + e];
+            hist[w * Et + e] = run;
+            run += c;
+        }
+        cnt[e] = run;
+    }
+    __syncthreads();
+
+    // exclusive scan of the padded bucket sizes over e = 0..Et (Et+1 entries,
+    // the last one padded with 0 so that off[Et] is the total); two entries
+    // per thread covers Et + 1 <= 2048.
+    {
+        const int i0 = 2 * tid, i1 = 2 * tid + 1;
+        const int p0 = i0 < Et ? (cnt[i0] + tile_m - 1) / tile_m * tile_m : 0;
+        const int p1 = i1 < Et ? (cnt[i1] + tile_m - 1) / tile_m * tile_m : 0;
+        const int mine = p0 + p1;
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int v = wsum[lane];
+            int wi = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+                if (lane >= o) wi += n;
+            }
+            wsum[lane] = wi - v;  // exclusive prefix of warp totals
+        }
+        __syncthreads();
+        const int excl = wsum[warp] + incl - mine;
+        if (i0 <= Et) off[i0] = excl;
+        if (i1 <= Et) off[i1] = excl + p0;
+    }
+    __syncthreads();
+
+    for (int i = tid; i < kWarps * Et; i += kThreads) hist[i] += off[i % Et];
+    for (int e = tid; e <= Et; e += kThreads) offsets_out[e] = off[e];
+    const int used = off[Et];
+    const int nt = used / tile_m;
+    if (tid == 0) *num_tiles = nt;
+    // bucket padding and the tail of sorted_pairs; tile -> expert map
+    for (int e = tid; e < Et; e += kThreads) {
+        for (int p = off[e] + cnt[e]; p < off[e + 1]; ++p) sorted_pairs[p] = -1;
+        for (int i = off[e] / tile_m; i < off[e + 1] / tile_m; ++i) tile_expert[i] = e;
+    }
+    for (int p = used + tid; p < cap; p += kThreads) sorted_pairs[p] = -1;
+    for (int i = nt + tid; i < max_tiles; i += kThreads) tile_expert[i] = -1;
+    __syncthreads();
+
+    // stable scatter
+    for (int base = q_begin; base < q_end; base += 32) {
+        const int q = base + lane;
+        int e = q < q_end ? __ldg(ids + q) : -1;
+        const bool valid = (unsigned)e < (unsigned)Et;
+        if (q < q_end && !valid) inv[q] = -1;
+        if (!valid) e = -1 - lane;  // unique per lane: matches nobody
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+        int b = 0;
+        if (valid) {
+            b = my_hist[e];
+            const int pos = b + __popc(peers & lanemask_lt());
+            sorted_pairs[pos] = q;
+            inv[q] = pos;
+        }
+        __syncwarp();
+        if (valid && (peers & lanemask_lt()) == 0) my_hist[e] = b + __popc(peers);
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+size_t permute_smem_bytes(int Et) { return sizeof(int32_t) * ((size_t)kWarps * Et + 2 * Et + 1 + kWarps); }
+
+cudaError_t launch_permute(const int32_t* ids, int T, int Kt, int Et, int tile_m, int cap,
+                           int max_tiles, int32_t* sorted_pairs, int32_t* offsets, int32_t* inv,
+                           int32_t* tile_expert, int32_t* num_tiles, cudaStream_t s) {
+    const size_t smem = permute_smem_bytes(Et);
+    cudaError_t err = ensure_dynamic_smem((const void*)permute_kernel, smem);
+    if (err != cudaSuccess) return err;
+    permute_kernel<<<1, kThreads, smem, s>>>(ids, T * Kt, Et, tile_m, cap, max_tiles, sorted_pairs,
+                                             offsets, inv, tile_expert, num_tiles);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,267 @@
+"""Thin Python binding of the libmoe C ABI (include/moe.h), same entry-point names.
+
+Argument marshalling only: every step runs in libmoe's CUDA kernels.  Torch
+is used for device memory and the current stream.  If the shared library is
+missing it is compiled with nvcc; if that is impossible the import fails --
+there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build_lib
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED_SHAPE = 2
+MOE_ERR_WORKSPACE_TOO_SMALL = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_INTERNAL = 5
+
+MOE_PATH_AUTO = 0
+MOE_PATH_DECODE = 1
+MOE_PATH_PREFILL = 2
+
+EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_permute_capacity",
+           "moe_permute_max_tiles", "moe_permute", "moe_ffn_workspace_size", "moe_ffn",
+           "moe_ffn_path", "moe_ffn_auto_path", "moe_ffn_gate_up", "moe_ffn_down", "moe_combine",
+           "moe_ffn_y_offset")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+def lib_path() -> str:
+    return build_lib.LIB
+
+
+def load(build: bool = True):
+    """Load libmoe.so (building it first if needed) and declare the signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = build_lib.build() if build else build_lib.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libmoe is not built ({path}); run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        vp, ci, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.moe_status_string.argtypes = [ci]
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_version.argtypes = []
+        L.moe_version.restype = ci
+        L.moe_route.argtypes = [vp, ci, ci, ci, ci, ci, vp, vp, vp]
+        L.moe_route.restype = ci
+        L.moe_permute_capacity.argtypes = [ci, ci, ci, ci]
+        L.moe_permute_capacity.restype = sz
+        L.moe_permute_max_tiles.argtypes = [ci, ci, ci, ci]
+        L.moe_permute_max_tiles.restype = sz
+        L.moe_permute.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp]
+        L.moe_permute.restype = ci
+        L.moe_ffn_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci]
+        L.moe_ffn_workspace_size.restype = sz
+        ffn_args = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, sz]
+        L.moe_ffn.argtypes = ffn_args + [vp]
+        L.moe_ffn.restype = ci
+        L.moe_ffn_path.argtypes = ffn_args + [ci, vp]
+        L.moe_ffn_path.restype = ci
+        L.moe_ffn_auto_path.argtypes = [ci, ci, ci, ci]
+        L.moe_ffn_auto_path.restype = ci
+        L.moe_ffn_gate_up.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, ci, vp]
+        L.moe_ffn_gate_up.restype = ci
+        L.moe_ffn_down.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, ci, vp]
+        L.moe_ffn_down.restype = ci
+        L.moe_combine.argtypes = [vp, ci, ci, ci, vp, vp]
+        L.moe_combine.restype = ci
+        L.moe_ffn_y_offset.argtypes = [ci, ci, ci, ci, ci]
+        L.moe_ffn_y_offset.restype = sz
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return load().moe_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, dtype_name: str):
+    import torch
+    assert t.is_cuda and t.is_contiguous(), f"{dtype_name} must be a contiguous CUDA tensor"
+    return t
+
+
+def moe_route(logits, K: int, with_shared: bool = True, renormalize: bool = True,
+              topk_ids=None, topk_w=None, stream=None):
+    """fp32 logits [T, E] -> (int32 ids [T, Kt], fp32 weights [T, Kt])."""
+    import torch
+    _dev(logits, "logits")
+    assert logits.dtype == torch.float32
+    T, E = logits.shape
+    Kt = K + (1 if with_shared else 0)
+    if topk_ids is None:
+        topk_ids = torch.empty((T, Kt), dtype=torch.int32, device=logits.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, Kt), dtype=torch.float32, device=logits.device)
+    _check(load().moe_route(_ptr(logits), T, E, K, int(with_shared), int(renormalize),
+                            _ptr(topk_ids), _ptr(topk_w), _stream(stream)), "moe_route")
+    return topk_ids, topk_w
+
+
+def moe_permute_capacity(T: int, Kt: int, Et: int, tile_m: int) -> int:
+    return int(load().moe_permute_capacity(T, Kt, Et, tile_m))
+
+
+def moe_permute_max_tiles(T: int, Kt: int, Et: int, tile_m: int) -> int:
+    return int(load().moe_permute_max_tiles(T, Kt, Et, tile_m))
+
+
+def alloc_permute(T: int, Kt: int, Et: int, tile_m: int, device="cuda") -> dict:
+    import torch
+    cap = moe_permute_capacity(T, Kt, Et, tile_m)
+    mt = moe_permute_max_tiles(T, Kt, Et, tile_m)
+    i32 = dict(dtype=torch.int32, device=device)
+    return dict(sorted_pairs=torch.empty(max(cap, 1), **i32)[:cap],
+                expert_offsets=torch.empty(Et + 1, **i32),
+                inv_pairs=torch.empty(max(T * Kt, 1), **i32)[:T * Kt],
+                tile_expert=torch.empty(max(mt, 1), **i32)[:mt],
+                num_tiles=torch.empty(1, **i32), T=T, Kt=Kt, Et=Et, tile_m=tile_m)
+
+
+def moe_permute(topk_ids, Et: int, tile_m: int, out: dict | None = None, stream=None) -> dict:
+    """int32 ids [T, Kt] -> dict of sorted_pairs, expert_offsets, inv_pairs,
+    tile_expert, num_tiles (device tensors) plus the sizes."""
+    T, Kt = topk_ids.shape
+    _dev(topk_ids, "topk_ids")
+    if out is None:
+        out = alloc_permute(T, Kt, Et, tile_m, topk_ids.device)
+    _check(load().moe_permute(_ptr(topk_ids), T, Kt, Et, tile_m, _ptr(out["sorted_pairs"]),
+                              _ptr(out["expert_offsets"]), _ptr(out["inv_pairs"]),
+                              _ptr(out["tile_expert"]), _ptr(out["num_tiles"]), _stream(stream)),
+           "moe_permute")
+    return out
+
+
+def moe_ffn_workspace_size(T: int, H: int, I: int, Et: int, Kt: int, tile_m: int) -> int:
+    return int(load().moe_ffn_workspace_size(T, H, I, Et, Kt, tile_m))
+
+
+def moe_ffn_auto_path(T: int, Kt: int, Et: int, tile_m: int) -> int:
+    return int(load().moe_ffn_auto_path(T, Kt, Et, tile_m))
+
+
+def alloc_workspace(T: int, H: int, I: int, Et: int, Kt: int, tile_m: int, device="cuda"):
+    import torch
+    n = moe_ffn_workspace_size(T, H, I, Et, Kt, tile_m)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def moe_ffn(x, w13, s13, w2, s2, topk_w, perm: dict, out=None, workspace=None,
+            path: int = MOE_PATH_AUTO, stream=None):
+    """bf16 x [T, H] -> bf16 out [T, H] through the grouped MXFP4 expert MLPs."""
+    import torch
+    T, H = x.shape
+    Et, twoI, _ = w13.shape
+    I = twoI // 2
+    Kt, tile_m = perm["Kt"], perm["tile_m"]
+    for t in (x, w13, s13, w2, s2, topk_w):
+        _dev(t, "ffn input")
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = alloc_workspace(T, H, I, Et, Kt, tile_m, x.device)
+    _check(load().moe_ffn_path(_ptr(x), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), _ptr(topk_w),
+                               _ptr(perm["sorted_pairs"]), _ptr(perm["expert_offsets"]),
+                               _ptr(perm["inv_pairs"]), _ptr(perm["tile_expert"]),
+                               _ptr(perm["num_tiles"]), T, H, I, Et, Kt, tile_m, _ptr(out),
+                               _ptr(workspace), workspace.numel(), int(path), _stream(stream)),
+           "moe_ffn")
+    return out
+
+
+def moe_ffn_y_offset(T: int, I: int, Et: int, Kt: int, tile_m: int) -> int:
+    return int(load().moe_ffn_y_offset(T, I, Et, Kt, tile_m))
+
+
+def ffn_views(workspace, T: int, H: int, I: int, Et: int, Kt: int, tile_m: int):
+    """(h bf16 [cap, I], y fp32 [T*Kt, H]) views of a moe_ffn workspace."""
+    import torch
+    cap = moe_permute_capacity(T, Kt, Et, tile_m)
+    off = moe_ffn_y_offset(T, I, Et, Kt, tile_m)
+    h = workspace[:cap * I * 2].view(torch.bfloat16).view(cap, I)
+    y = workspace[off:off + T * Kt * H * 4].view(torch.float32).view(T * Kt, H)
+    return h, y
+
+
+def moe_ffn_gate_up(x, w13, s13, perm: dict, h, path: int = MOE_PATH_AUTO, stream=None):
+    T, H = x.shape
+    Et, twoI, _ = w13.shape
+    _check(load().moe_ffn_gate_up(_ptr(x), _ptr(w13), _ptr(s13), _ptr(perm["sorted_pairs"]),
+                                  _ptr(perm["tile_expert"]), _ptr(perm["num_tiles"]), T, H,
+                                  twoI // 2, Et, perm["Kt"], perm["tile_m"], _ptr(h), int(path),
+                                  _stream(stream)), "moe_ffn_gate_up")
+    return h
+
+
+def moe_ffn_down(h, w2, s2, topk_w, perm: dict, y, T: int, path: int = MOE_PATH_AUTO,
+                 stream=None):
+    Et, H, halfI = w2.shape
+    _check(load().moe_ffn_down(_ptr(h), _ptr(w2), _ptr(s2), _ptr(topk_w),
+                               _ptr(perm["sorted_pairs"]), _ptr(perm["tile_expert"]),
+                               _ptr(perm["num_tiles"]), T, H, 2 * halfI, Et, perm["Kt"],
+                               perm["tile_m"], _ptr(y), int(path), _stream(stream)), "moe_ffn_down")
+    return y
+
+
+def moe_combine(y, T: int, H: int, Kt: int, out, stream=None):
+    _check(load().moe_combine(_ptr(y), T, H, Kt, _ptr(out), _stream(stream)), "moe_combine")
+    return out
+
+
+def moe_layer(logits, x, w13, s13, w2, s2, K: int, with_shared: bool = True,
+              renormalize: bool = True, tile_m: int = 8, path: int = MOE_PATH_AUTO,
+              bufs: dict | None = None, stream=None):
+    """The whole layer: route -> permute -> ffn, all on one stream.  `bufs`
+    (from alloc_layer) reuses preallocated device buffers."""
+    T, E = logits.shape
+    Et = w13.shape[0]
+    if bufs is None:
+        bufs = alloc_layer(T, E, K, with_shared, x.shape[1], w13.shape[1] // 2, Et, tile_m,
+                           x.device)
+    ids, w = moe_route(logits, K, with_shared, renormalize, bufs["topk_ids"], bufs["topk_w"],
+                       stream)
+    perm = moe_permute(ids, Et, tile_m, bufs["perm"], stream)
+    return moe_ffn(x, w13, s13, w2, s2, w, perm, bufs["out"], bufs["workspace"], path, stream)
+
+
+def alloc_layer(T, E, K, with_shared, H, I, Et, tile_m, device="cuda") -> dict:
+    import torch
+    Kt = K + (1 if with_shared else 0)
+    return dict(topk_ids=torch.empty((T, Kt), dtype=torch.int32, device=device),
+                topk_w=torch.empty((T, Kt), dtype=torch.float32, device=device),
+                perm=alloc_permute(T, Kt, Et, tile_m, device),
+                workspace=alloc_workspace(T, H, I, Et, Kt, tile_m, device),
+                out=torch.empty((T, H), dtype=torch.bfloat16, device=device))

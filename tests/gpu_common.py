@@ -1,0 +1,51 @@
+"""Helpers for the GPU parity tests: device upload and the parity bar.
+
+The bar for the FFN output (bf16 [T, H]) against the oracle:
+  per element |gpu - ref| <= 1e-2 * (|ref| + rms(ref)), rms over the whole
+  compared tensor, and relative L2 error ||gpu - ref|| / ||ref|| <= 2e-3.
+Routing ids, the permutation and every index output are compared bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+FFN_ELEM_TOL = 1e-2
+FFN_REL_L2 = 2e-3
+ROUTE_W_ATOL = 2e-6
+
+
+def to_dev(a: np.ndarray):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if a.dtype == np.uint16:
+        t = t.view(torch.int16).view(torch.bfloat16)
+    return t.cuda()
+
+
+def bf16_dev_to_f64(t) -> np.ndarray:
+    import torch
+    bits = t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def ffn_parity(gpu: np.ndarray, ref: np.ndarray, what: str = "") -> dict:
+    """Assert the parity bar; return the observed statistics."""
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    assert np.isfinite(gpu).all(), f"{what}: non-finite GPU output"
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    err = np.abs(gpu - ref)
+    bound = FFN_ELEM_TOL * (np.abs(ref) + rms)
+    worst = float((err / bound).max()) if err.size else 0.0
+    rel_l2 = float(np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-300))
+    stats = dict(worst_elem_ratio=worst, rel_l2=rel_l2, identical=float((gpu == ref).mean()))
+    assert worst <= 1.0, f"{what}: element error {worst:.3g} x bound {stats}"
+    assert rel_l2 <= FFN_REL_L2, f"{what}: rel L2 {rel_l2:.3g} {stats}"
+    return stats
+
+
+def upload_weights(d: dict) -> dict:
+    return {k: to_dev(d[k]) for k in ("w13", "s13", "w2", "s2")}

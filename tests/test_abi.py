@@ -1,0 +1,73 @@
+"""The C-ABI library loads and exports every entry point include/moe.h
+declares; host-side argument checks reject bad calls before any launch.
+CPU only: no call here reaches a CUDA kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mxfp4_mixture_experts_softmax_gb300 import libmoe
+    return libmoe.load()
+
+
+def test_header_declares_the_binding_names():
+    from mxfp4_mixture_experts_softmax_gb300 import libmoe
+    assert set(_declared()) == set(libmoe.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings_and_sizes(lib):
+    from mxfp4_mixture_experts_softmax_gb300 import libmoe as m
+    for s in range(6):
+        assert m.status_string(s).startswith("MOE_")
+    assert m.status_string(99).startswith("MOE_ERR_UNKNOWN")
+    assert m.moe_permute_capacity(64, 11, 513, 8) == 64 * 11 + 513 * 7
+    assert m.moe_permute_max_tiles(64, 11, 513, 8) == (64 * 11 + 513 * 7) // 8
+    assert m.moe_permute_capacity(-1, 11, 513, 8) == 0
+    cap = 64 * 11 + 513 * 7
+    ws = m.moe_ffn_workspace_size(64, 4096, 1024, 513, 11, 8)
+    assert ws >= cap * 1024 * 2 + 64 * 11 * 4096 * 4
+    assert m.moe_ffn_auto_path(64, 11, 513, 8) == m.MOE_PATH_DECODE
+
+
+def test_host_validation_rejects_before_launch(lib):
+    from mxfp4_mixture_experts_softmax_gb300 import libmoe as m
+    nul = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails validation
+    # route: negative T, K > E, E too large, NULL pointers
+    assert lib.moe_route(fake, -1, 8, 2, 0, 1, fake, fake, nul) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(fake, 4, 8, 9, 0, 1, fake, fake, nul) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_route(fake, 4, 2048, 2, 0, 1, fake, fake, nul) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_route(nul, 4, 8, 2, 0, 1, fake, fake, nul) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(nul, 0, 8, 2, 0, 1, nul, nul, nul) == m.MOE_OK  # T = 0: nothing to do
+    # permute: bad sizes, NULL outputs
+    assert lib.moe_permute(fake, 4, 2, 8, 0, fake, fake, fake, fake, fake, nul) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute(fake, 4, 40, 8, 8, fake, fake, fake, fake, fake, nul) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_permute(fake, 4, 2, 8, 8, fake, nul, fake, fake, fake, nul) == m.MOE_ERR_INVALID_ARG
+    # ffn: H not a multiple of 32, unsupported tile, tiny workspace, misaligned pointer
+    def ffn(T=4, H=256, I=128, Et=8, Kt=2, tile_m=8, ws=1 << 30, x=fake, path=0):
+        return lib.moe_ffn_path(x, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                                T, H, I, Et, Kt, tile_m, fake, fake, ws, path, nul)
+    assert ffn(H=250) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert ffn(tile_m=12, path=m.MOE_PATH_DECODE) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert ffn(ws=16) == m.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert ffn(x=ctypes.c_void_p(0x1008)) == m.MOE_ERR_INVALID_ARG
+    assert ffn(path=7) == m.MOE_ERR_INVALID_ARG
+    assert ffn(T=-2) == m.MOE_ERR_INVALID_ARG

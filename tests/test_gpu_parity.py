@@ -1,0 +1,265 @@
+"""GPU parity: libmoe (through its C ABI) against the CPU oracle.
+
+Routing ids and the permutation bit for bit; moe_ffn within the stated
+floating-point bar (gpu_common.ffn_parity).  Small shapes compare every
+output element; the full-size workloads compare every token of the 64-token
+decode step and a sample of tokens elsewhere, in the launch configuration the
+bench times.
+"""
+import numpy as np
+import pytest
+
+import gpu_common as gc
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # the suite is only collected for a GPU run
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+from mxfp4_mixture_experts_softmax_gb300 import libmoe  # noqa: E402  (loads libmoe, no fallback)
+from mxfp4_mixture_experts_softmax_gb300 import synth  # noqa: E402
+
+import oracle  # noqa: E402
+
+THREADS = synth.cpu_threads()
+ALL = list(synth.WORKLOADS)
+
+
+def _route_check(logits, K, shared, renorm=True):
+    ids_r, w_r = oracle.route(logits, K, shared, renorm)
+    ids_g, w_g = libmoe.moe_route(gc.to_dev(logits), K, shared, renorm)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(ids_g.cpu().numpy(), ids_r)
+    np.testing.assert_allclose(w_g.cpu().numpy(), w_r, rtol=0, atol=gc.ROUTE_W_ATOL)
+    return ids_r, w_r
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_route_workloads(name):
+    w = synth.WORKLOADS[name]
+    ids, wt = _route_check(synth.make_logits(w), w.K, w.with_shared)
+    np.testing.assert_allclose(wt[:, :w.K].sum(1), 1.0, atol=1e-6)
+
+
+@pytest.mark.parametrize("T,E,K", [(5, 1, 1), (33, 8, 2), (17, 33, 33), (9, 100, 7), (64, 512, 10),
+                                   (7, 1024, 32), (3, 64, 32)])
+def test_route_shapes(T, E, K):
+    rng = np.random.default_rng(T * 131 + E)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    _route_check(logits, K, True)
+    _route_check(logits, K, False, renorm=False)
+
+
+def test_route_ties_zeros_and_neg_inf():
+    rng = np.random.default_rng(7)
+    T, E = 40, 512
+    logits = (np.round(rng.standard_normal((T, E)) * 2) / 2).astype(np.float32)  # many ties
+    logits[0] = 0.0
+    logits[1, ::2] = -0.0
+    logits[2] = -np.inf
+    logits[2, 400] = 3.0
+    logits[2, 7] = 3.0
+    _route_check(logits, 10, True)
+
+
+@pytest.mark.parametrize("name", ALL)
+@pytest.mark.parametrize("tile_m", [8, 32, 128])
+def test_permute_workloads(name, tile_m):
+    w = synth.WORKLOADS[name]
+    ids, _ = oracle.route(synth.make_logits(w), w.K, w.with_shared)
+    _permute_check(ids, w.Et, tile_m)
+
+
+def _permute_check(ids, Et, tile_m):
+    ref = oracle.permute(ids, Et, tile_m)
+    got = libmoe.moe_permute(gc.to_dev(ids.astype(np.int32)), Et, tile_m)
+    torch.cuda.synchronize()
+    for k_ref, k_got in (("sorted_pairs", "sorted_pairs"), ("offsets", "expert_offsets"),
+                         ("inv", "inv_pairs"), ("tile_expert", "tile_expert")):
+        np.testing.assert_array_equal(got[k_got].cpu().numpy(), ref[k_ref], err_msg=k_ref)
+    assert int(got["num_tiles"].cpu()[0]) == ref["num_tiles"]
+
+
+@pytest.mark.parametrize("case", ["one_expert", "all_experts_max", "empty", "tile1", "tile256",
+                                  "single_token"])
+def test_permute_edges(case):
+    rng = np.random.default_rng(3)
+    if case == "one_expert":
+        ids, Et, tm = np.full((500, 1), 2, np.int32), 5, 32
+    elif case == "all_experts_max":
+        ids = np.stack([rng.permutation(1025)[:33] for _ in range(40)]).astype(np.int32)
+        Et, tm = 1025, 16
+    elif case == "empty":
+        ids, Et, tm = np.zeros((0, 11), np.int32), 513, 8
+    elif case == "tile1":
+        ids, Et, tm = rng.integers(0, 9, (100, 1)).astype(np.int32), 9, 1
+    elif case == "tile256":
+        ids = np.stack([rng.permutation(40)[:5] for _ in range(300)]).astype(np.int32)
+        Et, tm = 40, 256
+    else:
+        ids, Et, tm = np.array([[3, 0, 8]], np.int32), 9, 8
+    _permute_check(ids, Et, tm)
+
+
+# ------------------------------------------------------------------- ffn
+
+def _layer_inputs(w):
+    d = synth.make_inputs(w)
+    ids, wt = oracle.route(d["logits"], w.K, w.with_shared)
+    return d, ids, wt
+
+
+def _gpu_ffn(d, ids, wt, Et, tile_m, path=libmoe.MOE_PATH_AUTO, dev_w=None):
+    dev_w = dev_w or gc.upload_weights(d)
+    ids_d = gc.to_dev(ids)
+    perm = libmoe.moe_permute(ids_d, Et, tile_m)
+    out = libmoe.moe_ffn(gc.to_dev(d["x"]), dev_w["w13"], dev_w["s13"], dev_w["w2"], dev_w["s2"],
+                         gc.to_dev(wt), perm, path=path)
+    torch.cuda.synchronize()
+    return gc.bf16_dev_to_f64(out)
+
+
+SMALL = {
+    "tiny16": dict(),
+    "ragged37": dict(T=37, H=512, I=256, E=16, K=4, with_shared=True, seed=11),
+    "k_tail": dict(T=21, H=160, I=96, E=6, K=3, with_shared=True, seed=12),
+    "wide_k": dict(T=9, H=1024, I=512, E=12, K=5, with_shared=False, seed=13),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("tile_m", [8, 16, 32, 64])
+def test_ffn_small_full_output(name, tile_m):
+    w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL[name])
+    d, ids, wt = _layer_inputs(w)
+    ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt,
+                                    n_threads=THREADS))
+    got = _gpu_ffn(d, ids, wt, w.Et, tile_m, libmoe.MOE_PATH_DECODE)
+    gc.ffn_parity(got, ref, f"{name} tile_m={tile_m}")
+
+
+def test_ffn_tile_m_does_not_change_results():
+    w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL["ragged37"])
+    d, ids, wt = _layer_inputs(w)
+    outs = [_gpu_ffn(d, ids, wt, w.Et, tm, libmoe.MOE_PATH_DECODE) for tm in (8, 16, 32, 64)]
+    for o in outs[1:]:
+        np.testing.assert_array_equal(o, outs[0])
+
+
+def test_ffn_scale_bytes_above_128():
+    """Large E8M0 scales take the second power-of-two multiply."""
+    w = synth.scaled(synth.WORKLOADS["tiny16"], T=12, H=128, I=64, E=4, K=2, seed=21)
+    d, ids, wt = _layer_inputs(w)
+    rng = np.random.default_rng(0)
+    d["s13"] = rng.integers(118, 136, d["s13"].shape).astype(np.uint8)
+    d["s2"] = rng.integers(100, 120, d["s2"].shape).astype(np.uint8)
+    ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt))
+    gc.ffn_parity(_gpu_ffn(d, ids, wt, w.Et, 8, libmoe.MOE_PATH_DECODE), ref, "big scales")
+
+
+def test_ffn_w2_scale_increment_doubles_exactly():
+    w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL["ragged37"])
+    d, ids, wt = _layer_inputs(w)
+    a = _gpu_ffn(d, ids, wt, w.Et, 16, libmoe.MOE_PATH_DECODE)
+    d2 = dict(d, s2=d["s2"] + 1)
+    b = _gpu_ffn(d2, ids, wt, w.Et, 16, libmoe.MOE_PATH_DECODE)
+    np.testing.assert_array_equal(b, 2 * a)
+
+
+def test_ffn_token_permutation_equivariance():
+    w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL["ragged37"])
+    d, ids, wt = _layer_inputs(w)
+    a = _gpu_ffn(d, ids, wt, w.Et, 8, libmoe.MOE_PATH_DECODE)
+    p = np.random.default_rng(1).permutation(w.T)
+    d2 = dict(d, x=np.ascontiguousarray(d["x"][p]))
+    b = _gpu_ffn(d2, np.ascontiguousarray(ids[p]), np.ascontiguousarray(wt[p]), w.Et, 8,
+                 libmoe.MOE_PATH_DECODE)
+    np.testing.assert_array_equal(b, a[p])
+
+
+def test_shared_as_expert_equals_routed_plus_dense():
+    w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL["ragged37"])
+    d, ids, wt = _layer_inputs(w)
+    full = _gpu_ffn(d, ids, wt, w.Et, 8, libmoe.MOE_PATH_DECODE)
+    K = w.K
+    routed = _gpu_ffn(d, np.ascontiguousarray(ids[:, :K]), np.ascontiguousarray(wt[:, :K]), w.Et,
+                      8, libmoe.MOE_PATH_DECODE)
+    E = w.E
+    dense_w = {k: np.ascontiguousarray(d[k][E:E + 1]) for k in ("w13", "s13", "w2", "s2")}
+    dense = _gpu_ffn(dict(d, **dense_w), np.zeros((w.T, 1), np.int32),
+                     np.ones((w.T, 1), np.float32), 1, 8, libmoe.MOE_PATH_DECODE)
+    gc.ffn_parity(full, routed + dense, "shared == routed + dense")
+
+
+def test_ffn_empty_batch():
+    w = synth.scaled(synth.WORKLOADS["tiny16"], T=0)
+    d = synth.make_weights(w)
+    dev_w = gc.upload_weights(d)
+    ids = torch.zeros((0, w.Kt), dtype=torch.int32, device="cuda")
+    perm = libmoe.moe_permute(ids, w.Et, 8)
+    out = libmoe.moe_ffn(torch.zeros((0, w.H), dtype=torch.bfloat16, device="cuda"), dev_w["w13"],
+                         dev_w["s13"], dev_w["w2"], dev_w["s2"],
+                         torch.zeros((0, w.Kt), dtype=torch.float32, device="cuda"), perm)
+    torch.cuda.synchronize()
+    assert out.shape == (0, w.H)
+    assert int(perm["num_tiles"].cpu()[0]) == 0
+
+
+# ------------------------------------------------- full-size workloads
+
+FULL = {  # workload -> (tile_m as the bench runs it, tokens compared)
+    "decode64": (8, None),
+    "mtp_verify288": (8, 24),
+    "prefill1536": (8, 12),
+    "skewed_prefill8192": (8, 8),
+    "skewed_prefill8192_cal": (8, 8),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_ffn_full_size(name):
+    w = synth.WORKLOADS[name]
+    tile_m, n_tok = FULL[name]
+    d, ids, wt = _layer_inputs(w)
+    if n_tok is None:
+        tokens = np.arange(w.T, dtype=np.int32)
+    else:
+        rng = np.random.default_rng(99)
+        tokens = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, n_tok - 2, replace=False)]))
+        tokens = tokens.astype(np.int32)
+    ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt,
+                                    tokens=tokens, n_threads=THREADS))
+    dev_w = gc.upload_weights(d)
+    # the whole layer as the bench runs it: route -> permute -> ffn on the device
+    out = libmoe.moe_layer(gc.to_dev(d["logits"]), gc.to_dev(d["x"]), dev_w["w13"], dev_w["s13"],
+                           dev_w["w2"], dev_w["s2"], w.K, w.with_shared, tile_m=tile_m,
+                           path=libmoe.MOE_PATH_DECODE)
+    torch.cuda.synchronize()
+    got = gc.bf16_dev_to_f64(out)[tokens]
+    stats = gc.ffn_parity(got, ref, name)
+    print(name, stats)
+    del dev_w
+    torch.cuda.empty_cache()
+
+
+def test_layer_graph_capture_replays_identically():
+    w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL["ragged37"])
+    d = synth.make_inputs(w)
+    dev_w = gc.upload_weights(d)
+    logits, x = gc.to_dev(d["logits"]), gc.to_dev(d["x"])
+    bufs = libmoe.alloc_layer(w.T, w.E, w.K, w.with_shared, w.H, w.I, w.Et, 8)
+    eager = libmoe.moe_layer(logits, x, dev_w["w13"], dev_w["s13"], dev_w["w2"], dev_w["s2"], w.K,
+                             w.with_shared, tile_m=8, bufs=bufs).clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            libmoe.moe_layer(logits, x, dev_w["w13"], dev_w["s13"], dev_w["w2"], dev_w["s2"], w.K,
+                             w.with_shared, tile_m=8, bufs=bufs)
+    torch.cuda.current_stream().wait_stream(s)
+    bufs["out"].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(gc.bf16_dev_to_f64(bufs["out"]), gc.bf16_dev_to_f64(eager))
