@@ -40,6 +40,8 @@ def parse_args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="decode64")
     p.add_argument("--tile-m", type=int, default=8)
+    p.add_argument("--E", type=int, default=0,
+                   help="routed experts override (smaller cases for profiler captures)")
     p.add_argument("--path", default="auto", choices=["auto", "decode", "prefill"])
     p.add_argument("--replicas", type=int, default=2,
                    help="weight/input replicas rotated per step (keeps L2 cold)")
@@ -197,6 +199,8 @@ def run_ours(args, ws, rank, local):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo",
                                 device_id=dev if torch.cuda.is_available() else None)
     w = synth.WORKLOADS[args.workload]
+    if args.E:
+        w = synth.scaled(w, E=args.E, name=f"{w.name}_E{args.E}")
     path = {"auto": libmoe.MOE_PATH_AUTO, "decode": libmoe.MOE_PATH_DECODE,
             "prefill": libmoe.MOE_PATH_PREFILL}[args.path]
     tm = args.tile_m

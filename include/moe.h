@@ -203,6 +203,15 @@ moe_status_t moe_combine(const float* y, int T, int H, int Kt, uint16_t* out, cu
 /* Byte offset of y inside the moe_ffn workspace (h [cap, I] bf16 comes first). */
 size_t moe_ffn_y_offset(int T, int I, int Et, int Kt, int tile_m);
 
+/*
+ * moe_device_error -- reads (and with `clear` nonzero resets) the library's
+ * device error flag.  A kernel sets it when one of its bounded waits (the
+ * prefill path's mbarrier waits, 2 s each) gives up; the kernel then skips its
+ * output, releases its tensor memory and exits instead of hanging.  This call
+ * synchronises the current device.  *flag receives 0 (no error) or 1.
+ */
+moe_status_t moe_device_error(int* flag, int clear);
+
 /* The path MOE_PATH_AUTO picks for these sizes [VL, small-M vs large-M]. */
 moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m);
 

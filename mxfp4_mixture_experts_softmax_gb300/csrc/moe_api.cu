@@ -76,6 +76,11 @@ const char* moe_status_string(moe_status_t status) {
 
 int moe_version(void) { return 100; }
 
+moe_status_t moe_device_error(int* flag, int clear) {
+    if (!flag) return MOE_ERR_INVALID_ARG;
+    return cuda_status(read_device_error(flag, clear));
+}
+
 moe_status_t moe_route(const float* logits, int T, int E, int K, int with_shared, int renormalize,
                        int32_t* topk_ids, float* topk_w, cudaStream_t stream) {
     if (T < 0 || E < 1 || K < 1) return MOE_ERR_INVALID_ARG;

@@ -50,6 +50,7 @@ cudaError_t launch_decode_gate_up(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_prefill_gate_up(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_prefill_down(const GroupedGemm& g, cudaStream_t s);
+cudaError_t read_device_error(int* flag, int clear);
 cudaError_t launch_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t s);
 
 }  // namespace moe

@@ -27,7 +27,7 @@ MOE_PATH_PREFILL = 2
 EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_permute_capacity",
            "moe_permute_max_tiles", "moe_permute", "moe_ffn_workspace_size", "moe_ffn",
            "moe_ffn_path", "moe_ffn_auto_path", "moe_ffn_gate_up", "moe_ffn_down", "moe_combine",
-           "moe_ffn_y_offset")
+           "moe_ffn_y_offset", "moe_device_error")
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +83,8 @@ def load(build: bool = True):
         L.moe_combine.restype = ci
         L.moe_ffn_y_offset.argtypes = [ci, ci, ci, ci, ci]
         L.moe_ffn_y_offset.restype = sz
+        L.moe_device_error.argtypes = [vp, ci]
+        L.moe_device_error.restype = ci
         _lib = L
         return L
 
@@ -200,6 +202,13 @@ def moe_ffn(x, w13, s13, w2, s2, topk_w, perm: dict, out=None, workspace=None,
                                _ptr(workspace), workspace.numel(), int(path), _stream(stream)),
            "moe_ffn")
     return out
+
+
+def moe_device_error(clear: bool = True) -> int:
+    """The device error flag (1 if a bounded wait inside a kernel gave up)."""
+    flag = ctypes.c_int(0)
+    _check(load().moe_device_error(ctypes.byref(flag), int(clear)), "moe_device_error")
+    return flag.value
 
 
 def moe_ffn_y_offset(T: int, I: int, Et: int, Kt: int, tile_m: int) -> int:
