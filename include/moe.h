@@ -212,6 +212,39 @@ size_t moe_ffn_y_offset(int T, int I, int Et, int Kt, int tile_m);
  */
 moe_status_t moe_device_error(int* flag, int clear);
 
+/*
+ * moe_ffn_noalloc -- moe_ffn for callers that cannot allocate device memory
+ * (no cudaMalloc allowed where they run: inside a stream capture that must
+ * not allocate, or in a runtime or plugin that only owns fixed, pre-assigned
+ * device memory).  The paper has no counterpart; this is a deployment
+ * convenience.
+ *
+ * Same arguments, results and limits as moe_ffn, minus the workspace: the
+ * scratch (the bf16 SwiGLU intermediate and the fp32 per-pair outputs) lives
+ * in a fixed device array of MOE_NOALLOC_SCRATCH_BYTES inside the library,
+ * which every GPU that loads libmoe holds until the process exits.  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *   - Sizes whose moe_ffn_workspace_size() exceeds MOE_NOALLOC_SCRATCH_BYTES
+ *     are rejected with MOE_ERR_UNSUPPORTED_SHAPE before any launch (the
+ *     64-token decode step of a 4096/1024, 513-expert, top-10+1 layer needs
+ *     about 20 MiB with tile_m = 8).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array, and it keeps the last
+ *     call's contents.  Nothing in it needs to start at zero.  Calls whose
+ *     kernels overlap on the GPU (different streams without ordering, or
+ *     different host threads) race on the scratch and corrupt each other's
+ *     results: order them on one stream.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+moe_status_t moe_ffn_noalloc(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                             const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                             const int32_t* sorted_pairs, const int32_t* expert_offsets,
+                             const int32_t* inv_pairs, const int32_t* tile_expert,
+                             const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                             int tile_m, uint16_t* out, cudaStream_t stream);
+
 /* The path MOE_PATH_AUTO picks for these sizes [VL, small-M vs large-M]. */
 moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m);
 

@@ -27,7 +27,10 @@ MOE_PATH_PREFILL = 2
 EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_permute_capacity",
            "moe_permute_max_tiles", "moe_permute", "moe_ffn_workspace_size", "moe_ffn",
            "moe_ffn_path", "moe_ffn_auto_path", "moe_ffn_gate_up", "moe_ffn_down", "moe_combine",
-           "moe_ffn_y_offset", "moe_device_error")
+           "moe_ffn_y_offset", "moe_device_error", "moe_ffn_noalloc")
+
+# bytes of the fixed device scratch behind moe_ffn_noalloc (include/moe.h)
+MOE_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +86,8 @@ def load(build: bool = True):
         L.moe_combine.restype = ci
         L.moe_ffn_y_offset.argtypes = [ci, ci, ci, ci, ci]
         L.moe_ffn_y_offset.restype = sz
+        L.moe_ffn_noalloc.argtypes = ffn_args[:-2] + [vp]
+        L.moe_ffn_noalloc.restype = ci
         L.moe_device_error.argtypes = [vp, ci]
         L.moe_device_error.restype = ci
         _lib = L
@@ -209,6 +214,23 @@ def moe_device_error(clear: bool = True) -> int:
     flag = ctypes.c_int(0)
     _check(load().moe_device_error(ctypes.byref(flag), int(clear)), "moe_device_error")
     return flag.value
+
+
+def moe_ffn_noalloc(x, w13, s13, w2, s2, topk_w, perm: dict, out=None, stream=None):
+    """moe_ffn without a workspace argument: the scratch is the library's fixed
+    device array (for callers that cannot allocate device memory).  Calls on
+    one device share that array: do not overlap them on the GPU."""
+    import torch
+    T, H = x.shape
+    Et, twoI, _ = w13.shape
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _check(load().moe_ffn_noalloc(_ptr(x), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), _ptr(topk_w),
+                                  _ptr(perm["sorted_pairs"]), _ptr(perm["expert_offsets"]),
+                                  _ptr(perm["inv_pairs"]), _ptr(perm["tile_expert"]),
+                                  _ptr(perm["num_tiles"]), T, H, twoI // 2, Et, perm["Kt"],
+                                  perm["tile_m"], _ptr(out), _stream(stream)), "moe_ffn_noalloc")
+    return out
 
 
 def moe_ffn_y_offset(T: int, I: int, Et: int, Kt: int, tile_m: int) -> int:
