@@ -92,6 +92,36 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 copy measurement)"
 
 
+def tensor_peak():
+    """Dense bf16 tensor peak in TFLOP/s (burst: kernels are timed alone)."""
+    mp = measured_peaks()
+    if mp is not None:
+        v = _find_number(mp, ("bf16_tflops",))
+        if v:
+            return v, "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement)"
+
+
+def roofline_entry(kernel, bytes_, flops, seconds, traffic, traffic_src):
+    """The binding roofline of one kernel: whichever of HBM bytes and tensor
+    flops needs more time at peak."""
+    hbm, hbm_src = hbm_peak()
+    ten, ten_src = tensor_peak()
+    t_hbm = bytes_ / (hbm * 1e9)
+    t_ten = flops / (ten * 1e12)
+    hbm_ach = bytes_ / seconds / 1e9
+    ten_ach = flops / seconds / 1e12
+    if t_ten > t_hbm:
+        bound, ach, peak, unit, src = "tensor", ten_ach, ten, "TFLOP/s", ten_src
+    else:
+        bound, ach, peak, unit, src = "hbm", hbm_ach, hbm, "GB/s", hbm_src
+    return {"kernel": kernel, "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
+            "frac": ach / peak, "traffic": traffic,
+            "algorithmic_bytes_per_launch": int(bytes_), "flops_per_launch": int(flops),
+            "launch_us": seconds * 1e6, "peak_source": src, "traffic_source": traffic_src,
+            "hbm_frac": hbm_ach / hbm, "tensor_frac": ten_ach / ten}
+
+
 def traffic_from_profiles(kernel: str, workload: str, src_file: str):
     """dram bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source (sha256 recorded in the summary)."""
@@ -183,6 +213,22 @@ def layer_work(w, ids_host):
     flops = 2 * P * (2 * I * H + H * I)
     return dict(touched=touched, gate_up_bytes=gate_up, down_bytes=down, layer_bytes=layer,
                 flops=flops, gate_up_flops=2 * P * 2 * I * H)
+
+
+# ------------------------------------------------------------ ranks
+
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the time)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def weak_scaling_value(tokens_per_rank_step: int, steps: int, world: int, max_ms: float) -> float:
+    """All ranks' tokens divided by the slowest rank's time (tokens/s)."""
+    return tokens_per_rank_step * steps * world / (max_ms / 1e3)
 
 
 # ------------------------------------------------------------ our arm
@@ -298,23 +344,25 @@ def run_ours(args, ws, rank, local):
     e2e_ms = e0.elapsed_time(e1)
 
     if ws > 1:
-        t = torch.tensor([total_ms, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+        total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dev)
 
     result = None
     if rank == 0:
-        peak, peak_src = hbm_peak()
-        gu_s = per["gate_up"] / 1e3
-        achieved = work["gate_up_bytes"] / gu_s / 1e9
+        path_name = "prefill" if (args.path == "prefill" or (
+            args.path == "auto" and libmoe.moe_ffn_auto_path(w.T, w.Kt, w.Et, tm)
+            == libmoe.MOE_PATH_PREFILL)) else "decode"
+        src = "ffn_prefill.cu" if path_name == "prefill" else "ffn_decode.cu"
         traffic, traffic_src = traffic_from_profiles(
-            "decode_gate_up", args.workload,
-            os.path.join(ROOT, "mxfp4_mixture_experts_softmax_gb300", "csrc", "ffn_decode.cu"))
+            f"{path_name}_gate_up", w.name,
+            os.path.join(ROOT, "mxfp4_mixture_experts_softmax_gb300", "csrc", src))
+        gu = roofline_entry(f"{path_name}_gate_up", work["gate_up_bytes"], work["gate_up_flops"],
+                            per["gate_up"] / 1e3, traffic, traffic_src)
+        dn = roofline_entry(f"{path_name}_down", work["down_bytes"],
+                            work["flops"] - work["gate_up_flops"], per["down"] / 1e3, None, None)
         layer_s = sum(per.values()) / 1e3
-        tokens = w.T * K * ws
         result = {
             "metric": METRIC,
-            "value": tokens / (total_ms / 1e3),
+            "value": weak_scaling_value(w.T, K, ws, total_ms),
             "unit": "tokens/s",
             "n_gpus": ws,
             "steps": K,
@@ -328,32 +376,15 @@ def run_ours(args, ws, rank, local):
             "config": {
                 "workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K,
                 "shared_expert": w.with_shared, "Et": w.Et, "Kt": w.Kt, "tile_m": tm,
-                "path": args.path, "experts_touched": work["touched"],
+                "path": path_name, "experts_touched": work["touched"],
                 "parallelism": f"replicas x{ws} (weak scaling, tokens per GPU fixed)",
                 "l2": f"inputs larger than L2: {work['layer_bytes'] / 1e9:.2f} GB touched per "
                       f"step, {R} weight replicas rotated per step",
             },
-            "roofline": {
-                "kernel": "decode_gate_up" if args.path != "prefill" else "prefill_gate_up",
-                "bound": "hbm",
-                "achieved": achieved,
-                "peak": peak,
-                "unit": "GB/s",
-                "frac": achieved / peak,
-                "traffic": traffic,
-                "algorithmic_bytes_per_launch": work["gate_up_bytes"],
-                "launch_us": per["gate_up"] * 1e3,
-                "peak_source": peak_src,
-                "traffic_source": traffic_src,
-            },
-            "layer_roofline": {
-                "bound": "hbm",
-                "algorithmic_bytes_per_step": work["layer_bytes"],
-                "achieved": work["layer_bytes"] / layer_s / 1e9,
-                "frac": work["layer_bytes"] / layer_s / 1e9 / peak,
-                "unit": "GB/s",
-                "flops_per_step": work["flops"],
-            },
+            "roofline": gu,
+            "roofline_down": dn,
+            "layer_roofline": roofline_entry("layer", work["layer_bytes"], work["flops"],
+                                             layer_s, None, None),
             "kernels_us": {n: v * 1e3 for n, v in per.items()},
             "e2e": {"value": w.T * K * ws / (e2e_ms / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": int(host["logits"].nbytes + host["x"].nbytes),
