@@ -1,197 +1,332 @@
 // ffn_decode.cu -- small-M grouped MXFP4 GEMMs (decode path) and the combine.
 //
 // Decode steps move every touched expert's MXFP4 weights once and do little
-// arithmetic per byte, so the kernels are built around the weight stream:
-// each warp streams 16 weight rows with 16-byte loads straight into
-// registers, dequantises them there (fused MXFP4 MoE kernel with in-register
-// dequantisation: VibeSys Qwen3.5-397B on 4x MI300A, sections "baseline" and
-// "kernels and graph capture") and feeds legacy warp MMAs in a swap-AB
-// arrangement: the weight rows are the MMA's 16-row M side, the tile's tokens
-// its 8-column N side (narrow N tiles for small M: vLLM MiniMax M3 on MI355X,
-// section "local shape and tiling").
+// arithmetic per byte, so the kernels are built around the weight stream
+// (fused MXFP4 MoE kernel with in-register dequantisation: VibeSys
+// Qwen3.5-397B on 4x MI300A, sections "baseline" and "kernels and graph
+// capture"; narrow N tiles for small M: vLLM MiniMax M3 on MI355X, section
+// "local shape and tiling").
 //
-// A CTA owns one tile (tile_m rows of one expert, from moe_permute) and a
-// block of weight rows (gate_up: 64 gate rows + the 64 matching up rows, so
-// the SwiGLU epilogue has g and u in the same registers; down: 128 rows).
-// The tile's activation rows are staged once per 512-wide K chunk into shared
-// memory in the pair-interleaved, XOR-swizzled layout the B fragments read
-// conflict-free.
-//
-// K mapping inside one 256-wide K step: lane (r, c) = (lane/4, lane%4) loads
-// bytes [32c, 32c+32) of the step's 128 code bytes of its two rows, i.e.
-// k = 64c .. 64c+63 (two scale groups).  Word i of those bytes (codes
-// k = 64c+8i .. +7) feeds two MMAs: codes (0,4),(1,5) and (2,6),(3,7).  The
-// MMA's k slots are therefore a permutation of k; the activations in shared
-// memory use the same permutation, so every product pairs the right x[k].
+// A CTA owns one tile (tile_m token rows of one expert, from moe_permute) and
+// a block of 256 weight rows (gate_up: 128 gate rows and the 128 matching up
+// rows, so the SwiGLU epilogue has g and u in the same registers; down: 256
+// rows).  One producer warp streams the block's packed codes into a 4-stage
+// shared-memory ring with 2D TMA loads (two 128-row x 128-byte boxes per
+// stage, hardware 128-byte swizzle, mbarrier transaction counts); 16
+// consumer warps each own 16 rows:
+//   * ldmatrix.x4 hands lane c of every row quad the c-th 32-bit word (8
+//     codes) of a 32-wide scale group, so each pair of m16n8k16 MMAs sees one
+//     scale group per row;
+//   * codes become bf16 by bit placement (E2M1 * 2^-126, exact, e = 0 codes
+//     as bf16 subnormals, which the MMA consumes exactly) -- three integer ops
+//     per two values and no per-element multiply;
+//   * the activations were staged once, multiplied by 2^64 (exact) so that the
+//     products stay in the fp32 normal range, and each group's two MMAs go
+//     into a fresh fp32 partial that is added to the accumulator times
+//     2^126 * 2^(s-127) * 2^-64 = 2^(s-65): an exact power-of-two FMA.
+// The MMA's k slots are a fixed permutation of k (a code word yields pairs
+// (0,4),(1,5),(2,6),(3,7)); the staged activations use the same permutation
+// and an XOR swizzle that keeps the B-fragment loads conflict-free.
+#include <algorithm>
+
 #include "moe_internal.h"
 
 namespace moe {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kKC = 512;              // K per staged activation chunk
-constexpr int kChunks16 = kKC / 8;    // 16-byte chunks per staged row
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;    // + one producer warp
+constexpr int kRows = 256;                   // weight rows per CTA
+constexpr int kStageK = 256;                 // k per pipeline stage
+constexpr int kRowBytes = kStageK / 2;       // code bytes per row per stage (one TMA box row)
+constexpr int kBoxRows = 128;                // rows per TMA box
+constexpr int kStages = 4;
+constexpr int kStageBytes = kRows * kRowBytes;
+constexpr int kXBytes = 64 * 1024;           // staged activation chunk
+constexpr uint32_t kBf16TwoPow64 = 0x5F805F80u;  // bf16x2 (2^64, 2^64)
 
-template <int MODE, int NT>
-__global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GroupedGemm g) {
-    constexpr int TM = NT * 8;
-    extern __shared__ uint4 smem_u4[];
-    uint4* xs = smem_u4;                                      // [TM][kChunks16]
-    int32_t* qrow = reinterpret_cast<int32_t*>(xs + TM * kChunks16);  // [TM]
+template <int NT>
+struct DecodeSmem {
+    static constexpr int TM = NT * 8;
+    static constexpr int KC = kXBytes / (TM * 2);  // k per staged activation chunk
+    static constexpr int kX = kStages * kStageBytes;
+    static constexpr int kBars = kX + kXBytes;
+    static constexpr int kQ = kBars + 2 * kStages * 8;
+    static constexpr int kTotal = kQ + 2 * TM * 4 + 1024;  // + alignment slack
+};
 
-    const int tile = blockIdx.x;
-    if (tile >= __ldg(g.num_tiles)) return;
-    const int e = __ldg(g.tile_expert + tile);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = lane >> 2, c = lane & 3;
-
-    for (int j = threadIdx.x; j < TM; j += kThreads) qrow[j] = __ldg(g.sorted_pairs + tile * TM + j);
-
-    int row0, row1;
-    bool warp_valid;
+// Weight row (within the expert) held in CTA row rho, or -1 past the end.
+template <int MODE>
+__device__ __forceinline__ int cta_weight_row(int rho, int block, int I, int rows) {
     if (MODE == 0) {
-        const int n0 = blockIdx.y * 64 + warp * 8;
-        warp_valid = n0 < g.I;
-        row0 = n0 + r;
-        row1 = g.I + n0 + r;
-    } else {
-        const int m0 = blockIdx.y * 128 + warp * 16;
-        warp_valid = m0 < g.rows;
-        row0 = m0 + r;
-        row1 = m0 + r + 8;
+        const int n = block * 128 + (rho & 127);
+        return n < I ? (rho < 128 ? n : I + n) : -1;
     }
-    if (!warp_valid) row0 = row1 = 0;  // keep addresses in range; no loads are issued
+    const int m = block * kRows + rho;
+    return m < rows ? m : -1;
+}
+
+__device__ __forceinline__ float scale_factor(uint32_t s) {
+    return __uint_as_float((s + 62u) << 23);  // 2^(s - 65)
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul_bits(uint32_t a, uint32_t b) {
+    __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a),
+                               *reinterpret_cast<__nv_bfloat162*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Eight codes -> four bf16x2 of E2M1 * 2^-126 (see mxfp4_word_to_bf16x2_raw),
+// with the two placement multipliers passed in registers: as runtime values
+// they stay single integer multiply-adds on the FMA pipe instead of being
+// expanded into shift/add sequences on the integer ALU pipe, which the
+// decode kernels saturate.
+__device__ __forceinline__ void codes_to_bf16x2(uint32_t w, uint32_t mul_a, uint32_t mul_b,
+                                                uint32_t out[4]) {
+    const uint32_t hi = w >> 8;
+    out[0] = ((w & 0x000F000Fu) * mul_a) & 0x81C081C0u;
+    out[1] = ((w & 0x00F000F0u) * mul_b) & 0x81C081C0u;
+    out[2] = ((hi & 0x000F000Fu) * mul_a) & 0x81C081C0u;
+    out[3] = ((hi & 0x00F000F0u) * mul_b) & 0x81C081C0u;
+}
+
+// Persistent kernel: CTA b processes work items b, b + gridDim.x, ... where
+// item = tile * row_blocks + block.  The producer's stage ring runs across
+// items, so the next item's weights stream in while the consumers finish the
+// current one (epilogue, activation staging).
+template <int MODE, int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_gemm_kernel(const GroupedGemm g, const __grid_constant__ CUtensorMap codes_map) {
+    using L = DecodeSmem<NT>;
+    constexpr int TM = L::TM;
+    constexpr int KC = L::KC;
+    constexpr int XC = KC / 8;  // 16-byte chunks per staged activation row
+    extern __shared__ uint8_t smem_raw[];
+    // the 128-byte swizzle pattern repeats every 1024 bytes: align the ring
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* codes_s = smem;
+    uint4* xs = reinterpret_cast<uint4*>(smem + L::kX);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBars);
+    uint64_t* empty = full + kStages;
+    int32_t* qtok = reinterpret_cast<int32_t*>(smem + L::kQ);  // activation row, -1 = padding
+    int32_t* qpair = qtok + TM;                                  // pair index, -1 = padding
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = g.K;
-    const size_t cbytes = (size_t)K / 2, sbytes = (size_t)K / 32;
-    const uint8_t* cp0 = g.codes + ((size_t)e * g.rows + row0) * cbytes;
-    const uint8_t* cp1 = g.codes + ((size_t)e * g.rows + row1) * cbytes;
-    const uint8_t* sp0 = g.scales + ((size_t)e * g.rows + row0) * sbytes;
-    const uint8_t* sp1 = g.scales + ((size_t)e * g.rows + row1) * sbytes;
+    const int nsteps = (K + kStageK - 1) / kStageK;
+    const int row_blocks = MODE == 0 ? (g.I + 127) / 128 : (g.rows + kRows - 1) / kRows;
+    const int items = __ldg(g.num_tiles) * row_blocks;
 
-    float acc[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
-
-    const int nsteps = (K + 255) / 256;
-    // code registers: [row][half] 16 bytes each, plus their scale bytes
-    uint4 nxt[2][2];
-    uint32_t nsc[2][2];
-    auto load_step = [&](int st) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int kb = st * 256 + 64 * c + 32 * h;
-            const bool ok = warp_valid && kb < K;
-            nxt[0][h] = ok ? ldg_stream_v4(cp0 + kb / 2) : make_uint4(0, 0, 0, 0);
-            nxt[1][h] = ok ? ldg_stream_v4(cp1 + kb / 2) : make_uint4(0, 0, 0, 0);
-            nsc[0][h] = ok ? (uint32_t)__ldg(sp0 + kb / 32) : 127u;
-            nsc[1][h] = ok ? (uint32_t)__ldg(sp1 + kb / 32) : 127u;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
         }
-    };
-    load_step(0);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
 
-    for (int st = 0; st < nsteps; ++st) {
-        if ((st * 256) % kKC == 0) {
-            __syncthreads();
-            const int kc = st * 256;
-            for (int idx = threadIdx.x; idx < TM * kChunks16; idx += kThreads) {
-                const int j = idx / kChunks16, L = idx % kChunks16;
-                const int k = kc + L * 8;
-                const int q = qrow[j];
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (k < K && q >= 0) {
-                    const size_t arow = g.act_by_token ? (size_t)(q / g.Kt) : (size_t)(tile * TM + j);
-                    v = pair_interleave8(__ldg(reinterpret_cast<const uint4*>(g.act + arow * K + k)));
-                }
-                const int phys = L ^ (((L >> 3) & 3) | ((j & 1) << 2));
-                xs[j * kChunks16 + phys] = v;
-            }
-            __syncthreads();
-        }
-        uint4 cur[2][2];
-        uint32_t csc[2][2];
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                cur[a][h] = nxt[a][h];
-                csc[a][h] = nsc[a][h];
-            }
-        if (st + 1 < nsteps) load_step(st + 1);
-        if (!warp_valid) continue;
-
-        const int lbase = ((st * 256) % kKC) / 8 + 8 * c;  // step-local chunk of word 0
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t m0lo = e8m0_mult_lo(csc[0][h]), m1lo = e8m0_mult_lo(csc[1][h]);
-            const bool big = __any_sync(0xFFFFFFFFu, (csc[0][h] > 128u) | (csc[1][h] > 128u));
-            const uint32_t w0[4] = {cur[0][h].x, cur[0][h].y, cur[0][h].z, cur[0][h].w};
-            const uint32_t w1[4] = {cur[1][h].x, cur[1][h].y, cur[1][h].z, cur[1][h].w};
-#pragma unroll
-            for (int i4 = 0; i4 < 4; ++i4) {
-                uint32_t d0[4], d1[4];
-                mxfp4_word_to_bf16x2(w0[i4], m0lo, d0);
-                mxfp4_word_to_bf16x2(w1[i4], m1lo, d1);
-                if (big) {
-                    bf16x2_scale(d0, e8m0_mult_hi(csc[0][h]));
-                    bf16x2_scale(d1, e8m0_mult_hi(csc[1][h]));
-                }
-                const int i = 4 * h + i4;
-                const int L = lbase + i;
-                const int phys = L ^ (c | ((r & 1) << 2));
-                const uint32_t aA[4] = {d0[0], d1[0], d0[1], d1[1]};
-                const uint32_t aB[4] = {d0[2], d1[2], d0[3], d1[3]};
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    const uint4 b = xs[(n * 8 + r) * kChunks16 + phys];
-                    mma_bf16_16816(acc[n], aA, b.x, b.y);
-                    mma_bf16_16816(acc[n], aB, b.z, b.w);
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------- producer
+        if (lane == 0) {
+            uint32_t gs = 0;
+            for (int item = blockIdx.x; item < items; item += gridDim.x) {
+                const int tile = item / row_blocks, block = item % row_blocks;
+                const int e = __ldg(g.tile_expert + tile);
+                // rows of the two boxes in the map's row space (experts stacked);
+                // rows past this expert's block are loaded too and never used
+                const int row0 = e * g.rows + (MODE == 0 ? block * 128 : block * kRows);
+                const int row1 = MODE == 0 ? e * g.rows + g.I + block * 128 : row0 + kBoxRows;
+                for (int st = 0; st < nsteps; ++st, ++gs) {
+                    const int s = gs % kStages;
+                    if (gs >= kStages && !mbar_wait(&empty[s], ((gs / kStages) - 1) & 1)) return;
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
+                    const uint32_t dst = smem_u32(codes_s + s * kStageBytes);
+                    tma_load_2d(dst, &codes_map, st * kRowBytes, row0, &full[s]);
+                    tma_load_2d(dst + kBoxRows * kRowBytes, &codes_map, st * kRowBytes, row1, &full[s]);
                 }
             }
         }
+        return;
     }
 
-    if (!warp_valid) return;
+    // ---------------------------------------------------------- consumers
+    const int r = lane >> 2, c = lane & 3;
+    const uint32_t mul_a = g.mul_a, mul_b = g.mul_b;
+    const bool scales_vec = (K % kStageK) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 7) == 0);
+    const size_t sbytes = (size_t)K / 32;
+    // ldmatrix: matrix j = lane / 8 (0: rows r, group 2gp; 1: rows r + 8, group
+    // 2gp; 2, 3: the same for group 2gp + 1).  The TMA swizzle stores 16-byte
+    // chunk q of row rho at chunk q ^ (rho % 8), here q = 2gp + j/2.
+    const int mj = lane >> 3, mi = lane & 7;
+    const int lrho = MODE == 0 ? ((mj & 1) ? 128 : 0) + 8 * warp + mi : 16 * warp + (mj & 1) * 8 + mi;
+    uint32_t lm_off[4];
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int j = n * 8 + 2 * c + u;
-            const int q = qrow[j];
-            if (q < 0) continue;
-            const int p = tile * TM + j;
-            if (MODE == 0) {
-                const float gv = acc[n][u], uv = acc[n][2 + u];
-                g.h_out[(size_t)p * g.I + row0] = f32_to_bf16_bits(silu(gv) * uv);
+    for (int gp = 0; gp < 4; ++gp)
+        lm_off[gp] = smem_u32(codes_s) + lrho * kRowBytes + (((2 * gp + (mj >> 1)) ^ mi) << 4);
+    // staged activations of row r: group gl of a stage sits at chunk 4 * (gl ^ (r & 1)) + c
+    const int p = r & 1;
+    const uint32_t xb = smem_u32(xs) + (uint32_t)(r * XC + c) * 16u;
+    const uint32_t xb_even = xb + 64u * p, xb_odd = xb - 64u * p;
+
+    uint32_t gs = 0;
+    bool failed = false;
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        const int tile = item / row_blocks, block = item % row_blocks;
+        const int e = __ldg(g.tile_expert + tile);
+        named_bar_sync(1, kConsumers);  // previous item fully consumed
+        if (tid < TM) {
+            const int q = __ldg(g.sorted_pairs + tile * TM + tid);
+            qpair[tid] = q;
+            qtok[tid] = q < 0 ? -1 : (g.act_by_token ? q / g.Kt : tile * TM + tid);
+        }
+        const int rho0 = MODE == 0 ? 8 * warp + r : 16 * warp + r;
+        const int rho1 = MODE == 0 ? 128 + 8 * warp + r : 16 * warp + 8 + r;
+        const int wr0 = cta_weight_row<MODE>(rho0, block, g.I, g.rows);
+        const int wr1 = cta_weight_row<MODE>(rho1, block, g.I, g.rows);
+        const uint8_t* sp0 = g.scales + ((size_t)e * g.rows + max(wr0, 0)) * sbytes;
+        const uint8_t* sp1 = g.scales + ((size_t)e * g.rows + max(wr1, 0)) * sbytes;
+        auto load_scales = [&](int st, uint2& s0, uint2& s1) {
+            if (scales_vec) {
+                s0 = wr0 >= 0 ? __ldg(reinterpret_cast<const uint2*>(sp0 + st * 8)) : make_uint2(0, 0);
+                s1 = wr1 >= 0 ? __ldg(reinterpret_cast<const uint2*>(sp1 + st * 8)) : make_uint2(0, 0);
             } else {
-                const float wq = __ldg(g.topk_w + q);
-                float* y = g.y_out + (size_t)q * g.rows;
-                y[row0] = wq * acc[n][u];
-                y[row1] = wq * acc[n][2 + u];
+                uint32_t a[2] = {0, 0}, b[2] = {0, 0};
+                for (int gl = 0; gl < 8; ++gl) {
+                    const int gidx = st * 8 + gl;
+                    if (gidx * 32 < K) {
+                        if (wr0 >= 0) a[gl >> 2] |= (uint32_t)__ldg(sp0 + gidx) << (8 * (gl & 3));
+                        if (wr1 >= 0) b[gl >> 2] |= (uint32_t)__ldg(sp1 + gidx) << (8 * (gl & 3));
+                    }
+                }
+                s0 = make_uint2(a[0], a[1]);
+                s1 = make_uint2(b[0], b[1]);
+            }
+        };
+        uint2 nsc0, nsc1;
+        load_scales(0, nsc0, nsc1);
+        float acc[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+        named_bar_sync(1, kConsumers);  // qtok / qpair visible
+
+        for (int st = 0; st < nsteps; ++st, ++gs) {
+            const int kst = st * kStageK;
+            if (kst % KC == 0) {
+                // stage activation rows [kst, kst + KC): x 2^64, pair-interleaved, swizzled
+                if (kst > 0) named_bar_sync(1, kConsumers);
+                for (int idx = tid; idx < TM * XC; idx += kConsumers) {
+                    const int j = idx / XC, Lc = idx % XC;
+                    const int k = kst + 8 * Lc;
+                    const int t = qtok[j];
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (t >= 0 && k < K) {
+                        v = __ldg(reinterpret_cast<const uint4*>(g.act + (size_t)t * K + k));
+                        v.x = bf16x2_mul_bits(v.x, kBf16TwoPow64);
+                        v.y = bf16x2_mul_bits(v.y, kBf16TwoPow64);
+                        v.z = bf16x2_mul_bits(v.z, kBf16TwoPow64);
+                        v.w = bf16x2_mul_bits(v.w, kBf16TwoPow64);
+                        v = pair_interleave8(v);
+                    }
+                    xs[j * XC + (Lc ^ ((j & 1) << 2))] = v;
+                }
+                named_bar_sync(1, kConsumers);
+            }
+            const int s = gs % kStages;
+            const uint2 sc0 = nsc0, sc1 = nsc1;
+            if (st + 1 < nsteps) load_scales(st + 1, nsc0, nsc1);
+            if (!failed && !mbar_wait(&full[s], (gs / kStages) & 1)) failed = true;
+            if (!failed) {
+                const uint32_t soff = s * kStageBytes;
+                const uint32_t xoff = (uint32_t)(kst % KC) * 2u;  // bytes into the staged rows
+#pragma unroll
+                for (int gp = 0; gp < 4; ++gp) {
+                    uint32_t w[4];
+                    ldmatrix_x4(lm_off[gp] + soff, w);
+#pragma unroll
+                    for (int gi = 0; gi < 2; ++gi) {
+                        const int gl = 2 * gp + gi;
+                        const uint32_t b0 = __byte_perm(gl < 4 ? sc0.x : sc0.y, 0, 0x4440 + (gl & 3));
+                        const uint32_t b1 = __byte_perm(gl < 4 ? sc1.x : sc1.y, 0, 0x4440 + (gl & 3));
+                        // 2^(s - 65) as fp32 bits: (s + 62) << 23, by multiply-add
+                        const float f0 = __uint_as_float(b0 * g.exp_one + g.exp_bias);
+                        const float f1 = __uint_as_float(b1 * g.exp_one + g.exp_bias);
+                        uint32_t ta[4], tb[4];
+                        codes_to_bf16x2(w[gi ? 2 : 0], mul_a, mul_b, ta);
+                        codes_to_bf16x2(w[gi ? 3 : 1], mul_a, mul_b, tb);
+                        const uint32_t xa = ((gl & 1) ? xb_odd : xb_even) + xoff + 64u * gl;
+#pragma unroll
+                        for (int n = 0; n < NT; ++n) {
+                            uint4 b;
+                            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                         : "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                                         : "r"(xa + (uint32_t)(n * 8 * XC * 16)));
+                            float t4[4];
+                            mma_bf16_16816_z(t4, ta[0], tb[0], ta[1], tb[1], b.x, b.y);
+                            mma_bf16_16816_acc(t4, ta[2], tb[2], ta[3], tb[3], b.z, b.w);
+                            acc[n][0] = fmaf(t4[0], f0, acc[n][0]);
+                            acc[n][1] = fmaf(t4[1], f0, acc[n][1]);
+                            acc[n][2] = fmaf(t4[2], f1, acc[n][2]);
+                            acc[n][3] = fmaf(t4[3], f1, acc[n][3]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+
+        if (!failed) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int j = n * 8 + 2 * c + u;
+                    const int q = qpair[j];
+                    if (q < 0) continue;
+                    if (MODE == 0) {
+                        if (wr0 >= 0)
+                            g.h_out[(size_t)(tile * TM + j) * g.I + wr0] =
+                                f32_to_bf16_bits(silu(acc[n][u]) * acc[n][2 + u]);
+                    } else {
+                        const float wq = __ldg(g.topk_w + q);
+                        float* y = g.y_out + (size_t)q * g.rows;
+                        if (wr0 >= 0) y[wr0] = wq * acc[n][u];
+                        if (wr1 >= 0) y[wr1] = wq * acc[n][2 + u];
+                    }
+                }
             }
         }
     }
 }
 
 template <int MODE, int NT>
-cudaError_t launch_nt(const GroupedGemm& g, cudaStream_t s) {
-    const size_t smem = (size_t)NT * 8 * kChunks16 * sizeof(uint4) + NT * 8 * sizeof(int32_t);
+cudaError_t launch_nt(const GroupedGemm& g, const CUtensorMap& map, cudaStream_t s) {
+    const size_t smem = DecodeSmem<NT>::kTotal;
     cudaError_t err = ensure_dynamic_smem((const void*)decode_gemm_kernel<MODE, NT>, smem);
     if (err != cudaSuccess) return err;
-    const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
-    dim3 grid(g.max_tiles, row_blocks);
-    decode_gemm_kernel<MODE, NT><<<grid, kThreads, smem, s>>>(g);
+    const int row_blocks = MODE == 0 ? (g.I + 127) / 128 : (g.rows + kRows - 1) / kRows;
+    const long long max_items = (long long)g.max_tiles * row_blocks;
+    const int grid = (int)std::min<long long>(max_items, (long long)num_sms());
+    decode_gemm_kernel<MODE, NT><<<grid, kThreads, smem, s>>>(g, map);
     return cudaGetLastError();
 }
 
 template <int MODE>
 cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
     if (g.max_tiles == 0) return cudaSuccess;
+    // the packed codes of all experts as one 2D uint8 tensor [Et * rows, K / 2]
+    CUtensorMap map;
+    cudaError_t err = encode_codes_map(&map, g.codes, g.K / 2, (uint64_t)g.num_experts * g.rows,
+                                       kRowBytes, kBoxRows);
+    if (err != cudaSuccess) return err;
     switch (g.tile_m) {
-        case 8: return launch_nt<MODE, 1>(g, s);
-        case 16: return launch_nt<MODE, 2>(g, s);
-        case 32: return launch_nt<MODE, 4>(g, s);
-        case 64: return launch_nt<MODE, 8>(g, s);
+        case 8: return launch_nt<MODE, 1>(g, map, s);
+        case 16: return launch_nt<MODE, 2>(g, map, s);
+        case 32: return launch_nt<MODE, 4>(g, map, s);
+        case 64: return launch_nt<MODE, 8>(g, map, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -225,6 +360,13 @@ bool decode_tile_supported(int tile_m) {
 
 cudaError_t launch_decode_gate_up(const GroupedGemm& g, cudaStream_t s) { return launch_mode<0>(g, s); }
 cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s) { return launch_mode<1>(g, s); }
+
+cudaError_t read_device_error_decode(int* flag, int clear) {
+    cudaError_t err = cudaMemcpyFromSymbol(flag, g_device_error, sizeof(int));
+    if (err != cudaSuccess || !clear) return err;
+    const int zero = 0;
+    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+}
 
 cudaError_t launch_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t s) {
     const size_t n = (size_t)T * (H / 4);

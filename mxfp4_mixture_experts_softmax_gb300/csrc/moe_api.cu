@@ -36,6 +36,63 @@ cudaError_t ensure_dynamic_smem(const void* func, size_t bytes) {
     return cudaSuccess;
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+cudaError_t encode_2d_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int inner,
+                          uint64_t rows, uint64_t row_stride, int box_inner, int box_rows,
+                          CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_stride};
+    const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_codes_map(CUtensorMap* map, const void* base, int row_bytes, uint64_t rows,
+                             int box_bytes, int box_rows) {
+    return encode_2d_map(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, rows,
+                         (uint64_t)row_bytes, box_bytes, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int num_sms() {
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
 static bool trace_enabled() {
     static int v = -1;
     if (v < 0) {
@@ -78,7 +135,11 @@ int moe_version(void) { return 100; }
 
 moe_status_t moe_device_error(int* flag, int clear) {
     if (!flag) return MOE_ERR_INVALID_ARG;
-    return cuda_status(read_device_error(flag, clear));
+    int a = 0, b = 0;
+    cudaError_t err = read_device_error_prefill(&a, clear);
+    if (err == cudaSuccess) err = read_device_error_decode(&b, clear);
+    *flag = (a || b) ? 1 : 0;
+    return cuda_status(err);
 }
 
 moe_status_t moe_route(const float* logits, int T, int E, int K, int with_shared, int renormalize,
@@ -167,8 +228,10 @@ static bool ptrs_ok(std::initializer_list<const void*> ptrs, size_t align) {
 }
 
 static GroupedGemm base_gemm(const int32_t* sorted_pairs, const int32_t* tile_expert,
-                             const int32_t* num_tiles, int I, int Kt, int tile_m, int max_tiles) {
+                             const int32_t* num_tiles, int I, int Et, int Kt, int tile_m,
+                             int max_tiles) {
     GroupedGemm g{};
+    g.num_experts = Et;
     g.sorted_pairs = sorted_pairs;
     g.tile_expert = tile_expert;
     g.num_tiles = num_tiles;
@@ -201,12 +264,13 @@ moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_
         return MOE_ERR_INVALID_ARG;
     const int max_tiles = (int)(capacity64(T, Kt, Et, tile_m) / tile_m);
     trace("moe_ffn_gate_up", T, H, I, Et, Kt, tile_m, path);
-    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, I, Kt, tile_m, max_tiles);
+    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, I, Et, Kt, tile_m, max_tiles);
     g.codes = w13;
     g.scales = s13;
     g.rows = 2 * I;
     g.K = H;
     g.act = x;
+    g.act_rows = T;
     g.act_by_token = 1;
     g.h_out = h;
     cudaError_t err = path == MOE_PATH_DECODE ? launch_decode_gate_up(g, stream)
@@ -225,12 +289,13 @@ moe_status_t moe_ffn_down(const uint16_t* h, const uint8_t* w2, const uint8_t* s
         return MOE_ERR_INVALID_ARG;
     const int max_tiles = (int)(capacity64(T, Kt, Et, tile_m) / tile_m);
     trace("moe_ffn_down", T, H, I, Et, Kt, tile_m, path);
-    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, I, Kt, tile_m, max_tiles);
+    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, I, Et, Kt, tile_m, max_tiles);
     g.codes = w2;
     g.scales = s2;
     g.rows = H;
     g.K = I;
     g.act = h;
+    g.act_rows = (int)capacity64(T, Kt, Et, tile_m);
     g.act_by_token = 0;
     g.y_out = y;
     g.topk_w = topk_w;

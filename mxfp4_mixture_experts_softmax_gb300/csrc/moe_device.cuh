@@ -118,4 +118,136 @@ __device__ __forceinline__ uint4 pair_interleave8(uint4 v) {
     return r;
 }
 
+// ------------------------------------------------ async copies, mbarriers
+
+// Device error flag of this translation unit: set by a kernel whose bounded
+// wait gave up (each kernel file has its own; moe_device_error() reads all).
+static __device__ int g_device_error = 0;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// One bounded try: the thread may sleep up to ~0.5 ms inside the instruction
+// until the phase completes, instead of spinning on the issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(500000u)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Bounded wait for the phase with the given parity.  Gives up (returns
+// false) after kWaitLimitNs, or as soon as another CTA of the same kernel
+// file has raised the device error flag, so one failure cannot stall a grid.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*(volatile int*)&g_device_error) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicExch(&g_device_error, 1);
+            return false;
+        }
+    }
+}
+
+// 2D tiled TMA load of one box into shared memory, completing on the mbarrier.
+// c0 is the inner coordinate (bytes for a uint8 map; a multiple of 16).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+            smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+// Bulk (TMA engine) copy global -> shared, completing `bytes` on the mbarrier.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t r[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// Named barrier among `count` threads (a subset of the CTA).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// D = A * B with a zero accumulator (m16n8k16, bf16 in, fp32 out).
+__device__ __forceinline__ void mma_bf16_16816_z(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                 uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// D += A * B (m16n8k16, bf16 in, fp32 accumulate).
+__device__ __forceinline__ void mma_bf16_16816_acc(float d[4], uint32_t a0, uint32_t a1,
+                                                   uint32_t a2, uint32_t a3, uint32_t b0,
+                                                   uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Eight E2M1 codes -> four bf16x2 of value E2M1 * 2^-126 (exact; the e = 0
+// codes are bf16 subnormals), paired as in mxfp4_word_to_bf16x2 but without
+// the scale multiply: the caller applies 2^126 * 2^(s-127) to the fp32
+// partial sums instead.
+__device__ __forceinline__ void mxfp4_word_to_bf16x2_raw(uint32_t w, uint32_t out[4]) {
+    const uint32_t hi = w >> 8;
+    out[0] = ((w & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
+    out[1] = ((w & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
+    out[2] = ((hi & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
+    out[3] = ((hi & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
+}
+
 }  // namespace moe

@@ -1,6 +1,7 @@
 // moe_internal.h -- launchers shared between the libmoe translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -12,6 +13,17 @@ namespace moe {
 // Raises a kernel's dynamic shared memory limit once per device (idempotent;
 // the attribute is per function, so it stays set for later calls).
 cudaError_t ensure_dynamic_smem(const void* func, size_t bytes);
+
+// 2D TMA descriptor of a packed uint8 matrix [rows, row_bytes] (row-major),
+// box [box_rows, box_bytes], 128-byte swizzle, zero fill out of bounds.
+cudaError_t encode_codes_map(CUtensorMap* map, const void* base, int row_bytes, uint64_t rows,
+                             int box_bytes, int box_rows);
+
+// General 2D TMA descriptor: `inner` elements per row, `rows` rows,
+// `row_stride` bytes between rows, box [box_rows, box_inner] elements.
+cudaError_t encode_2d_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int inner,
+                          uint64_t rows, uint64_t row_stride, int box_inner, int box_rows,
+                          CUtensorMapSwizzle swizzle);
 
 cudaError_t launch_route(const float* logits, int T, int E, int K, int with_shared,
                          int renormalize, int32_t* ids, float* w, cudaStream_t s);
@@ -34,13 +46,21 @@ struct GroupedGemm {
     const int32_t* tile_expert;
     const int32_t* num_tiles;
     int Kt;
+    int num_experts;             // Et (experts stacked in codes / scales)
+    int act_rows;                // rows of `act` (T for x, cap for h)
     int tile_m;
     int max_tiles;
     int I;                       // SwiGLU: gate rows [0, I), up rows [I, 2I)
     uint16_t* h_out;             // SwiGLU output h [cap][I] (bf16)
     float* y_out;                // weighted output [T*Kt][H] (fp32)
     const float* topk_w;
+    // constants the decode kernels take as runtime values (see codes_to_bf16x2)
+    uint32_t mul_a = 0x1040u, mul_b = 0x0104u;  // 2^6 + 2^12, 2^2 + 2^8
+    uint32_t exp_one = 1u << 23, exp_bias = 62u << 23;
 };
+
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms();
 
 bool decode_tile_supported(int tile_m);
 bool prefill_tile_supported(int tile_m);
@@ -50,7 +70,8 @@ cudaError_t launch_decode_gate_up(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_prefill_gate_up(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_prefill_down(const GroupedGemm& g, cudaStream_t s);
-cudaError_t read_device_error(int* flag, int clear);
+cudaError_t read_device_error_prefill(int* flag, int clear);
+cudaError_t read_device_error_decode(int* flag, int clear);
 cudaError_t launch_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t s);
 
 }  // namespace moe
