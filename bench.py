@@ -280,10 +280,10 @@ def run_ours(args, ws, rank, local):
         perm = libmoe.moe_permute(ids, w.Et, tm, bufs["perm"])
         if ev is not None:
             ev[2].record(stream)
-        libmoe.moe_ffn_gate_up(xs[r], W["w13"], W["s13"], perm, h_buf, path)
+        libmoe.moe_ffn_gate_up(xs[r], W["w13"], W["s13"], perm, bufs["workspace"], path)
         if ev is not None:
             ev[3].record(stream)
-        libmoe.moe_ffn_down(h_buf, W["w2"], W["s2"], tw, perm, y_buf, w.T, path)
+        libmoe.moe_ffn_down(W["w2"], W["s2"], tw, perm, bufs["workspace"], w.T, path)
         if ev is not None:
             ev[4].record(stream)
         libmoe.moe_combine(y_buf, w.T, w.H, w.Kt, bufs["out"])

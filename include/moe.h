@@ -129,8 +129,9 @@ moe_status_t moe_permute(const int32_t* topk_ids, int T, int Kt, int Et, int til
 
 /*
  * moe_ffn_workspace_size -- bytes of device workspace moe_ffn needs:
- * the bf16 SwiGLU intermediate [cap, I] and the weighted fp32 per-pair
- * expert outputs [T*Kt, H], each 256-byte aligned.
+ * the bf16 SwiGLU intermediate [cap, I], the weighted fp32 per-pair expert
+ * outputs [T*Kt, H] and, when tile_m is a prefill tile height (32, 64, 128,
+ * 256), the tile-ordered bf16 activations [cap, H]; each 256-byte aligned.
  */
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
 
@@ -177,26 +178,30 @@ moe_status_t moe_ffn_path(const uint16_t* x, const uint8_t* w13, const uint8_t* 
                           moe_path_t path, cudaStream_t stream);
 
 /*
- * The three steps of moe_ffn as separate calls (moe_ffn runs exactly these,
- * in this order, on its workspace: h at byte 0, y at
- * moe_ffn_y_offset(T, I, Et, Kt, tile_m)).  `path` must resolve to the same
- * path for both GEMM calls (AUTO always does for the same sizes).
+ * The three steps of moe_ffn as separate calls; moe_ffn runs exactly these,
+ * in this order, on one workspace (at least moe_ffn_workspace_size() bytes):
+ *   h  bf16 [cap, I] at byte 0, y fp32 [T*Kt, H] at moe_ffn_y_offset(), and,
+ *   for tile heights the prefill path supports (32, 64, 128, 256), the
+ *   tile-ordered copy of the activations the prefill gate_up reads, after y.
+ * `path` must resolve to the same path for both GEMM calls (AUTO always does
+ * for the same sizes).
  *
  * moe_ffn_gate_up: h[p, n] = bf16(silu(g) * u) for every sorted position p
- *   that holds a pair (pads are not written); h is bf16 [cap, I].
+ *   that holds a pair (pads are not written).
  * moe_ffn_down:    y[q, m] = topk_w[q] * (W2[e] h_p)[m] for every pair q at
- *   position p; y is fp32 [T*Kt, H] (the routing-weighted expert outputs).
+ *   position p (the routing-weighted expert outputs).
  * moe_combine:     out[t, m] = bf16(sum over j = 0..Kt-1, ascending, of
  *   y[t*Kt + j, m]); out is bf16 [T, H].
  */
 moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
                              const int32_t* sorted_pairs, const int32_t* tile_expert,
                              const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
-                             int tile_m, uint16_t* h, moe_path_t path, cudaStream_t stream);
-moe_status_t moe_ffn_down(const uint16_t* h, const uint8_t* w2, const uint8_t* s2,
-                          const float* topk_w, const int32_t* sorted_pairs,
-                          const int32_t* tile_expert, const int32_t* num_tiles, int T, int H,
-                          int I, int Et, int Kt, int tile_m, float* y, moe_path_t path,
+                             int tile_m, void* workspace, size_t ws_bytes, moe_path_t path,
+                             cudaStream_t stream);
+moe_status_t moe_ffn_down(const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                          const int32_t* sorted_pairs, const int32_t* tile_expert,
+                          const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                          int tile_m, void* workspace, size_t ws_bytes, moe_path_t path,
                           cudaStream_t stream);
 moe_status_t moe_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t stream);
 

@@ -6,82 +6,53 @@
 // on MI355X, section "local shape and tiling"; padded and tuned prefill GEMM:
 // VibeSys Qwen3.5-397B on 4x MI300A, section "baseline").
 //
-// One CTA computes a 128-row block of one expert's weight matrix against one
-// tile of tile_m token rows (swap-AB: weights are the MMA's M = 128 side, the
-// tile's tokens its N = tile_m side), accumulating D[128, N] in fp32 in tensor
-// memory over the whole reduction:
-//   * per 64-wide K stage every thread dequantises one weight row (64 E2M1
-//     codes, exact to bf16) into the stage's A buffer and the tile's token rows
-//     are copied into the B buffer with cp.async (zero-filled for padding);
-//     both buffers use the 128-byte swizzled K-major layout the MMA reads;
-//   * one thread issues the four K = 16 MMAs of the stage and commits them to
-//     the stage's mbarrier, which frees the buffers for reuse kStages later;
-//   * the epilogue reads the accumulator from tensor memory (each warp its 32
-//     lanes) and applies SwiGLU (gate_up, gate and up rows interleaved so the
-//     partner value is one lane away) or the routing weight (down).
-// Every wait is bounded by the global timer; on timeout the kernel raises the
-// library's device error flag, drains its own MMAs (bounded), frees its tensor
-// memory and returns.
+// Work item = one tile of N = tile_m token rows of one expert x one block of
+// 128 weight rows (swap-AB: weights are the MMA's M = 128 side, tokens its N
+// side).  Persistent CTAs (one per SM) loop over the items; warp roles:
+//   * producer warp: 2D TMA loads of the block's packed codes (64 k per
+//     stage, prefetched into L2 ahead of the ring) and of the tile's token
+//     rows as one box in the 128-byte swizzled K-major layout the MMA reads
+//     (gate_up reads x gathered into tile order by gather_rows_kernel, down
+//     reads h, which is already in tile order);
+//   * 8 converter warps: exact bf16 dequantisation of the codes (E2M1 bit
+//     placement times 2^126 * 2^(s-127) by one bf16x2 multiply) into the
+//     stage's A buffer, same swizzled layout;
+//   * MMA warp: one thread issues the four K = 16 tcgen05.mma of each stage
+//     into the item's tensor-memory accumulator and commits them to the
+//     stage's mbarrier, which frees the stage;
+//   * 4 epilogue warps: read the finished accumulator (each warp its 32
+//     lanes), apply SwiGLU (gate and up rows interleaved, partner one lane
+//     away) or the routing weight, and store; the accumulator is double
+//     buffered so this overlaps the next item's MMAs.
+// Every wait is bounded (see mbar_wait); after a timeout each role stops, the
+// MMA thread drains its own MMAs (bounded), and tensor memory is freed.
+#include <algorithm>
+
 #include "moe_internal.h"
 
 namespace moe {
 
-__device__ int g_device_error = 0;
-
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kBK = 64;                       // K elements per stage (one 128-B row)
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kConvWarp0 = 2;
+constexpr int kConvWarps = 8;
+constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;  // 10..13: warp % 4 covers every lane quadrant
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 448
+constexpr int kBK = 64;                                   // k per stage (one 128-byte bf16 row)
 constexpr int kStages = 4;
-constexpr int kABytes = 128 * kBK * 2;        // 16 KB per A stage
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase with the given parity; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
+constexpr int kABytes = 128 * kBK * 2;                    // 16 KB bf16 A stage
+constexpr int kCodeBytes = 128 * (kBK / 2);               // 4 KB packed codes stage
+constexpr int kCodeBox = 64;                              // rows per codes box
+constexpr int kPrefetch = 12;                             // code stages prefetched into L2 ahead
 
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
 }
 
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte
@@ -132,39 +103,53 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t r[16]) {
 template <int N>
 struct PrefillSmem {
     static constexpr int kBBytes = N * kBK * 2;
-    static constexpr int kBars = 1024 * 0 + kStages * (kABytes + kBBytes);  // offset of barriers
-    static constexpr int kTotal = kBars + 256 + N * 4 + 1024;              // + alignment slack
+    static constexpr int kStage = kABytes + kBBytes + kCodeBytes;  // multiple of 1024
+    static constexpr int kBars = kStages * kStage;
+    static constexpr int kTotal = kBars + 256 + 1024;              // + alignment slack
 };
 
 template <int MODE, int N>
-__global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GroupedGemm g) {
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_gemm_kernel(const GroupedGemm g, const __grid_constant__ CUtensorMap codes_map,
+                        const __grid_constant__ CUtensorMap act_map) {
+    using L = PrefillSmem<N>;
     extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + kStages * kABytes;
-    constexpr int kBBytes = PrefillSmem<N>::kBBytes;
-    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + PrefillSmem<N>::kBars);
-    uint64_t* done = empty + kStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-    int32_t* qrow = reinterpret_cast<int32_t*>(tmem_slot + 4);
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L::kBars);  // codes + B landed
+    uint64_t* a_full = raw_full + kStages;                               // A converted
+    uint64_t* stage_free = a_full + kStages;                             // MMAs done with stage
+    uint64_t* acc_full = stage_free + kStages;                           // [2] accumulator ready
+    uint64_t* acc_free = acc_full + 2;                                   // [2] accumulator drained
+    uint64_t* drain = acc_free + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    auto stage_a = [&](int s) { return smem + s * L::kStage; };
+    auto stage_b = [&](int s) { return smem + s * L::kStage + kABytes; };
+    auto stage_c = [&](int s) { return smem + s * L::kStage + kABytes + L::kBBytes; };
 
-    const int tile = blockIdx.x;
-    if (tile >= __ldg(g.num_tiles)) return;  // uniform, before any barrier or tensor memory
-    const int e = __ldg(g.tile_expert + tile);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = g.K;
+    const int nk = (K + kBK - 1) / kBK;
+    const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
+    const int items = __ldg(g.num_tiles) * row_blocks;
+    constexpr uint32_t kTmemCols = 2 * N;
 
-    for (int j = tid; j < N; j += kThreads) qrow[j] = __ldg(g.sorted_pairs + tile * N + j);
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&empty[s], 1);
-        mbar_init(done, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&a_full[s], kConvWarps);
+            mbar_init(&stage_free[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_free[b], kEpiWarps);
+        }
+        mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
-                     "r"((uint32_t)N)
+                     "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -173,131 +158,208 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Grouped
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // this thread's weight row of the 128-row block
-    int arow;
-    bool rvalid;
-    if (MODE == 0) {
-        const int n = blockIdx.y * 64 + (tid >> 1);
-        rvalid = n < g.I;
-        arow = (tid & 1) ? g.I + n : n;
-    } else {
-        arow = blockIdx.y * 128 + tid;
-        rvalid = arow < g.rows;
-    }
-    if (!rvalid) arow = 0;
-    const uint8_t* cp = g.codes + ((size_t)e * g.rows + arow) * (size_t)(K / 2);
-    const uint8_t* sp = g.scales + ((size_t)e * g.rows + arow) * (size_t)(K / 32);
-
-    const int nk = (K + kBK - 1) / kBK;
-    uint4 nc[2];
-    uint32_t ns[2];
-    auto load_chunk = [&](int kc) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int kb = kc * kBK + 32 * h;
-            const bool ok = rvalid && kb < K;
-            nc[h] = ok ? __ldg(reinterpret_cast<const uint4*>(cp + kb / 2)) : make_uint4(0, 0, 0, 0);
-            ns[h] = ok ? (uint32_t)__ldg(sp + kb / 32) : 127u;
-        }
-    };
-    load_chunk(0);
-
-    constexpr uint32_t idesc = idesc_bf16(128, N);
-    bool failed = false;
-    for (int kc = 0; kc < nk; ++kc) {
-        const int s = kc % kStages;
-        if (kc >= kStages && !mbar_wait(&empty[s], (uint32_t)((kc / kStages - 1) & 1))) failed = true;
-        if (__syncthreads_or(failed)) {
-            failed = true;
-            break;
-        }
-        // B: the tile's token rows, 8 x 16 bytes per row, swizzled
-        uint8_t* b_st = sB + s * kBBytes;
-        for (int i = tid; i < N * 8; i += kThreads) {
-            const int j = i >> 3, ch = i & 7;
-            const int k = kc * kBK + ch * 8;
-            const int q = qrow[j];
-            const uint16_t* src = g.act;
-            uint32_t bytes = 0;
-            if (q >= 0 && k < K) {
-                const size_t brow = g.act_by_token ? (size_t)(q / g.Kt) : (size_t)(tile * N + j);
-                src = g.act + brow * K + k;
-                bytes = 16;
-            }
-            cp_async_16(smem_u32(b_st + j * 128 + ((ch ^ (j & 7)) << 4)), src, bytes);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        // A: dequantise this thread's row (64 codes) into natural k order
-        const uint4 cc[2] = {nc[0], nc[1]};
-        const uint32_t cs[2] = {ns[0], ns[1]};
-        if (kc + 1 < nk) load_chunk(kc + 1);
-        uint8_t* a_row = sA + s * kABytes + tid * 128;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t mlo = e8m0_mult_lo(cs[h]);
-            const bool big = cs[h] > 128u;
-            const uint32_t w4[4] = {cc[h].x, cc[h].y, cc[h].z, cc[h].w};
-#pragma unroll
-            for (int i4 = 0; i4 < 4; ++i4) {
-                uint32_t d[4];
-                mxfp4_word_to_bf16x2(w4[i4], mlo, d);
-                if (big) bf16x2_scale(d, e8m0_mult_hi(cs[h]));
-                uint4 v;
-                v.x = __byte_perm(d[0], d[1], 0x5410);  // (k0, k1)
-                v.y = __byte_perm(d[2], d[3], 0x5410);  // (k2, k3)
-                v.z = __byte_perm(d[0], d[1], 0x7632);  // (k4, k5)
-                v.w = __byte_perm(d[2], d[3], 0x7632);  // (k6, k7)
-                const int ch = 4 * h + i4;
-                *reinterpret_cast<uint4*>(a_row + ((ch ^ (tid & 7)) << 4)) = v;
-            }
-        }
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint64_t ad = sdesc_sw128(smem_u32(sA + s * kABytes));
-            const uint64_t bd = sdesc_sw128(smem_u32(b_st));
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)  // +32 bytes per K = 16 step inside the atom
-                mma_bf16_ss(tmem, ad + 2u * k, bd + 2u * k, idesc, (kc | k) != 0 ? 1u : 0u);
-            mma_commit(&empty[s]);
-        }
-    }
-    if (tid == 0) mma_commit(done);  // tracks every MMA this thread issued
-    const bool drained = mbar_wait(done, 0);
-    tc_fence_after();
-    if (!failed && drained) {
-#pragma unroll 1
-        for (int c0 = 0; c0 < N; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
-            const int r = 32 * warp + lane;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int j = c0 + i;
-                const float acc = __uint_as_float(v[i]);
-                if (MODE == 0) {
-                    const float partner = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-                    const int n = blockIdx.y * 64 + (r >> 1);
-                    const int q = qrow[j];
-                    if (!(lane & 1) && n < g.I && q >= 0)
-                        g.h_out[(size_t)(tile * N + j) * g.I + n] = f32_to_bf16_bits(silu(acc) * partner);
-                } else {
-                    const int m = blockIdx.y * 128 + r;
-                    const int q = qrow[j];
-                    if (m < g.rows && q >= 0) g.y_out[(size_t)q * g.rows + m] = __ldg(g.topk_w + q) * acc;
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------- producer
+        uint32_t gs = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+            const int tile = item / row_blocks, block = item % row_blocks;
+            const int e = __ldg(g.tile_expert + tile);
+            const int crow0 = e * g.rows + (MODE == 0 ? block * 64 : block * 128);
+            const int crow1 = MODE == 0 ? e * g.rows + g.I + block * 64 : crow0 + kCodeBox;
+            if (lane == 0)  // the item's first codes into L2 before the ring asks for them
+                for (int st = 0; st < kPrefetch && st < nk; ++st) {
+                    tma_prefetch_l2_2d(&codes_map, st * (kBK / 2), crow0);
+                    tma_prefetch_l2_2d(&codes_map, st * (kBK / 2), crow1);
+                }
+            for (int st = 0; st < nk; ++st, ++gs) {
+                const int s = gs % kStages;
+                if (lane == 0 && st + kPrefetch < nk) {
+                    tma_prefetch_l2_2d(&codes_map, (st + kPrefetch) * (kBK / 2), crow0);
+                    tma_prefetch_l2_2d(&codes_map, (st + kPrefetch) * (kBK / 2), crow1);
+                }
+                if (gs >= kStages && !mbar_wait(&stage_free[s], ((gs / kStages) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&raw_full[s], (uint32_t)(kCodeBytes + L::kBBytes));
+                    const uint32_t cdst = smem_u32(stage_c(s));
+                    tma_load_2d(cdst, &codes_map, st * (kBK / 2), crow0, &raw_full[s]);
+                    tma_load_2d(cdst + kCodeBox * (kBK / 2), &codes_map, st * (kBK / 2), crow1,
+                                &raw_full[s]);
+                    tma_load_2d(smem_u32(stage_b(s)), &act_map, st * kBK, tile * N, &raw_full[s]);
                 }
             }
         }
+        // wait (bounded) until the last loads landed before the CTA can exit
+        if (lane == 0)
+            for (int d = 0; d < kStages && d < (int)gs; ++d) {
+                const uint32_t u = gs - 1 - d;
+                if (!mbar_wait(&raw_full[u % kStages], (u / kStages) & 1)) break;
+            }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(128, N);
+            uint32_t gs = 0, it = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++it) {
+                const uint32_t b = it & 1;
+                if (it >= 2 && !mbar_wait(&acc_free[b], ((it >> 1) - 1) & 1)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + b * N;
+                for (int st = 0; st < nk; ++st, ++gs) {
+                    const int s = gs % kStages;
+                    // A converted (converters) and B landed (TMA, observed directly)
+                    if (!mbar_wait(&a_full[s], (gs / kStages) & 1) ||
+                        !mbar_wait(&raw_full[s], (gs / kStages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_sw128(smem_u32(stage_a(s)));
+                    const uint64_t bd = sdesc_sw128(smem_u32(stage_b(s)));
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k)  // +32 bytes per K = 16 inside the swizzle atom
+                        mma_bf16_ss(d_tmem, ad + 2u * k, bd + 2u * k, idesc, (st | k) != 0 ? 1u : 0u);
+                    mma_commit(&stage_free[s]);
+                }
+                if (ok) mma_commit(&acc_full[b]);
+            }
+            mma_commit(drain);  // every MMA this thread issued has completed when this arrives
+            mbar_wait(drain, 0);
+        }
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------------ converters
+        const int t = tid - kConvWarp0 * 32;  // 0..255
+        const int rho = t >> 1, h = t & 1;    // A row, 32-k half of the stage
+        const int crow = MODE == 0 ? ((rho & 1) ? kCodeBox + (rho >> 1) : rho >> 1) : rho;
+        const bool svec = (K % 512) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 15) == 0);
+        uint32_t gs = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+            const int tile = item / row_blocks, block = item % row_blocks;
+            const int e = __ldg(g.tile_expert + tile);
+            int wrow;
+            bool rvalid;
+            if (MODE == 0) {
+                const int n = block * 64 + (rho >> 1);
+                rvalid = n < g.I;
+                wrow = (rho & 1) ? g.I + n : n;
+            } else {
+                wrow = block * 128 + rho;
+                rvalid = wrow < g.rows;
+            }
+            const uint8_t* sp = g.scales + ((size_t)e * g.rows + (rvalid ? wrow : 0)) * (size_t)(K / 32);
+            // scale bytes arrive 16 at a time (8 stages x 2 groups), one block
+            // ahead, so their load latency never sits on a stage
+            auto load_sblock = [&](int blk) {
+                const int g0 = blk * 16;
+                if (!rvalid || g0 * 32 >= K) return make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+                if (svec) return __ldg(reinterpret_cast<const uint4*>(sp + g0));
+                uint32_t b[4] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu};
+                for (int i = 0; i < 16 && (g0 + i) * 32 < K; ++i)
+                    b[i >> 2] = (b[i >> 2] & ~(0xFFu << (8 * (i & 3)))) | ((uint32_t)__ldg(sp + g0 + i) << (8 * (i & 3)));
+                return make_uint4(b[0], b[1], b[2], b[3]);
+            };
+            uint4 sblk = load_sblock(0), nblk = load_sblock(1);
+            for (int st = 0; st < nk; ++st, ++gs) {
+                const int s = gs % kStages;
+                if (st > 0 && (st & 7) == 0) {
+                    sblk = nblk;
+                    nblk = load_sblock((st >> 3) + 1);
+                }
+                const int gi = 2 * (st & 7) + h;  // group within the 16-group block
+                const uint32_t word = (gi < 8) ? ((gi < 4) ? sblk.x : sblk.y) : ((gi < 12) ? sblk.z : sblk.w);
+                const uint32_t sc = (word >> (8 * (gi & 3))) & 0xFFu;
+                if (!mbar_wait(&raw_full[s], (gs / kStages) & 1)) {
+                    ok = false;
+                    break;
+                }
+                uint4 cw;
+                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
+                             : "r"(smem_u32(stage_c(s)) + crow * (kBK / 2) + 16 * h));
+                const uint32_t mlo = e8m0_mult_lo(sc);
+                const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+                const uint32_t arow = smem_u32(stage_a(s)) + rho * 128;
+#pragma unroll
+                for (int i4 = 0; i4 < 4; ++i4) {
+                    uint32_t d[4];
+                    mxfp4_word_to_bf16x2(w4[i4], mlo, d);
+                    if (sc > 128u) bf16x2_scale(d, e8m0_mult_hi(sc));
+                    uint4 v;
+                    v.x = __byte_perm(d[0], d[1], 0x5410);  // (k0, k1)
+                    v.y = __byte_perm(d[2], d[3], 0x5410);  // (k2, k3)
+                    v.z = __byte_perm(d[0], d[1], 0x7632);  // (k4, k5)
+                    v.w = __byte_perm(d[2], d[3], 0x7632);  // (k6, k7)
+                    const int ch = 4 * h + i4;
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                                     arow + ((ch ^ (rho & 7)) << 4)),
+                                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                 : "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[s]);
+            }
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int quad = warp & 3;  // tensor-memory lanes 32*quad .. 32*quad + 31
+        const int r = 32 * quad + lane;
+        uint32_t it = 0;
+        for (int item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+            const int tile = item / row_blocks, block = item % row_blocks;
+            const uint32_t b = it & 1;
+            // the tile's pair indices (and routing weights) once per item:
+            // column j lives in lane j % 32 of register j / 32
+            constexpr int kQ = N / 32;
+            int qv[kQ];
+            float wv[kQ];
+#pragma unroll
+            for (int u = 0; u < kQ; ++u) {
+                qv[u] = __ldg(g.sorted_pairs + tile * N + 32 * u + lane);
+                wv[u] = (MODE == 1 && qv[u] >= 0) ? __ldg(g.topk_w + qv[u]) : 0.0f;
+            }
+            if (!mbar_wait(&acc_full[b], (it >> 1) & 1)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * quad) << 16) + b * N + (uint32_t)c0, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int j = c0 + i;
+                    const float acc = __uint_as_float(v[i]);
+                    const int q = __shfl_sync(0xFFFFFFFFu, qv[j / 32], j % 32);
+                    if (MODE == 0) {
+                        const float partner = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
+                        const int n = block * 64 + (r >> 1);
+                        if (!(lane & 1) && n < g.I && q >= 0)
+                            g.h_out[(size_t)(tile * N + j) * g.I + n] = f32_to_bf16_bits(silu(acc) * partner);
+                    } else {
+                        const float wq = __shfl_sync(0xFFFFFFFFu, wv[j / 32], j % 32);
+                        const int m = block * 128 + r;
+                        if (m < g.rows && q >= 0) g.y_out[(size_t)q * g.rows + m] = wq * acc;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_free[b]);
+        }
     }
-    if ((failed || !drained) && tid == 0) atomicExch(&g_device_error, 1);
+
     tc_fence_before();
     __syncthreads();
-    if (warp == 0)
+    if (warp == kMmaWarp) {
+        tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"((uint32_t)N)
+                     "r"(kTmemCols)
                      : "memory");
+    }
 }
 
 template <int MODE, int N>
@@ -305,9 +367,19 @@ cudaError_t launch_n(const GroupedGemm& g, cudaStream_t s) {
     const size_t smem = PrefillSmem<N>::kTotal;
     cudaError_t err = ensure_dynamic_smem((const void*)prefill_gemm_kernel<MODE, N>, smem);
     if (err != cudaSuccess) return err;
+    CUtensorMap codes_map, act_map;
+    err = encode_2d_map(&codes_map, g.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K / 2,
+                        (uint64_t)g.num_experts * g.rows, g.K / 2, kBK / 2, kCodeBox,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (err != cudaSuccess) return err;
+    // activations in tile order (gathered x for gate_up, h for down): N rows per box
+    err = encode_2d_map(&act_map, g.act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.K, (uint64_t)g.act_rows,
+                        (uint64_t)g.K * 2, kBK, N, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
     const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
-    dim3 grid(g.max_tiles, row_blocks);
-    prefill_gemm_kernel<MODE, N><<<grid, kThreads, smem, s>>>(g);
+    const long long max_items = (long long)g.max_tiles * row_blocks;
+    const int grid = (int)std::min<long long>(max_items, (long long)num_sms());
+    prefill_gemm_kernel<MODE, N><<<grid, kThreads, smem, s>>>(g, codes_map, act_map);
     return cudaGetLastError();
 }
 
@@ -323,7 +395,33 @@ cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
     }
 }
 
+// xg[p] = x[token of sorted position p] for the rows of the used tiles, zero
+// for padding; 16 bytes per thread, grid-stride.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int H8,
+                                                          const int32_t* __restrict__ sorted_pairs,
+                                                          const int32_t* __restrict__ num_tiles,
+                                                          int tile_m, int Kt, uint4* __restrict__ xg) {
+    const size_t total = (size_t)__ldg(num_tiles) * tile_m * H8;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t p = i / H8, c = i % H8;
+        const int q = __ldg(sorted_pairs + p);
+        xg[i] = q >= 0 ? __ldg(x + (size_t)(q / Kt) * H8 + c) : make_uint4(0, 0, 0, 0);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_rows(const uint16_t* x, int H, const int32_t* sorted_pairs,
+                               const int32_t* num_tiles, int tile_m, int Kt, int cap, uint16_t* xg,
+                               cudaStream_t s) {
+    if (cap <= 0) return cudaSuccess;
+    const long long chunks = (long long)cap * (H / 8);
+    const int blocks = (int)std::min<long long>((chunks + 255) / 256, (long long)num_sms() * 8);
+    gather_rows_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), H / 8, sorted_pairs,
+                                              num_tiles, tile_m, Kt, reinterpret_cast<uint4*>(xg));
+    return cudaGetLastError();
+}
 
 bool prefill_tile_supported(int tile_m) {
     return tile_m == 32 || tile_m == 64 || tile_m == 128 || tile_m == 256;
@@ -332,7 +430,7 @@ bool prefill_shape_supported(int H, int I) { return H % 32 == 0 && I % 32 == 0; 
 cudaError_t launch_prefill_gate_up(const GroupedGemm& g, cudaStream_t s) { return launch_mode<0>(g, s); }
 cudaError_t launch_prefill_down(const GroupedGemm& g, cudaStream_t s) { return launch_mode<1>(g, s); }
 
-cudaError_t read_device_error(int* flag, int clear) {
+cudaError_t read_device_error_prefill(int* flag, int clear) {
     cudaError_t err = cudaMemcpyFromSymbol(flag, g_device_error, sizeof(int));
     if (err != cudaSuccess || !clear) return err;
     const int zero = 0;

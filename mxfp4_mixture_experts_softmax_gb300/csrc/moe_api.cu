@@ -181,11 +181,18 @@ moe_status_t moe_permute(const int32_t* topk_ids, int T, int Kt, int Et, int til
                                       num_tiles, stream));
 }
 
+static size_t y_offset(int64_t cap, int I) { return round_up((size_t)cap * I * sizeof(uint16_t), 256); }
+
+static size_t xg_offset(int64_t cap, int T, int H, int I, int Kt) {
+    return y_offset(cap, I) + round_up((size_t)T * Kt * H * sizeof(float), 256);
+}
+
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m) {
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     if (cap < 0 || H <= 0 || I <= 0) return 0;
-    return round_up((size_t)cap * I * sizeof(uint16_t), 256) +
-           round_up((size_t)T * Kt * H * sizeof(float), 256);
+    size_t bytes = xg_offset(cap, T, H, I, Kt);
+    if (prefill_tile_supported(tile_m)) bytes += round_up((size_t)cap * H * sizeof(uint16_t), 256);
+    return bytes;
 }
 
 moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m) {
@@ -251,53 +258,71 @@ static void trace(const char* step, int T, int H, int I, int Et, int Kt, int til
 size_t moe_ffn_y_offset(int T, int I, int Et, int Kt, int tile_m) {
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     if (cap < 0 || I <= 0) return 0;
-    return round_up((size_t)cap * I * sizeof(uint16_t), 256);
+    return y_offset(cap, I);
 }
 
 moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
                              const int32_t* sorted_pairs, const int32_t* tile_expert,
                              const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
-                             int tile_m, uint16_t* h, moe_path_t path, cudaStream_t stream) {
+                             int tile_m, void* workspace, size_t ws_bytes, moe_path_t path,
+                             cudaStream_t stream) {
     moe_status_t st = check_ffn_shape(T, H, I, Et, Kt, tile_m, &path);
     if (st != MOE_OK || T == 0) return st;
-    if (!ptrs_ok({x, w13, h}, 16) || !ptrs_ok({s13, sorted_pairs, tile_expert, num_tiles}, 4))
+    if (!ptrs_ok({x, w13, workspace}, 16) || !ptrs_ok({s13, sorted_pairs, tile_expert, num_tiles}, 4))
         return MOE_ERR_INVALID_ARG;
-    const int max_tiles = (int)(capacity64(T, Kt, Et, tile_m) / tile_m);
+    if (ws_bytes < moe_ffn_workspace_size(T, H, I, Et, Kt, tile_m)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    const int max_tiles = (int)(cap / tile_m);
     trace("moe_ffn_gate_up", T, H, I, Et, Kt, tile_m, path);
     GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, I, Et, Kt, tile_m, max_tiles);
     g.codes = w13;
     g.scales = s13;
     g.rows = 2 * I;
     g.K = H;
-    g.act = x;
-    g.act_rows = T;
-    g.act_by_token = 1;
-    g.h_out = h;
-    cudaError_t err = path == MOE_PATH_DECODE ? launch_decode_gate_up(g, stream)
-                                               : launch_prefill_gate_up(g, stream);
+    g.h_out = reinterpret_cast<uint16_t*>(workspace);
+    cudaError_t err;
+    if (path == MOE_PATH_DECODE) {
+        g.act = x;
+        g.act_rows = T;
+        g.act_by_token = 1;
+        err = launch_decode_gate_up(g, stream);
+    } else {
+        // the prefill GEMM reads its token rows as one box per stage: gather
+        // them into tile order first
+        uint16_t* xg = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(workspace) +
+                                                   xg_offset(cap, T, H, I, Kt));
+        err = launch_gather_rows(x, H, sorted_pairs, num_tiles, tile_m, Kt, (int)cap, xg, stream);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        g.act = xg;
+        g.act_rows = (int)cap;
+        g.act_by_token = 0;
+        err = launch_prefill_gate_up(g, stream);
+    }
     return cuda_status(err);
 }
 
-moe_status_t moe_ffn_down(const uint16_t* h, const uint8_t* w2, const uint8_t* s2,
-                          const float* topk_w, const int32_t* sorted_pairs,
-                          const int32_t* tile_expert, const int32_t* num_tiles, int T, int H,
-                          int I, int Et, int Kt, int tile_m, float* y, moe_path_t path,
+moe_status_t moe_ffn_down(const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                          const int32_t* sorted_pairs, const int32_t* tile_expert,
+                          const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                          int tile_m, void* workspace, size_t ws_bytes, moe_path_t path,
                           cudaStream_t stream) {
     moe_status_t st = check_ffn_shape(T, H, I, Et, Kt, tile_m, &path);
     if (st != MOE_OK || T == 0) return st;
-    if (!ptrs_ok({h, w2, y}, 16) || !ptrs_ok({s2, topk_w, sorted_pairs, tile_expert, num_tiles}, 4))
+    if (!ptrs_ok({w2, workspace}, 16) || !ptrs_ok({s2, topk_w, sorted_pairs, tile_expert, num_tiles}, 4))
         return MOE_ERR_INVALID_ARG;
-    const int max_tiles = (int)(capacity64(T, Kt, Et, tile_m) / tile_m);
+    if (ws_bytes < moe_ffn_workspace_size(T, H, I, Et, Kt, tile_m)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    const int max_tiles = (int)(cap / tile_m);
     trace("moe_ffn_down", T, H, I, Et, Kt, tile_m, path);
     GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, I, Et, Kt, tile_m, max_tiles);
     g.codes = w2;
     g.scales = s2;
     g.rows = H;
     g.K = I;
-    g.act = h;
-    g.act_rows = (int)capacity64(T, Kt, Et, tile_m);
+    g.act = reinterpret_cast<const uint16_t*>(workspace);
+    g.act_rows = (int)cap;
     g.act_by_token = 0;
-    g.y_out = y;
+    g.y_out = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + y_offset(cap, I));
     g.topk_w = topk_w;
     cudaError_t err = path == MOE_PATH_DECODE ? launch_decode_down(g, stream)
                                                : launch_prefill_down(g, stream);
@@ -325,15 +350,14 @@ moe_status_t moe_ffn_path(const uint16_t* x, const uint8_t* w13, const uint8_t* 
         !ptrs_ok({s13, s2, topk_w, sorted_pairs, expert_offsets, inv_pairs, tile_expert, num_tiles}, 4))
         return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe_ffn_workspace_size(T, H, I, Et, Kt, tile_m)) return MOE_ERR_WORKSPACE_TOO_SMALL;
-    uint16_t* h = reinterpret_cast<uint16_t*>(workspace);
-    float* y = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) +
-                                        moe_ffn_y_offset(T, I, Et, Kt, tile_m));
     st = moe_ffn_gate_up(x, w13, s13, sorted_pairs, tile_expert, num_tiles, T, H, I, Et, Kt, tile_m,
-                         h, path, stream);
+                         workspace, ws_bytes, path, stream);
     if (st != MOE_OK) return st;
-    st = moe_ffn_down(h, w2, s2, topk_w, sorted_pairs, tile_expert, num_tiles, T, H, I, Et, Kt,
-                      tile_m, y, path, stream);
+    st = moe_ffn_down(w2, s2, topk_w, sorted_pairs, tile_expert, num_tiles, T, H, I, Et, Kt, tile_m,
+                      workspace, ws_bytes, path, stream);
     if (st != MOE_OK) return st;
+    const float* y = reinterpret_cast<const float*>(reinterpret_cast<const char*>(workspace) +
+                                                    moe_ffn_y_offset(T, I, Et, Kt, tile_m));
     return moe_combine(y, T, H, Kt, out, stream);
 }
 

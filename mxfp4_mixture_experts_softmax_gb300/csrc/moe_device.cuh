@@ -157,17 +157,28 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // Bounded wait for the phase with the given parity.  Gives up (returns
 // false) after kWaitLimitNs, or as soon as another CTA of the same kernel
 // file has raised the device error flag, so one failure cannot stall a grid.
+// The flag and the clock are checked only every 64 polls, keeping the poll
+// itself a single shared-memory barrier test.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    while (true) {
+    for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*(volatile int*)&g_device_error) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
-            atomicExch(&g_device_error, 1);
-            return false;
+        if ((n & 63) == 0) {
+            if (*(volatile int*)&g_device_error) return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                atomicExch(&g_device_error, 1);
+                return false;
+            }
         }
     }
+}
+
+// Prefetch one 2D box of a tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap),
+                 "r"(c0), "r"(c1)
+                 : "memory");
 }
 
 // 2D tiled TMA load of one box into shared memory, completing on the mbarrier.

@@ -69,6 +69,10 @@ bool prefill_shape_supported(int H, int I);
 cudaError_t launch_decode_gate_up(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_prefill_gate_up(const GroupedGemm& g, cudaStream_t s);
+// xg[p] = x[sorted_pairs[p] / Kt] for the rows of the used tiles (0 for pads).
+cudaError_t launch_gather_rows(const uint16_t* x, int H, const int32_t* sorted_pairs,
+                               const int32_t* num_tiles, int tile_m, int Kt, int cap,
+                               uint16_t* xg, cudaStream_t s);
 cudaError_t launch_prefill_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t read_device_error_prefill(int* flag, int clear);
 cudaError_t read_device_error_decode(int* flag, int clear);

@@ -78,9 +78,9 @@ def load(build: bool = True):
         L.moe_ffn_path.restype = ci
         L.moe_ffn_auto_path.argtypes = [ci, ci, ci, ci]
         L.moe_ffn_auto_path.restype = ci
-        L.moe_ffn_gate_up.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, ci, vp]
+        L.moe_ffn_gate_up.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, sz, ci, vp]
         L.moe_ffn_gate_up.restype = ci
-        L.moe_ffn_down.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, ci, vp]
+        L.moe_ffn_down.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, sz, ci, vp]
         L.moe_ffn_down.restype = ci
         L.moe_combine.argtypes = [vp, ci, ci, ci, vp, vp]
         L.moe_combine.restype = ci
@@ -247,24 +247,26 @@ def ffn_views(workspace, T: int, H: int, I: int, Et: int, Kt: int, tile_m: int):
     return h, y
 
 
-def moe_ffn_gate_up(x, w13, s13, perm: dict, h, path: int = MOE_PATH_AUTO, stream=None):
+def moe_ffn_gate_up(x, w13, s13, perm: dict, workspace, path: int = MOE_PATH_AUTO, stream=None):
+    """gate_up + SwiGLU into the workspace's h (see ffn_views)."""
     T, H = x.shape
     Et, twoI, _ = w13.shape
     _check(load().moe_ffn_gate_up(_ptr(x), _ptr(w13), _ptr(s13), _ptr(perm["sorted_pairs"]),
                                   _ptr(perm["tile_expert"]), _ptr(perm["num_tiles"]), T, H,
-                                  twoI // 2, Et, perm["Kt"], perm["tile_m"], _ptr(h), int(path),
-                                  _stream(stream)), "moe_ffn_gate_up")
-    return h
+                                  twoI // 2, Et, perm["Kt"], perm["tile_m"], _ptr(workspace),
+                                  workspace.numel(), int(path), _stream(stream)), "moe_ffn_gate_up")
+    return workspace
 
 
-def moe_ffn_down(h, w2, s2, topk_w, perm: dict, y, T: int, path: int = MOE_PATH_AUTO,
+def moe_ffn_down(w2, s2, topk_w, perm: dict, workspace, T: int, path: int = MOE_PATH_AUTO,
                  stream=None):
+    """down x routing weight from the workspace's h into its y (see ffn_views)."""
     Et, H, halfI = w2.shape
-    _check(load().moe_ffn_down(_ptr(h), _ptr(w2), _ptr(s2), _ptr(topk_w),
-                               _ptr(perm["sorted_pairs"]), _ptr(perm["tile_expert"]),
-                               _ptr(perm["num_tiles"]), T, H, 2 * halfI, Et, perm["Kt"],
-                               perm["tile_m"], _ptr(y), int(path), _stream(stream)), "moe_ffn_down")
-    return y
+    _check(load().moe_ffn_down(_ptr(w2), _ptr(s2), _ptr(topk_w), _ptr(perm["sorted_pairs"]),
+                               _ptr(perm["tile_expert"]), _ptr(perm["num_tiles"]), T, H, 2 * halfI,
+                               Et, perm["Kt"], perm["tile_m"], _ptr(workspace), workspace.numel(),
+                               int(path), _stream(stream)), "moe_ffn_down")
+    return workspace
 
 
 def moe_combine(y, T: int, H: int, Kt: int, out, stream=None):
