@@ -14,7 +14,7 @@
 //     rows as one box in the 128-byte swizzled K-major layout the MMA reads
 //     (gate_up reads x gathered into tile order by gather_rows_kernel, down
 //     reads h, which is already in tile order);
-//   * 8 converter warps: exact bf16 dequantisation of the codes (E2M1 bit
+//   * 16 converter warps: exact bf16 dequantisation of the codes (E2M1 bit
 //     placement times 2^126 * 2^(s-127) by one bf16x2 multiply) into the
 //     stage's A buffer, same swizzled layout;
 //   * MMA warp: one thread issues the four K = 16 tcgen05.mma of each stage
@@ -37,10 +37,10 @@ namespace {
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kConvWarp0 = 2;
-constexpr int kConvWarps = 8;
-constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;  // 10..13: warp % 4 covers every lane quadrant
+constexpr int kConvWarps = 16;
+constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;  // 18..21: warp % 4 covers every lane quadrant
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 448
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 704
 constexpr int kBK = 64;                                   // k per stage (one 128-byte bf16 row)
 constexpr int kStages = 4;
 constexpr int kABytes = 128 * kBK * 2;                    // 16 KB bf16 A stage
@@ -167,16 +167,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int e = __ldg(g.tile_expert + tile);
             const int crow0 = e * g.rows + (MODE == 0 ? block * 64 : block * 128);
             const int crow1 = MODE == 0 ? e * g.rows + g.I + block * 64 : crow0 + kCodeBox;
-            if (lane == 0)  // the item's first codes into L2 before the ring asks for them
+            if (lane == 0)  // the item's first stages into L2 before the ring asks for them
                 for (int st = 0; st < kPrefetch && st < nk; ++st) {
                     tma_prefetch_l2_2d(&codes_map, st * (kBK / 2), crow0);
                     tma_prefetch_l2_2d(&codes_map, st * (kBK / 2), crow1);
+                    tma_prefetch_l2_2d(&act_map, st * kBK, tile * N);
                 }
             for (int st = 0; st < nk; ++st, ++gs) {
                 const int s = gs % kStages;
                 if (lane == 0 && st + kPrefetch < nk) {
                     tma_prefetch_l2_2d(&codes_map, (st + kPrefetch) * (kBK / 2), crow0);
                     tma_prefetch_l2_2d(&codes_map, (st + kPrefetch) * (kBK / 2), crow1);
+                    tma_prefetch_l2_2d(&act_map, (st + kPrefetch) * kBK, tile * N);
                 }
                 if (gs >= kStages && !mbar_wait(&stage_free[s], ((gs / kStages) - 1) & 1)) {
                     ok = false;
@@ -232,8 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------ converters
-        const int t = tid - kConvWarp0 * 32;  // 0..255
-        const int rho = t >> 1, h = t & 1;    // A row, 32-k half of the stage
+        const int t = tid - kConvWarp0 * 32;  // 0..511
+        const int rho = t >> 2, qh = t & 3;   // A row, 16-k quarter of the stage
+        const int h = qh >> 1;                // its 32-k scale group within the stage
         const int crow = MODE == 0 ? ((rho & 1) ? kCodeBox + (rho >> 1) : rho >> 1) : rho;
         const bool svec = (K % 512) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 15) == 0);
         uint32_t gs = 0;
@@ -277,24 +280,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                uint4 cw;
-                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
-                             : "r"(smem_u32(stage_c(s)) + crow * (kBK / 2) + 16 * h));
+                uint2 cw;
+                asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
+                             : "=r"(cw.x), "=r"(cw.y)
+                             : "r"(smem_u32(stage_c(s)) + crow * (kBK / 2) + 8 * qh));
                 const uint32_t mlo = e8m0_mult_lo(sc);
-                const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+                const uint32_t w2[2] = {cw.x, cw.y};
                 const uint32_t arow = smem_u32(stage_a(s)) + rho * 128;
 #pragma unroll
-                for (int i4 = 0; i4 < 4; ++i4) {
+                for (int i2 = 0; i2 < 2; ++i2) {
                     uint32_t d[4];
-                    mxfp4_word_to_bf16x2(w4[i4], mlo, d);
+                    mxfp4_word_to_bf16x2(w2[i2], mlo, d);
                     if (sc > 128u) bf16x2_scale(d, e8m0_mult_hi(sc));
                     uint4 v;
                     v.x = __byte_perm(d[0], d[1], 0x5410);  // (k0, k1)
                     v.y = __byte_perm(d[2], d[3], 0x5410);  // (k2, k3)
                     v.z = __byte_perm(d[0], d[1], 0x7632);  // (k4, k5)
                     v.w = __byte_perm(d[2], d[3], 0x7632);  // (k6, k7)
-                    const int ch = 4 * h + i4;
+                    const int ch = 2 * qh + i2;
                     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
                                      arow + ((ch ^ (rho & 7)) << 4)),
                                  "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
