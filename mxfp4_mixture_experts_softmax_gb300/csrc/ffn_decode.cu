@@ -68,10 +68,6 @@ __device__ __forceinline__ int cta_weight_row(int rho, int block, int I, int row
     return m < rows ? m : -1;
 }
 
-__device__ __forceinline__ float scale_factor(uint32_t s) {
-    return __uint_as_float((s + 62u) << 23);  // 2^(s - 65)
-}
-
 __device__ __forceinline__ uint32_t bf16x2_mul_bits(uint32_t a, uint32_t b) {
     __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a),
                                *reinterpret_cast<__nv_bfloat162*>(&b));

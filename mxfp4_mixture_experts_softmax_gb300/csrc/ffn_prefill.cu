@@ -89,7 +89,7 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t r[16]) {
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t* r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -97,8 +97,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t r[16]) {
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
 
 template <int N>
 struct PrefillSmem {
@@ -328,24 +328,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!mbar_wait(&acc_full[b], (it >> 1) & 1)) break;
             tc_fence_after();
+            // 32 columns per round trip: two loads, one wait
 #pragma unroll
-            for (int c0 = 0; c0 < N; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem + ((uint32_t)(32 * quad) << 16) + b * N + (uint32_t)c0, v);
+            for (int c0 = 0; c0 < N; c0 += 32) {
+                uint32_t v[32];
+                const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + b * N + (uint32_t)c0;
+                tmem_ld16_nowait(taddr, v);
+                tmem_ld16_nowait(taddr + 16, v + 16);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                const int q_lo = qv[c0 / 32];
+                if (MODE == 0) {
+                    // lane 2i holds gate row i, lane 2i+1 up row i: after one
+                    // exchange per column pair the even lane owns column j and
+                    // the odd lane column j + 1
+                    const int n = block * 64 + (r >> 1);
+                    const bool odd = lane & 1;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int j = c0 + i;
-                    const float acc = __uint_as_float(v[i]);
-                    const int q = __shfl_sync(0xFFFFFFFFu, qv[j / 32], j % 32);
-                    if (MODE == 0) {
-                        const float partner = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-                        const int n = block * 64 + (r >> 1);
-                        if (!(lane & 1) && n < g.I && q >= 0)
-                            g.h_out[(size_t)(tile * N + j) * g.I + n] = f32_to_bf16_bits(silu(acc) * partner);
-                    } else {
-                        const float wq = __shfl_sync(0xFFFFFFFFu, wv[j / 32], j % 32);
-                        const int m = block * 128 + r;
-                        if (m < g.rows && q >= 0) g.y_out[(size_t)q * g.rows + m] = wq * acc;
+                    for (int i = 0; i < 32; i += 2) {
+                        const float a0 = __uint_as_float(v[i]), a1 = __uint_as_float(v[i + 1]);
+                        const float other = __shfl_xor_sync(0xFFFFFFFFu, odd ? a0 : a1, 1);
+                        const int j = c0 + i + (odd ? 1 : 0);
+                        const float gate = odd ? other : a0;   // even: own gate j; odd: partner's gate j+1
+                        const float up = odd ? a1 : other;     // even: partner's up j; odd: own up j+1
+                        const int q = __shfl_sync(0xFFFFFFFFu, q_lo, j & 31);
+                        if (n < g.I && q >= 0)
+                            g.h_out[(size_t)(tile * N + j) * g.I + n] = f32_to_bf16_bits(silu(gate) * up);
+                    }
+                } else {
+                    const float w_lo = wv[c0 / 32];
+                    const int m = block * 128 + r;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int q = __shfl_sync(0xFFFFFFFFu, q_lo, i);
+                        const float wq = __shfl_sync(0xFFFFFFFFu, w_lo, i);
+                        if (m < g.rows && q >= 0) g.y_out[(size_t)q * g.rows + m] = wq * __uint_as_float(v[i]);
                     }
                 }
             }
