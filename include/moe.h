@@ -130,8 +130,10 @@ moe_status_t moe_permute(const int32_t* topk_ids, int T, int Kt, int Et, int til
 /*
  * moe_ffn_workspace_size -- bytes of device workspace moe_ffn needs:
  * the bf16 SwiGLU intermediate [cap, I], the weighted fp32 per-pair expert
- * outputs [T*Kt, H] and, when tile_m is a prefill tile height (32, 64, 128,
- * 256), the tile-ordered bf16 activations [cap, H]; each 256-byte aligned.
+ * outputs [T*Kt, H] and an activation area: room for the tile-ordered bf16
+ * activations [cap, H] when tile_m is a prefill tile height (32, 64, 128,
+ * 256), for the decode path's rescaled copy of x [T, H] when tile_m is a
+ * decode tile height, the larger of the two when both; each 256-byte aligned.
  */
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
 
@@ -180,14 +182,17 @@ moe_status_t moe_ffn_path(const uint16_t* x, const uint8_t* w13, const uint8_t* 
 /*
  * The three steps of moe_ffn as separate calls; moe_ffn runs exactly these,
  * in this order, on one workspace (at least moe_ffn_workspace_size() bytes):
- *   h  bf16 [cap, I] at byte 0, y fp32 [T*Kt, H] at moe_ffn_y_offset(), and,
- *   for tile heights the prefill path supports (32, 64, 128, 256), the
- *   tile-ordered copy of the activations the prefill gate_up reads, after y.
+ *   h  bf16 [cap, I] at byte 0, y fp32 [T*Kt, H] at moe_ffn_y_offset(), and
+ *   the activation area after y: the prefill gate_up's tile-ordered copy of
+ *   the activations, or the decode gate_up's copy of x times 2^64 with the
+ *   columns of each group of 8 in the order 0,4,1,5,2,6,3,7.
  * `path` must resolve to the same path for both GEMM calls (AUTO always does
- * for the same sizes).
+ * for the same sizes): the layout of h is the path's own.
  *
  * moe_ffn_gate_up: h[p, n] = bf16(silu(g) * u) for every sorted position p
- *   that holds a pair (pads are not written).
+ *   that holds a pair (pads are not written).  The prefill path stores h as
+ *   is; the decode path stores h * 2^64 (exact) with its columns permuted
+ *   within groups of 8 like x above, the layout its down GEMM stages.
  * moe_ffn_down:    y[q, m] = topk_w[q] * (W2[e] h_p)[m] for every pair q at
  *   position p (the routing-weighted expert outputs).
  * moe_combine:     out[t, m] = bf16(sum over j = 0..Kt-1, ascending, of

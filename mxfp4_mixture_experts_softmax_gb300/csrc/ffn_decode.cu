@@ -20,13 +20,17 @@
 //   * codes become bf16 by bit placement (E2M1 * 2^-126, exact, e = 0 codes
 //     as bf16 subnormals, which the MMA consumes exactly) -- three integer ops
 //     per two values and no per-element multiply;
-//   * the activations were staged once, multiplied by 2^64 (exact) so that the
-//     products stay in the fp32 normal range, and each group's two MMAs go
+//   * the activations are kept multiplied by 2^64 (exact) so that the
+//     products stay in the fp32 normal range, pair-interleaved to match the
+//     code pairing (prep_act_kernel for x; the gate_up epilogue writes h that
+//     way); a staging warp bulk-copies the tile's rows into a double-buffered
+//     chunk ahead of the consumers; each group's two MMAs go
 //     into a fresh fp32 partial that is added to the accumulator times
 //     2^126 * 2^(s-127) * 2^-64 = 2^(s-65): an exact power-of-two FMA.
 // The MMA's k slots are a fixed permutation of k (a code word yields pairs
-// (0,4),(1,5),(2,6),(3,7)); the staged activations use the same permutation
-// and an XOR swizzle that keeps the B-fragment loads conflict-free.
+// (0,4),(1,5),(2,6),(3,7)); the staged activations use the same permutation,
+// and a row pitch of 64 bytes past a multiple of 128 keeps the B-fragment
+// loads conflict-free.
 #include <algorithm>
 
 #include "moe_internal.h"
@@ -37,24 +41,27 @@ namespace {
 
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;    // + one producer warp
+constexpr int kLoadWarp = kConsumerWarps;        // TMA of the weight codes
+constexpr int kStageWarp = kConsumerWarps + 1;   // activation staging
+constexpr int kThreads = kConsumers + 64;
 constexpr int kRows = 256;                   // weight rows per CTA
 constexpr int kStageK = 256;                 // k per pipeline stage
 constexpr int kRowBytes = kStageK / 2;       // code bytes per row per stage (one TMA box row)
 constexpr int kBoxRows = 128;                // rows per TMA box
 constexpr int kStages = 4;
 constexpr int kStageBytes = kRows * kRowBytes;
-constexpr int kXBytes = 64 * 1024;           // staged activation chunk
+constexpr int kXBytes = 32 * 1024;           // one staged activation chunk (two buffers)
 constexpr uint32_t kBf16TwoPow64 = 0x5F805F80u;  // bf16x2 (2^64, 2^64)
 
 template <int NT>
 struct DecodeSmem {
     static constexpr int TM = NT * 8;
     static constexpr int KC = kXBytes / (TM * 2);  // k per staged activation chunk
+    static constexpr int kPitch = KC * 2 + 64;     // bytes per staged row: +4 bank groups per row
+    static constexpr int kXBuf = TM * kPitch;      // one staged chunk
     static constexpr int kX = kStages * kStageBytes;
-    static constexpr int kBars = kX + kXBytes;
-    static constexpr int kQ = kBars + 2 * kStages * 8;
-    static constexpr int kTotal = kQ + 2 * TM * 4 + 1024;  // + alignment slack
+    static constexpr int kBars = kX + 2 * kXBuf;
+    static constexpr int kTotal = kBars + (2 * kStages + 4) * 8 + 1024;  // + alignment slack
 };
 
 // Weight row (within the expert) held in CTA row rho, or -1 past the end.
@@ -89,43 +96,51 @@ __device__ __forceinline__ void codes_to_bf16x2(uint32_t w, uint32_t mul_a, uint
 }
 
 // Persistent kernel: CTA b processes work items b, b + gridDim.x, ... where
-// item = tile * row_blocks + block.  The producer's stage ring runs across
-// items, so the next item's weights stream in while the consumers finish the
-// current one (epilogue, activation staging).
+// item = tile * row_blocks + block.  Two helper warps run ahead of the 16
+// consumer warps across items: one streams the weight codes (TMA ring), one
+// stages the tiles' activation rows into a double-buffered chunk (x 2^64,
+// pair-interleaved, swizzled).  Consumers only wait on mbarriers.
 template <int MODE, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const GroupedGemm g, const __grid_constant__ CUtensorMap codes_map) {
     using L = DecodeSmem<NT>;
     constexpr int TM = L::TM;
     constexpr int KC = L::KC;
-    constexpr int XC = KC / 8;  // 16-byte chunks per staged activation row
     extern __shared__ uint8_t smem_raw[];
     // the 128-byte swizzle pattern repeats every 1024 bytes: align the ring
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* codes_s = smem;
-    uint4* xs = reinterpret_cast<uint4*>(smem + L::kX);
+    uint8_t* xs_s = smem + L::kX;  // [2][TM] rows of kPitch bytes
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBars);
     uint64_t* empty = full + kStages;
-    int32_t* qtok = reinterpret_cast<int32_t*>(smem + L::kQ);  // activation row, -1 = padding
-    int32_t* qpair = qtok + TM;                                  // pair index, -1 = padding
+    uint64_t* xfull = empty + kStages;  // [2] staged chunk ready
+    uint64_t* xempty = xfull + 2;       // [2] staged chunk consumed
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = g.K;
     const int nsteps = (K + kStageK - 1) / kStageK;
+    const int nchunks = (K + KC - 1) / KC;
     const int row_blocks = MODE == 0 ? (g.I + 127) / 128 : (g.rows + kRows - 1) / kRows;
     const int items = __ldg(g.num_tiles) * row_blocks;
 
+    // staged rows past K and padding rows are never copied: start them at zero
+    for (int i = tid; i < 2 * L::kXBuf / 16; i += kThreads)
+        reinterpret_cast<uint4*>(xs_s)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&xfull[b], 1);
+            mbar_init(&xempty[b], kConsumerWarps);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------- producer
+    if (warp == kLoadWarp) {
+        // ------------------------------------------------- weight codes (TMA)
         if (lane == 0) {
             uint32_t gs = 0;
             for (int item = blockIdx.x; item < items; item += gridDim.x) {
@@ -148,6 +163,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
+    if (warp == kStageWarp) {
+        // ------------------------------------------- activation staging
+        // rows of the pre-transformed activations (x 2^64, pair-interleaved:
+        // see prep_act_kernel and the gate_up epilogue) are plain contiguous
+        // copies: one bulk copy per tile row per chunk
+        uint32_t gc = 0;
+        for (int item = blockIdx.x; item < items; item += gridDim.x) {
+            const int tile = item / row_blocks;
+            int arow[TM > 32 ? 2 : 1];
+            uint32_t valid = 0;
+#pragma unroll
+            for (int h = 0; h < (TM > 32 ? 2 : 1); ++h) {
+                const int j = lane + 32 * h;
+                const int q = j < TM ? __ldg(g.sorted_pairs + tile * TM + j) : -1;
+                arow[h] = q < 0 ? -1 : (g.act_by_token ? q / g.Kt : tile * TM + j);
+                valid += __popc(__ballot_sync(0xFFFFFFFFu, arow[h] >= 0));
+            }
+            for (int c = 0; c < nchunks; ++c, ++gc) {
+                const int b = gc & 1;
+                if (gc >= 2 && !mbar_wait(&xempty[b], ((gc >> 1) - 1) & 1)) return;
+                const int kc = c * KC;
+                const uint32_t bytes = (uint32_t)min(KC, K - kc) * 2u;
+                if (lane == 0) mbar_arrive_expect_tx(&xfull[b], valid * bytes);
+                __syncwarp();
+                const uint32_t dst = smem_u32(xs_s) + b * L::kXBuf;
+#pragma unroll
+                for (int h = 0; h < (TM > 32 ? 2 : 1); ++h) {
+                    const int j = lane + 32 * h;
+                    if (arow[h] >= 0)
+                        bulk_copy_g2s(dst + j * L::kPitch, g.act + (size_t)arow[h] * K + kc, bytes,
+                                      &xfull[b]);
+                }
+            }
+        }
+        return;
+    }
+
     // ---------------------------------------------------------- consumers
     const int r = lane >> 2, c = lane & 3;
     const uint32_t mul_a = g.mul_a, mul_b = g.mul_b;
@@ -162,22 +214,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int gp = 0; gp < 4; ++gp)
         lm_off[gp] = smem_u32(codes_s) + lrho * kRowBytes + (((2 * gp + (mj >> 1)) ^ mi) << 4);
-    // staged activations of row r: group gl of a stage sits at chunk 4 * (gl ^ (r & 1)) + c
-    const int p = r & 1;
-    const uint32_t xb = smem_u32(xs) + (uint32_t)(r * XC + c) * 16u;
-    const uint32_t xb_even = xb + 64u * p, xb_odd = xb - 64u * p;
+    // staged activations of row r: group gl of a stage at byte 64 * gl + 16 * c
+    const uint32_t xb = smem_u32(xs_s) + (uint32_t)(r * L::kPitch + c * 16);
 
-    uint32_t gs = 0;
+    uint32_t gs = 0, gc = 0;
     bool failed = false;
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const int tile = item / row_blocks, block = item % row_blocks;
         const int e = __ldg(g.tile_expert + tile);
-        named_bar_sync(1, kConsumers);  // previous item fully consumed
-        if (tid < TM) {
-            const int q = __ldg(g.sorted_pairs + tile * TM + tid);
-            qpair[tid] = q;
-            qtok[tid] = q < 0 ? -1 : (g.act_by_token ? q / g.Kt : tile * TM + tid);
-        }
+        int qj[NT][2];  // pair index of this lane's two columns per n-tile (-1 = padding)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) qj[n][u] = __ldg(g.sorted_pairs + tile * TM + n * 8 + 2 * c + u);
         const int rho0 = MODE == 0 ? 8 * warp + r : 16 * warp + r;
         const int rho1 = MODE == 0 ? 128 + 8 * warp + r : 16 * warp + 8 + r;
         const int wr0 = cta_weight_row<MODE>(rho0, block, g.I, g.rows);
@@ -189,16 +238,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s0 = wr0 >= 0 ? __ldg(reinterpret_cast<const uint2*>(sp0 + st * 8)) : make_uint2(0, 0);
                 s1 = wr1 >= 0 ? __ldg(reinterpret_cast<const uint2*>(sp1 + st * 8)) : make_uint2(0, 0);
             } else {
-                uint32_t a[2] = {0, 0}, b[2] = {0, 0};
+                uint32_t a[2] = {0, 0}, bb[2] = {0, 0};
                 for (int gl = 0; gl < 8; ++gl) {
                     const int gidx = st * 8 + gl;
                     if (gidx * 32 < K) {
                         if (wr0 >= 0) a[gl >> 2] |= (uint32_t)__ldg(sp0 + gidx) << (8 * (gl & 3));
-                        if (wr1 >= 0) b[gl >> 2] |= (uint32_t)__ldg(sp1 + gidx) << (8 * (gl & 3));
+                        if (wr1 >= 0) bb[gl >> 2] |= (uint32_t)__ldg(sp1 + gidx) << (8 * (gl & 3));
                     }
                 }
                 s0 = make_uint2(a[0], a[1]);
-                s1 = make_uint2(b[0], b[1]);
+                s1 = make_uint2(bb[0], bb[1]);
             }
         };
         uint2 nsc0, nsc1;
@@ -206,29 +255,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float acc[NT][4];
 #pragma unroll
         for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
-        named_bar_sync(1, kConsumers);  // qtok / qpair visible
 
+        uint32_t xbuf = 0;
         for (int st = 0; st < nsteps; ++st, ++gs) {
             const int kst = st * kStageK;
-            if (kst % KC == 0) {
-                // stage activation rows [kst, kst + KC): x 2^64, pair-interleaved, swizzled
-                if (kst > 0) named_bar_sync(1, kConsumers);
-                for (int idx = tid; idx < TM * XC; idx += kConsumers) {
-                    const int j = idx / XC, Lc = idx % XC;
-                    const int k = kst + 8 * Lc;
-                    const int t = qtok[j];
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (t >= 0 && k < K) {
-                        v = __ldg(reinterpret_cast<const uint4*>(g.act + (size_t)t * K + k));
-                        v.x = bf16x2_mul_bits(v.x, kBf16TwoPow64);
-                        v.y = bf16x2_mul_bits(v.y, kBf16TwoPow64);
-                        v.z = bf16x2_mul_bits(v.z, kBf16TwoPow64);
-                        v.w = bf16x2_mul_bits(v.w, kBf16TwoPow64);
-                        v = pair_interleave8(v);
-                    }
-                    xs[j * XC + (Lc ^ ((j & 1) << 2))] = v;
-                }
-                named_bar_sync(1, kConsumers);
+            if (kst % KC == 0) {  // first stage of a staged chunk
+                xbuf = (gc & 1) * L::kXBuf;
+                if (!failed && !mbar_wait(&xfull[gc & 1], (gc >> 1) & 1)) failed = true;
             }
             const int s = gs % kStages;
             const uint2 sc0 = nsc0, sc1 = nsc1;
@@ -236,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!failed && !mbar_wait(&full[s], (gs / kStages) & 1)) failed = true;
             if (!failed) {
                 const uint32_t soff = s * kStageBytes;
-                const uint32_t xoff = (uint32_t)(kst % KC) * 2u;  // bytes into the staged rows
+                const uint32_t xoff = xbuf + (uint32_t)(kst % KC) * 2u;  // bytes into the staged rows
 #pragma unroll
                 for (int gp = 0; gp < 4; ++gp) {
                     uint32_t w[4];
@@ -252,16 +285,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t ta[4], tb[4];
                         codes_to_bf16x2(w[gi ? 2 : 0], mul_a, mul_b, ta);
                         codes_to_bf16x2(w[gi ? 3 : 1], mul_a, mul_b, tb);
-                        const uint32_t xa = ((gl & 1) ? xb_odd : xb_even) + xoff + 64u * gl;
+                        const uint32_t xa = xb + xoff + 64u * gl;
 #pragma unroll
                         for (int n = 0; n < NT; ++n) {
-                            uint4 b;
+                            uint4 bv;
                             asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                                         : "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
-                                         : "r"(xa + (uint32_t)(n * 8 * XC * 16)));
+                                         : "=r"(bv.x), "=r"(bv.y), "=r"(bv.z), "=r"(bv.w)
+                                         : "r"(xa + (uint32_t)(n * 8 * L::kPitch)));
                             float t4[4];
-                            mma_bf16_16816_z(t4, ta[0], tb[0], ta[1], tb[1], b.x, b.y);
-                            mma_bf16_16816_acc(t4, ta[2], tb[2], ta[3], tb[3], b.z, b.w);
+                            mma_bf16_16816_z(t4, ta[0], tb[0], ta[1], tb[1], bv.x, bv.y);
+                            mma_bf16_16816_acc(t4, ta[2], tb[2], ta[3], tb[3], bv.z, bv.w);
                             acc[n][0] = fmaf(t4[0], f0, acc[n][0]);
                             acc[n][1] = fmaf(t4[1], f0, acc[n][1]);
                             acc[n][2] = fmaf(t4[2], f1, acc[n][2]);
@@ -272,6 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            if ((kst + kStageK) % KC == 0 || st + 1 == nsteps) {  // last stage of the chunk
+                if (lane == 0) mbar_arrive(&xempty[gc & 1]);
+                ++gc;
+            }
         }
 
         if (!failed) {
@@ -280,12 +317,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int j = n * 8 + 2 * c + u;
-                    const int q = qpair[j];
+                    const int q = qj[n][u];
                     if (q < 0) continue;
                     if (MODE == 0) {
-                        if (wr0 >= 0)
-                            g.h_out[(size_t)(tile * TM + j) * g.I + wr0] =
-                                f32_to_bf16_bits(silu(acc[n][u]) * acc[n][2 + u]);
+                        // h as the down GEMM stages it: x 2^64 (exact), and
+                        // element i of each group of 8 at position 2 (i % 4) + i / 4
+                        if (wr0 >= 0) {
+                            const int col = (wr0 & ~7) | ((wr0 & 3) << 1) | ((wr0 >> 2) & 1);
+                            g.h_out[(size_t)(tile * TM + j) * g.I + col] =
+                                f32_to_bf16_bits(silu(acc[n][u]) * acc[n][2 + u] * 0x1p64f);
+                        }
                     } else {
                         const float wq = __ldg(g.topk_w + q);
                         float* y = g.y_out + (size_t)q * g.rows;
@@ -327,6 +368,21 @@ cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
     }
 }
 
+// xt = x * 2^64 (exact for |x| < 2^63), pair-interleaved within each group
+// of 8: the layout the decode GEMM's staging copies verbatim.
+__global__ void __launch_bounds__(256) prep_act_kernel(const uint4* __restrict__ x, size_t n16,
+                                                       uint4* __restrict__ xt) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+         i += (size_t)gridDim.x * blockDim.x) {
+        uint4 v = __ldg(x + i);
+        v.x = bf16x2_mul_bits(v.x, kBf16TwoPow64);
+        v.y = bf16x2_mul_bits(v.y, kBf16TwoPow64);
+        v.z = bf16x2_mul_bits(v.z, kBf16TwoPow64);
+        v.w = bf16x2_mul_bits(v.w, kBf16TwoPow64);
+        xt[i] = pair_interleave8(v);
+    }
+}
+
 // out[t][m] = bf16(sum over j ascending of y[t*Kt + j][m]); four columns per thread.
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y, int T, int H4,
                                                       int Kt, uint2* __restrict__ out) {
@@ -356,6 +412,15 @@ bool decode_tile_supported(int tile_m) {
 
 cudaError_t launch_decode_gate_up(const GroupedGemm& g, cudaStream_t s) { return launch_mode<0>(g, s); }
 cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s) { return launch_mode<1>(g, s); }
+
+cudaError_t launch_prep_act(const uint16_t* x, size_t elems, uint16_t* xt, cudaStream_t s) {
+    const size_t n16 = elems / 8;
+    if (n16 == 0) return cudaSuccess;
+    const int blocks = (int)std::min<size_t>((n16 + 255) / 256, (size_t)num_sms() * 8);
+    prep_act_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), n16,
+                                           reinterpret_cast<uint4*>(xt));
+    return cudaGetLastError();
+}
 
 cudaError_t read_device_error_decode(int* flag, int clear) {
     cudaError_t err = cudaMemcpyFromSymbol(flag, g_device_error, sizeof(int));

@@ -5,6 +5,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <initializer_list>
 #include <mutex>
 
@@ -187,12 +188,17 @@ static size_t xg_offset(int64_t cap, int T, int H, int I, int Kt) {
     return y_offset(cap, I) + round_up((size_t)T * Kt * H * sizeof(float), 256);
 }
 
+// the gathered activations (prefill) or the transformed x (decode) after y
+static size_t act_bytes(int64_t cap, int T, int H, int tile_m) {
+    size_t b = decode_tile_supported(tile_m) ? round_up((size_t)T * H * sizeof(uint16_t), 256) : 0;
+    if (prefill_tile_supported(tile_m)) b = std::max(b, round_up((size_t)cap * H * sizeof(uint16_t), 256));
+    return b;
+}
+
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m) {
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     if (cap < 0 || H <= 0 || I <= 0) return 0;
-    size_t bytes = xg_offset(cap, T, H, I, Kt);
-    if (prefill_tile_supported(tile_m)) bytes += round_up((size_t)cap * H * sizeof(uint16_t), 256);
-    return bytes;
+    return xg_offset(cap, T, H, I, Kt) + act_bytes(cap, T, H, tile_m);
 }
 
 moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m) {
@@ -282,7 +288,12 @@ moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_
     g.h_out = reinterpret_cast<uint16_t*>(workspace);
     cudaError_t err;
     if (path == MOE_PATH_DECODE) {
-        g.act = x;
+        // x * 2^64, pair-interleaved: the staging layout of the decode GEMM
+        uint16_t* xt = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(workspace) +
+                                                   xg_offset(cap, T, H, I, Kt));
+        err = launch_prep_act(x, (size_t)T * H, xt, stream);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        g.act = xt;
         g.act_rows = T;
         g.act_by_token = 1;
         err = launch_decode_gate_up(g, stream);

@@ -67,6 +67,8 @@ bool prefill_tile_supported(int tile_m);
 bool prefill_shape_supported(int H, int I);
 
 cudaError_t launch_decode_gate_up(const GroupedGemm& g, cudaStream_t s);
+// xt = x * 2^64, pair-interleaved within groups of 8 (the decode staging layout).
+cudaError_t launch_prep_act(const uint16_t* x, size_t elems, uint16_t* xt, cudaStream_t s);
 cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_prefill_gate_up(const GroupedGemm& g, cudaStream_t s);
 // xg[p] = x[sorted_pairs[p] / Kt] for the rows of the used tiles (0 for pads).

@@ -270,6 +270,30 @@ def test_layer_graph_capture_replays_identically():
     np.testing.assert_array_equal(gc.bf16_dev_to_f64(bufs["out"]), gc.bf16_dev_to_f64(eager))
 
 
+@pytest.mark.parametrize("path,tile_m", [(libmoe.MOE_PATH_DECODE, 8),
+                                         (libmoe.MOE_PATH_DECODE, 64),
+                                         (libmoe.MOE_PATH_PREFILL, 64)])
+def test_split_steps_equal_moe_ffn(path, tile_m):
+    """gate_up, down and combine as separate calls reproduce moe_ffn bit for bit."""
+    w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL["ragged37"])
+    d, ids, wt = _layer_inputs(w)
+    dev_w = gc.upload_weights(d)
+    x, topk_w = gc.to_dev(d["x"]), gc.to_dev(wt)
+    perm = libmoe.moe_permute(gc.to_dev(ids), w.Et, tile_m)
+    whole = libmoe.moe_ffn(x, dev_w["w13"], dev_w["s13"], dev_w["w2"], dev_w["s2"], topk_w, perm,
+                           path=path).clone()
+    ws = libmoe.alloc_workspace(w.T, w.H, w.I, w.Et, w.Kt, tile_m)
+    ws.fill_(0xFF)  # every byte the steps read must be written by an earlier step
+    libmoe.moe_ffn_gate_up(x, dev_w["w13"], dev_w["s13"], perm, ws, path)
+    libmoe.moe_ffn_down(dev_w["w2"], dev_w["s2"], topk_w, perm, ws, w.T, path)
+    _, y = libmoe.ffn_views(ws, w.T, w.H, w.I, w.Et, w.Kt, tile_m)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+    libmoe.moe_combine(y, w.T, w.H, w.Kt, out)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(gc.bf16_dev_to_f64(out), gc.bf16_dev_to_f64(whole))
+    assert np.isfinite(gc.bf16_dev_to_f64(out)).all()
+
+
 # ------------------------------------------------------ prefill (tcgen05)
 
 @pytest.mark.parametrize("name", list(SMALL))
