@@ -390,7 +390,9 @@ def run_ours(args, ws, rank, local):
                     "h2d_bytes_per_step": int(host["logits"].nbytes + host["x"].nbytes),
                     "d2h_bytes_per_step": int(w.T * w.H * 2),
                     "ms_per_step": e2e_ms / K},
-            "gpu_launches": 5 * K,
+            # route, permute, activation prep (decode: rescale x; prefill: gather
+            # rows by tile), gate_up, down, combine
+            "gpu_launches": 6 * K,
             "clocks": clocks,
         }
         if ws == 1 and not args.no_cpu_baseline:

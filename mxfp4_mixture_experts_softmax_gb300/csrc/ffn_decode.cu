@@ -17,20 +17,22 @@
 //   * ldmatrix.x4 hands lane c of every row quad the c-th 32-bit word (8
 //     codes) of a 32-wide scale group, so each pair of m16n8k16 MMAs sees one
 //     scale group per row;
-//   * codes become bf16 by bit placement (E2M1 * 2^-126, exact, e = 0 codes
-//     as bf16 subnormals, which the MMA consumes exactly) -- three integer ops
-//     per two values and no per-element multiply;
-//   * the activations are kept multiplied by 2^64 (exact) so that the
-//     products stay in the fp32 normal range, pair-interleaved to match the
-//     code pairing (prep_act_kernel for x; the gate_up epilogue writes h that
-//     way); a staging warp bulk-copies the tile's rows into a double-buffered
-//     chunk ahead of the consumers; each group's two MMAs go
-//     into a fresh fp32 partial that is added to the accumulator times
-//     2^126 * 2^(s-127) * 2^-64 = 2^(s-65): an exact power-of-two FMA.
-// The MMA's k slots are a fixed permutation of k (a code word yields pairs
-// (0,4),(1,5),(2,6),(3,7)); the staged activations use the same permutation,
-// and a row pitch of 64 bytes past a multiple of 128 keeps the B-fragment
-// loads conflict-free.
+//   * the hardware E2M1 -> f16x2 conversion turns each code byte into two
+//     f16 values (every E2M1 value is exact in f16): one conversion per two
+//     values, against three integer ops for a bit-placed bf16 pair;
+//   * the MMA takes both operands in one type, so the activation rows are
+//     carried as f16 scaled by a power of two per row (rows_to_f16_kernel:
+//     the row's largest magnitude lands in [2^14, 2^15), so every element at
+//     least 2^-29 of it converts exactly and smaller ones are rounded with an
+//     error below 2^-39 of it); the row factor is undone in the epilogue;
+//   * a staging warp bulk-copies the tile's rows into a double-buffered chunk
+//     ahead of the consumers; each group's two MMAs go into a fresh fp32
+//     partial that is added to the accumulator times 2^(s-126), an exact
+//     power-of-two FMA (the 2^-1 left over is folded into the row factor).
+// With consecutive codes converted pairwise, the MMA's k slots of lane c are
+// k = 8c .. 8c+7 of the group, so one 16-byte shared load per n-tile gives
+// both MMAs' B fragments; a row pitch of 64 bytes past a multiple of 128
+// keeps those loads conflict-free.
 #include <algorithm>
 
 #include "moe_internal.h"
@@ -51,7 +53,8 @@ constexpr int kBoxRows = 128;                // rows per TMA box
 constexpr int kStages = 4;
 constexpr int kStageBytes = kRows * kRowBytes;
 constexpr int kXBytes = 32 * 1024;           // one staged activation chunk (two buffers)
-constexpr uint32_t kBf16TwoPow64 = 0x5F805F80u;  // bf16x2 (2^64, 2^64)
+// the group factor is 2^(s-126); the row factor carries the remaining 2^-1
+constexpr float kGroupFactorBias = 0.5f;
 
 template <int NT>
 struct DecodeSmem {
@@ -75,31 +78,24 @@ __device__ __forceinline__ int cta_weight_row(int rho, int block, int I, int row
     return m < rows ? m : -1;
 }
 
-__device__ __forceinline__ uint32_t bf16x2_mul_bits(uint32_t a, uint32_t b) {
-    __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a),
-                               *reinterpret_cast<__nv_bfloat162*>(&b));
-    return *reinterpret_cast<uint32_t*>(&r);
-}
-
-// Eight codes -> four bf16x2 of E2M1 * 2^-126 (see mxfp4_word_to_bf16x2_raw),
-// with the two placement multipliers passed in registers: as runtime values
-// they stay single integer multiply-adds on the FMA pipe instead of being
-// expanded into shift/add sequences on the integer ALU pipe, which the
-// decode kernels saturate.
-__device__ __forceinline__ void codes_to_bf16x2(uint32_t w, uint32_t mul_a, uint32_t mul_b,
-                                                uint32_t out[4]) {
-    const uint32_t hi = w >> 8;
-    out[0] = ((w & 0x000F000Fu) * mul_a) & 0x81C081C0u;
-    out[1] = ((w & 0x00F000F0u) * mul_b) & 0x81C081C0u;
-    out[2] = ((hi & 0x000F000Fu) * mul_a) & 0x81C081C0u;
-    out[3] = ((hi & 0x00F000F0u) * mul_b) & 0x81C081C0u;
+// Eight codes (two per byte, the even k in the low nibble) -> four f16x2:
+// out[i] = (code 2i, code 2i + 1), low half first.
+__device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t out[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+        : "r"(w));
 }
 
 // Persistent kernel: CTA b processes work items b, b + gridDim.x, ... where
 // item = tile * row_blocks + block.  Two helper warps run ahead of the 16
 // consumer warps across items: one streams the weight codes (TMA ring), one
-// stages the tiles' activation rows into a double-buffered chunk (x 2^64,
-// pair-interleaved, swizzled).  Consumers only wait on mbarriers.
+// copies the tiles' f16 activation rows into a double-buffered chunk.
+// Consumers only wait on mbarriers.
 template <int MODE, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const GroupedGemm g, const __grid_constant__ CUtensorMap codes_map) {
@@ -165,8 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kStageWarp) {
         // ------------------------------------------- activation staging
-        // rows of the pre-transformed activations (x 2^64, pair-interleaved:
-        // see prep_act_kernel and the gate_up epilogue) are plain contiguous
+        // the f16 activation rows (rows_to_f16_kernel) are plain contiguous
         // copies: one bulk copy per tile row per chunk
         uint32_t gc = 0;
         for (int item = blockIdx.x; item < items; item += gridDim.x) {
@@ -202,7 +197,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------------------------------------------------- consumers
     const int r = lane >> 2, c = lane & 3;
-    const uint32_t mul_a = g.mul_a, mul_b = g.mul_b;
     const bool scales_vec = (K % kStageK) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 7) == 0);
     const size_t sbytes = (size_t)K / 32;
     // ldmatrix: matrix j = lane / 8 (0: rows r, group 2gp; 1: rows r + 8, group
@@ -279,12 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int gl = 2 * gp + gi;
                         const uint32_t b0 = __byte_perm(gl < 4 ? sc0.x : sc0.y, 0, 0x4440 + (gl & 3));
                         const uint32_t b1 = __byte_perm(gl < 4 ? sc1.x : sc1.y, 0, 0x4440 + (gl & 3));
-                        // 2^(s - 65) as fp32 bits: (s + 62) << 23, by multiply-add
+                        // 2^(s - 126) as fp32 bits: (s + 1) << 23, by multiply-add
                         const float f0 = __uint_as_float(b0 * g.exp_one + g.exp_bias);
                         const float f1 = __uint_as_float(b1 * g.exp_one + g.exp_bias);
                         uint32_t ta[4], tb[4];
-                        codes_to_bf16x2(w[gi ? 2 : 0], mul_a, mul_b, ta);
-                        codes_to_bf16x2(w[gi ? 3 : 1], mul_a, mul_b, tb);
+                        codes_to_f16x2(w[gi ? 2 : 0], ta);
+                        codes_to_f16x2(w[gi ? 3 : 1], tb);
                         const uint32_t xa = xb + xoff + 64u * gl;
 #pragma unroll
                         for (int n = 0; n < NT; ++n) {
@@ -293,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          : "=r"(bv.x), "=r"(bv.y), "=r"(bv.z), "=r"(bv.w)
                                          : "r"(xa + (uint32_t)(n * 8 * L::kPitch)));
                             float t4[4];
-                            mma_bf16_16816_z(t4, ta[0], tb[0], ta[1], tb[1], bv.x, bv.y);
-                            mma_bf16_16816_acc(t4, ta[2], tb[2], ta[3], tb[3], bv.z, bv.w);
+                            mma_f16_16816_z(t4, ta[0], tb[0], ta[1], tb[1], bv.x, bv.y);
+                            mma_f16_16816_acc(t4, ta[2], tb[2], ta[3], tb[3], bv.z, bv.w);
                             acc[n][0] = fmaf(t4[0], f0, acc[n][0]);
                             acc[n][1] = fmaf(t4[1], f0, acc[n][1]);
                             acc[n][2] = fmaf(t4[2], f1, acc[n][2]);
@@ -320,18 +314,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int q = qj[n][u];
                     if (q < 0) continue;
                     if (MODE == 0) {
-                        // h as the down GEMM stages it: x 2^64 (exact), and
-                        // element i of each group of 8 at position 2 (i % 4) + i / 4
-                        if (wr0 >= 0) {
-                            const int col = (wr0 & ~7) | ((wr0 & 3) << 1) | ((wr0 >> 2) & 1);
-                            g.h_out[(size_t)(tile * TM + j) * g.I + col] =
-                                f32_to_bf16_bits(silu(acc[n][u]) * acc[n][2 + u] * 0x1p64f);
-                        }
+                        const float rs = __ldg(g.act_rscale + q / g.Kt) * kGroupFactorBias;
+                        if (wr0 >= 0)
+                            g.h_out[(size_t)(tile * TM + j) * g.I + wr0] =
+                                f32_to_bf16_bits(silu(acc[n][u] * rs) * (acc[n][2 + u] * rs));
                     } else {
                         const float wq = __ldg(g.topk_w + q);
+                        const float rs = __ldg(g.act_rscale + tile * TM + j) * kGroupFactorBias;
                         float* y = g.y_out + (size_t)q * g.rows;
-                        if (wr0 >= 0) y[wr0] = wq * acc[n][u];
-                        if (wr1 >= 0) y[wr1] = wq * acc[n][2 + u];
+                        if (wr0 >= 0) y[wr0] = wq * (acc[n][u] * rs);
+                        if (wr1 >= 0) y[wr1] = wq * (acc[n][2 + u] * rs);
                     }
                 }
             }
@@ -368,19 +360,57 @@ cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
     }
 }
 
-// xt = x * 2^64 (exact for |x| < 2^63), pair-interleaved within each group
-// of 8: the layout the decode GEMM's staging copies verbatim.
-__global__ void __launch_bounds__(256) prep_act_kernel(const uint4* __restrict__ x, size_t n16,
-                                                       uint4* __restrict__ xt) {
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
-         i += (size_t)gridDim.x * blockDim.x) {
-        uint4 v = __ldg(x + i);
-        v.x = bf16x2_mul_bits(v.x, kBf16TwoPow64);
-        v.y = bf16x2_mul_bits(v.y, kBf16TwoPow64);
-        v.z = bf16x2_mul_bits(v.z, kBf16TwoPow64);
-        v.w = bf16x2_mul_bits(v.w, kBf16TwoPow64);
-        xt[i] = pair_interleave8(v);
+// One warp per row: dst[row] = f16(src[row] * 2^sigma) and rscale[row] =
+// 2^-sigma, with sigma = 14 - floor(log2(max |src[row]|)) clamped to
+// [-113, 112] (0 for an all-zero row), so the row's largest magnitude lands
+// in [2^14, 2^15).  bf16 has fewer significant bits than f16, so every
+// element that stays in the f16 normal range converts exactly.  Rows are
+// either all `rows` rows, or (sorted_pairs given) the positions of the used
+// tiles that hold a pair.  src may equal dst: each lane reads its elements
+// before it writes them.
+__global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* src, uint16_t* dst,
+                                                          int cols, int rows,
+                                                          const int32_t* __restrict__ sorted_pairs,
+                                                          const int32_t* __restrict__ num_tiles,
+                                                          int tile_m, float* __restrict__ rscale) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    if (sorted_pairs && (row >= __ldg(num_tiles) * tile_m || __ldg(sorted_pairs + row) < 0)) return;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)row * cols);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + (size_t)row * cols);
+    const int n16 = cols / 8;
+    uint32_t mx = 0;  // max |bf16| bit pattern (orders like the magnitude)
+    for (int i = lane; i < n16; i += 32) {
+        const uint4 v = s4[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    int sigma = 0;
+    if (mx != 0) {
+        // floor(log2) of a bf16 magnitude: its exponent field, or for a
+        // subnormal the position of its top mantissa bit
+        const int ef = (int)(mx >> 7);
+        const int e = ef > 0 ? ef - 127 : (31 - __clz((int)mx)) - 133;
+        sigma = min(max(14 - e, -113), 112);
+    }
+    const float up = __uint_as_float((uint32_t)(127 + sigma) << 23);
+    for (int i = lane; i < n16; i += 32) {
+        const uint4 v = s4[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float lo = __uint_as_float(w[k] << 16) * up;
+            const float hi = __uint_as_float(w[k] & 0xFFFF0000u) * up;
+            const __half2 hv = __floats2half2_rn(lo, hi);
+            o[k] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        d4[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (lane == 0) rscale[row] = __uint_as_float((uint32_t)(127 - sigma) << 23);
 }
 
 // out[t][m] = bf16(sum over j ascending of y[t*Kt + j][m]); four columns per thread.
@@ -413,12 +443,12 @@ bool decode_tile_supported(int tile_m) {
 cudaError_t launch_decode_gate_up(const GroupedGemm& g, cudaStream_t s) { return launch_mode<0>(g, s); }
 cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s) { return launch_mode<1>(g, s); }
 
-cudaError_t launch_prep_act(const uint16_t* x, size_t elems, uint16_t* xt, cudaStream_t s) {
-    const size_t n16 = elems / 8;
-    if (n16 == 0) return cudaSuccess;
-    const int blocks = (int)std::min<size_t>((n16 + 255) / 256, (size_t)num_sms() * 8);
-    prep_act_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), n16,
-                                           reinterpret_cast<uint4*>(xt));
+cudaError_t launch_rows_to_f16(const uint16_t* src, uint16_t* dst, int cols, int rows,
+                               const int32_t* sorted_pairs, const int32_t* num_tiles, int tile_m,
+                               float* rscale, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    rows_to_f16_kernel<<<(rows + 7) / 8, 256, 0, s>>>(src, dst, cols, rows, sorted_pairs,
+                                                      num_tiles, tile_m, rscale);
     return cudaGetLastError();
 }
 

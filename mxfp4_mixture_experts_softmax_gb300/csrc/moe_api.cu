@@ -195,10 +195,16 @@ static size_t act_bytes(int64_t cap, int T, int H, int tile_m) {
     return b;
 }
 
+// the decode path's row factors (T for x, then cap for h) after the activations
+static size_t rs_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) {
+    return xg_offset(cap, T, H, I, Kt) + act_bytes(cap, T, H, tile_m);
+}
+
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m) {
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     if (cap < 0 || H <= 0 || I <= 0) return 0;
-    return xg_offset(cap, T, H, I, Kt) + act_bytes(cap, T, H, tile_m);
+    const size_t rs = decode_tile_supported(tile_m) ? round_up((size_t)(T + cap) * sizeof(float), 256) : 0;
+    return rs_offset(cap, T, H, I, Kt, tile_m) + rs;
 }
 
 moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m) {
@@ -288,15 +294,21 @@ moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_
     g.h_out = reinterpret_cast<uint16_t*>(workspace);
     cudaError_t err;
     if (path == MOE_PATH_DECODE) {
-        // x * 2^64, pair-interleaved: the staging layout of the decode GEMM
-        uint16_t* xt = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(workspace) +
-                                                   xg_offset(cap, T, H, I, Kt));
-        err = launch_prep_act(x, (size_t)T * H, xt, stream);
+        // the decode GEMMs take f16 B rows scaled per row: x here, and h (in
+        // place) once the GEMM has written it
+        char* ws = reinterpret_cast<char*>(workspace);
+        uint16_t* xt = reinterpret_cast<uint16_t*>(ws + xg_offset(cap, T, H, I, Kt));
+        float* rs_x = reinterpret_cast<float*>(ws + rs_offset(cap, T, H, I, Kt, tile_m));
+        err = launch_rows_to_f16(x, xt, H, T, nullptr, nullptr, tile_m, rs_x, stream);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         g.act = xt;
+        g.act_rscale = rs_x;
         g.act_rows = T;
         g.act_by_token = 1;
         err = launch_decode_gate_up(g, stream);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        err = launch_rows_to_f16(g.h_out, g.h_out, I, (int)cap, sorted_pairs, num_tiles, tile_m,
+                                 rs_x + T, stream);
     } else {
         // the prefill GEMM reads its token rows as one box per stage: gather
         // them into tile order first
@@ -331,6 +343,8 @@ moe_status_t moe_ffn_down(const uint8_t* w2, const uint8_t* s2, const float* top
     g.rows = H;
     g.K = I;
     g.act = reinterpret_cast<const uint16_t*>(workspace);
+    g.act_rscale = reinterpret_cast<const float*>(reinterpret_cast<const char*>(workspace) +
+                                                  rs_offset(cap, T, H, I, Kt, tile_m)) + T;
     g.act_rows = (int)cap;
     g.act_by_token = 0;
     g.y_out = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + y_offset(cap, I));

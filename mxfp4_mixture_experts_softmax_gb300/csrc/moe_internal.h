@@ -40,7 +40,9 @@ struct GroupedGemm {
     const uint8_t* scales;       // [Et][rows][K/32]
     int rows;                    // weight rows per expert (2I for gate_up, H for down)
     int K;                       // reduction length (H for gate_up, I for down)
-    const uint16_t* act;         // bf16 B rows: x [T][H] (gate_up) or h [cap][I] (down)
+    const uint16_t* act;         // B rows: x [T][H] (gate_up) or h [cap][I] (down); bf16,
+                                 // or f16 scaled per row (decode path)
+    const float* act_rscale;     // decode path: factor undoing each act row's scaling
     int act_by_token;            // 1: B row = token q / Kt of the pair; 0: B row = sorted position
     const int32_t* sorted_pairs;
     const int32_t* tile_expert;
@@ -54,9 +56,9 @@ struct GroupedGemm {
     uint16_t* h_out;             // SwiGLU output h [cap][I] (bf16)
     float* y_out;                // weighted output [T*Kt][H] (fp32)
     const float* topk_w;
-    // constants the decode kernels take as runtime values (see codes_to_bf16x2)
-    uint32_t mul_a = 0x1040u, mul_b = 0x0104u;  // 2^6 + 2^12, 2^2 + 2^8
-    uint32_t exp_one = 1u << 23, exp_bias = 62u << 23;
+    // decode group factor 2^(s-126) as fp32 bits s * exp_one + exp_bias,
+    // taken as runtime values so the multiply-add stays one instruction
+    uint32_t exp_one = 1u << 23, exp_bias = 1u << 23;
 };
 
 // Streaming multiprocessors of the current device (cached per device).
@@ -67,8 +69,12 @@ bool prefill_tile_supported(int tile_m);
 bool prefill_shape_supported(int H, int I);
 
 cudaError_t launch_decode_gate_up(const GroupedGemm& g, cudaStream_t s);
-// xt = x * 2^64, pair-interleaved within groups of 8 (the decode staging layout).
-cudaError_t launch_prep_act(const uint16_t* x, size_t elems, uint16_t* xt, cudaStream_t s);
+// dst[row] = f16(src[row] * 2^sigma_row), rscale[row] = 2^-sigma_row (the
+// decode GEMMs' B rows); every row, or with sorted_pairs the used positions
+// that hold a pair.  src may equal dst.
+cudaError_t launch_rows_to_f16(const uint16_t* src, uint16_t* dst, int cols, int rows,
+                               const int32_t* sorted_pairs, const int32_t* num_tiles, int tile_m,
+                               float* rscale, cudaStream_t s);
 cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_prefill_gate_up(const GroupedGemm& g, cudaStream_t s);
 // xg[p] = x[sorted_pairs[p] / Kt] for the rows of the used tiles (0 for pads).

@@ -39,7 +39,9 @@ def ffn_parity(gpu: np.ndarray, ref: np.ndarray, what: str = "") -> dict:
     rms = float(np.sqrt(np.mean(ref ** 2)))
     err = np.abs(gpu - ref)
     bound = FFN_ELEM_TOL * (np.abs(ref) + rms)
-    worst = float((err / bound).max()) if err.size else 0.0
+    # where the bound is 0 (an all-zero reference) only an exact 0 passes
+    ratio = np.divide(err, bound, out=np.where(err > 0, np.inf, 0.0), where=bound > 0)
+    worst = float(ratio.max()) if err.size else 0.0
     rel_l2 = float(np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-300))
     stats = dict(worst_elem_ratio=worst, rel_l2=rel_l2, identical=float((gpu == ref).mean()))
     assert worst <= 1.0, f"{what}: element error {worst:.3g} x bound {stats}"

@@ -158,6 +158,28 @@ def test_ffn_scale_bytes_above_128():
     gc.ffn_parity(_gpu_ffn(d, ids, wt, w.Et, 8, libmoe.MOE_PATH_DECODE), ref, "big scales")
 
 
+@pytest.mark.parametrize("path,tile_m", [(libmoe.MOE_PATH_DECODE, 8), (libmoe.MOE_PATH_PREFILL, 32)])
+def test_ffn_activation_dynamic_range(path, tile_m):
+    """Token rows scaled by 2^-30 .. 2^30, an all-zero row and a row with one
+    element 2^40 above the rest: each output row meets the bar on its own
+    scale (the decode path re-encodes rows as f16 with a per-row factor)."""
+    w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL["ragged37"])
+    d, ids, wt = _layer_inputs(w)
+    xf = gc.bits_to_f64(d["x"])
+    exps = np.resize(np.array([-30, -12, 0, 9, 30]), w.T)
+    xf *= np.exp2(exps)[:, None]
+    xf[3] = 0.0
+    xf[7, 5] = 2.0 ** 40
+    d["x"] = (xf.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)  # exact: powers of two
+    assert np.array_equal(gc.bits_to_f64(d["x"]), xf)
+    ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt,
+                                    n_threads=THREADS))
+    got = _gpu_ffn(d, ids, wt, w.Et, tile_m, path)
+    assert (got[3] == 0).all() and (ref[3] == 0).all()
+    for t in range(w.T):
+        gc.ffn_parity(got[t], ref[t], f"row {t} (x scaled 2^{exps[t]})")
+
+
 def test_ffn_w2_scale_increment_doubles_exactly():
     w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL["ragged37"])
     d, ids, wt = _layer_inputs(w)
