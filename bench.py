@@ -390,9 +390,10 @@ def run_ours(args, ws, rank, local):
                     "h2d_bytes_per_step": int(host["logits"].nbytes + host["x"].nbytes),
                     "d2h_bytes_per_step": int(w.T * w.H * 2),
                     "ms_per_step": e2e_ms / K},
-            # route, permute, activation prep (decode: rescale x; prefill: gather
-            # rows by tile), gate_up, down, combine
-            "gpu_launches": 6 * K,
+            # decode: route, permute, x -> f16 rows, gate_up, h -> f16 rows, down,
+            # combine; prefill: route, permute, gather rows by tile, gate_up,
+            # down, combine
+            "gpu_launches": (7 if path_name == "decode" else 6) * K,
             "clocks": clocks,
         }
         if ws == 1 and not args.no_cpu_baseline:

@@ -8,24 +8,7 @@
 
 namespace moe {
 
-// ----------------------------------------------------------------- loads
-
-// 16-byte streaming load of weight bytes: read once per launch, so keep them
-// out of L1 (they still pass through L2, where concurrent tiles of the same
-// expert can share them).
-__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t ldg_stream_u16(const void* p) {
-    unsigned short r;
-    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
-    return r;
-}
+// ----------------------------------------------------------------- lanes
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
@@ -85,18 +68,6 @@ __device__ __forceinline__ void bf16x2_scale(uint32_t out[4], uint32_t mult) {
     }
 }
 
-// ----------------------------------------------------------- tensor cores
-
-// D = A * B + C, m16n8k16, bf16 inputs, fp32 accumulate (legacy warp MMA).
-__device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0,
-                                               uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // ------------------------------------------------------------- numerics
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
@@ -104,19 +75,6 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
     __nv_bfloat16 b = __float2bfloat16_rn(f);
     return *reinterpret_cast<uint16_t*>(&b);
-}
-
-// Activation layout in shared memory: each group of 8 consecutive bf16
-// elements x0..x7 is stored as (x0,x4),(x1,x5),(x2,x6),(x3,x7), matching the
-// code pairing of mxfp4_word_to_bf16x2, so that one 16-byte load yields the
-// two B fragments of the two MMAs fed by one code word.
-__device__ __forceinline__ uint4 pair_interleave8(uint4 v) {
-    uint4 r;
-    r.x = __byte_perm(v.x, v.z, 0x5410);
-    r.y = __byte_perm(v.x, v.z, 0x7632);
-    r.z = __byte_perm(v.y, v.w, 0x5410);
-    r.w = __byte_perm(v.y, v.w, 0x7632);
-    return r;
 }
 
 // ------------------------------------------------ async copies, mbarriers
@@ -224,32 +182,6 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t r[4]) {
                  : "r"(addr));
 }
 
-// Named barrier among `count` threads (a subset of the CTA).
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// D = A * B with a zero accumulator (m16n8k16, bf16 in, fp32 out).
-__device__ __forceinline__ void mma_bf16_16816_z(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                                 uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
-}
-
-// D += A * B (m16n8k16, bf16 in, fp32 accumulate).
-__device__ __forceinline__ void mma_bf16_16816_acc(float d[4], uint32_t a0, uint32_t a1,
-                                                   uint32_t a2, uint32_t a3, uint32_t b0,
-                                                   uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // D = A * B with a zero accumulator (m16n8k16, f16 in, fp32 out).
 __device__ __forceinline__ void mma_f16_16816_z(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                 uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -269,18 +201,6 @@ __device__ __forceinline__ void mma_f16_16816_acc(float d[4], uint32_t a0, uint3
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Eight E2M1 codes -> four bf16x2 of value E2M1 * 2^-126 (exact; the e = 0
-// codes are bf16 subnormals), paired as in mxfp4_word_to_bf16x2 but without
-// the scale multiply: the caller applies 2^126 * 2^(s-127) to the fp32
-// partial sums instead.
-__device__ __forceinline__ void mxfp4_word_to_bf16x2_raw(uint32_t w, uint32_t out[4]) {
-    const uint32_t hi = w >> 8;
-    out[0] = ((w & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
-    out[1] = ((w & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
-    out[2] = ((hi & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
-    out[3] = ((hi & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
 }
 
 }  // namespace moe
