@@ -130,11 +130,9 @@ moe_status_t moe_permute(const int32_t* topk_ids, int T, int Kt, int Et, int til
 /*
  * moe_ffn_workspace_size -- bytes of device workspace moe_ffn needs:
  * the 16-bit SwiGLU intermediate [cap, I], the weighted fp32 per-pair expert
- * outputs [T*Kt, H], an activation area (room for the tile-ordered bf16
- * activations [cap, H] when tile_m is a prefill tile height (32, 64, 128,
- * 256), for the decode path's f16 copy of x [T, H] when tile_m is a decode
- * tile height (8, 16, 32, 64), the larger of the two when both) and, for
- * decode tile heights, T + cap fp32 row factors; each 256-byte aligned.
+ * outputs [T*Kt, H], x as f16 rows [T, H], when tile_m is a prefill tile
+ * height (32, 64, 128, 256) their tile-ordered copy [cap, H], and T + cap
+ * fp32 row factors; each 256-byte aligned.
  */
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
 
@@ -155,15 +153,18 @@ size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
  *   g = W_gate[e] x_t, u = W_up[e] x_t (fp32 accumulation of exact
  *   products), h = bf16(silu(g) * u), y = W2[e] h (fp32);
  *   out_t = bf16(sum over j ascending of topk_w[t, j] * y_tj).
- * The decode path carries x and h as f16 scaled per row by a power of two
- * (largest magnitude in [2^14, 2^15)): elements at least 2^-29 of their
- * row's largest magnitude stay exact, smaller ones move by less than 2^-39
- * of it.  The prefill path carries them as bf16.
+ * Both paths carry x and h into the MMAs as f16 scaled per row by a power
+ * of two (largest magnitude in [2^14, 2^15)): elements at least 2^-29 of
+ * their row's largest magnitude stay exact, smaller ones move by less than
+ * 2^-39 of it.
  * Result tolerance against the plain fp32 definition: per element
  * |out - ref| <= 1e-2 * (|ref| + rms(ref)) and relative L2 error <= 2e-3
  * (the GEMM summation order differs; SwiGLU bf16 roundings may flip by 1 ulp).
- * Weights are exact: every E2M1 value times its E8M0 scale is applied
- * exactly for scale bytes 7..247 (2^-120..2^120).
+ * Weights are exact: the decode path applies each E8M0 scale as an exact
+ * power-of-two factor for scale bytes 7..247 (2^-120..2^120); the prefill
+ * path stores each weight row in f16 relative to its largest scale, exact
+ * for every group whose scale is within 2^36 of that largest (groups further
+ * below are rounded, at most 2^-37 of the row's largest weight).
  * Limits: H % 32 == 0, I % 32 == 0, H, I <= 65536, tile_m % 8 == 0 and
  * tile_m <= 64 for the decode path; the prefill path needs tile_m in
  * {32, 64, 128}.  Pointers 16-byte aligned.
@@ -188,17 +189,15 @@ moe_status_t moe_ffn_path(const uint16_t* x, const uint8_t* w13, const uint8_t* 
  * The three steps of moe_ffn as separate calls; moe_ffn runs exactly these,
  * in this order, on one workspace (at least moe_ffn_workspace_size() bytes):
  *   h  [cap, I] at byte 0, y fp32 [T*Kt, H] at moe_ffn_y_offset(), then
- *   the activation area (the prefill gate_up's tile-ordered copy of the
- *   activations, or the decode gate_up's f16 copy of x) and the decode
- *   path's row factors.
+ *   the activation area (x as scaled f16 rows, and for prefill tile heights
+ *   their tile-ordered copy) and the fp32 row factors of x and of h.
  * `path` must resolve to the same path for both GEMM calls (AUTO always does
- * for the same sizes): the encoding of h is the path's own.
+ * for the same sizes).
  *
  * moe_ffn_gate_up: h[p, n] = bf16(silu(g) * u) for every sorted position p
- *   that holds a pair (pads are not written).  The prefill path stores h as
- *   bf16; the decode path then re-encodes each row in place as f16 times a
- *   power of two per row (the row factors after the activation area), the
- *   form its down GEMM reads.
+ *   that holds a pair (pads are not written), then each such row re-encoded
+ *   in place as f16 times a power of two per row (the row factors after the
+ *   activation area), the form the down GEMMs read.
  * moe_ffn_down:    y[q, m] = topk_w[q] * (W2[e] h_p)[m] for every pair q at
  *   position p (the routing-weighted expert outputs).
  * moe_combine:     out[t, m] = bf16(sum over j = 0..Kt-1, ascending, of

@@ -13,10 +13,15 @@
 //     stage, prefetched into L2 ahead of the ring) and of the tile's token
 //     rows as one box in the 128-byte swizzled K-major layout the MMA reads
 //     (gate_up reads x gathered into tile order by gather_rows_kernel, down
-//     reads h, which is already in tile order);
-//   * 16 converter warps: exact bf16 dequantisation of the codes (E2M1 bit
-//     placement times 2^126 * 2^(s-127) by one bf16x2 multiply) into the
-//     stage's A buffer, same swizzled layout;
+//     reads h, which is already in tile order); both are f16 rows scaled per
+//     row by a power of two (rows_to_f16_kernel), the factor undone in the
+//     epilogue;
+//   * 16 converter warps: dequantisation of the codes into the stage's A
+//     buffer (same swizzled layout) by the hardware E2M1 -> f16x2 conversion
+//     and one f16x2 multiply by 2^(s - s_ref); s_ref = max(s) - 13 over the
+//     weight row, so the row's values fit f16 (largest 6 * 2^13) and every
+//     group within 2^36 of the row's largest scale stays exact; 2^(s_ref -
+//     127) is applied per row in the epilogue;
 //   * MMA warp: one thread issues the four K = 16 tcgen05.mma of each stage
 //     into the item's tensor-memory accumulator and commits them to the
 //     stage's mbarrier, which frees the stage;
@@ -42,7 +47,6 @@ constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;  // 18..21: warp % 4 covers e
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 704
 constexpr int kBK = 64;                                   // k per stage (one 128-byte bf16 row)
-constexpr int kStages = 4;
 constexpr int kABytes = 128 * kBK * 2;                    // 16 KB bf16 A stage
 constexpr int kCodeBytes = 128 * (kBK / 2);               // 4 KB packed codes stage
 constexpr int kCodeBox = 64;                              // rows per codes box
@@ -67,13 +71,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
     return d;
 }
 
-// Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor: f16 x f16 -> fp32 (a and b format fields 0), both
+// operands K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -100,10 +104,64 @@ __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t* r) {
 }
 
 
+// Largest E8M0 byte of a weight row's K/32 scales, read by `parts` threads
+// (part = 0..parts-1) that each take every parts-th 16-byte chunk (vec) or
+// byte; the caller combines the parts.
+__device__ __forceinline__ uint32_t row_scale_max_part(const uint8_t* sp, int ngroups, bool vec,
+                                                       int part, int parts) {
+    uint32_t m = 0;
+    if (vec) {
+        for (int c = part; c < ngroups / 16; c += parts) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(sp) + c);
+            m = __vmaxu4(m, __vmaxu4(__vmaxu4(v.x, v.y), __vmaxu4(v.z, v.w)));
+        }
+        m = __vmaxu4(m, m >> 16);
+        m = __vmaxu4(m, m >> 8);
+        return m & 0xFFu;
+    }
+    for (int i = part; i < ngroups; i += parts) m = max(m, (uint32_t)__ldg(sp + i));
+    return m;
+}
+
+// The row's reference exponent: its values are stored as f16 times 2^(s -
+// s_ref), at most 6 * 2^13.
+__device__ __forceinline__ int row_scale_ref(uint32_t smax) { return max((int)smax - 13, 1); }
+
+// f16x2 (2^e, 2^e) for the group scale s: e = s - s_ref <= 13; below 2^-24 it
+// rounds to zero (groups more than 2^36 under the row's largest).
+__device__ __forceinline__ uint32_t f16_group_mult(uint32_t s, int s_ref) {
+    const int e = min(max((int)s - s_ref, -30), 13);
+    const __half h = __float2half_rn(__uint_as_float((uint32_t)(e + 127) << 23));
+    return (uint32_t)__half_as_ushort(h) * 0x00010001u;
+}
+
+// Eight codes (two per byte, the even k in the low nibble) -> four f16x2
+// (k0,k1), (k2,k3), (k4,k5), (k6,k7), each multiplied by `mult`.
+__device__ __forceinline__ uint4 codes_to_f16x8(uint32_t w, uint32_t mult) {
+    uint32_t r0, r1, r2, r3;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+        : "r"(w));
+    uint4 v;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v.x) : "r"(r0), "r"(mult));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v.y) : "r"(r1), "r"(mult));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v.z) : "r"(r2), "r"(mult));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v.w) : "r"(r3), "r"(mult));
+    return v;
+}
+
 template <int N>
 struct PrefillSmem {
     static constexpr int kBBytes = N * kBK * 2;
     static constexpr int kStage = kABytes + kBBytes + kCodeBytes;  // multiple of 1024
+    // as many stages as fit: narrow tiles spend little time per stage in the
+    // MMA, so the ring has to cover the load latency with more of them
+    static constexpr int kStages = N <= 32 ? 8 : N <= 64 ? 7 : N <= 128 ? 6 : 4;
     static constexpr int kBars = kStages * kStage;
     static constexpr int kTotal = kBars + 256 + 1024;              // + alignment slack
 };
@@ -113,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_gemm_kernel(const GroupedGemm g, const __grid_constant__ CUtensorMap codes_map,
                         const __grid_constant__ CUtensorMap act_map) {
     using L = PrefillSmem<N>;
+    constexpr int kStages = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L::kBars);  // codes + B landed
@@ -203,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(128, N);
+            constexpr uint32_t idesc = idesc_f16(128, N);
             uint32_t gs = 0, it = 0;
             bool ok = true;
             for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++it) {
@@ -224,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd = sdesc_sw128(smem_u32(stage_b(s)));
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)  // +32 bytes per K = 16 inside the swizzle atom
-                        mma_bf16_ss(d_tmem, ad + 2u * k, bd + 2u * k, idesc, (st | k) != 0 ? 1u : 0u);
+                        mma_f16_ss(d_tmem, ad + 2u * k, bd + 2u * k, idesc, (st | k) != 0 ? 1u : 0u);
                     mma_commit(&stage_free[s]);
                 }
                 if (ok) mma_commit(&acc_full[b]);
@@ -255,15 +314,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rvalid = wrow < g.rows;
             }
             const uint8_t* sp = g.scales + ((size_t)e * g.rows + (rvalid ? wrow : 0)) * (size_t)(K / 32);
+            // the row's reference exponent: its four threads split the scan
+            uint32_t smax = rvalid ? row_scale_max_part(sp, K / 32, svec, qh, 4) : 0u;
+            smax = max(smax, __shfl_xor_sync(0xFFFFFFFFu, smax, 1));
+            smax = max(smax, __shfl_xor_sync(0xFFFFFFFFu, smax, 2));
+            const int s_ref = row_scale_ref(smax);
             // scale bytes arrive 16 at a time (8 stages x 2 groups), one block
             // ahead, so their load latency never sits on a stage
             auto load_sblock = [&](int blk) {
                 const int g0 = blk * 16;
-                if (!rvalid || g0 * 32 >= K) return make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+                if (!rvalid || g0 * 32 >= K) return make_uint4(0, 0, 0, 0);
                 if (svec) return __ldg(reinterpret_cast<const uint4*>(sp + g0));
-                uint32_t b[4] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu};
+                uint32_t b[4] = {0, 0, 0, 0};
                 for (int i = 0; i < 16 && (g0 + i) * 32 < K; ++i)
-                    b[i >> 2] = (b[i >> 2] & ~(0xFFu << (8 * (i & 3)))) | ((uint32_t)__ldg(sp + g0 + i) << (8 * (i & 3)));
+                    b[i >> 2] |= (uint32_t)__ldg(sp + g0 + i) << (8 * (i & 3));
                 return make_uint4(b[0], b[1], b[2], b[3]);
             };
             uint4 sblk = load_sblock(0), nblk = load_sblock(1);
@@ -275,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int gi = 2 * (st & 7) + h;  // group within the 16-group block
                 const uint32_t word = (gi < 8) ? ((gi < 4) ? sblk.x : sblk.y) : ((gi < 12) ? sblk.z : sblk.w);
-                const uint32_t sc = (word >> (8 * (gi & 3))) & 0xFFu;
+                const uint32_t mult = f16_group_mult((word >> (8 * (gi & 3))) & 0xFFu, s_ref);
                 if (!mbar_wait(&raw_full[s], (gs / kStages) & 1)) {
                     ok = false;
                     break;
@@ -284,19 +348,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
                              : "=r"(cw.x), "=r"(cw.y)
                              : "r"(smem_u32(stage_c(s)) + crow * (kBK / 2) + 8 * qh));
-                const uint32_t mlo = e8m0_mult_lo(sc);
-                const uint32_t w2[2] = {cw.x, cw.y};
                 const uint32_t arow = smem_u32(stage_a(s)) + rho * 128;
+                const uint32_t w2[2] = {cw.x, cw.y};
 #pragma unroll
                 for (int i2 = 0; i2 < 2; ++i2) {
-                    uint32_t d[4];
-                    mxfp4_word_to_bf16x2(w2[i2], mlo, d);
-                    if (sc > 128u) bf16x2_scale(d, e8m0_mult_hi(sc));
-                    uint4 v;
-                    v.x = __byte_perm(d[0], d[1], 0x5410);  // (k0, k1)
-                    v.y = __byte_perm(d[2], d[3], 0x5410);  // (k2, k3)
-                    v.z = __byte_perm(d[0], d[1], 0x7632);  // (k4, k5)
-                    v.w = __byte_perm(d[2], d[3], 0x7632);  // (k6, k7)
+                    const uint4 v = codes_to_f16x8(w2[i2], mult);
                     const int ch = 2 * qh + i2;
                     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
                                      arow + ((ch ^ (rho & 7)) << 4)),
@@ -312,19 +368,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------------- epilogue
         const int quad = warp & 3;  // tensor-memory lanes 32*quad .. 32*quad + 31
         const int r = 32 * quad + lane;
+        const bool svec = (K % 512) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 15) == 0);
         uint32_t it = 0;
         for (int item = blockIdx.x; item < items; item += gridDim.x, ++it) {
             const int tile = item / row_blocks, block = item % row_blocks;
+            const int e = __ldg(g.tile_expert + tile);
             const uint32_t b = it & 1;
-            // the tile's pair indices (and routing weights) once per item:
-            // column j lives in lane j % 32 of register j / 32
+            // this lane's weight row (accumulator lane r holds A row r) and its
+            // factor 2^(s_ref - 127), the part of the scales the converters
+            // left out
+            int wrow;
+            bool rvalid;
+            if (MODE == 0) {
+                const int n = block * 64 + (r >> 1);
+                rvalid = n < g.I;
+                wrow = (r & 1) ? g.I + n : n;
+            } else {
+                wrow = block * 128 + r;
+                rvalid = wrow < g.rows;
+            }
+            const uint8_t* sp = g.scales + ((size_t)e * g.rows + (rvalid ? wrow : 0)) * (size_t)(K / 32);
+            const float fr = __uint_as_float(
+                (uint32_t)row_scale_ref(rvalid ? row_scale_max_part(sp, K / 32, svec, 0, 1) : 0u) << 23);
+            // the tile's pair indices and column factors once per item:
+            // column j lives in lane j % 32 of register j / 32.  The column
+            // factor undoes the B row's scaling (per token for x, per
+            // position for h) and, in the down GEMM, includes the routing weight.
             constexpr int kQ = N / 32;
             int qv[kQ];
-            float wv[kQ];
+            float cv[kQ];
 #pragma unroll
             for (int u = 0; u < kQ; ++u) {
-                qv[u] = __ldg(g.sorted_pairs + tile * N + 32 * u + lane);
-                wv[u] = (MODE == 1 && qv[u] >= 0) ? __ldg(g.topk_w + qv[u]) : 0.0f;
+                const int p = tile * N + 32 * u + lane;
+                qv[u] = __ldg(g.sorted_pairs + p);
+                cv[u] = qv[u] < 0 ? 0.0f
+                        : MODE == 0 ? __ldg(g.act_rscale + qv[u] / g.Kt)
+                                    : __ldg(g.topk_w + qv[u]) * __ldg(g.act_rscale + p);
             }
             if (!mbar_wait(&acc_full[b], (it >> 1) & 1)) break;
             tc_fence_after();
@@ -337,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld16_nowait(taddr + 16, v + 16);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                 const int q_lo = qv[c0 / 32];
+                const float c_lo = cv[c0 / 32];
                 if (MODE == 0) {
                     // lane 2i holds gate row i, lane 2i+1 up row i: after one
                     // exchange per column pair the even lane owns column j and
@@ -345,23 +425,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool odd = lane & 1;
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
-                        const float a0 = __uint_as_float(v[i]), a1 = __uint_as_float(v[i + 1]);
+                        const float a0 = __uint_as_float(v[i]) * fr, a1 = __uint_as_float(v[i + 1]) * fr;
                         const float other = __shfl_xor_sync(0xFFFFFFFFu, odd ? a0 : a1, 1);
                         const int j = c0 + i + (odd ? 1 : 0);
                         const float gate = odd ? other : a0;   // even: own gate j; odd: partner's gate j+1
                         const float up = odd ? a1 : other;     // even: partner's up j; odd: own up j+1
                         const int q = __shfl_sync(0xFFFFFFFFu, q_lo, j & 31);
+                        const float fc = __shfl_sync(0xFFFFFFFFu, c_lo, j & 31);
                         if (n < g.I && q >= 0)
-                            g.h_out[(size_t)(tile * N + j) * g.I + n] = f32_to_bf16_bits(silu(gate) * up);
+                            g.h_out[(size_t)(tile * N + j) * g.I + n] =
+                                f32_to_bf16_bits(silu(gate * fc) * (up * fc));
                     }
                 } else {
-                    const float w_lo = wv[c0 / 32];
                     const int m = block * 128 + r;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int q = __shfl_sync(0xFFFFFFFFu, q_lo, i);
-                        const float wq = __shfl_sync(0xFFFFFFFFu, w_lo, i);
-                        if (m < g.rows && q >= 0) g.y_out[(size_t)q * g.rows + m] = wq * __uint_as_float(v[i]);
+                        const float fc = __shfl_sync(0xFFFFFFFFu, c_lo, i);
+                        if (m < g.rows && q >= 0)
+                            g.y_out[(size_t)q * g.rows + m] = fc * (__uint_as_float(v[i]) * fr);
                     }
                 }
             }
@@ -392,7 +474,7 @@ cudaError_t launch_n(const GroupedGemm& g, cudaStream_t s) {
                         CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
     // activations in tile order (gathered x for gate_up, h for down): N rows per box
-    err = encode_2d_map(&act_map, g.act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.K, (uint64_t)g.act_rows,
+    err = encode_2d_map(&act_map, g.act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g.K, (uint64_t)g.act_rows,
                         (uint64_t)g.K * 2, kBK, N, CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
     const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;

@@ -184,27 +184,26 @@ moe_status_t moe_permute(const int32_t* topk_ids, int T, int Kt, int Et, int til
 
 static size_t y_offset(int64_t cap, int I) { return round_up((size_t)cap * I * sizeof(uint16_t), 256); }
 
-static size_t xg_offset(int64_t cap, int T, int H, int I, int Kt) {
+// After y: x as scaled f16 rows [T, H] (both paths), the prefill path's
+// tile-ordered copy of them [cap, H] (prefill tile heights only), and the
+// fp32 row factors of x [T] and of h [cap].
+static size_t x16_offset(int64_t cap, int T, int H, int I, int Kt) {
     return y_offset(cap, I) + round_up((size_t)T * Kt * H * sizeof(float), 256);
 }
 
-// the gathered activations (prefill) or the transformed x (decode) after y
-static size_t act_bytes(int64_t cap, int T, int H, int tile_m) {
-    size_t b = decode_tile_supported(tile_m) ? round_up((size_t)T * H * sizeof(uint16_t), 256) : 0;
-    if (prefill_tile_supported(tile_m)) b = std::max(b, round_up((size_t)cap * H * sizeof(uint16_t), 256));
-    return b;
+static size_t xg_offset(int64_t cap, int T, int H, int I, int Kt) {
+    return x16_offset(cap, T, H, I, Kt) + round_up((size_t)T * H * sizeof(uint16_t), 256);
 }
 
-// the decode path's row factors (T for x, then cap for h) after the activations
 static size_t rs_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) {
-    return xg_offset(cap, T, H, I, Kt) + act_bytes(cap, T, H, tile_m);
+    const size_t xg = prefill_tile_supported(tile_m) ? round_up((size_t)cap * H * sizeof(uint16_t), 256) : 0;
+    return xg_offset(cap, T, H, I, Kt) + xg;
 }
 
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m) {
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     if (cap < 0 || H <= 0 || I <= 0) return 0;
-    const size_t rs = decode_tile_supported(tile_m) ? round_up((size_t)(T + cap) * sizeof(float), 256) : 0;
-    return rs_offset(cap, T, H, I, Kt, tile_m) + rs;
+    return rs_offset(cap, T, H, I, Kt, tile_m) + round_up((size_t)(T + cap) * sizeof(float), 256);
 }
 
 moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m) {
@@ -292,35 +291,33 @@ moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_
     g.rows = 2 * I;
     g.K = H;
     g.h_out = reinterpret_cast<uint16_t*>(workspace);
-    cudaError_t err;
+    // both GEMMs take f16 B rows scaled per row by a power of two: x here,
+    // and h (in place) once the GEMM has written it
+    char* ws = reinterpret_cast<char*>(workspace);
+    uint16_t* x16 = reinterpret_cast<uint16_t*>(ws + x16_offset(cap, T, H, I, Kt));
+    float* rs_x = reinterpret_cast<float*>(ws + rs_offset(cap, T, H, I, Kt, tile_m));
+    cudaError_t err = launch_rows_to_f16(x, x16, H, T, nullptr, nullptr, tile_m, rs_x, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    g.act_rscale = rs_x;  // indexed by token
     if (path == MOE_PATH_DECODE) {
-        // the decode GEMMs take f16 B rows scaled per row: x here, and h (in
-        // place) once the GEMM has written it
-        char* ws = reinterpret_cast<char*>(workspace);
-        uint16_t* xt = reinterpret_cast<uint16_t*>(ws + xg_offset(cap, T, H, I, Kt));
-        float* rs_x = reinterpret_cast<float*>(ws + rs_offset(cap, T, H, I, Kt, tile_m));
-        err = launch_rows_to_f16(x, xt, H, T, nullptr, nullptr, tile_m, rs_x, stream);
-        if (err != cudaSuccess) return MOE_ERR_CUDA;
-        g.act = xt;
-        g.act_rscale = rs_x;
+        g.act = x16;
         g.act_rows = T;
         g.act_by_token = 1;
         err = launch_decode_gate_up(g, stream);
-        if (err != cudaSuccess) return MOE_ERR_CUDA;
-        err = launch_rows_to_f16(g.h_out, g.h_out, I, (int)cap, sorted_pairs, num_tiles, tile_m,
-                                 rs_x + T, stream);
     } else {
         // the prefill GEMM reads its token rows as one box per stage: gather
         // them into tile order first
-        uint16_t* xg = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(workspace) +
-                                                   xg_offset(cap, T, H, I, Kt));
-        err = launch_gather_rows(x, H, sorted_pairs, num_tiles, tile_m, Kt, (int)cap, xg, stream);
+        uint16_t* xg = reinterpret_cast<uint16_t*>(ws + xg_offset(cap, T, H, I, Kt));
+        err = launch_gather_rows(x16, H, sorted_pairs, num_tiles, tile_m, Kt, (int)cap, xg, stream);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         g.act = xg;
         g.act_rows = (int)cap;
         g.act_by_token = 0;
         err = launch_prefill_gate_up(g, stream);
     }
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    err = launch_rows_to_f16(g.h_out, g.h_out, I, (int)cap, sorted_pairs, num_tiles, tile_m,
+                             rs_x + T, stream);
     return cuda_status(err);
 }
 

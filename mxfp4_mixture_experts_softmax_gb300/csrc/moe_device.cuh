@@ -16,58 +16,6 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
-// ------------------------------------------------------------ MXFP4 decode
-
-// Eight E2M1 codes (one 32-bit word, code i in bits 4i..4i+3, i.e. element
-// 2b in the low nibble of byte b) to four bf16x2 values, each pair holding
-// codes (i, i+4): out[0] = (c0, c4), out[1] = (c1, c5), out[2] = (c2, c6),
-// out[3] = (c3, c7), low half first.
-//
-// Bit placement: a code s|e1 e0|m copied to bf16 bit 15 (sign) and bits 8..6
-// (e1 e0 m) is exactly the E2M1 value times 2^-126: e = 0 lands in the bf16
-// subnormals (m * 2^-1 * 2^-126), e > 0 in exponent field e with mantissa
-// bit m.  Masking two nibbles 16 bits apart and multiplying by
-// (2^6 + 2^12) places both copies without overlapping carries; the final
-// mask keeps the magnitude copy (<<6) and the sign copy (<<12).  The
-// multiply by `mult` = 2^(s-1) (bf16x2) then applies 2^126 and the E8M0
-// scale 2^(s-127) in one exact power-of-two product.
-__device__ __forceinline__ void mxfp4_word_to_bf16x2(uint32_t w, uint32_t mult, uint32_t out[4]) {
-    const uint32_t hi = w >> 8;
-    uint32_t t[4];
-    t[0] = ((w & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
-    t[1] = ((w & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
-    t[2] = ((hi & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
-    t[3] = ((hi & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&t[i]);
-        __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162*>(&mult);
-        __nv_bfloat162 r = __hmul2(a, m);
-        out[i] = *reinterpret_cast<uint32_t*>(&r);
-    }
-}
-
-// bf16x2 multiplier 2^(s-1) in both halves for E8M0 byte s <= 128
-// (exponent field s + 126).
-__device__ __forceinline__ uint32_t e8m0_mult_lo(uint32_t s) {
-    return (min(s, 128u) + 126u) * 0x00800080u;
-}
-
-// Second multiplier 2^(s-128) for scale bytes above 128 (exponent s - 1).
-__device__ __forceinline__ uint32_t e8m0_mult_hi(uint32_t s) {
-    return (max(s, 128u) - 1u) * 0x00800080u;
-}
-
-__device__ __forceinline__ void bf16x2_scale(uint32_t out[4], uint32_t mult) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&out[i]);
-        __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162*>(&mult);
-        __nv_bfloat162 r = __hmul2(a, m);
-        out[i] = *reinterpret_cast<uint32_t*>(&r);
-    }
-}
-
 // ------------------------------------------------------------- numerics
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }

@@ -238,8 +238,8 @@ def moe_ffn_y_offset(T: int, I: int, Et: int, Kt: int, tile_m: int) -> int:
 
 
 def ffn_views(workspace, T: int, H: int, I: int, Et: int, Kt: int, tile_m: int):
-    """(h [cap, I] as bf16 bits, y fp32 [T*Kt, H]) views of a moe_ffn workspace (the decode
-    path re-encodes h as scaled f16: see moe_ffn_gate_up in include/moe.h)."""
+    """(h [cap, I] 16-bit, y fp32 [T*Kt, H]) views of a moe_ffn workspace (after the gate_up
+    step h holds scaled f16 rows: see moe_ffn_gate_up in include/moe.h)."""
     import torch
     cap = moe_permute_capacity(T, Kt, Et, tile_m)
     off = moe_ffn_y_offset(T, I, Et, Kt, tile_m)

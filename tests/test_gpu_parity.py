@@ -340,6 +340,23 @@ def test_prefill_scale_bytes_above_128():
     gc.ffn_parity(_gpu_ffn(d, ids, wt, w.Et, 32, libmoe.MOE_PATH_PREFILL), ref, "big scales")
 
 
+@pytest.mark.parametrize("path,tile_m", [(libmoe.MOE_PATH_DECODE, 8), (libmoe.MOE_PATH_PREFILL, 32)])
+def test_ffn_scales_spread_within_rows(path, tile_m):
+    """Scale bytes spread over 2^-60..2^20 inside each weight row, and rows
+    whose largest scale is tiny or huge (the prefill path stores each row
+    relative to its largest scale; groups more than 2^36 below it round)."""
+    w = synth.scaled(synth.WORKLOADS["tiny16"], T=20, H=512, I=128, E=4, K=2, seed=23)
+    d, ids, wt = _layer_inputs(w)
+    rng = np.random.default_rng(5)
+    d["s13"] = rng.integers(67, 148, d["s13"].shape).astype(np.uint8)
+    d["s13"][:, 0, :] = rng.integers(60, 70, d["s13"].shape[2])     # a row of tiny scales
+    d["s13"][:, 1, :] = rng.integers(140, 150, d["s13"].shape[2])   # a row of large ones
+    d["s2"] = rng.integers(90, 140, d["s2"].shape).astype(np.uint8)
+    ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt))
+    assert np.isfinite(ref).all()
+    gc.ffn_parity(_gpu_ffn(d, ids, wt, w.Et, tile_m, path), ref, "spread scales")
+
+
 def test_prefill_tile_m_and_permutation_invariance():
     w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL["ragged37"])
     d, ids, wt = _layer_inputs(w)
