@@ -16,19 +16,24 @@
 //     reads h, which is already in tile order); both are f16 rows scaled per
 //     row by a power of two (rows_to_f16_kernel), the factor undone in the
 //     epilogue;
-//   * 16 converter warps: dequantisation of the codes into the stage's A
-//     buffer (same swizzled layout) by the hardware E2M1 -> f16x2 conversion
-//     and one f16x2 multiply by 2^(s - s_ref); s_ref = max(s) - 13 over the
-//     weight row, so the row's values fit f16 (largest 6 * 2^13) and every
-//     group within 2^36 of the row's largest scale stays exact; 2^(s_ref -
-//     127) is applied per row in the epilogue;
+//   * 16 converter warps, four per tensor-memory lane quadrant, each owning
+//     every fourth stage for its quadrant's 32 weight rows: dequantisation of
+//     the codes by the hardware E2M1 -> f16x2 conversion and one f16x2
+//     multiply by 2^(s - s_ref) (s_ref = max(s) - 13 over the weight row, so
+//     the row fits f16, largest 6 * 2^13, and every group within 2^36 of the
+//     row's largest scale stays exact; 2^(s_ref - 127) is applied per row in
+//     the epilogue), written straight into the stage's A operand in tensor
+//     memory (tcgen05.st; row = lane), so A never passes through shared
+//     memory, whose bandwidth the B operand and the TMA writes need;
 //   * MMA warp: one thread issues the four K = 16 tcgen05.mma of each stage
-//     into the item's tensor-memory accumulator and commits them to the
-//     stage's mbarrier, which frees the stage;
+//     (A from tensor memory, B from shared memory) into the item's
+//     accumulator and commits them to the stage's mbarrier, which frees the
+//     stage (its shared-memory slot and its tensor-memory A columns);
 //   * 4 epilogue warps: read the finished accumulator (each warp its 32
 //     lanes), apply SwiGLU (gate and up rows interleaved, partner one lane
 //     away) or the routing weight, and store; the accumulator is double
-//     buffered so this overlaps the next item's MMAs.
+//     buffered (single for 256-wide tiles, for lack of tensor memory) so this
+//     overlaps the next item's MMAs.
 // Every wait is bounded (see mbar_wait); after a timeout each role stops, the
 // MMA thread drains its own MMAs (bounded), and tensor memory is freed.
 #include <algorithm>
@@ -46,8 +51,8 @@ constexpr int kConvWarps = 16;
 constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;  // 18..21: warp % 4 covers every lane quadrant
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 704
-constexpr int kBK = 64;                                   // k per stage (one 128-byte bf16 row)
-constexpr int kABytes = 128 * kBK * 2;                    // 16 KB bf16 A stage
+constexpr int kBK = 64;                                   // k per stage (one 128-byte f16 row)
+constexpr int kACols = kBK / 2;                           // tensor-memory columns of one A stage
 constexpr int kCodeBytes = 128 * (kBK / 2);               // 4 KB packed codes stage
 constexpr int kCodeBox = 64;                              // rows per codes box
 constexpr int kPrefetch = 12;                             // code stages prefetched into L2 ahead
@@ -77,13 +82,27 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+// D (tensor memory) += A (tensor memory) * B (shared memory descriptor).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 consecutive 32-bit tensor-memory columns of this thread's lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
 }
 
@@ -158,12 +177,14 @@ __device__ __forceinline__ uint4 codes_to_f16x8(uint32_t w, uint32_t mult) {
 template <int N>
 struct PrefillSmem {
     static constexpr int kBBytes = N * kBK * 2;
-    static constexpr int kStage = kABytes + kBBytes + kCodeBytes;  // multiple of 1024
-    // as many stages as fit: narrow tiles spend little time per stage in the
-    // MMA, so the ring has to cover the load latency with more of them
-    static constexpr int kStages = N <= 32 ? 8 : N <= 64 ? 7 : N <= 128 ? 6 : 4;
+    static constexpr int kStage = kBBytes + kCodeBytes;            // multiple of 1024
+    static constexpr int kStages = N <= 128 ? 8 : 6;
     static constexpr int kBars = kStages * kStage;
     static constexpr int kTotal = kBars + 256 + 1024;              // + alignment slack
+    // tensor memory (512 columns): the accumulators, then the A stages
+    static constexpr int kAccBufs = 2 * N + kStages * kACols <= 512 ? 2 : 1;
+    static constexpr int kACol0 = kAccBufs * N;
+    static_assert(kACol0 + kStages * kACols <= 512, "tensor memory");
 };
 
 template <int MODE, int N>
@@ -181,24 +202,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* acc_free = acc_full + 2;                                   // [2] accumulator drained
     uint64_t* drain = acc_free + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-    auto stage_a = [&](int s) { return smem + s * L::kStage; };
-    auto stage_b = [&](int s) { return smem + s * L::kStage + kABytes; };
-    auto stage_c = [&](int s) { return smem + s * L::kStage + kABytes + L::kBBytes; };
+    constexpr int kAccBufs = L::kAccBufs;
+    auto stage_b = [&](int s) { return smem + s * L::kStage; };
+    auto stage_c = [&](int s) { return smem + s * L::kStage + L::kBBytes; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = g.K;
     const int nk = (K + kBK - 1) / kBK;
     const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
     const int items = __ldg(g.num_tiles) * row_blocks;
-    constexpr uint32_t kTmemCols = 2 * N;
+    constexpr uint32_t kTmemCols = 512;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&raw_full[s], 1);
-            mbar_init(&a_full[s], kConvWarps);
+            mbar_init(&a_full[s], 4);  // one converter warp per lane quadrant
             mbar_init(&stage_free[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_free[b], kEpiWarps);
         }
@@ -266,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t gs = 0, it = 0;
             bool ok = true;
             for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++it) {
-                const uint32_t b = it & 1;
-                if (it >= 2 && !mbar_wait(&acc_free[b], ((it >> 1) - 1) & 1)) break;
+                const uint32_t b = it % kAccBufs;
+                if (it >= (uint32_t)kAccBufs && !mbar_wait(&acc_free[b], ((it / kAccBufs) - 1) & 1)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + b * N;
                 for (int st = 0; st < nk; ++st, ++gs) {
@@ -279,11 +300,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sdesc_sw128(smem_u32(stage_a(s)));
+                    const uint32_t a_tmem = tmem + (uint32_t)(L::kACol0 + s * kACols);
                     const uint64_t bd = sdesc_sw128(smem_u32(stage_b(s)));
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)  // +32 bytes per K = 16 inside the swizzle atom
-                        mma_f16_ss(d_tmem, ad + 2u * k, bd + 2u * k, idesc, (st | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < kBK / 16; ++k)  // A: 8 columns per K = 16; B: +32 bytes in the swizzle atom
+                        mma_f16_ts(d_tmem, a_tmem + 8u * k, bd + 2u * k, idesc, (st | k) != 0 ? 1u : 0u);
                     mma_commit(&stage_free[s]);
                 }
                 if (ok) mma_commit(&acc_full[b]);
@@ -293,11 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------ converters
-        const int t = tid - kConvWarp0 * 32;  // 0..511
-        const int rho = t >> 2, qh = t & 3;   // A row, 16-k quarter of the stage
-        const int h = qh >> 1;                // its 32-k scale group within the stage
+        // warp w serves lane quadrant w % 4 (the tensor-memory lanes it may
+        // write) and owns the stages with gs % 4 == (w - kConvWarp0) / 4
+        const int quad = warp & 3, part = (warp - kConvWarp0) >> 2;
+        const int rho = 32 * quad + lane;  // A row = tensor-memory lane
         const int crow = MODE == 0 ? ((rho & 1) ? kCodeBox + (rho >> 1) : rho >> 1) : rho;
         const bool svec = (K % 512) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 15) == 0);
+        const int ngroups = K / 32;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)L::kACol0;
         uint32_t gs = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
@@ -313,53 +337,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wrow = block * 128 + rho;
                 rvalid = wrow < g.rows;
             }
-            const uint8_t* sp = g.scales + ((size_t)e * g.rows + (rvalid ? wrow : 0)) * (size_t)(K / 32);
-            // the row's reference exponent: its four threads split the scan
-            uint32_t smax = rvalid ? row_scale_max_part(sp, K / 32, svec, qh, 4) : 0u;
-            smax = max(smax, __shfl_xor_sync(0xFFFFFFFFu, smax, 1));
-            smax = max(smax, __shfl_xor_sync(0xFFFFFFFFu, smax, 2));
-            const int s_ref = row_scale_ref(smax);
-            // scale bytes arrive 16 at a time (8 stages x 2 groups), one block
-            // ahead, so their load latency never sits on a stage
-            auto load_sblock = [&](int blk) {
-                const int g0 = blk * 16;
-                if (!rvalid || g0 * 32 >= K) return make_uint4(0, 0, 0, 0);
-                if (svec) return __ldg(reinterpret_cast<const uint4*>(sp + g0));
-                uint32_t b[4] = {0, 0, 0, 0};
-                for (int i = 0; i < 16 && (g0 + i) * 32 < K; ++i)
-                    b[i >> 2] |= (uint32_t)__ldg(sp + g0 + i) << (8 * (i & 3));
-                return make_uint4(b[0], b[1], b[2], b[3]);
+            const uint8_t* sp = g.scales + ((size_t)e * g.rows + (rvalid ? wrow : 0)) * (size_t)ngroups;
+            const int s_ref = row_scale_ref(rvalid ? row_scale_max_part(sp, ngroups, svec, 0, 1) : 0u);
+            auto scale_at = [&](int gidx) {
+                return (rvalid && gidx < ngroups) ? (uint32_t)__ldg(sp + gidx) : 0u;
             };
-            uint4 sblk = load_sblock(0), nblk = load_sblock(1);
             for (int st = 0; st < nk; ++st, ++gs) {
+                if ((int)(gs & 3u) != part) continue;
                 const int s = gs % kStages;
-                if (st > 0 && (st & 7) == 0) {
-                    sblk = nblk;
-                    nblk = load_sblock((st >> 3) + 1);
-                }
-                const int gi = 2 * (st & 7) + h;  // group within the 16-group block
-                const uint32_t word = (gi < 8) ? ((gi < 4) ? sblk.x : sblk.y) : ((gi < 12) ? sblk.z : sblk.w);
-                const uint32_t mult = f16_group_mult((word >> (8 * (gi & 3))) & 0xFFu, s_ref);
+                const uint32_t m0 = f16_group_mult(scale_at(2 * st), s_ref);
+                const uint32_t m1 = f16_group_mult(scale_at(2 * st + 1), s_ref);
                 if (!mbar_wait(&raw_full[s], (gs / kStages) & 1)) {
                     ok = false;
                     break;
                 }
-                uint2 cw;
-                asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
-                             : "=r"(cw.x), "=r"(cw.y)
-                             : "r"(smem_u32(stage_c(s)) + crow * (kBK / 2) + 8 * qh));
-                const uint32_t arow = smem_u32(stage_a(s)) + rho * 128;
-                const uint32_t w2[2] = {cw.x, cw.y};
+                tc_fence_after();  // after the MMAs that last read this A stage
+                uint4 c[2];
+                const uint32_t cs = smem_u32(stage_c(s)) + crow * (kBK / 2);
+                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(c[0].x), "=r"(c[0].y), "=r"(c[0].z), "=r"(c[0].w)
+                             : "r"(cs));
+                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(c[1].x), "=r"(c[1].y), "=r"(c[1].z), "=r"(c[1].w)
+                             : "r"(cs + 16));
+                uint32_t a[32];  // column j of the stage = f16x2 (k 2j, 2j + 1)
 #pragma unroll
-                for (int i2 = 0; i2 < 2; ++i2) {
-                    const uint4 v = codes_to_f16x8(w2[i2], mult);
-                    const int ch = 2 * qh + i2;
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
-                                     arow + ((ch ^ (rho & 7)) << 4)),
-                                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                                 : "memory");
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint32_t w[4] = {c[hh].x, c[hh].y, c[hh].z, c[hh].w};
+                    const uint32_t m = hh ? m1 : m0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 v = codes_to_f16x8(w[i], m);
+                        a[16 * hh + 4 * i + 0] = v.x;
+                        a[16 * hh + 4 * i + 1] = v.y;
+                        a[16 * hh + 4 * i + 2] = v.z;
+                        a[16 * hh + 4 * i + 3] = v.w;
+                    }
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tmem_st32(lane_base + (uint32_t)(s * kACols), a);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[s]);
             }
@@ -373,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int item = blockIdx.x; item < items; item += gridDim.x, ++it) {
             const int tile = item / row_blocks, block = item % row_blocks;
             const int e = __ldg(g.tile_expert + tile);
-            const uint32_t b = it & 1;
+            const uint32_t b = it % kAccBufs;
             // this lane's weight row (accumulator lane r holds A row r) and its
             // factor 2^(s_ref - 127), the part of the scales the converters
             // left out
@@ -405,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         : MODE == 0 ? __ldg(g.act_rscale + qv[u] / g.Kt)
                                     : __ldg(g.topk_w + qv[u]) * __ldg(g.act_rscale + p);
             }
-            if (!mbar_wait(&acc_full[b], (it >> 1) & 1)) break;
+            if (!mbar_wait(&acc_full[b], (it / kAccBufs) & 1)) break;
             tc_fence_after();
             // 32 columns per round trip: two loads, one wait
 #pragma unroll
