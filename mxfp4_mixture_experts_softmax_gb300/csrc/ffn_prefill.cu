@@ -178,7 +178,12 @@ template <int N>
 struct PrefillSmem {
     static constexpr int kBBytes = N * kBK * 2;
     static constexpr int kStage = kBBytes + kCodeBytes;            // multiple of 1024
-    static constexpr int kStages = N <= 128 ? 8 : 6;
+    // Converter warp (quadrant, part) owns the stages with gs % 4 == part; with
+    // a ring of a multiple of 4 slots each slot belongs to one part, so every
+    // barrier's phases are observed in order (a parity wait is unambiguous
+    // only one phase ahead).
+    static constexpr int kStages = N <= 128 ? 8 : 4;
+    static_assert(kStages % 4 == 0, "slot ownership");
     static constexpr int kBars = kStages * kStage;
     static constexpr int kTotal = kBars + 256 + 1024;              // + alignment slack
     // tensor memory (512 columns): the accumulators, then the A stages
@@ -293,9 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d_tmem = tmem + b * N;
                 for (int st = 0; st < nk; ++st, ++gs) {
                     const int s = gs % kStages;
-                    // A converted (converters) and B landed (TMA, observed directly)
-                    if (!mbar_wait(&a_full[s], (gs / kStages) & 1) ||
-                        !mbar_wait(&raw_full[s], (gs / kStages) & 1)) {
+                    // A converted; the converters arrive only after seeing the
+                    // stage's TMA barrier, so B has landed too
+                    if (!mbar_wait(&a_full[s], (gs / kStages) & 1)) {
                         ok = false;
                         break;
                     }
