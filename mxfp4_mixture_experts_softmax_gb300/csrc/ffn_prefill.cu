@@ -200,10 +200,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kStages = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L::kBars);  // codes + B landed
-    uint64_t* a_full = raw_full + kStages;                               // A converted
-    uint64_t* stage_free = a_full + kStages;                             // MMAs done with stage
-    uint64_t* acc_full = stage_free + kStages;                           // [2] accumulator ready
+    // The MMA thread waits and commits once per pair of stages (stages 2P and
+    // 2P + 1 share pair barrier P mod kPairs): its per-stage barrier work,
+    // not the tensor pipe, bounds the loop otherwise.
+    constexpr int kPairs = kStages / 2;
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L::kBars);  // codes + B landed, per slot
+    uint64_t* a_full = raw_full + kStages;                               // A converted, per pair
+    uint64_t* stage_free = a_full + kPairs;                              // MMAs done with a pair
+    uint64_t* acc_full = stage_free + kPairs;                            // [2] accumulator ready
     uint64_t* acc_free = acc_full + 2;                                   // [2] accumulator drained
     uint64_t* drain = acc_free + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -213,16 +217,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = g.K;
-    const int nk = (K + kBK - 1) / kBK;
+    // stages per item, rounded up to whole pairs (a padding stage reads zero codes)
+    const int nk = ((K + kBK - 1) / kBK + 1) & ~1;
     const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
     const int items = __ldg(g.num_tiles) * row_blocks;
     constexpr uint32_t kTmemCols = 512;
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&raw_full[s], 1);
-            mbar_init(&a_full[s], 4);  // one converter warp per lane quadrant
-            mbar_init(&stage_free[s], 1);
+        for (int s = 0; s < kStages; ++s) mbar_init(&raw_full[s], 1);
+        for (int p = 0; p < kPairs; ++p) {
+            mbar_init(&a_full[p], 8);  // one converter warp per lane quadrant and stage
+            mbar_init(&stage_free[p], 1);
         }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -265,7 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_prefetch_l2_2d(&codes_map, (st + kPrefetch) * (kBK / 2), crow1);
                     tma_prefetch_l2_2d(&act_map, (st + kPrefetch) * kBK, tile * N);
                 }
-                if (gs >= kStages && !mbar_wait(&stage_free[s], ((gs / kStages) - 1) & 1)) {
+                // both slots of a pair come free with the pair's commit
+                if (gs >= kStages && (gs & 1) == 0 &&
+                    !mbar_wait(&stage_free[(gs >> 1) % kPairs], ((gs / kStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -296,21 +303,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it >= (uint32_t)kAccBufs && !mbar_wait(&acc_free[b], ((it / kAccBufs) - 1) & 1)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + b * N;
-                for (int st = 0; st < nk; ++st, ++gs) {
-                    const int s = gs % kStages;
-                    // A converted; the converters arrive only after seeing the
-                    // stage's TMA barrier, so B has landed too
-                    if (!mbar_wait(&a_full[s], (gs / kStages) & 1)) {
+                for (int st = 0; st < nk; st += 2, gs += 2) {
+                    const int pr = (gs >> 1) % kPairs;
+                    // both stages' A converted; the converters arrive only after
+                    // seeing their stage's TMA barrier, so B has landed too
+                    if (!mbar_wait(&a_full[pr], (gs / kStages) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_tmem = tmem + (uint32_t)(L::kACol0 + s * kACols);
-                    const uint64_t bd = sdesc_sw128(smem_u32(stage_b(s)));
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)  // A: 8 columns per K = 16; B: +32 bytes in the swizzle atom
-                        mma_f16_ts(d_tmem, a_tmem + 8u * k, bd + 2u * k, idesc, (st | k) != 0 ? 1u : 0u);
-                    mma_commit(&stage_free[s]);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int s = (gs + h2) % kStages;
+                        const uint32_t a_tmem = tmem + (uint32_t)(L::kACol0 + s * kACols);
+                        const uint64_t bd = sdesc_sw128(smem_u32(stage_b(s)));
+#pragma unroll
+                        for (int k = 0; k < kBK / 16; ++k)  // A: 8 columns per K = 16; B: +32 bytes in the swizzle atom
+                            mma_f16_ts(d_tmem, a_tmem + 8u * k, bd + 2u * k, idesc,
+                                       (st | h2 | k) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&stage_free[pr]);
                 }
                 if (ok) mma_commit(&acc_full[b]);
             }
@@ -383,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[s]);
+                if (lane == 0) mbar_arrive(&a_full[(gs >> 1) % kPairs]);
             }
         }
     } else {
