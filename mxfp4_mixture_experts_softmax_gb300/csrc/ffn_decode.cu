@@ -99,6 +99,7 @@ __device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t out[4]) {
 template <int MODE, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const GroupedGemm g, const __grid_constant__ CUtensorMap codes_map) {
+    pdl_begin();
     using L = DecodeSmem<NT>;
     constexpr int TM = L::TM;
     constexpr int KC = L::KC;
@@ -339,8 +340,7 @@ cudaError_t launch_nt(const GroupedGemm& g, const CUtensorMap& map, cudaStream_t
     const int row_blocks = MODE == 0 ? (g.I + 127) / 128 : (g.rows + kRows - 1) / kRows;
     const long long max_items = (long long)g.max_tiles * row_blocks;
     const int grid = (int)std::min<long long>(max_items, (long long)num_sms());
-    decode_gemm_kernel<MODE, NT><<<grid, kThreads, smem, s>>>(g, map);
-    return cudaGetLastError();
+    return launch_pdl(decode_gemm_kernel<MODE, NT>, dim3(grid), dim3(kThreads), smem, s, g, map);
 }
 
 template <int MODE>
@@ -373,6 +373,7 @@ __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* src, u
                                                           const int32_t* __restrict__ sorted_pairs,
                                                           const int32_t* __restrict__ num_tiles,
                                                           int tile_m, float* __restrict__ rscale) {
+    pdl_begin();
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (row >= rows) return;
     if (sorted_pairs && (row >= __ldg(num_tiles) * tile_m || __ldg(sorted_pairs + row) < 0)) return;
@@ -416,6 +417,7 @@ __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* src, u
 // out[t][m] = bf16(sum over j ascending of y[t*Kt + j][m]); four columns per thread.
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y, int T, int H4,
                                                       int Kt, uint2* __restrict__ out) {
+    pdl_begin();
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (size_t)T * H4) return;
     const size_t t = i / H4, m = i % H4;
@@ -447,9 +449,8 @@ cudaError_t launch_rows_to_f16(const uint16_t* src, uint16_t* dst, int cols, int
                                const int32_t* sorted_pairs, const int32_t* num_tiles, int tile_m,
                                float* rscale, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
-    rows_to_f16_kernel<<<(rows + 7) / 8, 256, 0, s>>>(src, dst, cols, rows, sorted_pairs,
-                                                      num_tiles, tile_m, rscale);
-    return cudaGetLastError();
+    return launch_pdl(rows_to_f16_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, src, dst, cols,
+                      rows, sorted_pairs, num_tiles, tile_m, rscale);
 }
 
 cudaError_t read_device_error_decode(int* flag, int clear) {
@@ -464,9 +465,9 @@ cudaError_t launch_combine(const float* y, int T, int H, int Kt, uint16_t* out, 
     if (n == 0) return cudaSuccess;
     const int threads = 256;
     const unsigned blocks = (unsigned)((n + threads - 1) / threads);
-    combine_kernel<<<blocks, threads, 0, s>>>(reinterpret_cast<const float4*>(y), T, H / 4, Kt,
-                                              reinterpret_cast<uint2*>(out));
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(blocks), dim3(threads), 0, s,
+                      reinterpret_cast<const float4*>(y), T, H / 4, Kt,
+                      reinterpret_cast<uint2*>(out));
 }
 
 }  // namespace moe

@@ -196,6 +196,7 @@ template <int MODE, int N>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_gemm_kernel(const GroupedGemm g, const __grid_constant__ CUtensorMap codes_map,
                         const __grid_constant__ CUtensorMap act_map) {
+    pdl_begin();
     using L = PrefillSmem<N>;
     constexpr int kStages = L::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -514,8 +515,8 @@ cudaError_t launch_n(const GroupedGemm& g, cudaStream_t s) {
     const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
     const long long max_items = (long long)g.max_tiles * row_blocks;
     const int grid = (int)std::min<long long>(max_items, (long long)num_sms());
-    prefill_gemm_kernel<MODE, N><<<grid, kThreads, smem, s>>>(g, codes_map, act_map);
-    return cudaGetLastError();
+    return launch_pdl(prefill_gemm_kernel<MODE, N>, dim3(grid), dim3(kThreads), smem, s, g,
+                      codes_map, act_map);
 }
 
 template <int MODE>
@@ -536,6 +537,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int32_t* __restrict__ sorted_pairs,
                                                           const int32_t* __restrict__ num_tiles,
                                                           int tile_m, int Kt, uint4* __restrict__ xg) {
+    pdl_begin();
     const size_t total = (size_t)__ldg(num_tiles) * tile_m * H8;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
@@ -553,9 +555,9 @@ cudaError_t launch_gather_rows(const uint16_t* x, int H, const int32_t* sorted_p
     if (cap <= 0) return cudaSuccess;
     const long long chunks = (long long)cap * (H / 8);
     const int blocks = (int)std::min<long long>((chunks + 255) / 256, (long long)num_sms() * 8);
-    gather_rows_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), H / 8, sorted_pairs,
-                                              num_tiles, tile_m, Kt, reinterpret_cast<uint4*>(xg));
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s,
+                      reinterpret_cast<const uint4*>(x), H / 8, sorted_pairs, num_tiles, tile_m,
+                      Kt, reinterpret_cast<uint4*>(xg));
 }
 
 bool prefill_tile_supported(int tile_m) {

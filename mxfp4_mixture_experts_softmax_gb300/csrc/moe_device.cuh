@@ -16,6 +16,20 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
+// ------------------------------------------------- programmatic launches
+
+// Every kernel of the layer starts with this: it lets the next kernel in the
+// stream be scheduled now (its blocks wait in their own pdl_begin), then waits
+// until the previous kernel has completed and its writes are visible.  Reads
+// and writes of global memory all come after it, so stream order is kept;
+// what overlaps is launch latency and block scheduling.  Both instructions are
+// no-ops for a kernel launched without the programmatic-serialization
+// attribute.
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------- numerics
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }

@@ -61,6 +61,25 @@ struct GroupedGemm {
     uint32_t exp_one = 1u << 23, exp_bias = 1u << 23;
 };
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel in the stream is still running; every kernel of
+// the library begins with pdl_begin(), which waits for that kernel to finish.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
 

@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    int max_tiles, int32_t* __restrict__ sorted_pairs,
                    int32_t* __restrict__ offsets_out, int32_t* __restrict__ inv,
                    int32_t* __restrict__ tile_expert, int32_t* __restrict__ num_tiles) {
+    pdl_begin();
     extern __shared__ int32_t smem[];
     int32_t* hist = smem;                      // [kWarps][Et]: counts, then write cursors
     int32_t* cnt = hist + kWarps * Et;         // [Et]
@@ -140,9 +141,8 @@ cudaError_t launch_permute(const int32_t* ids, int T, int Kt, int Et, int tile_m
     const size_t smem = permute_smem_bytes(Et);
     cudaError_t err = ensure_dynamic_smem((const void*)permute_kernel, smem);
     if (err != cudaSuccess) return err;
-    permute_kernel<<<1, kThreads, smem, s>>>(ids, T * Kt, Et, tile_m, cap, max_tiles, sorted_pairs,
-                                             offsets, inv, tile_expert, num_tiles);
-    return cudaGetLastError();
+    return launch_pdl(permute_kernel, dim3(1), dim3(kThreads), smem, s, ids, T * Kt, Et, tile_m, cap,
+                      max_tiles, sorted_pairs, offsets, inv, tile_expert, num_tiles);
 }
 
 }  // namespace moe

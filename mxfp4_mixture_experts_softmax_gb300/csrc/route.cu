@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
                                                     int K, int with_shared, int renormalize,
                                                     int32_t* __restrict__ topk_ids,
                                                     float* __restrict__ topk_w) {
+    pdl_begin();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -105,8 +106,8 @@ cudaError_t launch(const float* logits, int T, int E, int K, int ws, int rn, int
                    float* w, cudaStream_t s) {
     const int warps = 8;
     dim3 grid((T + warps - 1) / warps);
-    route_kernel<VPL><<<grid, warps * 32, 0, s>>>(logits, T, E, K, ws, rn, ids, w);
-    return cudaGetLastError();
+    return launch_pdl(route_kernel<VPL>, dim3(grid), dim3(warps * 32), 0, s, logits, T, E, K, ws, rn,
+                      ids, w);
 }
 
 }  // namespace
