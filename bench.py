@@ -276,28 +276,26 @@ def run_ours(args, ws, rank, local):
         W = weights[r]
         if ev is not None:
             ev[0].record(stream)
-        ids, tw = libmoe.moe_route(logits[r], w.K, w.with_shared, w.renormalize,
-                                   bufs["topk_ids"], bufs["topk_w"])
+        # routing + permutation: one launch up to MOE_ROUTE_PERMUTE_FUSED_MAX_T tokens
+        ids, tw, perm = libmoe.moe_route_permute(logits[r], w.K, tm, w.with_shared, w.renormalize,
+                                                 bufs["topk_ids"], bufs["topk_w"], bufs["perm"])
         if ev is not None:
             ev[1].record(stream)
-        perm = libmoe.moe_permute(ids, w.Et, tm, bufs["perm"])
-        if ev is not None:
-            ev[2].record(stream)
         if gemm_ev is not None:
             gemm_ev[0].record(stream)
         libmoe.moe_ffn_gate_up(xs[r], W["w13"], W["s13"], perm, bufs["workspace"], path)
         if ev is not None:
-            ev[3].record(stream)
+            ev[2].record(stream)
         if gemm_ev is not None:
             gemm_ev[1].record(stream)
         libmoe.moe_ffn_down(W["w2"], W["s2"], tw, perm, bufs["workspace"], w.T, path)
         if ev is not None:
-            ev[4].record(stream)
+            ev[3].record(stream)
         if gemm_ev is not None:
             gemm_ev[2].record(stream)
         libmoe.moe_combine(y_buf, w.T, w.H, w.Kt, bufs["out"])
         if ev is not None:
-            ev[5].record(stream)
+            ev[4].record(stream)
 
     for i in range(args.warmup):
         step(i)
@@ -325,11 +323,11 @@ def run_ours(args, ws, rank, local):
             "down": statistics.mean(g[1].elapsed_time(g[2]) for g in gevs)}
     # per-call breakdown (after the timed region: events between every call)
     KB = min(K, 10)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(KB)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(KB)]
     for i in range(KB):
         step(i, ev=evs[i])
     torch.cuda.synchronize(dev)
-    names = ["route", "permute", "gate_up", "down", "combine"]
+    names = ["route_permute", "gate_up", "down", "combine"]
     per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(KB))
            for j, n in enumerate(names)}
     per.update(gemm)  # the GEMM steps as timed inside the timed region
@@ -408,10 +406,11 @@ def run_ours(args, ws, rank, local):
                     "h2d_bytes_per_step": int(host["logits"].nbytes + host["x"].nbytes),
                     "d2h_bytes_per_step": int(w.T * w.H * 2),
                     "ms_per_step": e2e_ms / K},
-            # decode: route, permute, x -> f16 rows, gate_up, h -> f16 rows, down,
-            # combine; prefill: route, permute, gather rows by tile, gate_up,
-            # down, combine
-            "gpu_launches": (7 if path_name == "decode" else 6) * K,
+            # route + permute (one launch up to MOE_ROUTE_PERMUTE_FUSED_MAX_T
+            # tokens, else two), x -> f16 rows, [prefill: gather rows by tile],
+            # gate_up, h -> f16 rows, down, combine
+            "gpu_launches": ((1 if w.T <= libmoe.MOE_ROUTE_PERMUTE_FUSED_MAX_T else 2)
+                             + (6 if path_name == "prefill" else 5)) * K,
             "clocks": clocks,
         }
         if ws == 1 and not args.no_cpu_baseline:

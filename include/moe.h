@@ -95,6 +95,21 @@ moe_status_t moe_route(const float* logits, int T, int E, int K, int with_shared
                        int32_t* topk_ids, float* topk_w, cudaStream_t stream);
 
 /*
+ * moe_route_ex -- moe_route with a per-token weight for the shared slot.
+ *
+ *   shared_w   fp32 [T] or NULL: the weight of slot K for each token (for
+ *              models that gate the shared expert per token, e.g. by a
+ *              sigmoid of a gate logit computed by the caller); NULL means
+ *              weight 1 as in moe_route.  Only allowed with with_shared.
+ * The pages fix the shared expert's weight only for the fused equal-width
+ * case [IX, PR #20736]; the gate itself is the caller's.  Everything else as
+ * moe_route; the routed slots do not depend on shared_w.
+ */
+moe_status_t moe_route_ex(const float* logits, const float* shared_w, int T, int E, int K,
+                          int with_shared, int renormalize, int32_t* topk_ids, float* topk_w,
+                          cudaStream_t stream);
+
+/*
  * moe_permute_capacity -- number of int32 entries of `sorted_pairs`:
  *   cap = T*Kt + Et*(tile_m - 1); max_tiles = cap / tile_m entries of
  *   `tile_expert`.  Returns 0 for invalid sizes.
@@ -126,6 +141,22 @@ size_t moe_permute_max_tiles(int T, int Kt, int Et, int tile_m);
 moe_status_t moe_permute(const int32_t* topk_ids, int T, int Kt, int Et, int tile_m,
                          int32_t* sorted_pairs, int32_t* expert_offsets, int32_t* inv_pairs,
                          int32_t* tile_expert, int32_t* num_tiles, cudaStream_t stream);
+
+/*
+ * moe_route_permute -- moe_route_ex followed by moe_permute (Kt = K + shared,
+ * Et = E + shared), bit-identical to the two calls.  For T up to
+ * MOE_ROUTE_PERMUTE_FUSED_MAX_T both run in one launch of one block (tiny
+ * batches are bound by launch latency, not by this work [VS, "kernels and
+ * graph capture"]); above it one block would route too many tokens per warp,
+ * so the two kernels run.  Arguments, limits and errors are those of the two
+ * calls.
+ */
+#define MOE_ROUTE_PERMUTE_FUSED_MAX_T 32
+moe_status_t moe_route_permute(const float* logits, const float* shared_w, int T, int E, int K,
+                               int with_shared, int renormalize, int tile_m, int32_t* topk_ids,
+                               float* topk_w, int32_t* sorted_pairs, int32_t* expert_offsets,
+                               int32_t* inv_pairs, int32_t* tile_expert, int32_t* num_tiles,
+                               cudaStream_t stream);
 
 /*
  * moe_ffn_workspace_size -- bytes of device workspace moe_ffn needs:

@@ -143,15 +143,30 @@ moe_status_t moe_device_error(int* flag, int clear) {
     return cuda_status(err);
 }
 
-moe_status_t moe_route(const float* logits, int T, int E, int K, int with_shared, int renormalize,
-                       int32_t* topk_ids, float* topk_w, cudaStream_t stream) {
+static moe_status_t check_route(const float* logits, const float* shared_w, int T, int E, int K,
+                                int with_shared, const int32_t* topk_ids, const float* topk_w) {
     if (T < 0 || E < 1 || K < 1) return MOE_ERR_INVALID_ARG;
     if (E > 1024 || K > 32 || K > E) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (T == 0) return MOE_OK;
     if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
     if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4)) return MOE_ERR_INVALID_ARG;
-    return cuda_status(launch_route(logits, T, E, K, with_shared ? 1 : 0, renormalize ? 1 : 0,
-                                    topk_ids, topk_w, stream));
+    if (shared_w && (!with_shared || !aligned(shared_w, 4))) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status_t moe_route_ex(const float* logits, const float* shared_w, int T, int E, int K,
+                          int with_shared, int renormalize, int32_t* topk_ids, float* topk_w,
+                          cudaStream_t stream) {
+    const moe_status_t st = check_route(logits, shared_w, T, E, K, with_shared, topk_ids, topk_w);
+    if (st != MOE_OK || T == 0) return st;
+    return cuda_status(launch_route(logits, shared_w, T, E, K, with_shared ? 1 : 0,
+                                    renormalize ? 1 : 0, topk_ids, topk_w, stream));
+}
+
+moe_status_t moe_route(const float* logits, int T, int E, int K, int with_shared, int renormalize,
+                       int32_t* topk_ids, float* topk_w, cudaStream_t stream) {
+    return moe_route_ex(logits, nullptr, T, E, K, with_shared, renormalize, topk_ids, topk_w,
+                        stream);
 }
 
 size_t moe_permute_capacity(int T, int Kt, int Et, int tile_m) {
@@ -164,9 +179,10 @@ size_t moe_permute_max_tiles(int T, int Kt, int Et, int tile_m) {
     return cap < 0 ? 0 : (size_t)(cap / tile_m);
 }
 
-moe_status_t moe_permute(const int32_t* topk_ids, int T, int Kt, int Et, int tile_m,
-                         int32_t* sorted_pairs, int32_t* expert_offsets, int32_t* inv_pairs,
-                         int32_t* tile_expert, int32_t* num_tiles, cudaStream_t stream) {
+static moe_status_t check_permute(const int32_t* topk_ids, int T, int Kt, int Et, int tile_m,
+                                  const int32_t* sorted_pairs, const int32_t* expert_offsets,
+                                  const int32_t* inv_pairs, const int32_t* tile_expert,
+                                  const int32_t* num_tiles, int64_t* cap_out) {
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     if (cap < 0) return MOE_ERR_INVALID_ARG;
     if (Kt > 33 || Et > 1025 || tile_m > 256 || cap >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -177,9 +193,47 @@ moe_status_t moe_permute(const int32_t* topk_ids, int T, int Kt, int Et, int til
     const void* ptrs[] = {topk_ids, sorted_pairs, expert_offsets, inv_pairs, tile_expert, num_tiles};
     for (const void* p : ptrs)
         if (p && !aligned(p, 4)) return MOE_ERR_INVALID_ARG;
+    *cap_out = cap;
+    return MOE_OK;
+}
+
+moe_status_t moe_permute(const int32_t* topk_ids, int T, int Kt, int Et, int tile_m,
+                         int32_t* sorted_pairs, int32_t* expert_offsets, int32_t* inv_pairs,
+                         int32_t* tile_expert, int32_t* num_tiles, cudaStream_t stream) {
+    int64_t cap = 0;
+    const moe_status_t st = check_permute(topk_ids, T, Kt, Et, tile_m, sorted_pairs,
+                                          expert_offsets, inv_pairs, tile_expert, num_tiles, &cap);
+    if (st != MOE_OK) return st;
     return cuda_status(launch_permute(topk_ids, T, Kt, Et, tile_m, (int)cap, (int)(cap / tile_m),
                                       sorted_pairs, expert_offsets, inv_pairs, tile_expert,
                                       num_tiles, stream));
+}
+
+moe_status_t moe_route_permute(const float* logits, const float* shared_w, int T, int E, int K,
+                               int with_shared, int renormalize, int tile_m, int32_t* topk_ids,
+                               float* topk_w, int32_t* sorted_pairs, int32_t* expert_offsets,
+                               int32_t* inv_pairs, int32_t* tile_expert, int32_t* num_tiles,
+                               cudaStream_t stream) {
+    moe_status_t st = check_route(logits, shared_w, T, E, K, with_shared, topk_ids, topk_w);
+    if (st != MOE_OK) return st;
+    const int Kt = K + (with_shared ? 1 : 0), Et = E + (with_shared ? 1 : 0);
+    int64_t cap = 0;
+    st = check_permute(topk_ids, T, Kt, Et, tile_m, sorted_pairs, expert_offsets, inv_pairs,
+                       tile_expert, num_tiles, &cap);
+    if (st != MOE_OK) return st;
+    if (T == 0 || T > MOE_ROUTE_PERMUTE_FUSED_MAX_T) {
+        // larger batches: the routing is spread over many blocks
+        st = moe_route_ex(logits, shared_w, T, E, K, with_shared, renormalize, topk_ids, topk_w,
+                          stream);
+        if (st != MOE_OK) return st;
+        return moe_permute(topk_ids, T, Kt, Et, tile_m, sorted_pairs, expert_offsets, inv_pairs,
+                           tile_expert, num_tiles, stream);
+    }
+    return cuda_status(launch_route_permute(logits, shared_w, T, E, K, with_shared ? 1 : 0,
+                                            renormalize ? 1 : 0, tile_m, (int)cap,
+                                            (int)(cap / tile_m), topk_ids, topk_w, sorted_pairs,
+                                            expert_offsets, inv_pairs, tile_expert, num_tiles,
+                                            stream));
 }
 
 static size_t y_offset(int64_t cap, int I) { return round_up((size_t)cap * I * sizeof(uint16_t), 256); }

@@ -25,8 +25,14 @@ cudaError_t encode_2d_map(CUtensorMap* map, const void* base, CUtensorMapDataTyp
                           uint64_t rows, uint64_t row_stride, int box_inner, int box_rows,
                           CUtensorMapSwizzle swizzle);
 
-cudaError_t launch_route(const float* logits, int T, int E, int K, int with_shared,
-                         int renormalize, int32_t* ids, float* w, cudaStream_t s);
+cudaError_t launch_route(const float* logits, const float* shared_w, int T, int E, int K,
+                         int with_shared, int renormalize, int32_t* ids, float* w, cudaStream_t s);
+// Routing and permutation in one single-block launch (small batches).
+cudaError_t launch_route_permute(const float* logits, const float* shared_w, int T, int E, int K,
+                                 int with_shared, int renormalize, int tile_m, int cap,
+                                 int max_tiles, int32_t* ids, float* w, int32_t* sorted_pairs,
+                                 int32_t* offsets, int32_t* inv, int32_t* tile_expert,
+                                 int32_t* num_tiles, cudaStream_t s);
 
 size_t permute_smem_bytes(int Et);
 cudaError_t launch_permute(const int32_t* ids, int T, int Kt, int Et, int tile_m, int cap,

@@ -17,7 +17,13 @@
 //     the same expert find each other with __match_any_sync and take
 //     consecutive positions in lane order.
 // Slices are contiguous and in warp order, so the result is the stable sort.
+//
+// route_permute_kernel runs the routing (route_device.cuh) of a small batch and
+// this permutation in the same block, one launch instead of two; the ids it
+// permutes were written by the block itself, so they are read with ordinary
+// (not read-only cached) loads after a block barrier.
 #include "moe_internal.h"
+#include "route_device.cuh"
 
 namespace moe {
 
@@ -26,12 +32,20 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 
-__global__ void __launch_bounds__(kThreads, 1)
-    permute_kernel(const int32_t* __restrict__ ids, int P, int Et, int tile_m, int cap,
-                   int max_tiles, int32_t* __restrict__ sorted_pairs,
-                   int32_t* __restrict__ offsets_out, int32_t* __restrict__ inv,
-                   int32_t* __restrict__ tile_expert, int32_t* __restrict__ num_tiles) {
-    pdl_begin();
+// ids written earlier by this kernel must not come through the read-only path
+template <bool kOwnIds>
+__device__ __forceinline__ int load_id(const int32_t* ids, int q) {
+    return kOwnIds ? ids[q] : __ldg(ids + q);
+}
+
+template <bool kOwnIds>
+__device__ __forceinline__ void permute_block(const int32_t* ids, int P, int Et, int tile_m,
+                                              int cap, int max_tiles,
+                                              int32_t* __restrict__ sorted_pairs,
+                                              int32_t* __restrict__ offsets_out,
+                                              int32_t* __restrict__ inv,
+                                              int32_t* __restrict__ tile_expert,
+                                              int32_t* __restrict__ num_tiles) {
     extern __shared__ int32_t smem[];
     int32_t* hist = smem;                      // [kWarps][Et]: counts, then write cursors
     int32_t* cnt = hist + kWarps * Et;         // [Et]
@@ -46,7 +60,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q_begin = min(P, warp * chunk), q_end = min(P, q_begin + chunk);
     int32_t* my_hist = hist + warp * Et;
     for (int q = q_begin + lane; q < q_end; q += 32) {
-        const int e = __ldg(ids + q);
+        const int e = load_id<kOwnIds>(ids, q);
         if ((unsigned)e < (unsigned)Et) atomicAdd(&my_hist[e], 1);
     }
     __syncthreads();
@@ -113,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // stable scatter
     for (int base = q_begin; base < q_end; base += 32) {
         const int q = base + lane;
-        int e = q < q_end ? __ldg(ids + q) : -1;
+        int e = q < q_end ? load_id<kOwnIds>(ids, q) : -1;
         const bool valid = (unsigned)e < (unsigned)Et;
         if (q < q_end && !valid) inv[q] = -1;
         if (!valid) e = -1 - lane;  // unique per lane: matches nobody
@@ -131,6 +145,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+__global__ void __launch_bounds__(kThreads, 1)
+    permute_kernel(const int32_t* __restrict__ ids, int P, int Et, int tile_m, int cap,
+                   int max_tiles, int32_t* __restrict__ sorted_pairs,
+                   int32_t* __restrict__ offsets_out, int32_t* __restrict__ inv,
+                   int32_t* __restrict__ tile_expert, int32_t* __restrict__ num_tiles) {
+    pdl_begin();
+    permute_block<false>(ids, P, Et, tile_m, cap, max_tiles, sorted_pairs, offsets_out, inv,
+                         tile_expert, num_tiles);
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(kThreads, 1)
+    route_permute_kernel(const float* __restrict__ logits, const float* __restrict__ shared_w,
+                         int T, int E, int K, int with_shared, int renormalize, int tile_m, int cap,
+                         int max_tiles, int32_t* topk_ids, float* __restrict__ topk_w,
+                         int32_t* __restrict__ sorted_pairs, int32_t* __restrict__ offsets_out,
+                         int32_t* __restrict__ inv, int32_t* __restrict__ tile_expert,
+                         int32_t* __restrict__ num_tiles) {
+    pdl_begin();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int Kt = K + (with_shared ? 1 : 0);
+    for (int t = warp; t < T; t += kWarps)
+        route_token<VPL>(logits + (size_t)t * E, E, K, with_shared, renormalize,
+                         shared_w ? __ldg(shared_w + t) : 1.0f, topk_ids + (size_t)t * Kt,
+                         topk_w + (size_t)t * Kt, lane);
+    __syncthreads();  // the block's id writes are visible to the whole block
+    permute_block<true>(topk_ids, T * Kt, E + (with_shared ? 1 : 0), tile_m, cap, max_tiles,
+                        sorted_pairs, offsets_out, inv, tile_expert, num_tiles);
+}
+
+template <int VPL>
+cudaError_t launch_fused(const float* logits, const float* sw, int T, int E, int K, int ws,
+                         int rn, int tile_m, int cap, int max_tiles, int32_t* ids, float* w,
+                         int32_t* sorted_pairs, int32_t* offsets, int32_t* inv,
+                         int32_t* tile_expert, int32_t* num_tiles, cudaStream_t s) {
+    const size_t smem = permute_smem_bytes(E + (ws ? 1 : 0));
+    cudaError_t err = ensure_dynamic_smem((const void*)route_permute_kernel<VPL>, smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(route_permute_kernel<VPL>, dim3(1), dim3(kThreads), smem, s, logits, sw, T, E,
+                      K, ws, rn, tile_m, cap, max_tiles, ids, w, sorted_pairs, offsets, inv,
+                      tile_expert, num_tiles);
+}
+
 }  // namespace
 
 size_t permute_smem_bytes(int Et) { return sizeof(int32_t) * ((size_t)kWarps * Et + 2 * Et + 1 + kWarps); }
@@ -143,6 +200,28 @@ cudaError_t launch_permute(const int32_t* ids, int T, int Kt, int Et, int tile_m
     if (err != cudaSuccess) return err;
     return launch_pdl(permute_kernel, dim3(1), dim3(kThreads), smem, s, ids, T * Kt, Et, tile_m, cap,
                       max_tiles, sorted_pairs, offsets, inv, tile_expert, num_tiles);
+}
+
+}  // namespace moe
+
+namespace moe {
+
+cudaError_t launch_route_permute(const float* logits, const float* shared_w, int T, int E, int K,
+                                 int with_shared, int renormalize, int tile_m, int cap,
+                                 int max_tiles, int32_t* ids, float* w, int32_t* sorted_pairs,
+                                 int32_t* offsets, int32_t* inv, int32_t* tile_expert,
+                                 int32_t* num_tiles, cudaStream_t s) {
+#define MOE_FUSED(V)                                                                           \
+    return launch_fused<V>(logits, shared_w, T, E, K, with_shared, renormalize, tile_m, cap,     \
+                           max_tiles, ids, w, sorted_pairs, offsets, inv, tile_expert, num_tiles, \
+                           s)
+    if (E <= 32) MOE_FUSED(1);
+    if (E <= 64) MOE_FUSED(2);
+    if (E <= 128) MOE_FUSED(4);
+    if (E <= 256) MOE_FUSED(8);
+    if (E <= 512) MOE_FUSED(16);
+    MOE_FUSED(32);
+#undef MOE_FUSED
 }
 
 }  // namespace moe

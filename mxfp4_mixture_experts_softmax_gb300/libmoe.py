@@ -24,13 +24,16 @@ MOE_PATH_AUTO = 0
 MOE_PATH_DECODE = 1
 MOE_PATH_PREFILL = 2
 
-EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_permute_capacity",
-           "moe_permute_max_tiles", "moe_permute", "moe_ffn_workspace_size", "moe_ffn",
+EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_route_ex", "moe_permute_capacity",
+           "moe_permute_max_tiles", "moe_permute", "moe_route_permute", "moe_ffn_workspace_size",
+           "moe_ffn",
            "moe_ffn_path", "moe_ffn_auto_path", "moe_ffn_gate_up", "moe_ffn_down", "moe_combine",
            "moe_ffn_y_offset", "moe_device_error", "moe_ffn_noalloc")
 
 # bytes of the fixed device scratch behind moe_ffn_noalloc (include/moe.h)
 MOE_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+# batches up to this many tokens route and permute in one launch (include/moe.h)
+MOE_ROUTE_PERMUTE_FUSED_MAX_T = 32
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +66,11 @@ def load(build: bool = True):
         L.moe_version.restype = ci
         L.moe_route.argtypes = [vp, ci, ci, ci, ci, ci, vp, vp, vp]
         L.moe_route.restype = ci
+        L.moe_route_ex.argtypes = [vp, vp, ci, ci, ci, ci, ci, vp, vp, vp]
+        L.moe_route_ex.restype = ci
+        L.moe_route_permute.argtypes = [vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, vp,
+                                        vp]
+        L.moe_route_permute.restype = ci
         L.moe_permute_capacity.argtypes = [ci, ci, ci, ci]
         L.moe_permute_capacity.restype = sz
         L.moe_permute_max_tiles.argtypes = [ci, ci, ci, ci]
@@ -121,9 +129,7 @@ def _dev(t, dtype_name: str):
     return t
 
 
-def moe_route(logits, K: int, with_shared: bool = True, renormalize: bool = True,
-              topk_ids=None, topk_w=None, stream=None):
-    """fp32 logits [T, E] -> (int32 ids [T, Kt], fp32 weights [T, Kt])."""
+def _route_outputs(logits, K, with_shared, topk_ids, topk_w, shared_w):
     import torch
     _dev(logits, "logits")
     assert logits.dtype == torch.float32
@@ -133,9 +139,42 @@ def moe_route(logits, K: int, with_shared: bool = True, renormalize: bool = True
         topk_ids = torch.empty((T, Kt), dtype=torch.int32, device=logits.device)
     if topk_w is None:
         topk_w = torch.empty((T, Kt), dtype=torch.float32, device=logits.device)
-    _check(load().moe_route(_ptr(logits), T, E, K, int(with_shared), int(renormalize),
-                            _ptr(topk_ids), _ptr(topk_w), _stream(stream)), "moe_route")
+    if shared_w is not None:
+        _dev(shared_w, "shared_w")
+        assert shared_w.dtype == torch.float32 and shared_w.shape == (T,)
+    return T, E, Kt, topk_ids, topk_w
+
+
+def moe_route(logits, K: int, with_shared: bool = True, renormalize: bool = True,
+              topk_ids=None, topk_w=None, stream=None, shared_w=None):
+    """fp32 logits [T, E] -> (int32 ids [T, Kt], fp32 weights [T, Kt]).  shared_w (fp32 [T],
+    optional): per-token weight of the shared slot (moe_route_ex)."""
+    T, E, Kt, topk_ids, topk_w = _route_outputs(logits, K, with_shared, topk_ids, topk_w, shared_w)
+    if shared_w is None:
+        _check(load().moe_route(_ptr(logits), T, E, K, int(with_shared), int(renormalize),
+                                _ptr(topk_ids), _ptr(topk_w), _stream(stream)), "moe_route")
+    else:
+        _check(load().moe_route_ex(_ptr(logits), _ptr(shared_w), T, E, K, int(with_shared),
+                                   int(renormalize), _ptr(topk_ids), _ptr(topk_w),
+                                   _stream(stream)), "moe_route_ex")
     return topk_ids, topk_w
+
+
+def moe_route_permute(logits, K: int, tile_m: int, with_shared: bool = True,
+                      renormalize: bool = True, topk_ids=None, topk_w=None,
+                      perm: dict | None = None, shared_w=None, stream=None):
+    """moe_route_ex + moe_permute in one call (one launch for small batches):
+    returns (ids, weights, perm dict as from moe_permute)."""
+    T, E, Kt, topk_ids, topk_w = _route_outputs(logits, K, with_shared, topk_ids, topk_w, shared_w)
+    Et = E + (1 if with_shared else 0)
+    if perm is None:
+        perm = alloc_permute(T, Kt, Et, tile_m, logits.device)
+    _check(load().moe_route_permute(_ptr(logits), _ptr(shared_w), T, E, K, int(with_shared),
+                                    int(renormalize), tile_m, _ptr(topk_ids), _ptr(topk_w),
+                                    _ptr(perm["sorted_pairs"]), _ptr(perm["expert_offsets"]),
+                                    _ptr(perm["inv_pairs"]), _ptr(perm["tile_expert"]),
+                                    _ptr(perm["num_tiles"]), _stream(stream)), "moe_route_permute")
+    return topk_ids, topk_w, perm
 
 
 def moe_permute_capacity(T: int, Kt: int, Et: int, tile_m: int) -> int:
@@ -285,9 +324,10 @@ def moe_layer(logits, x, w13, s13, w2, s2, K: int, with_shared: bool = True,
     if bufs is None:
         bufs = alloc_layer(T, E, K, with_shared, x.shape[1], w13.shape[1] // 2, Et, tile_m,
                            x.device)
-    ids, w = moe_route(logits, K, with_shared, renormalize, bufs["topk_ids"], bufs["topk_w"],
-                       stream)
-    perm = moe_permute(ids, Et, tile_m, bufs["perm"], stream)
+    if Et != E + (1 if with_shared else 0):
+        raise ValueError("weights must hold E experts plus the shared one when with_shared")
+    ids, w, perm = moe_route_permute(logits, K, tile_m, with_shared, renormalize, bufs["topk_ids"],
+                                     bufs["topk_w"], bufs["perm"], stream=stream)
     return moe_ffn(x, w13, s13, w2, s2, w, perm, bufs["out"], bufs["workspace"], path, stream)
 
 

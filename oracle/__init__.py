@@ -40,7 +40,7 @@ def _load():
             build()
             lib = ctypes.CDLL(_LIB)
             vp, ci = ctypes.c_void_p, ctypes.c_int
-            lib.moe_ref_route.argtypes = [vp, ci, ci, ci, ci, ci, vp, vp]
+            lib.moe_ref_route.argtypes = [vp, vp, ci, ci, ci, ci, ci, vp, vp]
             lib.moe_ref_route.restype = ci
             lib.moe_ref_permute.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, vp, vp]
             lib.moe_ref_permute.restype = ci
@@ -80,15 +80,20 @@ def _check(rc, what):
         raise OracleError(f"{what} failed with status {rc}")
 
 
-def route(logits: np.ndarray, K: int, with_shared: bool, renormalize: bool = True):
-    """fp32 logits [T, E] -> (ids int32 [T, Kt], weights fp32 [T, Kt])."""
+def route(logits: np.ndarray, K: int, with_shared: bool, renormalize: bool = True,
+          shared_w: np.ndarray | None = None):
+    """fp32 logits [T, E] -> (ids int32 [T, Kt], weights fp32 [T, Kt]).  shared_w (fp32 [T],
+    optional) is the shared slot's weight per token; 1.0 when absent."""
     logits = np.ascontiguousarray(logits, np.float32)
     T, E = logits.shape
     Kt = K + (1 if with_shared else 0)
     ids = np.empty((T, Kt), np.int32)
     w = np.empty((T, Kt), np.float32)
-    _check(_load().moe_ref_route(_p(logits), T, E, K, int(with_shared), int(renormalize),
-                                 _p(ids), _p(w)), "route")
+    sw = None if shared_w is None else np.ascontiguousarray(shared_w, np.float32)
+    if sw is not None and sw.shape != (T,):
+        raise ValueError("shared_w must be [T]")
+    _check(_load().moe_ref_route(_p(logits), None if sw is None else _p(sw), T, E, K,
+                                 int(with_shared), int(renormalize), _p(ids), _p(w)), "route")
     return ids, w
 
 

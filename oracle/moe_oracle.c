@@ -117,8 +117,8 @@ float moe_ref_silu(float g) { return g / (1.0f + expf(-g)); }
  * holds expert E with weight 1.  Selecting on logits is the same as selecting
  * on probabilities (softmax is monotone) but free of ties created by rounding
  * in exp. */
-int moe_ref_route(const float* logits, int T, int E, int K, int with_shared, int renormalize,
-                  int32_t* topk_ids, float* topk_w) {
+int moe_ref_route(const float* logits, const float* shared_w, int T, int E, int K,
+                  int with_shared, int renormalize, int32_t* topk_ids, float* topk_w) {
     if (T < 0 || E < 1 || K < 1 || K > E) return REF_ERR_ARG;
     int Kt = K + (with_shared ? 1 : 0);
     float* p = (float*)malloc(sizeof(float) * (size_t)E);
@@ -159,7 +159,7 @@ int moe_ref_route(const float* logits, int T, int E, int K, int with_shared, int
         for (int k = 0; k < K; ++k) w[k] = renormalize ? p[ids[k]] / s : p[ids[k]];
         if (with_shared) {
             ids[K] = E;
-            w[K] = 1.0f;
+            w[K] = shared_w ? shared_w[t] : 1.0f; /* caller-supplied weight, e.g. a sigmoid gate */
         }
     }
     free(p);

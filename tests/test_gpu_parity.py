@@ -63,6 +63,45 @@ def test_route_ties_zeros_and_neg_inf():
     _route_check(logits, 10, True)
 
 
+@pytest.mark.parametrize("T,E,K,shared,tile_m", [(1, 8, 2, False, 8), (16, 8, 2, False, 8),
+                                                 (32, 512, 10, True, 8), (32, 1024, 32, True, 128),
+                                                 (33, 512, 10, True, 32), (37, 16, 4, True, 16),
+                                                 (64, 512, 10, True, 8), (288, 512, 10, True, 64),
+                                                 (0, 64, 4, True, 8)])
+def test_route_permute_equals_route_then_permute(T, E, K, shared, tile_m):
+    """The fused call (one launch up to MOE_ROUTE_PERMUTE_FUSED_MAX_T tokens) is bit-identical to
+    moe_route + moe_permute and to the oracle, with and without per-token shared weights."""
+    rng = np.random.default_rng(T * 7 + E)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    sw = (1.0 / (1.0 + np.exp(-rng.standard_normal(T)))).astype(np.float32) if shared else None
+    ids_r, w_r = oracle.route(logits, K, shared, True, shared_w=sw)
+    Et = E + (1 if shared else 0)
+    p_r = oracle.permute(ids_r, Et, tile_m)
+    ld = gc.to_dev(logits)
+    sw_d = gc.to_dev(sw) if sw is not None else None
+    ids_f, w_f, perm_f = libmoe.moe_route_permute(ld, K, tile_m, shared, True, shared_w=sw_d)
+    ids_s, w_s = libmoe.moe_route(ld, K, shared, True, shared_w=sw_d)
+    perm_s = libmoe.moe_permute(ids_s, Et, tile_m)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(ids_f.cpu().numpy(), ids_r)
+    np.testing.assert_array_equal(ids_f.cpu().numpy(), ids_s.cpu().numpy())
+    np.testing.assert_array_equal(w_f.cpu().numpy(), w_s.cpu().numpy())
+    np.testing.assert_allclose(w_f.cpu().numpy(), w_r, rtol=0, atol=gc.ROUTE_W_ATOL)
+    if shared:
+        np.testing.assert_array_equal(w_f.cpu().numpy()[:, K], sw)
+    for key in ("sorted_pairs", "expert_offsets", "inv_pairs", "tile_expert", "num_tiles"):
+        np.testing.assert_array_equal(perm_f[key].cpu().numpy(), perm_s[key].cpu().numpy(), key)
+    np.testing.assert_array_equal(perm_f["sorted_pairs"].cpu().numpy(), p_r["sorted_pairs"])
+    np.testing.assert_array_equal(perm_f["expert_offsets"].cpu().numpy(), p_r["offsets"])
+
+
+def test_route_shared_weight_rejected_without_shared_slot():
+    logits = torch.zeros((4, 16), dtype=torch.float32, device="cuda")
+    sw = torch.ones(4, dtype=torch.float32, device="cuda")
+    with pytest.raises(libmoe.MoeError):
+        libmoe.moe_route(logits, 2, False, True, shared_w=sw)
+
+
 @pytest.mark.parametrize("name", ALL)
 @pytest.mark.parametrize("tile_m", [8, 32, 128])
 def test_permute_workloads(name, tile_m):

@@ -131,3 +131,22 @@ def test_permute_rejects_bad_ids(oracle_mod):
     ids = np.array([[0, 9]], np.int32)
     with pytest.raises(oracle_mod.OracleError):
         oracle_mod.permute(ids, 8, 4)
+
+
+def test_route_shared_weight_per_token(oracle_mod):
+    """A caller-supplied shared-slot weight (e.g. a sigmoid gate per token) lands in slot K
+    unchanged and leaves the routed slots as they are with the default weight 1."""
+    rng = np.random.default_rng(17)
+    T, E, K = 23, 64, 6
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    gate = rng.standard_normal(T).astype(np.float32)
+    sw = (1.0 / (1.0 + np.exp(-gate.astype(np.float64)))).astype(np.float32)
+    ids0, w0 = oracle_mod.route(logits, K, True)
+    ids1, w1 = oracle_mod.route(logits, K, True, shared_w=sw)
+    np.testing.assert_array_equal(ids1, ids0)
+    np.testing.assert_array_equal(w1[:, :K], w0[:, :K])
+    assert (w0[:, K] == 1.0).all()
+    np.testing.assert_array_equal(w1[:, K], sw)
+    np.testing.assert_array_equal(ids1[:, K], np.full(T, E))
+    with pytest.raises(ValueError):
+        oracle_mod.route(logits, K, True, shared_w=sw[:-1])
