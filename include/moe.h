@@ -246,6 +246,42 @@ moe_status_t moe_ffn_down(const uint8_t* w2, const uint8_t* s2, const float* top
                           cudaStream_t stream);
 moe_status_t moe_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t stream);
 
+/* moe_combine plus one more fp32 [T, H] term added last (NULL: none). */
+moe_status_t moe_combine_ex(const float* y, const float* y_extra, int T, int H, int Kt,
+                            uint16_t* out, cudaStream_t stream);
+
+/*
+ * moe_ffn_dense_shared -- the layer with a shared expert whose width Is
+ * differs from the routed experts' I, run as a separate dense MXFP4 MLP over
+ * every token: the pages fuse the shared expert into the routed dispatch only
+ * when the widths are equal [IX, PR #20736], and describe the unfused shared
+ * expert as a separate dense MLP path [VL, "shared expert fusion"].
+ *
+ *   x, w13, s13, w2, s2, topk_w, sorted_pairs, ..., num_tiles, T, H, I, Et,
+ *            Kt, tile_m: the routed layer as for moe_ffn (routed with
+ *            with_shared = 0, or with a fused shared slot of its own).
+ *   w13s     uint8 [1, 2*Is, H/2], s13s [1, 2*Is, H/32], w2s [1, H, Is/2],
+ *            s2s [1, H, Is/32]: the shared expert, same format.
+ *   shared_w fp32 [T] per-token weight of the shared expert, or NULL for 1.
+ *   workspace: at least moe_ffn_dense_shared_workspace_size() bytes.
+ * out_t = bf16(sum over the routed slots j ascending of topk_w[t,j] * y_tj,
+ *              then + shared_w[t] * y_shared_t), each y as in moe_ffn (fp32),
+ * with y_shared = W2s bf16(silu(W_gate_s x_t) * (W_up_s x_t)).  With Is = I
+ * and the shared weights stored as expert E this equals the fused layer
+ * (shared slot last) bit for bit.  Limits: those of moe_ffn for both (I, Et,
+ * Kt) and (Is, 1, 1); the path of each part is chosen as by MOE_PATH_AUTO.
+ */
+size_t moe_ffn_dense_shared_workspace_size(int T, int H, int I, int Et, int Kt, int Is, int tile_m);
+moe_status_t moe_ffn_dense_shared(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                                  const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                                  const int32_t* sorted_pairs, const int32_t* expert_offsets,
+                                  const int32_t* inv_pairs, const int32_t* tile_expert,
+                                  const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                                  int tile_m, const uint8_t* w13s, const uint8_t* s13s,
+                                  const uint8_t* w2s, const uint8_t* s2s, int Is,
+                                  const float* shared_w, uint16_t* out, void* workspace,
+                                  size_t ws_bytes, cudaStream_t stream);
+
 /* Byte offset of y inside the moe_ffn workspace (h [cap, I], 16-bit, comes first). */
 size_t moe_ffn_y_offset(int T, int I, int Et, int Kt, int tile_m);
 

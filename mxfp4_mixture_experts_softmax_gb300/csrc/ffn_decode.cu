@@ -414,8 +414,11 @@ __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* src, u
     if (lane == 0) rscale[row] = __uint_as_float((uint32_t)(127 - sigma) << 23);
 }
 
-// out[t][m] = bf16(sum over j ascending of y[t*Kt + j][m]); four columns per thread.
-__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y, int T, int H4,
+// out[t][m] = bf16(sum over j ascending of y[t*Kt + j][m], then + y2[t][m] when
+// y2 is given: a shared expert run as a separate dense MLP comes last, where
+// the fused shared slot K would be); four columns per thread.
+__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y,
+                                                      const float4* __restrict__ y2, int T, int H4,
                                                       int Kt, uint2* __restrict__ out) {
     pdl_begin();
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -425,6 +428,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < Kt; ++j) {
         const float4 v = __ldg(yt + (size_t)j * H4);
+        a.x += v.x;
+        a.y += v.y;
+        a.z += v.z;
+        a.w += v.w;
+    }
+    if (y2) {
+        const float4 v = __ldg(y2 + t * H4 + m);
         a.x += v.x;
         a.y += v.y;
         a.z += v.z;
@@ -460,14 +470,42 @@ cudaError_t read_device_error_decode(int* flag, int clear) {
     return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
 }
 
-cudaError_t launch_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t s) {
+cudaError_t launch_combine(const float* y, const float* y2, int T, int H, int Kt, uint16_t* out,
+                           cudaStream_t s) {
     const size_t n = (size_t)T * (H / 4);
     if (n == 0) return cudaSuccess;
     const int threads = 256;
     const unsigned blocks = (unsigned)((n + threads - 1) / threads);
     return launch_pdl(combine_kernel, dim3(blocks), dim3(threads), 0, s,
-                      reinterpret_cast<const float4*>(y), T, H / 4, Kt,
-                      reinterpret_cast<uint2*>(out));
+                      reinterpret_cast<const float4*>(y), reinterpret_cast<const float4*>(y2), T,
+                      H / 4, Kt, reinterpret_cast<uint2*>(out));
+}
+
+// The trivial grouping of a single dense expert over all T tokens (Kt = 1):
+// sorted_pairs[p] = p for p < T, -1 after; every used tile belongs to expert
+// 0; weights fill `w` with 1 when no per-token weights are given.
+__global__ void __launch_bounds__(256) identity_perm_kernel(int T, int tile_m, int cap,
+                                                            int max_tiles,
+                                                            int32_t* __restrict__ sorted_pairs,
+                                                            int32_t* __restrict__ tile_expert,
+                                                            int32_t* __restrict__ num_tiles,
+                                                            float* __restrict__ ones) {
+    pdl_begin();
+    const int nt = (T + tile_m - 1) / tile_m;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < cap; i += gridDim.x * blockDim.x) {
+        sorted_pairs[i] = i < T ? i : -1;
+        if (i < max_tiles) tile_expert[i] = i < nt ? 0 : -1;
+        if (ones && i < T) ones[i] = 1.0f;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) *num_tiles = nt;
+}
+
+cudaError_t launch_identity_perm(int T, int tile_m, int cap, int max_tiles, int32_t* sorted_pairs,
+                                 int32_t* tile_expert, int32_t* num_tiles, float* ones,
+                                 cudaStream_t s) {
+    const int blocks = std::max(1, std::min((cap + 255) / 256, num_sms() * 4));
+    return launch_pdl(identity_perm_kernel, dim3(blocks), dim3(256), 0, s, T, tile_m, cap,
+                      max_tiles, sorted_pairs, tile_expert, num_tiles, ones);
 }
 
 }  // namespace moe

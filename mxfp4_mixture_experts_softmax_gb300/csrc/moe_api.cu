@@ -405,12 +405,101 @@ moe_status_t moe_ffn_down(const uint8_t* w2, const uint8_t* s2, const float* top
     return cuda_status(err);
 }
 
-moe_status_t moe_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t stream) {
+moe_status_t moe_combine_ex(const float* y, const float* y_extra, int T, int H, int Kt,
+                            uint16_t* out, cudaStream_t stream) {
     if (T < 0 || H <= 0 || Kt < 1) return MOE_ERR_INVALID_ARG;
     if (H % 4 || Kt > 33) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (T == 0) return MOE_OK;
-    if (!ptrs_ok({y, out}, 16)) return MOE_ERR_INVALID_ARG;
-    return cuda_status(launch_combine(y, T, H, Kt, out, stream));
+    if (!ptrs_ok({y, out}, 16) || (y_extra && !aligned(y_extra, 16))) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_combine(y, y_extra, T, H, Kt, out, stream));
+}
+
+moe_status_t moe_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t stream) {
+    return moe_combine_ex(y, nullptr, T, H, Kt, out, stream);
+}
+
+// ---------------------------------------------- shared expert of another width
+// Workspace: the routed layer's moe_ffn workspace, then the dense expert's
+// grouping (sorted_pairs [cap_s], tile_expert [cap_s / tile_m], num_tiles,
+// unit weights [T]), then the dense expert's own moe_ffn workspace.
+struct DenseSharedLayout {
+    size_t routed, perm, ones, tiles, count, dense, total;
+    int64_t cap_s;
+};
+
+static bool dense_shared_layout(int T, int H, int I, int Et, int Kt, int Is, int tile_m,
+                                DenseSharedLayout* L) {
+    const size_t r = moe_ffn_workspace_size(T, H, I, Et, Kt, tile_m);
+    const size_t d = moe_ffn_workspace_size(T, H, Is, 1, 1, tile_m);
+    const int64_t cap_s = capacity64(T, 1, 1, tile_m);
+    if ((r == 0 && T != 0) || (d == 0 && T != 0) || cap_s < 0) return false;
+    L->cap_s = cap_s;
+    L->routed = 0;
+    L->perm = round_up(r, 256);
+    L->tiles = L->perm + round_up((size_t)cap_s * 4, 256);
+    L->count = L->tiles + round_up((size_t)(cap_s / tile_m + 1) * 4, 256);
+    L->ones = L->count + 256;
+    L->dense = L->ones + round_up((size_t)T * 4 + 4, 256);
+    L->total = L->dense + d;
+    return true;
+}
+
+size_t moe_ffn_dense_shared_workspace_size(int T, int H, int I, int Et, int Kt, int Is, int tile_m) {
+    DenseSharedLayout L;
+    return dense_shared_layout(T, H, I, Et, Kt, Is, tile_m, &L) ? L.total : 0;
+}
+
+moe_status_t moe_ffn_dense_shared(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                                  const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                                  const int32_t* sorted_pairs, const int32_t* expert_offsets,
+                                  const int32_t* inv_pairs, const int32_t* tile_expert,
+                                  const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                                  int tile_m, const uint8_t* w13s, const uint8_t* s13s,
+                                  const uint8_t* w2s, const uint8_t* s2s, int Is,
+                                  const float* shared_w, uint16_t* out, void* workspace,
+                                  size_t ws_bytes, cudaStream_t stream) {
+    moe_path_t p_routed = MOE_PATH_AUTO, p_dense = MOE_PATH_AUTO;
+    moe_status_t st = check_ffn_shape(T, H, I, Et, Kt, tile_m, &p_routed);
+    if (st != MOE_OK) return st;
+    st = check_ffn_shape(T, H, Is, 1, 1, tile_m, &p_dense);
+    if (st != MOE_OK || T == 0) return st;
+    if (!ptrs_ok({x, w13, w2, w13s, w2s, out, workspace}, 16) ||
+        !ptrs_ok({s13, s2, s13s, s2s, topk_w, sorted_pairs, expert_offsets, inv_pairs, tile_expert,
+                  num_tiles}, 4) ||
+        (shared_w && !aligned(shared_w, 4)))
+        return MOE_ERR_INVALID_ARG;
+    DenseSharedLayout L;
+    if (!dense_shared_layout(T, H, I, Et, Kt, Is, tile_m, &L)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    char* ws = reinterpret_cast<char*>(workspace);
+    const size_t r_bytes = moe_ffn_workspace_size(T, H, I, Et, Kt, tile_m);
+    const size_t d_bytes = moe_ffn_workspace_size(T, H, Is, 1, 1, tile_m);
+    // the routed experts
+    st = moe_ffn_gate_up(x, w13, s13, sorted_pairs, tile_expert, num_tiles, T, H, I, Et, Kt, tile_m,
+                         ws, r_bytes, p_routed, stream);
+    if (st != MOE_OK) return st;
+    st = moe_ffn_down(w2, s2, topk_w, sorted_pairs, tile_expert, num_tiles, T, H, I, Et, Kt, tile_m,
+                      ws, r_bytes, p_routed, stream);
+    if (st != MOE_OK) return st;
+    // the shared expert over every token, weight shared_w[t] (1 when null)
+    int32_t* sp_s = reinterpret_cast<int32_t*>(ws + L.perm);
+    int32_t* te_s = reinterpret_cast<int32_t*>(ws + L.tiles);
+    int32_t* nt_s = reinterpret_cast<int32_t*>(ws + L.count);
+    float* ones = reinterpret_cast<float*>(ws + L.ones);
+    char* dws = ws + L.dense;
+    if (launch_identity_perm(T, tile_m, (int)L.cap_s, (int)(L.cap_s / tile_m), sp_s, te_s, nt_s,
+                             shared_w ? nullptr : ones, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    st = moe_ffn_gate_up(x, w13s, s13s, sp_s, te_s, nt_s, T, H, Is, 1, 1, tile_m, dws, d_bytes,
+                         p_dense, stream);
+    if (st != MOE_OK) return st;
+    st = moe_ffn_down(w2s, s2s, shared_w ? shared_w : ones, sp_s, te_s, nt_s, T, H, Is, 1, 1, tile_m,
+                      dws, d_bytes, p_dense, stream);
+    if (st != MOE_OK) return st;
+    // routed slots in order, then the shared expert
+    const float* y = reinterpret_cast<const float*>(ws + moe_ffn_y_offset(T, I, Et, Kt, tile_m));
+    const float* ys = reinterpret_cast<const float*>(dws + moe_ffn_y_offset(T, Is, 1, 1, tile_m));
+    return moe_combine_ex(y, ys, T, H, Kt, out, stream);
 }
 
 moe_status_t moe_ffn_path(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,

@@ -109,6 +109,12 @@ cudaError_t launch_gather_rows(const uint16_t* x, int H, const int32_t* sorted_p
 cudaError_t launch_prefill_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t read_device_error_prefill(int* flag, int clear);
 cudaError_t read_device_error_decode(int* flag, int clear);
-cudaError_t launch_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t s);
+// out = bf16(sum of the Kt slot rows of y, then + y2's row when y2 is not null)
+cudaError_t launch_combine(const float* y, const float* y2, int T, int H, int Kt, uint16_t* out,
+                           cudaStream_t s);
+// grouping of one dense expert over T tokens (Kt = 1); ones[T] = 1 if given
+cudaError_t launch_identity_perm(int T, int tile_m, int cap, int max_tiles, int32_t* sorted_pairs,
+                                 int32_t* tile_expert, int32_t* num_tiles, float* ones,
+                                 cudaStream_t s);
 
 }  // namespace moe

@@ -28,7 +28,8 @@ EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_route_ex", "moe
            "moe_permute_max_tiles", "moe_permute", "moe_route_permute", "moe_ffn_workspace_size",
            "moe_ffn",
            "moe_ffn_path", "moe_ffn_auto_path", "moe_ffn_gate_up", "moe_ffn_down", "moe_combine",
-           "moe_ffn_y_offset", "moe_device_error", "moe_ffn_noalloc")
+           "moe_ffn_y_offset", "moe_device_error", "moe_ffn_noalloc", "moe_combine_ex",
+           "moe_ffn_dense_shared_workspace_size", "moe_ffn_dense_shared")
 
 # bytes of the fixed device scratch behind moe_ffn_noalloc (include/moe.h)
 MOE_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -96,6 +97,12 @@ def load(build: bool = True):
         L.moe_ffn_y_offset.restype = sz
         L.moe_ffn_noalloc.argtypes = ffn_args[:-2] + [vp]
         L.moe_ffn_noalloc.restype = ci
+        L.moe_combine_ex.argtypes = [vp, vp, ci, ci, ci, vp, vp]
+        L.moe_combine_ex.restype = ci
+        L.moe_ffn_dense_shared_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci, ci]
+        L.moe_ffn_dense_shared_workspace_size.restype = sz
+        L.moe_ffn_dense_shared.argtypes = (ffn_args[:17] + [vp, vp, vp, vp, ci, vp, vp, vp, sz, vp])
+        L.moe_ffn_dense_shared.restype = ci
         L.moe_device_error.argtypes = [vp, ci]
         L.moe_device_error.restype = ci
         _lib = L
@@ -339,3 +346,26 @@ def alloc_layer(T, E, K, with_shared, H, I, Et, tile_m, device="cuda") -> dict:
                 perm=alloc_permute(T, Kt, Et, tile_m, device),
                 workspace=alloc_workspace(T, H, I, Et, Kt, tile_m, device),
                 out=torch.empty((T, H), dtype=torch.bfloat16, device=device))
+
+
+def moe_ffn_dense_shared(x, w13, s13, w2, s2, topk_w, perm: dict, w13s, s13s, w2s, s2s,
+                         shared_w=None, out=None, workspace=None, stream=None):
+    """Routed layer + a shared expert of another width run as a dense MLP over all tokens
+    (include/moe.h, moe_ffn_dense_shared)."""
+    import torch
+    T, H = x.shape
+    Et, twoI, _ = w13.shape
+    Is = w13s.shape[1] // 2
+    Kt, tm = perm["Kt"], perm["tile_m"]
+    n = int(load().moe_ffn_dense_shared_workspace_size(T, H, twoI // 2, Et, Kt, Is, tm))
+    if workspace is None:
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _check(load().moe_ffn_dense_shared(
+        _ptr(x), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), _ptr(topk_w),
+        _ptr(perm["sorted_pairs"]), _ptr(perm["expert_offsets"]), _ptr(perm["inv_pairs"]),
+        _ptr(perm["tile_expert"]), _ptr(perm["num_tiles"]), T, H, twoI // 2, Et, Kt, tm,
+        _ptr(w13s), _ptr(s13s), _ptr(w2s), _ptr(s2s), Is, _ptr(shared_w), _ptr(out),
+        _ptr(workspace), workspace.numel(), _stream(stream)), "moe_ffn_dense_shared")
+    return out

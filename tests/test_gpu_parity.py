@@ -435,3 +435,59 @@ def test_prefill_full_size(name):
     print(name, "prefill", stats)
     del dev_w
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------- shared expert of another width
+
+def _dense_shared_case(I_s, seed=31, T=37, with_gate=True):
+    w = synth.scaled(synth.WORKLOADS["tiny16"], T=T, H=512, I=128, E=16, K=4, with_shared=False,
+                     seed=seed)
+    d, ids, wt = _layer_inputs(w)
+    ws = synth.scaled(synth.WORKLOADS["tiny16"], T=T, H=512, I=I_s, E=1, K=1, with_shared=False,
+                      seed=seed + 1)
+    dsh = synth.make_weights(ws)
+    rng = np.random.default_rng(seed)
+    sw = (1.0 / (1.0 + np.exp(-rng.standard_normal(T)))).astype(np.float32) if with_gate else None
+    return w, d, ids, wt, dsh, sw
+
+
+@pytest.mark.parametrize("I_s,gate", [(96, True), (192, False), (128, True)])
+def test_dense_shared_expert_against_oracle(I_s, gate):
+    """Routed slots (fp32, ascending) then the dense shared expert, rounded once to bf16."""
+    w, d, ids, wt, dsh, sw = _dense_shared_case(I_s, with_gate=gate)
+    _, f_routed = oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt, want_f32=True)
+    sw_col = (sw if sw is not None else np.ones(w.T, np.float32)).reshape(-1, 1)
+    _, f_shared = oracle.ffn(d["x"], dsh["w13"], dsh["s13"], dsh["w2"], dsh["s2"],
+                             np.zeros((w.T, 1), np.int32), sw_col, want_f32=True)
+    total = (f_routed.astype(np.float32) + f_shared.astype(np.float32)).astype(np.float32)
+    ref = gc.bits_to_f64(np.vectorize(oracle.f32_to_bf16, otypes=[np.uint16])(total))
+    dev_w, dev_s = gc.upload_weights(d), gc.upload_weights(dsh)
+    perm = libmoe.moe_permute(gc.to_dev(ids), w.Et, 8)
+    out = libmoe.moe_ffn_dense_shared(gc.to_dev(d["x"]), dev_w["w13"], dev_w["s13"], dev_w["w2"],
+                                      dev_w["s2"], gc.to_dev(wt), perm, dev_s["w13"], dev_s["s13"],
+                                      dev_s["w2"], dev_s["s2"],
+                                      shared_w=gc.to_dev(sw) if sw is not None else None)
+    torch.cuda.synchronize()
+    gc.ffn_parity(gc.bf16_dev_to_f64(out), ref, f"dense shared Is={I_s}")
+
+
+def test_dense_shared_equal_width_equals_fused_shared_slot():
+    """With Is = I and the shared expert's weights, the separate dense path gives the fused
+    layer's bytes exactly (the shared term is added last in both)."""
+    w, d, ids, wt, dsh, sw = _dense_shared_case(128, seed=41)
+    # the fused layer: the shared expert as expert E in slot K with weight sw
+    fused_w = {k: np.concatenate([d[k], dsh[k]], axis=0) for k in ("w13", "s13", "w2", "s2")}
+    ids_f = np.concatenate([ids, np.full((w.T, 1), w.E, np.int32)], axis=1)
+    wt_f = np.concatenate([wt, sw.reshape(-1, 1)], axis=1)
+    dev_f = gc.upload_weights(fused_w)
+    perm_f = libmoe.moe_permute(gc.to_dev(ids_f), w.E + 1, 8)
+    fused = libmoe.moe_ffn(gc.to_dev(d["x"]), dev_f["w13"], dev_f["s13"], dev_f["w2"], dev_f["s2"],
+                           gc.to_dev(wt_f), perm_f, path=libmoe.MOE_PATH_DECODE)
+    dev_w, dev_s = gc.upload_weights(d), gc.upload_weights(dsh)
+    perm = libmoe.moe_permute(gc.to_dev(ids), w.Et, 8)
+    dense = libmoe.moe_ffn_dense_shared(gc.to_dev(d["x"]), dev_w["w13"], dev_w["s13"],
+                                        dev_w["w2"], dev_w["s2"], gc.to_dev(wt), perm,
+                                        dev_s["w13"], dev_s["s13"], dev_s["w2"], dev_s["s2"],
+                                        shared_w=gc.to_dev(sw))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(gc.bf16_dev_to_f64(dense), gc.bf16_dev_to_f64(fused))
