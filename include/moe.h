@@ -287,12 +287,30 @@ size_t moe_ffn_y_offset(int T, int I, int Et, int Kt, int tile_m);
 
 /*
  * moe_device_error -- reads (and with `clear` nonzero resets) the library's
- * device error flag.  A kernel sets it when one of its bounded waits (the
- * prefill path's mbarrier waits, 2 s each) gives up; the kernel then skips its
- * output, releases its tensor memory and exits instead of hanging.  This call
- * synchronises the current device.  *flag receives 0 (no error) or 1.
+ * device error flags.  *flag receives a bit set: bit 0 (value 1) when one of
+ * the kernels' bounded mbarrier waits (2 s each) gave up (the kernel then
+ * skips its output, releases its tensor memory and exits instead of
+ * hanging); bit 1 (value 2) when a kernel met an index outside its inputs'
+ * range -- a tile's expert outside [0, Et), a pair index >= T*Kt, a tile
+ * count above the buffers' -- and skipped that work instead of reading or
+ * writing out of bounds (inputs not produced by moe_permute for these
+ * sizes).  0 means no error.  Bit 0 is sticky: while it is set, the
+ * kernels' waits give up at once (so one failure cannot stall later grids),
+ * so clear it before relying on further results.  This call synchronises the
+ * current device.
  */
 moe_status_t moe_device_error(int* flag, int clear);
+
+/*
+ * moe_selftest_wait_timeout -- diagnostic: launches one block that waits on
+ * an mbarrier nothing arrives at, through the same bounded wait the GEMM
+ * kernels use, with a limit of limit_us microseconds (1..10^6).  The wait
+ * gives up, raises the device error flag (value 1 of moe_device_error) and the
+ * kernel returns; the context stays usable.  It lets a test drive the
+ * failure path without faulting or hanging the GPU.  The pages have no
+ * counterpart.
+ */
+moe_status_t moe_selftest_wait_timeout(int limit_us, cudaStream_t stream);
 
 /*
  * moe_ffn_noalloc -- moe_ffn for callers that cannot allocate device memory

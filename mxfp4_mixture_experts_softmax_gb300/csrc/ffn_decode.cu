@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nsteps = (K + kStageK - 1) / kStageK;
     const int nchunks = (K + KC - 1) / KC;
     const int row_blocks = MODE == 0 ? (g.I + 127) / 128 : (g.rows + kRows - 1) / kRows;
-    const int items = __ldg(g.num_tiles) * row_blocks;
+    const int items = checked_tiles(g) * row_blocks;
 
     // staged rows past K and padding rows are never copied: start them at zero
     for (int i = tid; i < 2 * L::kXBuf / 16; i += kThreads)
@@ -142,7 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t gs = 0;
             for (int item = blockIdx.x; item < items; item += gridDim.x) {
                 const int tile = item / row_blocks, block = item % row_blocks;
-                const int e = __ldg(g.tile_expert + tile);
+                const int e = checked_expert(g, tile, block == 0);
+                if (e < 0) continue;  // skipped by every role
                 // rows of the two boxes in the map's row space (experts stacked);
                 // rows past this expert's block are loaded too and never used
                 const int row0 = e * g.rows + (MODE == 0 ? block * 128 : block * kRows);
@@ -167,12 +168,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t gc = 0;
         for (int item = blockIdx.x; item < items; item += gridDim.x) {
             const int tile = item / row_blocks;
+            if (checked_expert(g, tile, false) < 0) continue;
             int arow[TM > 32 ? 2 : 1];
             uint32_t valid = 0;
 #pragma unroll
             for (int h = 0; h < (TM > 32 ? 2 : 1); ++h) {
                 const int j = lane + 32 * h;
-                const int q = j < TM ? __ldg(g.sorted_pairs + tile * TM + j) : -1;
+                const int q = j < TM ? checked_pair(g, tile * TM + j) : -1;
                 arow[h] = q < 0 ? -1 : (g.act_by_token ? q / g.Kt : tile * TM + j);
                 valid += __popc(__ballot_sync(0xFFFFFFFFu, arow[h] >= 0));
             }
@@ -216,12 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool failed = false;
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const int tile = item / row_blocks, block = item % row_blocks;
-        const int e = __ldg(g.tile_expert + tile);
+        const int e = checked_expert(g, tile, false);
+        if (e < 0) continue;
         int qj[NT][2];  // pair index of this lane's two columns per n-tile (-1 = padding)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
 #pragma unroll
-            for (int u = 0; u < 2; ++u) qj[n][u] = __ldg(g.sorted_pairs + tile * TM + n * 8 + 2 * c + u);
+            for (int u = 0; u < 2; ++u) qj[n][u] = checked_pair(g, tile * TM + n * 8 + 2 * c + u);
         const int rho0 = MODE == 0 ? 8 * warp + r : 16 * warp + r;
         const int rho1 = MODE == 0 ? 128 + 8 * warp + r : 16 * warp + 8 + r;
         const int wr0 = cta_weight_row<MODE>(rho0, block, g.I, g.rows);
@@ -463,11 +466,33 @@ cudaError_t launch_rows_to_f16(const uint16_t* src, uint16_t* dst, int cols, int
                       rows, sorted_pairs, num_tiles, tile_m, rscale);
 }
 
+// Waits on a barrier that nothing arrives at: the bounded wait gives up after
+// limit_ns, raises the device error flag and the kernel returns.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns) {
+    pdl_begin();
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait_for(&bar, 0, limit_ns);
+}
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s) {
+    return launch_pdl(wait_selftest_kernel, dim3(1), dim3(32), 0, s, limit_ns);
+}
+
 cudaError_t read_device_error_decode(int* flag, int clear) {
-    cudaError_t err = cudaMemcpyFromSymbol(flag, g_device_error, sizeof(int));
-    if (err != cudaSuccess || !clear) return err;
+    int wait = 0, index = 0;
+    cudaError_t err = cudaMemcpyFromSymbol(&wait, g_device_error, sizeof(int));
+    if (err == cudaSuccess) err = cudaMemcpyFromSymbol(&index, g_index_error, sizeof(int));
+    if (err != cudaSuccess) return err;
+    *flag = (wait ? 1 : 0) | (index ? 2 : 0);
+    if (!clear) return cudaSuccess;
     const int zero = 0;
-    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    err = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    return err == cudaSuccess ? cudaMemcpyToSymbol(g_index_error, &zero, sizeof(int)) : err;
 }
 
 cudaError_t launch_combine(const float* y, const float* y2, int T, int H, int Kt, uint16_t* out,

@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // stages per item, rounded up to whole pairs (a padding stage reads zero codes)
     const int nk = ((K + kBK - 1) / kBK + 1) & ~1;
     const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
-    const int items = __ldg(g.num_tiles) * row_blocks;
+    const int items = checked_tiles(g) * row_blocks;
     constexpr uint32_t kTmemCols = 512;
 
     if (tid == 0) {
@@ -255,7 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
             const int tile = item / row_blocks, block = item % row_blocks;
-            const int e = __ldg(g.tile_expert + tile);
+            const int e = checked_expert(g, tile, block == 0);
+            if (e < 0) continue;  // skipped by every role
             const int crow0 = e * g.rows + (MODE == 0 ? block * 64 : block * 128);
             const int crow1 = MODE == 0 ? e * g.rows + g.I + block * 64 : crow0 + kCodeBox;
             if (lane == 0)  // the item's first stages into L2 before the ring asks for them
@@ -299,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc = idesc_f16(128, N);
             uint32_t gs = 0, it = 0;
             bool ok = true;
-            for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++it) {
+            for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+                if (checked_expert(g, item / row_blocks, false) < 0) continue;
                 const uint32_t b = it % kAccBufs;
                 if (it >= (uint32_t)kAccBufs && !mbar_wait(&acc_free[b], ((it / kAccBufs) - 1) & 1)) break;
                 tc_fence_after();
@@ -326,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(&stage_free[pr]);
                 }
                 if (ok) mma_commit(&acc_full[b]);
+                ++it;  // items processed (skipped ones use no accumulator)
             }
             mma_commit(drain);  // every MMA this thread issued has completed when this arrives
             mbar_wait(drain, 0);
@@ -344,7 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
             const int tile = item / row_blocks, block = item % row_blocks;
-            const int e = __ldg(g.tile_expert + tile);
+            const int e = checked_expert(g, tile, false);
+            if (e < 0) continue;
             int wrow;
             bool rvalid;
             if (MODE == 0) {
@@ -405,9 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = 32 * quad + lane;
         const bool svec = (K % 512) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 15) == 0);
         uint32_t it = 0;
-        for (int item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+        for (int item = blockIdx.x; item < items; item += gridDim.x) {
             const int tile = item / row_blocks, block = item % row_blocks;
-            const int e = __ldg(g.tile_expert + tile);
+            const int e = checked_expert(g, tile, false);
+            if (e < 0) continue;
             const uint32_t b = it % kAccBufs;
             // this lane's weight row (accumulator lane r holds A row r) and its
             // factor 2^(s_ref - 127), the part of the scales the converters
@@ -435,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < kQ; ++u) {
                 const int p = tile * N + 32 * u + lane;
-                qv[u] = __ldg(g.sorted_pairs + p);
+                qv[u] = checked_pair(g, p);
                 cv[u] = qv[u] < 0 ? 0.0f
                         : MODE == 0 ? __ldg(g.act_rscale + qv[u] / g.Kt)
                                     : __ldg(g.topk_w + qv[u]) * __ldg(g.act_rscale + p);
@@ -485,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_free[b]);
+            ++it;
         }
     }
 
@@ -536,13 +542,19 @@ cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int H8,
                                                           const int32_t* __restrict__ sorted_pairs,
                                                           const int32_t* __restrict__ num_tiles,
-                                                          int tile_m, int Kt, uint4* __restrict__ xg) {
+                                                          int tile_m, int Kt, int cap, int num_pairs,
+                                                          uint4* __restrict__ xg) {
     pdl_begin();
-    const size_t total = (size_t)__ldg(num_tiles) * tile_m * H8;
+    const int rows = min(max(__ldg(num_tiles), 0) * tile_m, cap);  // clamped like checked_tiles
+    const size_t total = (size_t)rows * H8;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
         const size_t p = i / H8, c = i % H8;
-        const int q = __ldg(sorted_pairs + p);
+        int q = __ldg(sorted_pairs + p);
+        if (q >= num_pairs) {
+            if (c == 0) flag_index_error();
+            q = -1;
+        }
         xg[i] = q >= 0 ? __ldg(x + (size_t)(q / Kt) * H8 + c) : make_uint4(0, 0, 0, 0);
     }
 }
@@ -550,14 +562,14 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 }  // namespace
 
 cudaError_t launch_gather_rows(const uint16_t* x, int H, const int32_t* sorted_pairs,
-                               const int32_t* num_tiles, int tile_m, int Kt, int cap, uint16_t* xg,
-                               cudaStream_t s) {
+                               const int32_t* num_tiles, int tile_m, int Kt, int cap, int num_pairs,
+                               uint16_t* xg, cudaStream_t s) {
     if (cap <= 0) return cudaSuccess;
     const long long chunks = (long long)cap * (H / 8);
     const int blocks = (int)std::min<long long>((chunks + 255) / 256, (long long)num_sms() * 8);
     return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s,
                       reinterpret_cast<const uint4*>(x), H / 8, sorted_pairs, num_tiles, tile_m,
-                      Kt, reinterpret_cast<uint4*>(xg));
+                      Kt, cap, num_pairs, reinterpret_cast<uint4*>(xg));
 }
 
 bool prefill_tile_supported(int tile_m) {
@@ -568,10 +580,15 @@ cudaError_t launch_prefill_gate_up(const GroupedGemm& g, cudaStream_t s) { retur
 cudaError_t launch_prefill_down(const GroupedGemm& g, cudaStream_t s) { return launch_mode<1>(g, s); }
 
 cudaError_t read_device_error_prefill(int* flag, int clear) {
-    cudaError_t err = cudaMemcpyFromSymbol(flag, g_device_error, sizeof(int));
-    if (err != cudaSuccess || !clear) return err;
+    int wait = 0, index = 0;
+    cudaError_t err = cudaMemcpyFromSymbol(&wait, g_device_error, sizeof(int));
+    if (err == cudaSuccess) err = cudaMemcpyFromSymbol(&index, g_index_error, sizeof(int));
+    if (err != cudaSuccess) return err;
+    *flag = (wait ? 1 : 0) | (index ? 2 : 0);
+    if (!clear) return cudaSuccess;
     const int zero = 0;
-    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    err = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    return err == cudaSuccess ? cudaMemcpyToSymbol(g_index_error, &zero, sizeof(int)) : err;
 }
 
 }  // namespace moe

@@ -139,8 +139,13 @@ moe_status_t moe_device_error(int* flag, int clear) {
     int a = 0, b = 0;
     cudaError_t err = read_device_error_prefill(&a, clear);
     if (err == cudaSuccess) err = read_device_error_decode(&b, clear);
-    *flag = (a || b) ? 1 : 0;
+    *flag = a | b;
     return cuda_status(err);
+}
+
+moe_status_t moe_selftest_wait_timeout(int limit_us, cudaStream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_wait_selftest((unsigned long long)limit_us * 1000ull, stream));
 }
 
 static moe_status_t check_route(const float* logits, const float* shared_w, int T, int E, int K,
@@ -300,9 +305,10 @@ static bool ptrs_ok(std::initializer_list<const void*> ptrs, size_t align) {
 }
 
 static GroupedGemm base_gemm(const int32_t* sorted_pairs, const int32_t* tile_expert,
-                             const int32_t* num_tiles, int I, int Et, int Kt, int tile_m,
+                             const int32_t* num_tiles, int T, int I, int Et, int Kt, int tile_m,
                              int max_tiles) {
     GroupedGemm g{};
+    g.num_pairs = T * Kt;
     g.num_experts = Et;
     g.sorted_pairs = sorted_pairs;
     g.tile_expert = tile_expert;
@@ -339,7 +345,7 @@ moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     const int max_tiles = (int)(cap / tile_m);
     trace("moe_ffn_gate_up", T, H, I, Et, Kt, tile_m, path);
-    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, I, Et, Kt, tile_m, max_tiles);
+    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, T, I, Et, Kt, tile_m, max_tiles);
     g.codes = w13;
     g.scales = s13;
     g.rows = 2 * I;
@@ -362,7 +368,8 @@ moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_
         // the prefill GEMM reads its token rows as one box per stage: gather
         // them into tile order first
         uint16_t* xg = reinterpret_cast<uint16_t*>(ws + xg_offset(cap, T, H, I, Kt));
-        err = launch_gather_rows(x16, H, sorted_pairs, num_tiles, tile_m, Kt, (int)cap, xg, stream);
+        err = launch_gather_rows(x16, H, sorted_pairs, num_tiles, tile_m, Kt, (int)cap, T * Kt, xg,
+                                 stream);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         g.act = xg;
         g.act_rows = (int)cap;
@@ -388,7 +395,7 @@ moe_status_t moe_ffn_down(const uint8_t* w2, const uint8_t* s2, const float* top
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     const int max_tiles = (int)(cap / tile_m);
     trace("moe_ffn_down", T, H, I, Et, Kt, tile_m, path);
-    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, I, Et, Kt, tile_m, max_tiles);
+    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, T, I, Et, Kt, tile_m, max_tiles);
     g.codes = w2;
     g.scales = s2;
     g.rows = H;

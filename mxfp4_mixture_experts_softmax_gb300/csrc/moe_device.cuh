@@ -44,6 +44,12 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
 // Device error flag of this translation unit: set by a kernel whose bounded
 // wait gave up (each kernel file has its own; moe_device_error() reads all).
 static __device__ int g_device_error = 0;
+// Set when a kernel meets an index outside its inputs' range (a tile's expert,
+// a pair index, the tile count) and skips that work instead of reading or
+// writing out of bounds.  Not read by the waits: every role skips the same
+// work, so the pipelines stay in step.
+static __device__ int g_index_error = 0;
+__device__ __forceinline__ void flag_index_error() { atomicOr(&g_index_error, 1); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -80,19 +86,23 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // file has raised the device error flag, so one failure cannot stall a grid.
 // The flag and the clock are checked only every 64 polls, keeping the poll
 // itself a single shared-memory barrier test.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 63) == 0) {
             if (*(volatile int*)&g_device_error) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            if (global_ns() - t0 > limit_ns) {
                 atomicExch(&g_device_error, 1);
                 return false;
             }
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 // Prefetch one 2D box of a tensor map into L2 (no shared memory, no barrier).

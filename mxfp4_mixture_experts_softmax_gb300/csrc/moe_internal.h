@@ -58,6 +58,7 @@ struct GroupedGemm {
     int act_rows;                // rows of `act` (T for x, cap for h)
     int tile_m;
     int max_tiles;
+    int num_pairs;               // T * Kt: valid pair indices are [0, num_pairs)
     int I;                       // SwiGLU: gate rows [0, I), up rows [I, 2I)
     uint16_t* h_out;             // SwiGLU output h [cap][I] (bf16)
     float* y_out;                // weighted output [T*Kt][H] (fp32)
@@ -104,14 +105,47 @@ cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_prefill_gate_up(const GroupedGemm& g, cudaStream_t s);
 // xg[p] = x[sorted_pairs[p] / Kt] for the rows of the used tiles (0 for pads).
 cudaError_t launch_gather_rows(const uint16_t* x, int H, const int32_t* sorted_pairs,
-                               const int32_t* num_tiles, int tile_m, int Kt, int cap,
+                               const int32_t* num_tiles, int tile_m, int Kt, int cap, int num_pairs,
                                uint16_t* xg, cudaStream_t s);
 cudaError_t launch_prefill_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t read_device_error_prefill(int* flag, int clear);
+// one block waiting on a barrier that never completes, for limit_ns
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
 cudaError_t read_device_error_decode(int* flag, int clear);
 // out = bf16(sum of the Kt slot rows of y, then + y2's row when y2 is not null)
 cudaError_t launch_combine(const float* y, const float* y2, int T, int H, int Kt, uint16_t* out,
                            cudaStream_t s);
+// Items of a grouped GEMM launch: the device's tile count, clamped to the
+// tiles the buffers hold (a larger count is flagged as an index error).
+__device__ __forceinline__ int checked_tiles(const GroupedGemm& g) {
+    const int nt = __ldg(g.num_tiles);
+    if (nt < 0 || nt > g.max_tiles) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag_index_error();
+        return nt < 0 ? 0 : g.max_tiles;
+    }
+    return nt;
+}
+
+// The expert of a tile, or -1 (flagged) when it is outside [0, num_experts).
+__device__ __forceinline__ int checked_expert(const GroupedGemm& g, int tile, bool flag) {
+    const int e = __ldg(g.tile_expert + tile);
+    if ((unsigned)e >= (unsigned)g.num_experts) {
+        if (flag) flag_index_error();
+        return -1;
+    }
+    return e;
+}
+
+// A sorted position's pair index, or -1 for padding and (flagged) out of range.
+__device__ __forceinline__ int checked_pair(const GroupedGemm& g, int pos) {
+    const int q = __ldg(g.sorted_pairs + pos);
+    if (q >= g.num_pairs) {
+        flag_index_error();
+        return -1;
+    }
+    return q;
+}
+
 // grouping of one dense expert over T tokens (Kt = 1); ones[T] = 1 if given
 cudaError_t launch_identity_perm(int T, int tile_m, int cap, int max_tiles, int32_t* sorted_pairs,
                                  int32_t* tile_expert, int32_t* num_tiles, float* ones,

@@ -29,7 +29,8 @@ EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_route_ex", "moe
            "moe_ffn",
            "moe_ffn_path", "moe_ffn_auto_path", "moe_ffn_gate_up", "moe_ffn_down", "moe_combine",
            "moe_ffn_y_offset", "moe_device_error", "moe_ffn_noalloc", "moe_combine_ex",
-           "moe_ffn_dense_shared_workspace_size", "moe_ffn_dense_shared")
+           "moe_ffn_dense_shared_workspace_size", "moe_ffn_dense_shared",
+           "moe_selftest_wait_timeout")
 
 # bytes of the fixed device scratch behind moe_ffn_noalloc (include/moe.h)
 MOE_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -103,6 +104,8 @@ def load(build: bool = True):
         L.moe_ffn_dense_shared_workspace_size.restype = sz
         L.moe_ffn_dense_shared.argtypes = (ffn_args[:17] + [vp, vp, vp, vp, ci, vp, vp, vp, sz, vp])
         L.moe_ffn_dense_shared.restype = ci
+        L.moe_selftest_wait_timeout.argtypes = [ci, vp]
+        L.moe_selftest_wait_timeout.restype = ci
         L.moe_device_error.argtypes = [vp, ci]
         L.moe_device_error.restype = ci
         _lib = L
@@ -256,10 +259,17 @@ def moe_ffn(x, w13, s13, w2, s2, topk_w, perm: dict, out=None, workspace=None,
 
 
 def moe_device_error(clear: bool = True) -> int:
-    """The device error flag (1 if a bounded wait inside a kernel gave up)."""
+    """The device error bits: 1 = a bounded wait inside a kernel gave up, 2 = an index out of
+    range was met and that work skipped (include/moe.h)."""
     flag = ctypes.c_int(0)
     _check(load().moe_device_error(ctypes.byref(flag), int(clear)), "moe_device_error")
     return flag.value
+
+
+def moe_selftest_wait_timeout(limit_us: int = 2000, stream=None):
+    """Diagnostic: a bounded wait that runs out (include/moe.h)."""
+    _check(load().moe_selftest_wait_timeout(int(limit_us), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def moe_ffn_noalloc(x, w13, s13, w2, s2, topk_w, perm: dict, out=None, stream=None):
