@@ -387,7 +387,7 @@ def run_ours(args, ws, rank, local):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16",
+            "dtype": "f16",  # MMA operand type (bf16 in and out, fp32 accumulation)
             "data": "synthetic (seeded; random MXFP4 weights, N(0,1) activations and logits)",
             "config": {
                 "workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K,

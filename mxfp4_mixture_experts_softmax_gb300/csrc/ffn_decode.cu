@@ -468,7 +468,7 @@ cudaError_t launch_rows_to_f16(const uint16_t* src, uint16_t* dst, int cols, int
 
 // Waits on a barrier that nothing arrives at: the bounded wait gives up after
 // limit_ns, raises the device error flag and the kernel returns.
-__global__ void wait_selftest_kernel(unsigned long long limit_ns) {
+static __global__ void wait_selftest_kernel(unsigned long long limit_ns) {
     pdl_begin();
     __shared__ uint64_t bar;
     if (threadIdx.x == 0) {
@@ -509,7 +509,7 @@ cudaError_t launch_combine(const float* y, const float* y2, int T, int H, int Kt
 // The trivial grouping of a single dense expert over all T tokens (Kt = 1):
 // sorted_pairs[p] = p for p < T, -1 after; every used tile belongs to expert
 // 0; weights fill `w` with 1 when no per-token weights are given.
-__global__ void __launch_bounds__(256) identity_perm_kernel(int T, int tile_m, int cap,
+static __global__ void __launch_bounds__(256) identity_perm_kernel(int T, int tile_m, int cap,
                                                             int max_tiles,
                                                             int32_t* __restrict__ sorted_pairs,
                                                             int32_t* __restrict__ tile_expert,
