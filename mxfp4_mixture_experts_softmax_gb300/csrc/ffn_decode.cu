@@ -333,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
+    pdl_end();
 }
 
 template <int MODE, int NT>
@@ -415,6 +416,7 @@ __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* src, u
         d4[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
     if (lane == 0) rscale[row] = __uint_as_float((uint32_t)(127 - sigma) << 23);
+    pdl_end();
 }
 
 // out[t][m] = bf16(sum over j ascending of y[t*Kt + j][m], then + y2[t][m] when
@@ -447,6 +449,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
     o.x = (uint32_t)f32_to_bf16_bits(a.x) | ((uint32_t)f32_to_bf16_bits(a.y) << 16);
     o.y = (uint32_t)f32_to_bf16_bits(a.z) | ((uint32_t)f32_to_bf16_bits(a.w) << 16);
     out[i] = o;
+    pdl_end();
 }
 
 }  // namespace
@@ -477,6 +480,7 @@ static __global__ void wait_selftest_kernel(unsigned long long limit_ns) {
     }
     __syncthreads();
     if (threadIdx.x == 0) mbar_wait_for(&bar, 0, limit_ns);
+    pdl_end();
 }
 
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s) {
@@ -523,6 +527,7 @@ static __global__ void __launch_bounds__(256) identity_perm_kernel(int T, int ti
         if (ones && i < T) ones[i] = 1.0f;
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) *num_tiles = nt;
+    pdl_end();
 }
 
 cudaError_t launch_identity_perm(int T, int tile_m, int cap, int max_tiles, int32_t* sorted_pairs,

@@ -502,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      "r"(kTmemCols)
                      : "memory");
     }
+    pdl_end();
 }
 
 template <int MODE, int N>
@@ -538,7 +539,7 @@ cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
 }
 
 // xg[p] = x[token of sorted position p] for the rows of the used tiles, zero
-// for padding; 16 bytes per thread, grid-stride.
+// for padding; one block per row (grid-stride over rows), 16 bytes per thread.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int H8,
                                                           const int32_t* __restrict__ sorted_pairs,
                                                           const int32_t* __restrict__ num_tiles,
@@ -546,17 +547,21 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           uint4* __restrict__ xg) {
     pdl_begin();
     const int rows = min(max(__ldg(num_tiles), 0) * tile_m, cap);  // clamped like checked_tiles
-    const size_t total = (size_t)rows * H8;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (size_t)gridDim.x * blockDim.x) {
-        const size_t p = i / H8, c = i % H8;
+    for (int p = blockIdx.x; p < rows; p += gridDim.x) {
         int q = __ldg(sorted_pairs + p);
         if (q >= num_pairs) {
-            if (c == 0) flag_index_error();
+            if (threadIdx.x == 0) flag_index_error();
             q = -1;
         }
-        xg[i] = q >= 0 ? __ldg(x + (size_t)(q / Kt) * H8 + c) : make_uint4(0, 0, 0, 0);
+        uint4* dst = xg + (size_t)p * H8;
+        if (q < 0) {
+            for (int c = threadIdx.x; c < H8; c += blockDim.x) dst[c] = make_uint4(0, 0, 0, 0);
+        } else {
+            const uint4* src = x + (size_t)(q / Kt) * H8;
+            for (int c = threadIdx.x; c < H8; c += blockDim.x) dst[c] = __ldg(src + c);
+        }
     }
+    pdl_end();
 }
 
 }  // namespace
@@ -565,8 +570,7 @@ cudaError_t launch_gather_rows(const uint16_t* x, int H, const int32_t* sorted_p
                                const int32_t* num_tiles, int tile_m, int Kt, int cap, int num_pairs,
                                uint16_t* xg, cudaStream_t s) {
     if (cap <= 0) return cudaSuccess;
-    const long long chunks = (long long)cap * (H / 8);
-    const int blocks = (int)std::min<long long>((chunks + 255) / 256, (long long)num_sms() * 8);
+    const int blocks = std::min(cap, num_sms() * 16);
     return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s,
                       reinterpret_cast<const uint4*>(x), H / 8, sorted_pairs, num_tiles, tile_m,
                       Kt, cap, num_pairs, reinterpret_cast<uint4*>(xg));

@@ -18,16 +18,20 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 
 // ------------------------------------------------- programmatic launches
 
-// Every kernel of the layer starts with this: it lets the next kernel in the
-// stream be scheduled now (its blocks wait in their own pdl_begin), then waits
-// until the previous kernel has completed and its writes are visible.  Reads
-// and writes of global memory all come after it, so stream order is kept;
-// what overlaps is launch latency and block scheduling.  Both instructions are
-// no-ops for a kernel launched without the programmatic-serialization
-// attribute.
-__device__ __forceinline__ void pdl_begin() {
+// Every kernel of the layer starts with pdl_begin: it waits until the previous
+// kernel in the stream has completed and its writes are visible, and all of
+// the kernel's global loads and stores come after it, so stream order is
+// kept.  Each kernel ends with pdl_end, after its last load, which lets the
+// next kernel be scheduled while this one's last blocks finish: what overlaps
+// is launch latency.  The trigger is not given earlier on purpose: a kernel
+// two launches ahead could then become resident while this one still loads,
+// and lines that this kernel leaves in a shared L1 could be stale by the time
+// that kernel reads the addresses (rewritten in between by the kernel in the
+// middle).  Both instructions are no-ops for a kernel launched without the
+// programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_begin() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_end() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------- numerics

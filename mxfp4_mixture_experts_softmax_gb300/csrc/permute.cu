@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_begin();
     permute_block<false>(ids, P, Et, tile_m, cap, max_tiles, sorted_pairs, offsets_out, inv,
                          tile_expert, num_tiles);
+    pdl_end();
 }
 
 template <int VPL>
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();  // the block's id writes are visible to the whole block
     permute_block<true>(topk_ids, T * Kt, E + (with_shared ? 1 : 0), tile_m, cap, max_tiles,
                         sorted_pairs, offsets_out, inv, tile_expert, num_tiles);
+    pdl_end();
 }
 
 template <int VPL>

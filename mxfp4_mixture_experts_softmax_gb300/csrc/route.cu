@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
     route_token<VPL>(logits + (size_t)t * E, E, K, with_shared, renormalize,
                      shared_w ? __ldg(shared_w + t) : 1.0f, topk_ids + (size_t)t * Kt,
                      topk_w + (size_t)t * Kt, lane);
+    pdl_end();
 }
 
 template <int VPL>
