@@ -58,6 +58,13 @@ def _load():
             lib.moe_ref_silu.restype = ctypes.c_float
             lib.moe_ref_f32_to_bf16.argtypes = [ctypes.c_float]
             lib.moe_ref_f32_to_bf16.restype = ctypes.c_uint16
+            lib.moe_ref_e2m1_round.argtypes = [ctypes.c_double]
+            lib.moe_ref_e2m1_round.restype = ci
+            lib.moe_ref_quantize_mxfp4.argtypes = [vp, ci, vp, vp]
+            lib.moe_ref_quantize_mxfp4.restype = ci
+            lib.moe_ref_ffn_mxfp4act.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci,
+                                                 vp, ci, vp, vp, vp, vp, vp, ci]
+            lib.moe_ref_ffn_mxfp4act.restype = ci
             lib.moe_ref_max_threads.argtypes = []
             lib.moe_ref_max_threads.restype = ci
             _lib = lib
@@ -168,3 +175,61 @@ def f32_to_bf16(f: float) -> int:
 
 def max_threads() -> int:
     return int(_load().moe_ref_max_threads())
+
+
+def e2m1_round(v: float) -> int:
+    """E2M1 code of v rounded to nearest (ties to the even code, saturating at 6, sign kept)."""
+    return int(_load().moe_ref_e2m1_round(float(v)))
+
+
+def quantize_mxfp4(v: np.ndarray):
+    """MXFP4 quantisation along the last axis (length a multiple of 32):
+    fp32 [..., n] -> (codes uint8 [..., n/2], scales uint8 [..., n/32])."""
+    v = np.ascontiguousarray(v, np.float32)
+    n = v.shape[-1]
+    if n % 32:
+        raise ValueError("last axis must be a multiple of 32")
+    rows = v.reshape(-1, n)
+    codes = np.empty((rows.shape[0], n // 2), np.uint8)
+    scales = np.empty((rows.shape[0], n // 32), np.uint8)
+    lib = _load()
+    for r in range(rows.shape[0]):
+        _check(lib.moe_ref_quantize_mxfp4(_p(rows[r]), n, _p(codes[r]), _p(scales[r])),
+               "quantize_mxfp4")
+    return codes.reshape(*v.shape[:-1], n // 2), scales.reshape(*v.shape[:-1], n // 32)
+
+
+def ffn_mxfp4act(x, w13, s13, w2, s2, ids, w, tokens=None, want_f32=False, want_h=False,
+                 n_threads=1):
+    """Per-token loop oracle of the layer with MXFP4-quantised activations (x
+    and the SwiGLU output).  Returns out (bf16 bits [n, H]); with want_f32 also
+    the fp32 accumulator; with want_h also dict(a fp32 [n*Kt, I] = SwiGLU output
+    before quantisation, codes uint8 [n*Kt, I/2], scales uint8 [n*Kt, I/32]),
+    row i*Kt + j for requested token i and slot j."""
+    x = np.ascontiguousarray(x, np.uint16)
+    T, H = x.shape
+    Et, twoI, _ = w13.shape
+    I = twoI // 2
+    ids = np.ascontiguousarray(ids, np.int32)
+    w = np.ascontiguousarray(w, np.float32)
+    Kt = ids.shape[1]
+    tok = None if tokens is None else np.ascontiguousarray(tokens, np.int32)
+    n = T if tok is None else tok.size
+    out = np.empty((n, H), np.uint16)
+    of = np.empty((n, H), np.float32) if want_f32 else None
+    h = None
+    if want_h:
+        h = dict(a=np.empty((n * Kt, I), np.float32), codes=np.empty((n * Kt, I // 2), np.uint8),
+                 scales=np.empty((n * Kt, I // 32), np.uint8))
+    for arr in (w13, s13, w2, s2):
+        assert arr.dtype == np.uint8 and arr.flags["C_CONTIGUOUS"]
+    _check(_load().moe_ref_ffn_mxfp4act(
+        _p(x), _p(w13), _p(s13), _p(w2), _p(s2), _p(ids), _p(w), T, H, I, Et, Kt, _p(tok), n,
+        _p(out), _p(of), None if h is None else _p(h["a"]), None if h is None else _p(h["codes"]),
+        None if h is None else _p(h["scales"]), int(n_threads)), "ffn_mxfp4act")
+    res = [out]
+    if want_f32:
+        res.append(of)
+    if want_h:
+        res.append(h)
+    return res[0] if len(res) == 1 else tuple(res)

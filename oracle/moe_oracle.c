@@ -351,6 +351,192 @@ int moe_ref_ffn_grouped(const uint16_t* x, const uint8_t* w13, const uint8_t* s1
     return REF_OK;
 }
 
+/* ------------------------------------------- MXFP4-quantised activations */
+
+/* E2M1 code (0..15) of v rounded to the nearest E2M1 value: the magnitude
+ * goes to the nearest of the eight non-negative values (equal distance: the
+ * even code, i.e. the value whose last mantissa bit is 0), magnitudes above
+ * 6 to 6 (saturation); the sign bit of v is kept, so a negative v that rounds
+ * to zero gives code 8 (-0).  v must be finite. */
+static int ref_e2m1_round(double v) {
+    double a = fabs(v);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c < 8; ++c) {
+        double d = fabs(a - (double)ref_e2m1_value[c]);
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) != 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return best | (signbit(v) ? 8 : 0);
+}
+
+int moe_ref_e2m1_round(double v) { return ref_e2m1_round(v); }
+
+/* MXFP4 quantisation of n values (n a multiple of 32), following the OCP
+ * Microscaling Formats (MX) v1.0 conversion: for each block of 32 consecutive
+ * values, amax = the largest magnitude; the shared exponent is
+ * e = floor(log2(amax)) - 2, where 2 is the exponent of E2M1's largest value
+ * (6 = 1.5 * 2^2), clamped to the E8M0 range [-127, 127]; the block's scale
+ * byte is e + 127 and element k's code is ref_e2m1_round(v_k / 2^e).  A block
+ * whose values are all zero gets scale byte 0 and zero codes.  Codes are
+ * packed two per byte, element 2i in the low nibble.  The pages fuse this
+ * quantisation into the activation kernel that feeds an MXFP4 x MXFP4 GEMM
+ * (OpenRelay, "Gemma 4 31B from B200 to MI355X": section "optimisation 4",
+ * the fused GELU + up projection + MXFP4 quantisation kernel; section "how
+ * far from the ceiling", matmuls measured against the MXFP4 peak); they do
+ * not print the rounding, so the OCP rule is the reading taken here.
+ * Returns REF_ERR_NAN on a non-finite value. */
+int moe_ref_quantize_mxfp4(const float* v, int n, uint8_t* codes, uint8_t* scales) {
+    if (n < 0 || n % 32 != 0) return REF_ERR_ARG;
+    for (int b = 0; b < n / 32; ++b) {
+        const float* blk = v + 32 * b;
+        double amax = 0.0;
+        for (int k = 0; k < 32; ++k) {
+            if (!isfinite(blk[k])) return REF_ERR_NAN;
+            if (fabs((double)blk[k]) > amax) amax = fabs((double)blk[k]);
+        }
+        int e;
+        if (amax == 0.0) {
+            e = -127;
+        } else {
+            int ex;
+            frexp(amax, &ex); /* amax = m * 2^ex, m in [0.5, 1): floor(log2(amax)) = ex - 1 */
+            e = ex - 1 - 2;
+            if (e < -127) e = -127;
+            if (e > 127) e = 127;
+        }
+        scales[b] = (uint8_t)(amax == 0.0 ? 0 : e + 127);
+        for (int k = 0; k < 32; k += 2) {
+            int c0 = amax == 0.0 ? 0 : ref_e2m1_round(ldexp((double)blk[k], -e));
+            int c1 = amax == 0.0 ? 0 : ref_e2m1_round(ldexp((double)blk[k + 1], -e));
+            codes[(32 * b + k) / 2] = (uint8_t)(c0 | (c1 << 4));
+        }
+    }
+    return REF_OK;
+}
+
+/* One (token, expert) pair with MXFP4-quantised activations:
+ *   xq  = dequantise(quantise_mxfp4(x))                 (blocks of 32 along H)
+ *   g_n = sum_k W13[n][k] xq[k],  u_n = sum_k W13[I+n][k] xq[k]  (fp32, k ascending)
+ *   a_n = silu(g_n) * u_n                                (fp32, not rounded)
+ *   hq  = dequantise(quantise_mxfp4(a))                  (blocks of 32 along I)
+ *   y_m = sum_n W2[m][n] hq[n]                           (fp32, n ascending)
+ * a (the pre-quantisation SwiGLU output), hcodes and hscales receive the
+ * intermediate values. */
+static int ref_expert_forward_mxfp4(const float* xq, const uint8_t* w13, const uint8_t* s13,
+                                    const uint8_t* w2, const uint8_t* s2, int H, int I,
+                                    float* a, uint8_t* hcodes, uint8_t* hscales, float* y) {
+    float* wg = (float*)malloc(sizeof(float) * (size_t)H);
+    float* wu = (float*)malloc(sizeof(float) * (size_t)H);
+    float* wd = (float*)malloc(sizeof(float) * (size_t)I);
+    float* hq = (float*)malloc(sizeof(float) * (size_t)I);
+    for (int n = 0; n < I; ++n) {
+        ref_decode_row(w13 + (size_t)n * (H / 2), s13 + (size_t)n * (H / 32), H, wg);
+        ref_decode_row(w13 + (size_t)(I + n) * (H / 2), s13 + (size_t)(I + n) * (H / 32), H, wu);
+        float g = 0.0f, u = 0.0f;
+        for (int k = 0; k < H; ++k) {
+            g += wg[k] * xq[k];
+            u += wu[k] * xq[k];
+        }
+        a[n] = moe_ref_silu(g) * u;
+    }
+    int rc = moe_ref_quantize_mxfp4(a, I, hcodes, hscales);
+    if (rc == REF_OK) {
+        ref_decode_row(hcodes, hscales, I, hq);
+        for (int m = 0; m < H; ++m) {
+            ref_decode_row(w2 + (size_t)m * (I / 2), s2 + (size_t)m * (I / 32), I, wd);
+            float acc = 0.0f;
+            for (int n = 0; n < I; ++n) acc += wd[n] * hq[n];
+            y[m] = acc;
+        }
+    }
+    free(wg);
+    free(wu);
+    free(wd);
+    free(hq);
+    return rc;
+}
+
+/* The layer with MXFP4-quantised activations, per-token loop: like moe_ref_ffn
+ * with each expert evaluated by ref_expert_forward_mxfp4 on the token's
+ * quantised row.  For the requested tokens (tokens / n_tokens as in
+ * moe_ref_ffn), the optional outputs receive per pair (row i * Kt + j): a_out
+ * [.., I] the SwiGLU output before quantisation, hcodes_out [.., I/2] and
+ * hscales_out [.., I/32] its MXFP4 encoding.  H % 32 == 0, I % 32 == 0. */
+int moe_ref_ffn_mxfp4act(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                         const uint8_t* w2, const uint8_t* s2, const int32_t* topk_ids,
+                         const float* topk_w, int T, int H, int I, int Et, int Kt,
+                         const int32_t* tokens, int n_tokens, uint16_t* out, float* out_f32,
+                         float* a_out, uint8_t* hcodes_out, uint8_t* hscales_out, int n_threads) {
+    if (!ref_ffn_args_ok(T, H, I, Et, Kt) || n_tokens < 0) return REF_ERR_ARG;
+    if (!tokens && n_tokens != T) return REF_ERR_ARG;
+    for (int i = 0; i < n_tokens; ++i) {
+        int t = tokens ? tokens[i] : i;
+        if (t < 0 || t >= T) return REF_ERR_ARG;
+        for (int j = 0; j < Kt; ++j) {
+            int e = topk_ids[(size_t)t * Kt + j];
+            if (e < 0 || e >= Et) return REF_ERR_ARG;
+        }
+    }
+    size_t w13_e = (size_t)2 * I * (H / 2), s13_e = (size_t)2 * I * (H / 32);
+    size_t w2_e = (size_t)H * (I / 2), s2_e = (size_t)H * (I / 32);
+    int status = REF_OK;
+#ifdef _OPENMP
+    if (n_threads < 1) n_threads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
+#endif
+    for (int i = 0; i < n_tokens; ++i) {
+        int t = tokens ? tokens[i] : i;
+        float* xf = (float*)malloc(sizeof(float) * (size_t)H);
+        float* xq = (float*)malloc(sizeof(float) * (size_t)H);
+        uint8_t* xc = (uint8_t*)malloc((size_t)H / 2);
+        uint8_t* xs = (uint8_t*)malloc((size_t)H / 32);
+        float* a = (float*)malloc(sizeof(float) * (size_t)I);
+        uint8_t* hc = (uint8_t*)malloc((size_t)I / 2);
+        uint8_t* hs = (uint8_t*)malloc((size_t)I / 32);
+        float* y = (float*)malloc(sizeof(float) * (size_t)H);
+        float* acc = (float*)malloc(sizeof(float) * (size_t)H);
+        for (int k = 0; k < H; ++k) xf[k] = moe_ref_bf16_to_f32(x[(size_t)t * H + k]);
+        int rc = moe_ref_quantize_mxfp4(xf, H, xc, xs);
+        if (rc == REF_OK) ref_decode_row(xc, xs, H, xq);
+        for (int m = 0; m < H; ++m) acc[m] = 0.0f;
+        for (int j = 0; j < Kt && rc == REF_OK; ++j) {
+            int e = topk_ids[(size_t)t * Kt + j];
+            float wj = topk_w[(size_t)t * Kt + j];
+            rc = ref_expert_forward_mxfp4(xq, w13 + e * w13_e, s13 + e * s13_e, w2 + e * w2_e,
+                                          s2 + e * s2_e, H, I, a, hc, hs, y);
+            if (rc != REF_OK) break;
+            size_t r = (size_t)i * Kt + j;
+            if (a_out) memcpy(a_out + r * I, a, sizeof(float) * (size_t)I);
+            if (hcodes_out) memcpy(hcodes_out + r * (I / 2), hc, (size_t)I / 2);
+            if (hscales_out) memcpy(hscales_out + r * (I / 32), hs, (size_t)I / 32);
+            for (int m = 0; m < H; ++m) acc[m] += wj * y[m];
+        }
+        if (rc != REF_OK) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            status = rc;
+        }
+        for (int m = 0; m < H; ++m) {
+            out[(size_t)i * H + m] = moe_ref_f32_to_bf16(acc[m]);
+            if (out_f32) out_f32[(size_t)i * H + m] = acc[m];
+        }
+        free(xf);
+        free(xq);
+        free(xc);
+        free(xs);
+        free(a);
+        free(hc);
+        free(hs);
+        free(y);
+        free(acc);
+    }
+    return status;
+}
+
 int moe_ref_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -118,3 +118,56 @@ def ffn(x_bits, w13, s13, w2, s2, ids, w):
             e = int(ids[t, j])
             out[t] += float(w[t, j]) * expert_mlp(x64[t:t + 1], w13[e], s13[e], w2[e], s2[e])[0]
     return out
+
+
+# ------------------------------------------------ MXFP4-quantised activations
+# Written from the E2M1 format (1 sign, 2 exponent, 1 mantissa bit, bias 1) and
+# the OCP Microscaling v1.0 scale rule, not from the oracle's search over the
+# value table: rounding to nearest-even within each binade, where the spacing
+# is fixed, and the shared exponent found by a search on its defining
+# inequality 2^(e+2) <= amax < 2^(e+3).
+
+def e2m1_round_binade(v: float) -> int:
+    """E2M1 code of v: round to the binade's grid (spacing 0.5 below 2, 1 in
+    [2, 4), 2 in [4, 8)) with Python's round-half-even, saturate at 6."""
+    a = abs(float(v))
+    if a < 2.0:
+        q = round(a * 2.0) / 2.0      # multiples of 0.5; even multiple = even code
+    elif a < 4.0:
+        q = float(round(a))
+    else:
+        q = round(a / 2.0) * 2.0
+    q = min(q, 6.0)
+    mags = [e2m1_closed_form(c) for c in range(8)]
+    code = mags.index(q)
+    return code | (8 if np.signbit(v) else 0)
+
+
+def mx_shared_exponent(amax: float) -> int:
+    """Smallest e in [-127, 127] with amax < 2^(e+3), i.e. 2^(e+2) <= amax
+    unless clamped."""
+    e = -127
+    while e < 127 and not (amax < 2.0 ** (e + 3)):
+        e += 1
+    return e
+
+
+def quantize_mxfp4(v: np.ndarray):
+    """float [..., n] -> (codes uint8 [..., n/2], scales uint8 [..., n/32])."""
+    v = np.asarray(v, np.float64)
+    n = v.shape[-1]
+    rows = v.reshape(-1, n)
+    codes = np.zeros((rows.shape[0], n // 2), np.uint8)
+    scales = np.zeros((rows.shape[0], n // 32), np.uint8)
+    for r in range(rows.shape[0]):
+        for b in range(n // 32):
+            blk = rows[r, 32 * b:32 * b + 32]
+            amax = float(np.abs(blk).max())
+            if amax == 0.0:
+                continue
+            e = mx_shared_exponent(amax)
+            scales[r, b] = e + 127
+            cs = [e2m1_round_binade(x / 2.0 ** e) for x in blk]
+            for i in range(16):
+                codes[r, 16 * b + i] = cs[2 * i] | (cs[2 * i + 1] << 4)
+    return codes.reshape(*v.shape[:-1], n // 2), scales.reshape(*v.shape[:-1], n // 32)
