@@ -345,6 +345,88 @@ moe_status_t moe_ffn_noalloc(const uint16_t* x, const uint8_t* w13, const uint8_
                              const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
                              int tile_m, uint16_t* out, cudaStream_t stream);
 
+/*
+ * ---------------------------------------------- MXFP4-quantised activations
+ * The layer variant whose GEMMs run MXFP4 x MXFP4 on the block-scaled tensor
+ * cores: x and the SwiGLU output are quantised to MXFP4 before the GEMM that
+ * reads them.  [OR] OpenRelay, "Gemma 4 31B from B200 to MI355X": section
+ * "optimisation 4" (a fused activation + up projection + MXFP4 quantisation
+ * kernel) and section "how far from the ceiling" (the matmuls measured
+ * against the MXFP4 peak).  The pages print no rounding rule; this library
+ * uses the OCP Microscaling v1.0 conversion, per 32 consecutive values:
+ *   e      = floor(log2(max |v|)) - 2, clamped to e >= -127
+ *   scale  = E8M0 byte e + 127 (byte 0 when every value is zero)
+ *   code_k = E2M1 nearest to v_k / 2^e, ties to the even code, magnitudes
+ *            above 6 saturating to 6, the sign of v_k kept
+ * codes packed two per byte, element 2i in the low nibble.
+ */
+
+/*
+ * moe_quantize_mxfp4 -- MXFP4 encoding of a bf16 matrix, row by row.
+ *   x      [rows, cols] bf16 (16-byte aligned), cols a multiple of 32.
+ *   codes  [rows, cols/2] (16-byte aligned), scales [rows, cols/32]: written.
+ * Bit-exact with the rule above.  MOE_ERR_UNSUPPORTED_SHAPE when cols % 32.
+ */
+moe_status_t moe_quantize_mxfp4(const uint16_t* x, int rows, int cols, uint8_t* codes,
+                                uint8_t* scales, cudaStream_t stream);
+
+/*
+ * moe_ffn_mxfp4act_workspace_size -- bytes of device workspace the calls
+ * below need: x codes [T, H/2] and scales [T, H/32], x codes in tile order
+ * [cap, H/2], h codes [cap, I/2] and scales [cap, I/32], y fp32 [T*Kt, H].
+ */
+size_t moe_ffn_mxfp4act_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
+
+/*
+ * moe_ffn_mxfp4act -- the expert FFN and combine with MXFP4 activations.
+ * Arguments, grouping and output as for moe_ffn; per pair (t, j), e = the
+ * pair's expert:
+ *   xq  = decode(quantise(x_t))                  (blocks of 32 along H)
+ *   g_n = W13[e][n] . xq,  u_n = W13[e][I+n] . xq (fp32 accumulation)
+ *   h   = decode(quantise(silu(g) * u))          (fp32 SwiGLU, blocks of 32 along I)
+ *   y   = topk_w[t, j] * (W2[e] . h)             (fp32)
+ *   out_t = bf16(sum over j ascending of y)
+ * Both GEMMs are tcgen05 block-scaled MXFP4 x MXFP4 contractions; the scales
+ * of weights and activations are applied inside the MMA.
+ * Limits: H % 128 == 0, I % 128 == 0, tile_m in {32, 64, 128, 256}, plus
+ * moe_ffn's limits; MOE_ERR_UNSUPPORTED_SHAPE otherwise.
+ * Numerics: x's encoding is exact (its inputs are bf16); h's encoding is
+ * decided on fp32 values whose accumulation order differs from a sequential
+ * sum, so an element lying within rounding distance of an E2M1 decision
+ * boundary may land on the neighbouring code.
+ */
+moe_status_t moe_ffn_mxfp4act(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                              const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                              const int32_t* sorted_pairs, const int32_t* expert_offsets,
+                              const int32_t* inv_pairs, const int32_t* tile_expert,
+                              const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                              int tile_m, uint16_t* out, void* workspace, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/*
+ * The two steps of moe_ffn_mxfp4act (it runs exactly these on one workspace):
+ *   moe_ffn_mxfp4act_gate_up: quantises x, gathers its code rows into tile
+ *     order and writes h's encoding for every sorted position p of the used
+ *     tiles (codes row p, scales row p; padding positions encode zeros);
+ *   moe_ffn_mxfp4act_down: the down GEMM from that encoding, scaled by the
+ *     routing weight, and the combine into out.
+ * moe_ffn_mxfp4act_h_offsets gives the byte offsets of h's codes [cap, I/2]
+ * and scales [cap, I/32] inside the workspace, so a caller can inspect h or
+ * supply its own.
+ */
+moe_status_t moe_ffn_mxfp4act_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                                      const int32_t* sorted_pairs, const int32_t* tile_expert,
+                                      const int32_t* num_tiles, int T, int H, int I, int Et,
+                                      int Kt, int tile_m, void* workspace, size_t ws_bytes,
+                                      cudaStream_t stream);
+moe_status_t moe_ffn_mxfp4act_down(const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                                   const int32_t* sorted_pairs, const int32_t* tile_expert,
+                                   const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                                   int tile_m, uint16_t* out, void* workspace, size_t ws_bytes,
+                                   cudaStream_t stream);
+moe_status_t moe_ffn_mxfp4act_h_offsets(int T, int H, int I, int Et, int Kt, int tile_m,
+                                        size_t* codes_offset, size_t* scales_offset);
+
 /* The path MOE_PATH_AUTO picks for these sizes [VL, small-M vs large-M]. */
 moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m);
 

@@ -1,0 +1,545 @@
+// ffn_mxfp4act.cu -- the expert FFN with MXFP4-quantised activations: x and
+// the SwiGLU output are quantised to MXFP4 and both GEMMs run as block-scaled
+// MXFP4 x MXFP4 contractions on the 5th-generation tensor cores
+// (tcgen05.mma kind::mxf4, E8M0 scales applied by the MMA itself).
+//
+// The pages fuse the activation with an MXFP4 quantisation that feeds an
+// MXFP4 GEMM and measure the matmuls against the MXFP4 peak (OpenRelay,
+// "Gemma 4 31B from B200 to MI355X", section "optimisation 4" and section
+// "how far from the ceiling").  Quantisation follows the OCP Microscaling v1.0
+// conversion: per 32 consecutive values, shared exponent e = floor(log2 amax)
+// - 2 (clamped to >= -127; scale byte e + 127, byte 0 for an all-zero block),
+// each value v / 2^e rounded to the nearest E2M1 value (ties to even,
+// saturating at 6) by the hardware conversion cvt.rn.satfinite.e2m1x2.f32.
+//
+// GEMM work item = one tile of N = tile_m token rows of one expert x one
+// block of 128 weight rows (64 gate + 64 up rows for gate_up; 128 rows of W2
+// for down); weights are the MMA's M side, tokens its N side.  Persistent
+// CTAs (one per SM), 320 threads:
+//   * producer warp: 2D TMA loads (128-byte swizzle) of the weight codes (two
+//     64-row boxes) and of the tile's activation codes (one N-row box), 256 k
+//     per stage, one transaction barrier per pair of stages;
+//   * MMA warp: one thread issues the four K = 64 MMAs of each stage, waits
+//     and commits once per pair of stages;
+//   * 4 scale warps, one per tensor-memory lane quadrant: write the stage's
+//     scale factors into tensor memory (tcgen05.st).  The MMA reads the
+//     weight row r's scale at lane r, column base + r / 32 (quadrant q reads
+//     column q), and token column n's at lane 32 q + n % 32, column base +
+//     n / 32 in every quadrant q; byte j of a 32-bit cell is k group j of a
+//     128-k chunk, the MMA's scale id (0 or 2) picks the pair of groups;
+//   * 4 epilogue warps: down scales the fp32 accumulator by the routing
+//     weight and stores y; gate_up passes each 32-column slice of the
+//     accumulator through shared memory (transposed), so each thread holds
+//     16 consecutive i of one token: SwiGLU in fp32, then MXFP4 quantisation
+//     of each 32-block of i (two threads per block), codes and scale stored.
+// Every wait is bounded (see mbar_wait); after a timeout each role stops, the
+// MMA thread drains its own MMAs (bounded), and tensor memory is freed.
+#include <algorithm>
+
+#include "moe_internal.h"
+#include "tcgen05.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kScaleWarp0 = 2;   // 2..5: warp % 4 covers every lane quadrant
+constexpr int kEpiWarp0 = 6;     // 6..9
+constexpr int kEpiThreads = 128;
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;  // 320
+constexpr int kBK = 256;                         // k per stage: one 128-byte row of packed codes
+constexpr int kRowBytes = kBK / 2;
+constexpr int kABytes = 128 * kRowBytes;         // 16 KB weight stage
+constexpr int kABox = 64;                        // weight rows per TMA box
+constexpr int kPrefetch = 8;                     // weight stages prefetched into L2 ahead
+
+template <int N>
+struct MxLayout {
+    static constexpr int kBBytes = N * kRowBytes;
+    static constexpr int kStage = kABytes + kBBytes;  // multiple of 1024
+    static constexpr int kStages = N >= 256 ? 4 : N >= 128 ? 6 : N >= 64 ? 8 : 10;
+    static_assert(kStages % 2 == 0, "whole pairs");
+    static constexpr int kPairs = kStages / 2;
+    static constexpr int kStgRow = 132;             // fp32 staging row (one column), padded
+    static constexpr int kStgBytes = 32 * kStgRow * 4;
+    static constexpr int kRing = kStages * kStage;
+    static constexpr int kTotal = kRing + kStgBytes + 256 + 1024;  // + barriers, alignment slack
+    static constexpr int kNJ = N / 32;              // 32-column groups of the tile
+    // tensor memory (512 columns): accumulators, then per stage 32 columns of
+    // scale factors, each 128-k chunk's block starting on a multiple of 8
+    // columns: weights (4 columns used) at +0 and +8, tokens (kNJ <= 8
+    // columns) at +16 and +24
+    static constexpr int kSfCols = 32;
+    static constexpr int kAccBufs = 2 * N + kStages * kSfCols <= 512 ? 2 : 1;
+    static constexpr int kSfCol0 = kAccBufs * N;
+    static_assert(kSfCol0 + kStages * kSfCols <= 512, "tensor memory");
+};
+
+// Instruction descriptor, kind::mxf4: E2M1 x E2M1 -> fp32, E8M0 scales, both
+// operands K-major, M x N, scale id `sf` for both operands.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, int sf) {
+    return ((uint32_t)sf << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24) | ((uint32_t)sf << 29);
+}
+
+// D (tensor memory) += A * B, both from shared memory, scale factors of A
+// and B in tensor memory (block size 32 along K).
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], "
+        "[%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+template <int NC>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* v);
+template <>
+__device__ __forceinline__ void tmem_st_cols<1>(uint32_t taddr, const uint32_t* v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v[0]) : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st_cols<2>(uint32_t taddr, const uint32_t* v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1])
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st_cols<4>(uint32_t taddr, const uint32_t* v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st_cols<8>(uint32_t taddr, const uint32_t* v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                     taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                 "r"(v[7])
+                 : "memory");
+}
+
+// ------------------------------------------------------------ quantisation
+
+// Two values -> one byte of E2M1 codes (lo in the low nibble), rounded to
+// nearest even with saturation to +-6 by the hardware conversion.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Scale byte of a block whose largest magnitude is amax (>= 0):
+// floor(log2 amax) - 2 + 127 = biased exponent - 2, clamped at 0 (zero and
+// subnormal amax, and blocks whose exponent would fall below -127).
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
+    return (uint32_t)max((int)((__float_as_uint(amax) >> 23) & 0xFFu) - 2, 0);
+}
+
+// 2^-(sbyte - 127) as fp32 (sbyte <= 252, so the exponent field 254 - sbyte
+// stays finite).
+__device__ __forceinline__ float mx_inv_scale(uint32_t sbyte) {
+    return __uint_as_float((254u - sbyte) << 23);
+}
+
+// Eight values times f -> four bytes of codes (v[0] in the lowest nibble).
+__device__ __forceinline__ uint32_t e2m1x8(const float* v, float f) {
+    return e2m1x2(v[0] * f, v[1] * f) | (e2m1x2(v[2] * f, v[3] * f) << 8) |
+           (e2m1x2(v[4] * f, v[5] * f) << 16) | (e2m1x2(v[6] * f, v[7] * f) << 24);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// One thread per 32-value block: 64 bytes of bf16 in, 16 bytes of codes and
+// one scale byte out.  Blocks are numbered row-major, so block i of the
+// whole matrix starts at element 32 i.
+__global__ void __launch_bounds__(256) quantize_mxfp4_kernel(const uint4* __restrict__ x,
+                                                             long long nblocks,
+                                                             uint4* __restrict__ codes,
+                                                             uint8_t* __restrict__ scales) {
+    pdl_begin();
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nblocks;
+         i += (long long)gridDim.x * blockDim.x) {
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 w = __ldg(x + 4 * i + c);
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[8 * c + 2 * j] = bf16_lo(u[j]);
+                v[8 * c + 2 * j + 1] = bf16_hi(u[j]);
+            }
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(v[k]));
+        const uint32_t sb = mx_scale_byte(amax);
+        const float f = mx_inv_scale(sb);
+        codes[i] = make_uint4(e2m1x8(v, f), e2m1x8(v + 8, f), e2m1x8(v + 16, f), e2m1x8(v + 24, f));
+        scales[i] = (uint8_t)sb;
+    }
+    pdl_end();
+}
+
+// ------------------------------------------------------------------ GEMM
+
+template <int MODE, int N>
+__global__ void __launch_bounds__(kThreads, 1)
+    mxf4_gemm_kernel(const GroupedGemm g, const __grid_constant__ CUtensorMap a_map,
+                     const __grid_constant__ CUtensorMap b_map) {
+    pdl_begin();
+    using L = MxLayout<N>;
+    constexpr int kStages = L::kStages, kPairs = L::kPairs, kNJ = L::kNJ;
+    constexpr int kAccBufs = L::kAccBufs;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    float* stg = reinterpret_cast<float*>(smem + L::kRing);
+    uint64_t* tma_full = reinterpret_cast<uint64_t*>(smem + L::kRing + L::kStgBytes);  // per pair
+    uint64_t* sf_full = tma_full + kPairs;        // scale factors written, per pair
+    uint64_t* stage_free = sf_full + kPairs;      // MMAs done with a pair
+    uint64_t* acc_full = stage_free + kPairs;     // [2]
+    uint64_t* acc_free = acc_full + 2;            // [2]
+    uint64_t* drain = acc_free + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    auto stage_a = [&](int s) { return smem + s * L::kStage; };
+    auto stage_b = [&](int s) { return smem + s * L::kStage + kABytes; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int K = g.K, KG = K / 32;
+    const int nk = ((K + kBK - 1) / kBK + 1) & ~1;  // stages per item, whole pairs
+    const int row_blocks = MODE == 0 ? g.I / 64 : g.rows / 128;
+    const int items = checked_tiles(g) * row_blocks;
+    constexpr uint32_t kTmemCols = 512;
+
+    if (tid == 0) {
+        for (int p = 0; p < kPairs; ++p) {
+            mbar_init(&tma_full[p], 1);
+            mbar_init(&sf_full[p], 4);
+            mbar_init(&stage_free[p], 1);
+        }
+        for (int b = 0; b < kAccBufs; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_free[b], 4);
+        }
+        mbar_init(drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------- producer
+        if (lane == 0) {
+            uint32_t gs = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+                const int tile = item / row_blocks, block = item % row_blocks;
+                const int e = checked_expert(g, tile, block == 0);
+                if (e < 0) continue;  // skipped by every role
+                const int ar0 = e * g.rows + (MODE == 0 ? block * 64 : block * 128);
+                const int ar1 = MODE == 0 ? e * g.rows + g.I + block * 64 : ar0 + kABox;
+                for (int st = 0; st < kPrefetch && st < nk; ++st) {
+                    tma_prefetch_l2_2d(&a_map, st * kRowBytes, ar0);
+                    tma_prefetch_l2_2d(&a_map, st * kRowBytes, ar1);
+                }
+                for (int st = 0; st < nk; ++st, ++gs) {
+                    const int s = gs % kStages, pr = (gs >> 1) % kPairs;
+                    if (st + kPrefetch < nk) {
+                        tma_prefetch_l2_2d(&a_map, (st + kPrefetch) * kRowBytes, ar0);
+                        tma_prefetch_l2_2d(&a_map, (st + kPrefetch) * kRowBytes, ar1);
+                    }
+                    if ((gs & 1) == 0) {  // both slots of a pair come free with one commit
+                        if (gs >= kStages && !mbar_wait(&stage_free[pr], ((gs / kStages) - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&tma_full[pr], (uint32_t)(2 * L::kStage));
+                    }
+                    const uint32_t a = smem_u32(stage_a(s));
+                    tma_load_2d(a, &a_map, st * kRowBytes, ar0, &tma_full[pr]);
+                    tma_load_2d(a + kABox * kRowBytes, &a_map, st * kRowBytes, ar1, &tma_full[pr]);
+                    tma_load_2d(smem_u32(stage_b(s)), &b_map, st * kRowBytes, tile * N, &tma_full[pr]);
+                }
+            }
+            // wait (bounded) until the last loads landed before the CTA can exit
+            for (int d = 0; d < kStages && d < (int)gs; d += 2) {
+                const uint32_t u = gs - 1 - d;
+                if (!mbar_wait(&tma_full[(u >> 1) % kPairs], (u / kStages) & 1)) break;
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            constexpr uint32_t idesc0 = idesc_mxf4(128, N, 0), idesc2 = idesc_mxf4(128, N, 2);
+            uint32_t gs = 0, it = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+                if (checked_expert(g, item / row_blocks, false) < 0) continue;
+                const uint32_t b = it % kAccBufs;
+                if (it >= (uint32_t)kAccBufs && !mbar_wait(&acc_free[b], ((it / kAccBufs) - 1) & 1)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + b * N;
+                for (int st = 0; st < nk; st += 2, gs += 2) {
+                    const int pr = (gs >> 1) % kPairs;
+                    const uint32_t par = (gs / kStages) & 1;
+                    if (!mbar_wait(&tma_full[pr], par) || !mbar_wait(&sf_full[pr], par)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int s = (gs + h2) % kStages;
+                        const uint64_t ad = sdesc_sw128(smem_u32(stage_a(s)));
+                        const uint64_t bd = sdesc_sw128(smem_u32(stage_b(s)));
+                        const uint32_t sf = tmem + (uint32_t)(L::kSfCol0 + s * L::kSfCols);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {  // K = 64 each: +32 bytes in the swizzle atom
+                            const int c = kk >> 1;
+                            mma_mxf4(d_tmem, ad + 2u * kk, bd + 2u * kk, (kk & 1) ? idesc2 : idesc0,
+                                     sf + 8u * c, sf + 16u + 8u * c, (st | h2 | kk) != 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(&stage_free[pr]);
+                }
+                if (ok) mma_commit(&acc_full[b]);
+                ++it;  // items processed (skipped ones use no accumulator)
+            }
+            mma_commit(drain);  // every MMA this thread issued has completed when this arrives
+            mbar_wait(drain, 0);
+        }
+    } else if (warp >= kScaleWarp0 && warp < kEpiWarp0) {
+        // ---------------------------------------------------- scale factors
+        const int quad = warp & 3;
+        const int rho = 32 * quad + lane;  // weight row of the stage = accumulator lane
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)L::kSfCol0;
+        uint32_t gs = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+            const int tile = item / row_blocks, block = item % row_blocks;
+            const int e = checked_expert(g, tile, false);
+            if (e < 0) continue;
+            const int wrow = MODE == 0 ? (rho < 64 ? block * 64 + rho : g.I + block * 64 + rho - 64)
+                                       : block * 128 + rho;
+            const uint8_t* sa = g.scales + ((size_t)e * g.rows + wrow) * (size_t)KG;
+            const uint8_t* sb[kNJ];
+#pragma unroll
+            for (int j = 0; j < kNJ; ++j) {
+                const int p = tile * N + 32 * j + lane;
+                if (MODE == 0) {
+                    const int q = checked_pair(g, p);
+                    sb[j] = q < 0 ? nullptr : g.act_scales + (size_t)(q / g.Kt) * KG;
+                } else {
+                    sb[j] = g.act_scales + (size_t)p * KG;
+                }
+            }
+            for (int st = 0; st < nk; st += 2, gs += 2) {
+                const int pr = (gs >> 1) % kPairs;
+                // the pair's scales first (global loads do not touch the ring)
+                uint32_t av[4], bv[4][kNJ];
+#pragma unroll
+                for (int hc = 0; hc < 4; ++hc) {  // hc = 2 * (stage of the pair) + chunk
+                    const int grp = 8 * st + 4 * hc;
+                    av[hc] = grp < KG ? __ldg(reinterpret_cast<const uint32_t*>(sa + grp)) : 0u;
+#pragma unroll
+                    for (int j = 0; j < kNJ; ++j)
+                        bv[hc][j] = (sb[j] && grp < KG)
+                                        ? __ldg(reinterpret_cast<const uint32_t*>(sb[j] + grp))
+                                        : 0u;
+                }
+                if (gs >= kStages && !mbar_wait(&stage_free[pr], ((gs / kStages) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();  // after the MMAs that last read these columns
+#pragma unroll
+                for (int hc = 0; hc < 4; ++hc) {
+                    const int s = (gs + (hc >> 1)) % kStages, c = hc & 1;
+                    const uint32_t col = lane_base + (uint32_t)(s * L::kSfCols);
+                    tmem_st_cols<1>(col + 8u * c + (uint32_t)quad, &av[hc]);
+                    tmem_st_cols<kNJ>(col + 16u + 8u * c, bv[hc]);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_full[pr]);
+            }
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int quad = warp & 3;                        // lanes 32 quad .. 32 quad + 31
+        const int et = (warp - kEpiWarp0) * 32 + lane;    // 0..127
+        uint32_t it = 0;
+        for (int item = blockIdx.x; item < items; item += gridDim.x) {
+            const int tile = item / row_blocks, block = item % row_blocks;
+            const int e = checked_expert(g, tile, false);
+            if (e < 0) continue;
+            const uint32_t b = it % kAccBufs;
+            int qv[kNJ];
+            float wv[kNJ];
+            if (MODE == 1) {
+#pragma unroll
+                for (int u = 0; u < kNJ; ++u) {
+                    qv[u] = checked_pair(g, tile * N + 32 * u + lane);
+                    wv[u] = qv[u] < 0 ? 0.0f : __ldg(g.topk_w + qv[u]);
+                }
+            }
+            if (!mbar_wait(&acc_full[b], (it / kAccBufs) & 1)) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < N; c0 += 32) {
+                uint32_t v[32];
+                const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + b * N + (uint32_t)c0;
+                tmem_ld16_nowait(taddr, v);
+                tmem_ld16_nowait(taddr + 16, v + 16);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (c0 + 32 == N) {  // the accumulator is drained: the next item may use it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_free[b]);
+                }
+                if (MODE == 1) {
+                    const int m = block * 128 + 32 * quad + lane;
+                    int q_lo = qv[0];
+                    float w_lo = wv[0];
+#pragma unroll
+                    for (int u = 1; u < kNJ; ++u)  // register select, no local memory
+                        if (u == c0 / 32) {
+                            q_lo = qv[u];
+                            w_lo = wv[u];
+                        }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int q = __shfl_sync(0xFFFFFFFFu, q_lo, i);
+                        const float w = __shfl_sync(0xFFFFFFFFu, w_lo, i);
+                        if (q >= 0) g.y_out[(size_t)q * g.rows + m] = w * __uint_as_float(v[i]);
+                    }
+                } else {
+                    // transpose through shared memory: stg[column][accumulator row]
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) stg[i * L::kStgRow + 32 * quad + lane] = __uint_as_float(v[i]);
+                    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+                    // thread -> (column, 32-block of i, half): rows 0..63 are the
+                    // gate rows of i = block * 64 + row, rows 64..127 the up rows
+                    const int half = et & 1, col = (et >> 1) & 31, blk = et >> 6;
+                    const float* gp = stg + col * L::kStgRow + 32 * blk + 16 * half;
+                    float a[16];
+                    float amax = 0.0f;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const float4 gv = *reinterpret_cast<const float4*>(gp + 4 * k4);
+                        const float4 uv = *reinterpret_cast<const float4*>(gp + 64 + 4 * k4);
+                        a[4 * k4 + 0] = silu(gv.x) * uv.x;
+                        a[4 * k4 + 1] = silu(gv.y) * uv.y;
+                        a[4 * k4 + 2] = silu(gv.z) * uv.z;
+                        a[4 * k4 + 3] = silu(gv.w) * uv.w;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(a[k]));
+                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+                    const uint32_t sbyte = mx_scale_byte(amax);
+                    const float f = mx_inv_scale(sbyte);
+                    const size_t p = (size_t)tile * N + c0 + col;
+                    const int i0 = block * 64 + 32 * blk + 16 * half;
+                    *reinterpret_cast<uint2*>(g.hq_codes + p * (size_t)(g.I / 2) + i0 / 2) =
+                        make_uint2(e2m1x8(a, f), e2m1x8(a + 8, f));
+                    if (half == 0) g.hq_scales[p * (size_t)(g.I / 32) + i0 / 32] = (uint8_t)sbyte;
+                    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+                }
+            }
+            ++it;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+    pdl_end();
+}
+
+template <int MODE, int N>
+cudaError_t launch_n(const GroupedGemm& g, cudaStream_t s) {
+    const size_t smem = MxLayout<N>::kTotal;
+    cudaError_t err = ensure_dynamic_smem((const void*)mxf4_gemm_kernel<MODE, N>, smem);
+    if (err != cudaSuccess) return err;
+    CUtensorMap a_map, b_map;
+    err = encode_codes_map(&a_map, g.codes, g.K / 2, (uint64_t)g.num_experts * g.rows, kRowBytes, kABox);
+    if (err != cudaSuccess) return err;
+    err = encode_codes_map(&b_map, g.act, g.K / 2, (uint64_t)g.act_rows, kRowBytes, N);
+    if (err != cudaSuccess) return err;
+    const int row_blocks = MODE == 0 ? g.I / 64 : g.rows / 128;
+    const long long max_items = (long long)g.max_tiles * row_blocks;
+    const int grid = (int)std::min<long long>(max_items, (long long)num_sms());
+    return launch_pdl(mxf4_gemm_kernel<MODE, N>, dim3(grid), dim3(kThreads), smem, s, g, a_map, b_map);
+}
+
+template <int MODE>
+cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
+    if (g.max_tiles == 0) return cudaSuccess;
+    switch (g.tile_m) {
+        case 32: return launch_n<MODE, 32>(g, s);
+        case 64: return launch_n<MODE, 64>(g, s);
+        case 128: return launch_n<MODE, 128>(g, s);
+        case 256: return launch_n<MODE, 256>(g, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_mxfp4(const uint16_t* x, int rows, int cols, uint8_t* codes,
+                                  uint8_t* scales, cudaStream_t s) {
+    const long long nblocks = (long long)rows * (cols / 32);
+    if (nblocks <= 0) return cudaSuccess;
+    const int blocks = (int)std::min<long long>((nblocks + 255) / 256, (long long)num_sms() * 8);
+    return launch_pdl(quantize_mxfp4_kernel, dim3(blocks), dim3(256), 0, s,
+                      reinterpret_cast<const uint4*>(x), nblocks, reinterpret_cast<uint4*>(codes),
+                      scales);
+}
+
+bool mxfp4act_tile_supported(int tile_m) {
+    return tile_m == 32 || tile_m == 64 || tile_m == 128 || tile_m == 256;
+}
+bool mxfp4act_shape_supported(int H, int I) { return H % 128 == 0 && I % 128 == 0; }
+cudaError_t launch_mxfp4act_gate_up(const GroupedGemm& g, cudaStream_t s) { return launch_mode<0>(g, s); }
+cudaError_t launch_mxfp4act_down(const GroupedGemm& g, cudaStream_t s) { return launch_mode<1>(g, s); }
+
+cudaError_t read_device_error_mxfp4act(int* flag, int clear) {
+    int wait = 0, index = 0;
+    cudaError_t err = cudaMemcpyFromSymbol(&wait, g_device_error, sizeof(int));
+    if (err == cudaSuccess) err = cudaMemcpyFromSymbol(&index, g_index_error, sizeof(int));
+    if (err != cudaSuccess) return err;
+    *flag = (wait ? 1 : 0) | (index ? 2 : 0);
+    if (!clear) return cudaSuccess;
+    const int zero = 0;
+    err = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    return err == cudaSuccess ? cudaMemcpyToSymbol(g_index_error, &zero, sizeof(int)) : err;
+}
+
+}  // namespace moe

@@ -39,6 +39,7 @@
 #include <algorithm>
 
 #include "moe_internal.h"
+#include "tcgen05.cuh"
 
 namespace moe {
 
@@ -56,25 +57,6 @@ constexpr int kACols = kBK / 2;                           // tensor-memory colum
 constexpr int kCodeBytes = 128 * (kBK / 2);               // 4 KB packed codes stage
 constexpr int kCodeBox = 64;                              // rows per codes box
 constexpr int kPrefetch = 12;                             // code stages prefetched into L2 ahead
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor for a K-major operand in the 128-byte
-// swizzled layout: 8-row groups of 128-byte rows, 1024 bytes apart.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr >> 4) & 0x3FFFu);          // start address
-    d |= (uint64_t)1u << 16;                          // leading byte offset (unused here)
-    d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;    // stride byte offset: next 8 rows
-    d |= (uint64_t)1u << 46;                          // descriptor version
-    d |= (uint64_t)2u << 61;                          // 128-byte swizzle
-    return d;
-}
 
 // Instruction descriptor: f16 x f16 -> fp32 (a and b format fields 0), both
 // operands K-major, M x N.
@@ -104,22 +86,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
         "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
         "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t* r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
 }
 
 

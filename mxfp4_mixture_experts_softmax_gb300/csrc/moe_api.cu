@@ -137,9 +137,11 @@ int moe_version(void) { return 100; }
 moe_status_t moe_device_error(int* flag, int clear) {
     if (!flag) return MOE_ERR_INVALID_ARG;
     int a = 0, b = 0;
+    int c = 0;
     cudaError_t err = read_device_error_prefill(&a, clear);
     if (err == cudaSuccess) err = read_device_error_decode(&b, clear);
-    *flag = a | b;
+    if (err == cudaSuccess) err = read_device_error_mxfp4act(&c, clear);
+    *flag = a | b | c;
     return cuda_status(err);
 }
 
@@ -542,6 +544,147 @@ moe_status_t moe_ffn(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, 
     return moe_ffn_path(x, w13, s13, w2, s2, topk_w, sorted_pairs, expert_offsets, inv_pairs,
                         tile_expert, num_tiles, T, H, I, Et, Kt, tile_m, out, workspace, ws_bytes,
                         MOE_PATH_AUTO, stream);
+}
+
+// ------------------------------------------------ MXFP4-quantised activations
+// Workspace: x codes [T, H/2], x scales [T, H/32], x codes gathered into tile
+// order [cap, H/2], h codes [cap, I/2], h scales [cap, I/32], y fp32 [T*Kt, H];
+// each region starts on a 256-byte boundary.
+struct MxLayoutWs {
+    size_t xc, xs, xg, hc, hs, y, total;
+};
+
+static bool mx_layout(int T, int H, int I, int Et, int Kt, int tile_m, MxLayoutWs* L) {
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    if (cap < 0 || T < 0 || H <= 0 || I <= 0 || Kt <= 0) return false;
+    L->xc = 0;
+    L->xs = L->xc + round_up((size_t)T * (H / 2), 256);
+    L->xg = L->xs + round_up((size_t)T * (H / 32), 256);
+    L->hc = L->xg + round_up((size_t)cap * (H / 2), 256);
+    L->hs = L->hc + round_up((size_t)cap * (I / 2), 256);
+    L->y = L->hs + round_up((size_t)cap * (I / 32), 256);
+    L->total = L->y + round_up((size_t)T * Kt * H * sizeof(float), 256);
+    return true;
+}
+
+size_t moe_ffn_mxfp4act_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m) {
+    MxLayoutWs L;
+    return mx_layout(T, H, I, Et, Kt, tile_m, &L) ? L.total : 0;
+}
+
+moe_status_t moe_ffn_mxfp4act_h_offsets(int T, int H, int I, int Et, int Kt, int tile_m,
+                                        size_t* codes_offset, size_t* scales_offset) {
+    MxLayoutWs L;
+    if (!codes_offset || !scales_offset || !mx_layout(T, H, I, Et, Kt, tile_m, &L))
+        return MOE_ERR_INVALID_ARG;
+    *codes_offset = L.hc;
+    *scales_offset = L.hs;
+    return MOE_OK;
+}
+
+static moe_status_t check_mx_shape(int T, int H, int I, int Et, int Kt, int tile_m) {
+    moe_path_t p = MOE_PATH_PREFILL;  // the general limits; the tile heights are checked below
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    if (cap < 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+    if (!mxfp4act_tile_supported(tile_m) || !mxfp4act_shape_supported(H, I))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    return check_ffn_shape(T, H, I, Et, Kt, tile_m, &p);
+}
+
+moe_status_t moe_quantize_mxfp4(const uint16_t* x, int rows, int cols, uint8_t* codes,
+                                uint8_t* scales, cudaStream_t stream) {
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (cols % 32 || (int64_t)rows * cols >= ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!ptrs_ok({x, codes}, 16) || !scales) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_quantize_mxfp4(x, rows, cols, codes, scales, stream));
+}
+
+moe_status_t moe_ffn_mxfp4act_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                                      const int32_t* sorted_pairs, const int32_t* tile_expert,
+                                      const int32_t* num_tiles, int T, int H, int I, int Et,
+                                      int Kt, int tile_m, void* workspace, size_t ws_bytes,
+                                      cudaStream_t stream) {
+    moe_status_t st = check_mx_shape(T, H, I, Et, Kt, tile_m);
+    if (st != MOE_OK || T == 0) return st;
+    if (!ptrs_ok({x, w13, workspace}, 16) || !ptrs_ok({s13, sorted_pairs, tile_expert, num_tiles}, 4))
+        return MOE_ERR_INVALID_ARG;
+    MxLayoutWs L;
+    mx_layout(T, H, I, Et, Kt, tile_m, &L);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    char* ws = reinterpret_cast<char*>(workspace);
+    cudaError_t err = launch_quantize_mxfp4(x, T, H, reinterpret_cast<uint8_t*>(ws + L.xc),
+                                            reinterpret_cast<uint8_t*>(ws + L.xs), stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    // the GEMM reads each tile's token rows as one box per stage: gather the
+    // code rows (H/2 bytes each) into tile order; the scales stay by token
+    err = launch_gather_rows(reinterpret_cast<const uint16_t*>(ws + L.xc), H / 4, sorted_pairs,
+                             num_tiles, tile_m, Kt, (int)cap, T * Kt,
+                             reinterpret_cast<uint16_t*>(ws + L.xg), stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, T, I, Et, Kt, tile_m,
+                              (int)(cap / tile_m));
+    g.codes = w13;
+    g.scales = s13;
+    g.rows = 2 * I;
+    g.K = H;
+    g.act = reinterpret_cast<const uint16_t*>(ws + L.xg);
+    g.act_rows = (int)cap;
+    g.act_scales = reinterpret_cast<const uint8_t*>(ws + L.xs);
+    g.hq_codes = reinterpret_cast<uint8_t*>(ws + L.hc);
+    g.hq_scales = reinterpret_cast<uint8_t*>(ws + L.hs);
+    trace("moe_ffn_mxfp4act_gate_up", T, H, I, Et, Kt, tile_m, MOE_PATH_PREFILL);
+    return cuda_status(launch_mxfp4act_gate_up(g, stream));
+}
+
+moe_status_t moe_ffn_mxfp4act_down(const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                                   const int32_t* sorted_pairs, const int32_t* tile_expert,
+                                   const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                                   int tile_m, uint16_t* out, void* workspace, size_t ws_bytes,
+                                   cudaStream_t stream) {
+    moe_status_t st = check_mx_shape(T, H, I, Et, Kt, tile_m);
+    if (st != MOE_OK || T == 0) return st;
+    if (!ptrs_ok({w2, out, workspace}, 16) ||
+        !ptrs_ok({s2, topk_w, sorted_pairs, tile_expert, num_tiles}, 4))
+        return MOE_ERR_INVALID_ARG;
+    MxLayoutWs L;
+    mx_layout(T, H, I, Et, Kt, tile_m, &L);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    char* ws = reinterpret_cast<char*>(workspace);
+    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, T, I, Et, Kt, tile_m,
+                              (int)(cap / tile_m));
+    g.codes = w2;
+    g.scales = s2;
+    g.rows = H;
+    g.K = I;
+    g.act = reinterpret_cast<const uint16_t*>(ws + L.hc);
+    g.act_rows = (int)cap;
+    g.act_scales = reinterpret_cast<const uint8_t*>(ws + L.hs);
+    g.y_out = reinterpret_cast<float*>(ws + L.y);
+    g.topk_w = topk_w;
+    trace("moe_ffn_mxfp4act_down", T, H, I, Et, Kt, tile_m, MOE_PATH_PREFILL);
+    cudaError_t err = launch_mxfp4act_down(g, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(launch_combine(g.y_out, nullptr, T, H, Kt, out, stream));
+}
+
+moe_status_t moe_ffn_mxfp4act(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                              const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                              const int32_t* sorted_pairs, const int32_t* expert_offsets,
+                              const int32_t* inv_pairs, const int32_t* tile_expert,
+                              const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
+                              int tile_m, uint16_t* out, void* workspace, size_t ws_bytes,
+                              cudaStream_t stream) {
+    moe_status_t st = check_mx_shape(T, H, I, Et, Kt, tile_m);
+    if (st != MOE_OK || T == 0) return st;
+    if (!ptrs_ok({expert_offsets, inv_pairs}, 4)) return MOE_ERR_INVALID_ARG;
+    st = moe_ffn_mxfp4act_gate_up(x, w13, s13, sorted_pairs, tile_expert, num_tiles, T, H, I, Et,
+                                  Kt, tile_m, workspace, ws_bytes, stream);
+    if (st != MOE_OK) return st;
+    return moe_ffn_mxfp4act_down(w2, s2, topk_w, sorted_pairs, tile_expert, num_tiles, T, H, I, Et,
+                                 Kt, tile_m, out, workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -63,6 +63,13 @@ struct GroupedGemm {
     uint16_t* h_out;             // SwiGLU output h [cap][I] (bf16)
     float* y_out;                // weighted output [T*Kt][H] (fp32)
     const float* topk_w;
+    // MXFP4-activation GEMMs: B rows are packed E2M1 codes ([act_rows][K/2],
+    // passed in `act`) with E8M0 scales act_scales ([T][K/32] by token for
+    // gate_up, [cap][K/32] by sorted position for down); gate_up writes h as
+    // codes hq_codes [cap][I/2] and scales hq_scales [cap][I/32]
+    const uint8_t* act_scales;
+    uint8_t* hq_codes;
+    uint8_t* hq_scales;
     // decode group factor 2^(s-126) as fp32 bits s * exp_one + exp_bias,
     // taken as runtime values so the multiply-add stays one instruction
     uint32_t exp_one = 1u << 23, exp_bias = 1u << 23;
@@ -145,6 +152,17 @@ __device__ __forceinline__ int checked_pair(const GroupedGemm& g, int pos) {
     }
     return q;
 }
+
+// MXFP4 activations: codes [rows][cols/2] and scales [rows][cols/32] of bf16
+// rows (cols a multiple of 32), OCP MX rounding (see ffn_mxfp4act.cu).
+cudaError_t launch_quantize_mxfp4(const uint16_t* x, int rows, int cols, uint8_t* codes,
+                                  uint8_t* scales, cudaStream_t s);
+bool mxfp4act_tile_supported(int tile_m);
+bool mxfp4act_shape_supported(int H, int I);
+// block-scaled MXFP4 x MXFP4 grouped GEMMs (tcgen05 kind::mxf4)
+cudaError_t launch_mxfp4act_gate_up(const GroupedGemm& g, cudaStream_t s);
+cudaError_t launch_mxfp4act_down(const GroupedGemm& g, cudaStream_t s);
+cudaError_t read_device_error_mxfp4act(int* flag, int clear);
 
 // grouping of one dense expert over T tokens (Kt = 1); ones[T] = 1 if given
 cudaError_t launch_identity_perm(int T, int tile_m, int cap, int max_tiles, int32_t* sorted_pairs,

@@ -1,0 +1,49 @@
+// tcgen05.cuh -- 5th-generation tensor-core helpers (sm_103a): fences, the
+// shared-memory matrix descriptor, MMA commit and tensor-memory loads.
+#pragma once
+
+#include "moe_device.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand in the 128-byte
+// swizzled layout: 8-row groups of 128-byte rows, 1024 bytes apart.  Adding
+// 2 to the descriptor moves its start 32 bytes along K inside the swizzle atom.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)1u << 16;                          // leading byte offset (unused here)
+    d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;    // stride byte offset: next 8 rows
+    d |= (uint64_t)1u << 46;                          // descriptor version
+    d |= (uint64_t)2u << 61;                          // 128-byte swizzle
+    return d;
+}
+
+// Arrives on the mbarrier once every tcgen05 operation this thread issued
+// before it has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// 16 consecutive 32-bit tensor-memory columns of this thread's lane (the
+// caller waits with tcgen05.wait::ld before using them).
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+}  // namespace moe

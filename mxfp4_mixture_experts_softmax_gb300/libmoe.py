@@ -30,7 +30,9 @@ EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_route_ex", "moe
            "moe_ffn_path", "moe_ffn_auto_path", "moe_ffn_gate_up", "moe_ffn_down", "moe_combine",
            "moe_ffn_y_offset", "moe_device_error", "moe_ffn_noalloc", "moe_combine_ex",
            "moe_ffn_dense_shared_workspace_size", "moe_ffn_dense_shared",
-           "moe_selftest_wait_timeout")
+           "moe_selftest_wait_timeout", "moe_quantize_mxfp4", "moe_ffn_mxfp4act_workspace_size",
+           "moe_ffn_mxfp4act", "moe_ffn_mxfp4act_gate_up", "moe_ffn_mxfp4act_down",
+           "moe_ffn_mxfp4act_h_offsets")
 
 # bytes of the fixed device scratch behind moe_ffn_noalloc (include/moe.h)
 MOE_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -106,6 +108,20 @@ def load(build: bool = True):
         L.moe_ffn_dense_shared.restype = ci
         L.moe_selftest_wait_timeout.argtypes = [ci, vp]
         L.moe_selftest_wait_timeout.restype = ci
+        L.moe_quantize_mxfp4.argtypes = [vp, ci, ci, vp, vp, vp]
+        L.moe_quantize_mxfp4.restype = ci
+        L.moe_ffn_mxfp4act_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci]
+        L.moe_ffn_mxfp4act_workspace_size.restype = sz
+        L.moe_ffn_mxfp4act.argtypes = ffn_args + [vp]
+        L.moe_ffn_mxfp4act.restype = ci
+        L.moe_ffn_mxfp4act_gate_up.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, sz,
+                                               vp]
+        L.moe_ffn_mxfp4act_gate_up.restype = ci
+        L.moe_ffn_mxfp4act_down.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp,
+                                            sz, vp]
+        L.moe_ffn_mxfp4act_down.restype = ci
+        L.moe_ffn_mxfp4act_h_offsets.argtypes = [ci, ci, ci, ci, ci, ci, vp, vp]
+        L.moe_ffn_mxfp4act_h_offsets.restype = ci
         L.moe_device_error.argtypes = [vp, ci]
         L.moe_device_error.restype = ci
         _lib = L
@@ -379,3 +395,84 @@ def moe_ffn_dense_shared(x, w13, s13, w2, s2, topk_w, perm: dict, w13s, s13s, w2
         _ptr(w13s), _ptr(s13s), _ptr(w2s), _ptr(s2s), Is, _ptr(shared_w), _ptr(out),
         _ptr(workspace), workspace.numel(), _stream(stream)), "moe_ffn_dense_shared")
     return out
+
+
+# ------------------------------------------------ MXFP4-quantised activations
+
+def moe_quantize_mxfp4(x, codes=None, scales=None, stream=None):
+    """bf16 [rows, cols] -> (codes uint8 [rows, cols/2], scales uint8 [rows, cols/32]),
+    OCP MX rounding (include/moe.h)."""
+    import torch
+    _dev(x, "x")
+    rows, cols = x.shape
+    if codes is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device)
+    _check(load().moe_quantize_mxfp4(_ptr(x), rows, cols, _ptr(codes), _ptr(scales),
+                                     _stream(stream)), "moe_quantize_mxfp4")
+    return codes, scales
+
+
+def moe_ffn_mxfp4act_workspace_size(T: int, H: int, I: int, Et: int, Kt: int, tile_m: int) -> int:
+    return int(load().moe_ffn_mxfp4act_workspace_size(T, H, I, Et, Kt, tile_m))
+
+
+def alloc_workspace_mxfp4act(T: int, H: int, I: int, Et: int, Kt: int, tile_m: int,
+                             device="cuda"):
+    import torch
+    n = moe_ffn_mxfp4act_workspace_size(T, H, I, Et, Kt, tile_m)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def moe_ffn_mxfp4act(x, w13, s13, w2, s2, topk_w, perm: dict, out=None, workspace=None,
+                     stream=None):
+    """The expert FFN with MXFP4-quantised activations (both GEMMs block-scaled MXFP4 x MXFP4)."""
+    import torch
+    T, H = x.shape
+    Et, twoI, _ = w13.shape
+    Kt, tile_m = perm["Kt"], perm["tile_m"]
+    for t in (x, w13, s13, w2, s2, topk_w):
+        _dev(t, "ffn input")
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = alloc_workspace_mxfp4act(T, H, twoI // 2, Et, Kt, tile_m, x.device)
+    _check(load().moe_ffn_mxfp4act(_ptr(x), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), _ptr(topk_w),
+                                   _ptr(perm["sorted_pairs"]), _ptr(perm["expert_offsets"]),
+                                   _ptr(perm["inv_pairs"]), _ptr(perm["tile_expert"]),
+                                   _ptr(perm["num_tiles"]), T, H, twoI // 2, Et, Kt, tile_m,
+                                   _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_ffn_mxfp4act")
+    return out
+
+
+def moe_ffn_mxfp4act_gate_up(x, w13, s13, perm: dict, workspace, stream=None):
+    T, H = x.shape
+    Et, twoI, _ = w13.shape
+    _check(load().moe_ffn_mxfp4act_gate_up(
+        _ptr(x), _ptr(w13), _ptr(s13), _ptr(perm["sorted_pairs"]), _ptr(perm["tile_expert"]),
+        _ptr(perm["num_tiles"]), T, H, twoI // 2, Et, perm["Kt"], perm["tile_m"], _ptr(workspace),
+        workspace.numel(), _stream(stream)), "moe_ffn_mxfp4act_gate_up")
+    return workspace
+
+
+def moe_ffn_mxfp4act_down(w2, s2, topk_w, perm: dict, workspace, T: int, out, stream=None):
+    Et, H, halfI = w2.shape
+    _check(load().moe_ffn_mxfp4act_down(
+        _ptr(w2), _ptr(s2), _ptr(topk_w), _ptr(perm["sorted_pairs"]), _ptr(perm["tile_expert"]),
+        _ptr(perm["num_tiles"]), T, H, 2 * halfI, Et, perm["Kt"], perm["tile_m"], _ptr(out),
+        _ptr(workspace), workspace.numel(), _stream(stream)), "moe_ffn_mxfp4act_down")
+    return out
+
+
+def mxfp4act_h_views(workspace, T: int, H: int, I: int, Et: int, Kt: int, tile_m: int):
+    """(h codes uint8 [cap, I/2], h scales uint8 [cap, I/32]) views of a moe_ffn_mxfp4act
+    workspace, rows by sorted position."""
+    co, so = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(load().moe_ffn_mxfp4act_h_offsets(T, H, I, Et, Kt, tile_m, ctypes.byref(co),
+                                             ctypes.byref(so)), "moe_ffn_mxfp4act_h_offsets")
+    cap = moe_permute_capacity(T, Kt, Et, tile_m)
+    codes = workspace[co.value:co.value + cap * (I // 2)].view(cap, I // 2)
+    scales = workspace[so.value:so.value + cap * (I // 32)].view(cap, I // 32)
+    return codes, scales
