@@ -39,7 +39,9 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="decode64")
-    p.add_argument("--tile-m", type=int, default=8)
+    p.add_argument("--tile-m", type=int, default=0,
+                   help="rows per expert tile (default: 8 for bf16; for mxfp4 32 below 16 mean "
+                        "rows per expert, else 128)")
     p.add_argument("--E", type=int, default=0,
                    help="routed experts override (smaller cases for profiler captures)")
     p.add_argument("--path", default="auto", choices=["auto", "decode", "prefill"])
@@ -48,6 +50,9 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--act", default="bf16", choices=["bf16", "mxfp4"],
+                   help="activations: bf16 (the layer as specified) or MXFP4-quantised "
+                        "(moe_ffn_mxfp4act, block-scaled MXFP4 x MXFP4 GEMMs)")
     return p.parse_args()
 
 
@@ -102,11 +107,18 @@ def tensor_peak():
     return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement)"
 
 
-def roofline_entry(kernel, bytes_, flops, seconds, traffic, traffic_src):
+# nominal dense FP4 / BF16 tensor rate on GB300 (13.5 / 2.25 PFLOP/s)
+FP4_OVER_BF16 = 6.0
+
+
+def roofline_entry(kernel, bytes_, flops, seconds, traffic, traffic_src, fp4=False):
     """The binding roofline of one kernel: whichever of HBM bytes and tensor
-    flops needs more time at peak."""
+    flops needs more time at peak.  fp4: the contraction runs on MXFP4
+    operands, so its peak is the bf16 peak times the nominal FP4/BF16 ratio."""
     hbm, hbm_src = hbm_peak()
     ten, ten_src = tensor_peak()
+    if fp4:
+        ten, ten_src = ten * FP4_OVER_BF16, f"derived: {ten_src} x {FP4_OVER_BF16:g} (nominal FP4/BF16)"
     t_hbm = bytes_ / (hbm * 1e9)
     t_ten = flops / (ten * 1e12)
     hbm_ach = bytes_ / seconds / 1e9
@@ -198,8 +210,10 @@ def gpu_id_for(device_index: int) -> str:
 
 # ------------------------------------------------------- algorithmic work
 
-def layer_work(w, ids_host):
-    """Algorithmic HBM bytes and flops of one step, from the actual routing."""
+def layer_work(w, ids_host, act="bf16"):
+    """Algorithmic HBM bytes and flops of one step, from the actual routing.
+    act="mxfp4": x and h move as MXFP4 (codes + scales), and the down step
+    includes the combine (y read, out written)."""
     import numpy as np
     from mxfp4_mixture_experts_softmax_gb300 import synth
     touched = int(np.unique(ids_host).size)
@@ -211,6 +225,12 @@ def layer_work(w, ids_host):
     layer = (touched * synth.weight_bytes_per_expert(w) + T * H * 4 + P * I * 4
              + T * w.E * 4)                                     # + x, out, h, logits
     flops = 2 * P * (2 * I * H + H * I)
+    if act == "mxfp4":
+        xq, hq = H // 2 + H // 32, I // 2 + I // 32       # MXFP4 bytes per row
+        gate_up = touched * w13_b + T * H * 2 + T * xq + 2 * P * xq + P * hq
+        down = touched * w2_b + P * hq + 2 * P * H * 4 + T * H * 2
+        layer = touched * synth.weight_bytes_per_expert(w) + T * H * 4 + P * (2 * hq + 2 * xq) \
+            + 2 * P * H * 4 + T * w.E * 4
     return dict(touched=touched, gate_up_bytes=gate_up, down_bytes=down, layer_bytes=layer,
                 flops=flops, gate_up_flops=2 * P * 2 * I * H)
 
@@ -250,6 +270,8 @@ def run_ours(args, ws, rank, local):
     path = {"auto": libmoe.MOE_PATH_AUTO, "decode": libmoe.MOE_PATH_DECODE,
             "prefill": libmoe.MOE_PATH_PREFILL}[args.path]
     tm = args.tile_m
+    if not tm:
+        tm = 8 if args.act == "bf16" else (32 if w.T * w.Kt < 16 * w.Et else 128)
     host = synth.make_inputs(w)
 
     def up(a):
@@ -264,8 +286,11 @@ def run_ours(args, ws, rank, local):
         weights.append({k: v.clone() for k, v in weights[0].items()})
     logits = [up(host["logits"]) for _ in range(R)]
     xs = [up(host["x"]) for _ in range(R)]
+    mx = args.act == "mxfp4"
     bufs = libmoe.alloc_layer(w.T, w.E, w.K, w.with_shared, w.H, w.I, w.Et, tm, dev)
     h_buf, y_buf = libmoe.ffn_views(bufs["workspace"], w.T, w.H, w.I, w.Et, w.Kt, tm)
+    if mx:  # the MXFP4-activation workspace replaces the bf16 one
+        bufs["workspace"] = libmoe.alloc_workspace_mxfp4act(w.T, w.H, w.I, w.Et, w.Kt, tm, dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(i, ev=None, gemm_ev=None):
@@ -283,17 +308,25 @@ def run_ours(args, ws, rank, local):
             ev[1].record(stream)
         if gemm_ev is not None:
             gemm_ev[0].record(stream)
-        libmoe.moe_ffn_gate_up(xs[r], W["w13"], W["s13"], perm, bufs["workspace"], path)
+        if mx:
+            libmoe.moe_ffn_mxfp4act_gate_up(xs[r], W["w13"], W["s13"], perm, bufs["workspace"])
+        else:
+            libmoe.moe_ffn_gate_up(xs[r], W["w13"], W["s13"], perm, bufs["workspace"], path)
         if ev is not None:
             ev[2].record(stream)
         if gemm_ev is not None:
             gemm_ev[1].record(stream)
-        libmoe.moe_ffn_down(W["w2"], W["s2"], tw, perm, bufs["workspace"], w.T, path)
+        if mx:  # down GEMM and the combine into out
+            libmoe.moe_ffn_mxfp4act_down(W["w2"], W["s2"], tw, perm, bufs["workspace"], w.T,
+                                         bufs["out"])
+        else:
+            libmoe.moe_ffn_down(W["w2"], W["s2"], tw, perm, bufs["workspace"], w.T, path)
         if ev is not None:
             ev[3].record(stream)
         if gemm_ev is not None:
             gemm_ev[2].record(stream)
-        libmoe.moe_combine(y_buf, w.T, w.H, w.Kt, bufs["out"])
+        if not mx:
+            libmoe.moe_combine(y_buf, w.T, w.H, w.Kt, bufs["out"])
         if ev is not None:
             ev[4].record(stream)
 
@@ -301,7 +334,7 @@ def run_ours(args, ws, rank, local):
         step(i)
     torch.cuda.synchronize(dev)
     ids_host = bufs["topk_ids"].cpu().numpy()
-    work = layer_work(w, ids_host)
+    work = layer_work(w, ids_host, args.act)
 
     K = args.steps
     gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
@@ -343,9 +376,17 @@ def run_ours(args, ws, rank, local):
     def e2e_step():
         logits[0].copy_(pin_logits, non_blocking=True)
         xs[0].copy_(pin_x, non_blocking=True)
-        libmoe.moe_layer(logits[0], xs[0], weights[0]["w13"], weights[0]["s13"],
-                         weights[0]["w2"], weights[0]["s2"], w.K, w.with_shared, w.renormalize,
-                         tile_m=tm, path=path, bufs=bufs)
+        if mx:
+            _, tw, perm = libmoe.moe_route_permute(logits[0], w.K, tm, w.with_shared,
+                                                   w.renormalize, bufs["topk_ids"],
+                                                   bufs["topk_w"], bufs["perm"])
+            libmoe.moe_ffn_mxfp4act(xs[0], weights[0]["w13"], weights[0]["s13"],
+                                    weights[0]["w2"], weights[0]["s2"], tw, perm, bufs["out"],
+                                    bufs["workspace"])
+        else:
+            libmoe.moe_layer(logits[0], xs[0], weights[0]["w13"], weights[0]["s13"],
+                             weights[0]["w2"], weights[0]["s2"], w.K, w.with_shared,
+                             w.renormalize, tile_m=tm, path=path, bufs=bufs)
         pin_out.copy_(bufs["out"], non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
@@ -367,14 +408,18 @@ def run_ours(args, ws, rank, local):
         path_name = "prefill" if (args.path == "prefill" or (
             args.path == "auto" and libmoe.moe_ffn_auto_path(w.T, w.Kt, w.Et, tm)
             == libmoe.MOE_PATH_PREFILL)) else "decode"
-        src = "ffn_prefill.cu" if path_name == "prefill" else "ffn_decode.cu"
+        if mx:
+            path_name = "mxfp4act"
+        src = {"prefill": "ffn_prefill.cu", "decode": "ffn_decode.cu",
+               "mxfp4act": "ffn_mxfp4act.cu"}[path_name]
         traffic, traffic_src = traffic_from_profiles(
             f"{path_name}_gate_up", w.name,
             os.path.join(ROOT, "mxfp4_mixture_experts_softmax_gb300", "csrc", src))
         gu = roofline_entry(f"{path_name}_gate_up", work["gate_up_bytes"], work["gate_up_flops"],
-                            per["gate_up"] / 1e3, traffic, traffic_src)
-        dn = roofline_entry(f"{path_name}_down", work["down_bytes"],
-                            work["flops"] - work["gate_up_flops"], per["down"] / 1e3, None, None)
+                            per["gate_up"] / 1e3, traffic, traffic_src, fp4=mx)
+        dn = roofline_entry(f"{path_name}_down" + ("_combine" if mx else ""), work["down_bytes"],
+                            work["flops"] - work["gate_up_flops"], per["down"] / 1e3, None, None,
+                            fp4=mx)
         layer_s = total_ms / K / 1e3  # the whole step, gaps between launches included
         result = {
             "metric": METRIC,
@@ -387,12 +432,14 @@ def run_ours(args, ws, rank, local):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f16",  # MMA operand type (bf16 in and out, fp32 accumulation)
+            # MMA operand type (bf16 in and out, fp32 accumulation)
+            "dtype": "e2m1" if mx else "f16",
             "data": "synthetic (seeded; random MXFP4 weights, N(0,1) activations and logits)",
             "config": {
                 "workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K,
                 "shared_expert": w.with_shared, "Et": w.Et, "Kt": w.Kt, "tile_m": tm,
                 "path": path_name, "experts_touched": work["touched"],
+                "activations": "mxfp4 (OCP MX quantisation of x and h)" if mx else "bf16",
                 "parallelism": f"replicas x{ws} (weak scaling, tokens per GPU fixed)",
                 "l2": f"inputs larger than L2: {work['layer_bytes'] / 1e9:.2f} GB touched per "
                       f"step, {R} weight replicas rotated per step",
@@ -400,21 +447,22 @@ def run_ours(args, ws, rank, local):
             "roofline": gu,
             "roofline_down": dn,
             "layer_roofline": roofline_entry("layer", work["layer_bytes"], work["flops"],
-                                             layer_s, None, None),
+                                             layer_s, None, None, fp4=mx),
             "kernels_us": {n: v * 1e3 for n, v in per.items()},
             "e2e": {"value": w.T * K * ws / (e2e_ms / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": int(host["logits"].nbytes + host["x"].nbytes),
                     "d2h_bytes_per_step": int(w.T * w.H * 2),
                     "ms_per_step": e2e_ms / K},
             # route + permute (one launch up to MOE_ROUTE_PERMUTE_FUSED_MAX_T
-            # tokens, else two), x -> f16 rows, [prefill: gather rows by tile],
-            # gate_up, h -> f16 rows, down, combine
+            # tokens, else two), then bf16: x -> f16 rows, [prefill: gather rows
+            # by tile], gate_up, h -> f16 rows, down, combine; mxfp4: quantise
+            # x, gather code rows, gate_up, down, combine
             "gpu_launches": ((1 if w.T <= libmoe.MOE_ROUTE_PERMUTE_FUSED_MAX_T else 2)
                              + (6 if path_name == "prefill" else 5)) * K,
             "clocks": clocks,
         }
         if ws == 1 and not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(w, host, ids_host, args.cpu_seconds)
+            result["cpu_baseline"] = cpu_baseline(w, host, ids_host, args.cpu_seconds, args.act)
     if ws > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -423,17 +471,18 @@ def run_ours(args, ws, rank, local):
 
 # ---------------------------------------------------------- the oracle
 
-def _oracle_sample(w, host, ids, wt, n_tokens, threads, offset=0):
+def _oracle_sample(w, host, ids, wt, n_tokens, threads, offset=0, act="bf16"):
     import numpy as np
     import oracle
     toks = ((np.arange(n_tokens) + offset) % w.T).astype(np.int32)
+    fn = oracle.ffn_mxfp4act if act == "mxfp4" else oracle.ffn
     t0 = time.perf_counter()
-    oracle.ffn(host["x"], host["w13"], host["s13"], host["w2"], host["s2"], ids, wt,
-               tokens=toks, n_threads=threads)
+    fn(host["x"], host["w13"], host["s13"], host["w2"], host["s2"], ids, wt, tokens=toks,
+       n_threads=threads)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(w, host, ids_unused, target_s):
+def cpu_baseline(w, host, ids_unused, target_s, act="bf16"):
     """The CPU oracle as it stands, timed on this host's cores on a bounded
     sample of the same workload (whole tokens: routing plus all Kt experts)."""
     import oracle
@@ -443,12 +492,12 @@ def cpu_baseline(w, host, ids_unused, target_s):
     ids, wt = oracle.route(host["logits"], w.K, w.with_shared, w.renormalize)
     route_s = time.perf_counter() - t0
     n = threads
-    dt = _oracle_sample(w, host, ids, wt, n, threads)
+    dt = _oracle_sample(w, host, ids, wt, n, threads, act=act)
     total_tok, total_s = n, dt
     while total_s < target_s and total_tok < 4 * w.T:
         n2 = max(threads, int(n * (target_s - total_s) / max(dt, 1e-3)) // threads * threads)
         n2 = min(n2, 4 * w.T - total_tok)
-        dt = _oracle_sample(w, host, ids, wt, n2, threads, offset=total_tok)
+        dt = _oracle_sample(w, host, ids, wt, n2, threads, offset=total_tok, act=act)
         total_tok += n2
         total_s += dt
     per_tok_route = route_s / w.T
@@ -472,7 +521,7 @@ def run_reference(args, ws, rank):
 
     def step(i):
         ids, wt = oracle.route(host["logits"], w.K, w.with_shared, w.renormalize)
-        _oracle_sample(w, host, ids, wt, n, threads, offset=i * n)
+        _oracle_sample(w, host, ids, wt, n, threads, offset=i * n, act=args.act)
 
     for i in range(args.warmup):
         step(i)
@@ -489,7 +538,7 @@ def run_reference(args, ws, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded)",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K,
-                   "shared_expert": w.with_shared},
+                   "shared_expert": w.with_shared, "activations": args.act},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,

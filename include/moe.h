@@ -372,8 +372,11 @@ moe_status_t moe_quantize_mxfp4(const uint16_t* x, int rows, int cols, uint8_t* 
 
 /*
  * moe_ffn_mxfp4act_workspace_size -- bytes of device workspace the calls
- * below need: x codes [T, H/2] and scales [T, H/32], x codes in tile order
- * [cap, H/2], h codes [cap, I/2] and scales [cap, I/32], y fp32 [T*Kt, H].
+ * below need: x codes [T, H/2] and scales [T, H/32], both again in tile
+ * order [cap, ...], h codes [cap, I/2] and scales [cap, I/32], the routing
+ * weight of each sorted position fp32 [cap], and y fp32 blocked by 128
+ * output rows [H/128, cap, 128] (row block, sorted position, row), so each
+ * down-GEMM work item writes one contiguous run.
  */
 size_t moe_ffn_mxfp4act_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
 
@@ -390,10 +393,12 @@ size_t moe_ffn_mxfp4act_workspace_size(int T, int H, int I, int Et, int Kt, int 
  * of weights and activations are applied inside the MMA.
  * Limits: H % 128 == 0, I % 128 == 0, tile_m in {32, 64, 128, 256}, plus
  * moe_ffn's limits; MOE_ERR_UNSUPPORTED_SHAPE otherwise.
- * Numerics: x's encoding is exact (its inputs are bf16); h's encoding is
- * decided on fp32 values whose accumulation order differs from a sequential
- * sum, so an element lying within rounding distance of an E2M1 decision
- * boundary may land on the neighbouring code.
+ * Numerics: x's encoding is exact (its inputs are bf16).  h's encoding is
+ * decided on fp32 values: the GEMM's fp32 sums (exact for the configured
+ * scale ranges, whose products and partial sums fit 24 bits) and silu
+ * computed with the fast exponential and division, a few ulp from the
+ * correctly rounded result, so an element lying within that distance of an
+ * E2M1 decision boundary may land on the neighbouring code.
  */
 moe_status_t moe_ffn_mxfp4act(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
                               const uint8_t* w2, const uint8_t* s2, const float* topk_w,
@@ -409,7 +414,8 @@ moe_status_t moe_ffn_mxfp4act(const uint16_t* x, const uint8_t* w13, const uint8
  *     order and writes h's encoding for every sorted position p of the used
  *     tiles (codes row p, scales row p; padding positions encode zeros);
  *   moe_ffn_mxfp4act_down: the down GEMM from that encoding, scaled by the
- *     routing weight, and the combine into out.
+ *     routing weight, and the combine into out (inv_pairs: the position of
+ *     each pair, from moe_permute).
  * moe_ffn_mxfp4act_h_offsets gives the byte offsets of h's codes [cap, I/2]
  * and scales [cap, I/32] inside the workspace, so a caller can inspect h or
  * supply its own.
@@ -420,10 +426,10 @@ moe_status_t moe_ffn_mxfp4act_gate_up(const uint16_t* x, const uint8_t* w13, con
                                       int Kt, int tile_m, void* workspace, size_t ws_bytes,
                                       cudaStream_t stream);
 moe_status_t moe_ffn_mxfp4act_down(const uint8_t* w2, const uint8_t* s2, const float* topk_w,
-                                   const int32_t* sorted_pairs, const int32_t* tile_expert,
-                                   const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
-                                   int tile_m, uint16_t* out, void* workspace, size_t ws_bytes,
-                                   cudaStream_t stream);
+                                   const int32_t* sorted_pairs, const int32_t* inv_pairs,
+                                   const int32_t* tile_expert, const int32_t* num_tiles, int T,
+                                   int H, int I, int Et, int Kt, int tile_m, uint16_t* out,
+                                   void* workspace, size_t ws_bytes, cudaStream_t stream);
 moe_status_t moe_ffn_mxfp4act_h_offsets(int T, int H, int I, int Et, int Kt, int tile_m,
                                         size_t* codes_offset, size_t* scales_offset);
 

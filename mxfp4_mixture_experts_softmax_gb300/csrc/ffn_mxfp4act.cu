@@ -18,17 +18,22 @@
 // CTAs (one per SM), 320 threads:
 //   * producer warp: 2D TMA loads (128-byte swizzle) of the weight codes (two
 //     64-row boxes) and of the tile's activation codes (one N-row box), 256 k
-//     per stage, one transaction barrier per pair of stages;
+//     per stage, one transaction barrier per pair of stages; with K % 512 ==
+//     0 also the pair's 16 scale bytes of every weight row and token row;
 //   * MMA warp: one thread issues the four K = 64 MMAs of each stage, waits
 //     and commits once per pair of stages;
 //   * 4 scale warps, one per tensor-memory lane quadrant: write the stage's
-//     scale factors into tensor memory (tcgen05.st).  The MMA reads the
+//     scale factors into tensor memory (tcgen05.st), read from the pair's
+//     shared-memory slot (or, for other K, loaded from global memory).  The MMA reads the
 //     weight row r's scale at lane r, column base + r / 32 (quadrant q reads
 //     column q), and token column n's at lane 32 q + n % 32, column base +
 //     n / 32 in every quadrant q; byte j of a 32-bit cell is k group j of a
 //     128-k chunk, the MMA's scale id (0 or 2) picks the pair of groups;
 //   * 4 epilogue warps: down scales the fp32 accumulator by the routing
-//     weight and stores y; gate_up passes each 32-column slice of the
+//     weight and stores it to y blocked as [H/128][cap][128] (row block,
+//     sorted position, row in block), so an item's output is one contiguous
+//     64 KB run of DRAM writes instead of 128-byte pieces 16 KB apart;
+//     the combine gathers each token's positions from it; gate_up passes each 32-column slice of the
 //     accumulator through shared memory (transposed), so each thread holds
 //     16 consecutive i of one token: SwiGLU in fp32, then MXFP4 quantisation
 //     of each 32-block of i (two threads per block), codes and scale stored.
@@ -55,17 +60,28 @@ constexpr int kABytes = 128 * kRowBytes;         // 16 KB weight stage
 constexpr int kABox = 64;                        // weight rows per TMA box
 constexpr int kPrefetch = 8;                     // weight stages prefetched into L2 ahead
 
-template <int N>
+constexpr int kSmemLimit = 232448;               // dynamic shared memory per block
+
+template <int MODE, int N>
 struct MxLayout {
     static constexpr int kBBytes = N * kRowBytes;
     static constexpr int kStage = kABytes + kBBytes;  // multiple of 1024
-    static constexpr int kStages = N >= 256 ? 4 : N >= 128 ? 6 : N >= 64 ? 8 : 10;
-    static_assert(kStages % 2 == 0, "whole pairs");
-    static constexpr int kPairs = kStages / 2;
+    // scale bytes of one pair of stages (16 per row: 512 k), TMA-loaded
+    static constexpr int kSfaBytes = 128 * 16;
+    static constexpr int kSfPairBytes = kSfaBytes + N * 16;
     static constexpr int kStgRow = 132;             // fp32 staging row (one column), padded
-    static constexpr int kStgBytes = 32 * kStgRow * 4;
+    static constexpr int kStgBytes = MODE == 0 ? 32 * kStgRow * 4 : 0;  // gate_up epilogue only
+    // the deepest even ring that fits (at most 10 stages)
+    static constexpr int kFit = (kSmemLimit - 1024 - 256 - kStgBytes) / (kStage + kSfPairBytes / 2);
+    static constexpr int kStages = (kFit > 10 ? 10 : kFit) & ~1;
+    static_assert(kStages >= 4, "ring depth");
+    static constexpr int kPairs = kStages / 2;
     static constexpr int kRing = kStages * kStage;
-    static constexpr int kTotal = kRing + kStgBytes + 256 + 1024;  // + barriers, alignment slack
+    static constexpr int kSf = kRing;               // scale slots, one per pair
+    static constexpr int kStg = kSf + kPairs * kSfPairBytes;
+    static constexpr int kBar = kStg + kStgBytes;
+    static constexpr int kTotal = kBar + 256 + 1024;  // + barriers, alignment slack
+    static_assert(kTotal <= kSmemLimit, "shared memory");
     static constexpr int kNJ = N / 32;              // 32-column groups of the tile
     // tensor memory (512 columns): accumulators, then per stage 32 columns of
     // scale factors, each 128-k chunk's block starting on a multiple of 8
@@ -195,18 +211,32 @@ __global__ void __launch_bounds__(256) quantize_mxfp4_kernel(const uint4* __rest
 
 // ------------------------------------------------------------------ GEMM
 
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+
+// silu(g) * u in fp32 with the fast exponential and division (a few ulp from
+// the correctly rounded operations).
+__device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+
 template <int MODE, int N>
 __global__ void __launch_bounds__(kThreads, 1)
     mxf4_gemm_kernel(const GroupedGemm g, const __grid_constant__ CUtensorMap a_map,
-                     const __grid_constant__ CUtensorMap b_map) {
+                     const __grid_constant__ CUtensorMap b_map,
+                     const __grid_constant__ CUtensorMap sfa_map,
+                     const __grid_constant__ CUtensorMap sfb_map) {
     pdl_begin();
-    using L = MxLayout<N>;
+    using L = MxLayout<MODE, N>;
     constexpr int kStages = L::kStages, kPairs = L::kPairs, kNJ = L::kNJ;
     constexpr int kAccBufs = L::kAccBufs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    float* stg = reinterpret_cast<float*>(smem + L::kRing);
-    uint64_t* tma_full = reinterpret_cast<uint64_t*>(smem + L::kRing + L::kStgBytes);  // per pair
+    float* stg = reinterpret_cast<float*>(smem + L::kStg);
+    uint64_t* tma_full = reinterpret_cast<uint64_t*>(smem + L::kBar);  // per pair
     uint64_t* sf_full = tma_full + kPairs;        // scale factors written, per pair
     uint64_t* stage_free = sf_full + kPairs;      // MMAs done with a pair
     uint64_t* acc_full = stage_free + kPairs;     // [2]
@@ -215,6 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     auto stage_a = [&](int s) { return smem + s * L::kStage; };
     auto stage_b = [&](int s) { return smem + s * L::kStage + kABytes; };
+    auto sf_slot = [&](int pr) { return smem + L::kSf + pr * L::kSfPairBytes; };
+    const bool sf_tma = g.sf_tma != 0;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = g.K, KG = K / 32;
@@ -274,7 +306,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&tma_full[pr], (uint32_t)(2 * L::kStage));
+                        mbar_arrive_expect_tx(&tma_full[pr],
+                                              (uint32_t)(2 * L::kStage + (sf_tma ? L::kSfPairBytes : 0)));
+                        if (sf_tma) {  // the pair's 16 scale groups of each row
+                            const uint32_t sfd = smem_u32(sf_slot(pr));
+                            const int kx = (st >> 1) * 16;
+                            tma_load_2d(sfd, &sfa_map, kx, ar0, &tma_full[pr]);
+                            tma_load_2d(sfd + kABox * 16, &sfa_map, kx, ar1, &tma_full[pr]);
+                            tma_load_2d(sfd + L::kSfaBytes, &sfb_map, kx, tile * N, &tma_full[pr]);
+                        }
                     }
                     const uint32_t a = smem_u32(stage_a(s));
                     tma_load_2d(a, &a_map, st * kRowBytes, ar0, &tma_full[pr]);
@@ -347,7 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < kNJ; ++j) {
                 const int p = tile * N + 32 * j + lane;
-                if (MODE == 0) {
+                if (sf_tma) {
+                    sb[j] = nullptr;
+                } else if (MODE == 0) {
                     const int q = checked_pair(g, p);
                     sb[j] = q < 0 ? nullptr : g.act_scales + (size_t)(q / g.Kt) * KG;
                 } else {
@@ -356,21 +398,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int st = 0; st < nk; st += 2, gs += 2) {
                 const int pr = (gs >> 1) % kPairs;
-                // the pair's scales first (global loads do not touch the ring)
+                // hc = 2 * (stage of the pair) + chunk: 4 scale bytes of a 128-k chunk
                 uint32_t av[4], bv[4][kNJ];
+                if (sf_tma) {
+                    // the pair's slot is filled once the producer saw the MMAs
+                    // that last read these tensor-memory columns complete
+                    if (!mbar_wait(&tma_full[pr], (gs / kStages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint4 a4 = lds128(sf_slot(pr) + rho * 16);
+                    av[0] = a4.x, av[1] = a4.y, av[2] = a4.z, av[3] = a4.w;
 #pragma unroll
-                for (int hc = 0; hc < 4; ++hc) {  // hc = 2 * (stage of the pair) + chunk
-                    const int grp = 8 * st + 4 * hc;
-                    av[hc] = grp < KG ? __ldg(reinterpret_cast<const uint32_t*>(sa + grp)) : 0u;
+                    for (int j = 0; j < kNJ; ++j) {
+                        const uint4 b4 = lds128(sf_slot(pr) + L::kSfaBytes + (32 * j + lane) * 16);
+                        bv[0][j] = b4.x, bv[1][j] = b4.y, bv[2][j] = b4.z, bv[3][j] = b4.w;
+                    }
+                } else {
+                    // global loads first (they do not touch the ring)
 #pragma unroll
-                    for (int j = 0; j < kNJ; ++j)
-                        bv[hc][j] = (sb[j] && grp < KG)
-                                        ? __ldg(reinterpret_cast<const uint32_t*>(sb[j] + grp))
-                                        : 0u;
-                }
-                if (gs >= kStages && !mbar_wait(&stage_free[pr], ((gs / kStages) - 1) & 1)) {
-                    ok = false;
-                    break;
+                    for (int hc = 0; hc < 4; ++hc) {
+                        const int grp = 8 * st + 4 * hc;
+                        av[hc] = grp < KG ? __ldg(reinterpret_cast<const uint32_t*>(sa + grp)) : 0u;
+#pragma unroll
+                        for (int j = 0; j < kNJ; ++j)
+                            bv[hc][j] = (sb[j] && grp < KG)
+                                            ? __ldg(reinterpret_cast<const uint32_t*>(sb[j] + grp))
+                                            : 0u;
+                    }
+                    if (gs >= kStages && !mbar_wait(&stage_free[pr], ((gs / kStages) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 tc_fence_after();  // after the MMAs that last read these columns
 #pragma unroll
@@ -391,22 +450,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;                        // lanes 32 quad .. 32 quad + 31
         const int et = (warp - kEpiWarp0) * 32 + lane;    // 0..127
         uint32_t it = 0;
+        // down: pair index and routing weight of each column, loaded one item
+        // ahead (qn, wn hold those of `item` at the top of the loop)
+        int qn[kNJ], qv[kNJ];
+        float wn[kNJ], wv[kNJ];
+        auto load_cols = [&](int item) {
+            if (MODE == 1 && item < items) {
+                const int tile = item / row_blocks;
+#pragma unroll
+                for (int u = 0; u < kNJ; ++u) {
+                    const int p = tile * N + 32 * u + lane;
+                    qn[u] = checked_pair(g, p);
+                    wn[u] = __ldg(g.w_pos + p);
+                }
+            }
+        };
+        load_cols(blockIdx.x);
         for (int item = blockIdx.x; item < items; item += gridDim.x) {
             const int tile = item / row_blocks, block = item % row_blocks;
             const int e = checked_expert(g, tile, false);
-            if (e < 0) continue;
-            const uint32_t b = it % kAccBufs;
-            int qv[kNJ];
-            float wv[kNJ];
-            if (MODE == 1) {
-#pragma unroll
-                for (int u = 0; u < kNJ; ++u) {
-                    qv[u] = checked_pair(g, tile * N + 32 * u + lane);
-                    wv[u] = qv[u] < 0 ? 0.0f : __ldg(g.topk_w + qv[u]);
-                }
+            if (e < 0) {
+                load_cols(item + gridDim.x);
+                continue;
             }
+            const uint32_t b = it % kAccBufs;
+#pragma unroll
+            for (int u = 0; u < kNJ; ++u) qv[u] = qn[u], wv[u] = wn[u];
             if (!mbar_wait(&acc_full[b], (it / kAccBufs) & 1)) break;
             tc_fence_after();
+            load_cols(item + gridDim.x);
 #pragma unroll 1
             for (int c0 = 0; c0 < N; c0 += 32) {
                 uint32_t v[32];
@@ -420,7 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(&acc_free[b]);
                 }
                 if (MODE == 1) {
-                    const int m = block * 128 + 32 * quad + lane;
+                    float* yb = g.y_out + ((size_t)block * g.act_rows + (size_t)tile * N + c0) * 128 +
+                                32 * quad + lane;
                     int q_lo = qv[0];
                     float w_lo = wv[0];
 #pragma unroll
@@ -433,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i) {
                         const int q = __shfl_sync(0xFFFFFFFFu, q_lo, i);
                         const float w = __shfl_sync(0xFFFFFFFFu, w_lo, i);
-                        if (q >= 0) g.y_out[(size_t)q * g.rows + m] = w * __uint_as_float(v[i]);
+                        if (q >= 0) yb[(size_t)i * 128] = w * __uint_as_float(v[i]);
                     }
                 } else {
                     // transpose through shared memory: stg[column][accumulator row]
@@ -450,10 +523,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k4 = 0; k4 < 4; ++k4) {
                         const float4 gv = *reinterpret_cast<const float4*>(gp + 4 * k4);
                         const float4 uv = *reinterpret_cast<const float4*>(gp + 64 + 4 * k4);
-                        a[4 * k4 + 0] = silu(gv.x) * uv.x;
-                        a[4 * k4 + 1] = silu(gv.y) * uv.y;
-                        a[4 * k4 + 2] = silu(gv.z) * uv.z;
-                        a[4 * k4 + 3] = silu(gv.w) * uv.w;
+                        a[4 * k4 + 0] = swiglu(gv.x, uv.x);
+                        a[4 * k4 + 1] = swiglu(gv.y, uv.y);
+                        a[4 * k4 + 2] = swiglu(gv.z, uv.z);
+                        a[4 * k4 + 3] = swiglu(gv.w, uv.w);
                     }
 #pragma unroll
                     for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(a[k]));
@@ -485,18 +558,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int MODE, int N>
 cudaError_t launch_n(const GroupedGemm& g, cudaStream_t s) {
-    const size_t smem = MxLayout<N>::kTotal;
+    const size_t smem = MxLayout<MODE, N>::kTotal;
     cudaError_t err = ensure_dynamic_smem((const void*)mxf4_gemm_kernel<MODE, N>, smem);
     if (err != cudaSuccess) return err;
-    CUtensorMap a_map, b_map;
+    CUtensorMap a_map, b_map, sfa_map, sfb_map;
     err = encode_codes_map(&a_map, g.codes, g.K / 2, (uint64_t)g.num_experts * g.rows, kRowBytes, kABox);
     if (err != cudaSuccess) return err;
     err = encode_codes_map(&b_map, g.act, g.K / 2, (uint64_t)g.act_rows, kRowBytes, N);
     if (err != cudaSuccess) return err;
+    if (g.sf_tma) {  // scale rows of K/32 bytes (a multiple of 16), 16-byte boxes
+        err = encode_2d_map(&sfa_map, g.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K / 32,
+                            (uint64_t)g.num_experts * g.rows, (uint64_t)(g.K / 32), 16, kABox,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (err != cudaSuccess) return err;
+        err = encode_2d_map(&sfb_map, g.act_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K / 32,
+                            (uint64_t)g.act_rows, (uint64_t)(g.K / 32), 16, N,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (err != cudaSuccess) return err;
+    } else {  // not read
+        sfa_map = a_map;
+        sfb_map = b_map;
+    }
     const int row_blocks = MODE == 0 ? g.I / 64 : g.rows / 128;
     const long long max_items = (long long)g.max_tiles * row_blocks;
     const int grid = (int)std::min<long long>(max_items, (long long)num_sms());
-    return launch_pdl(mxf4_gemm_kernel<MODE, N>, dim3(grid), dim3(kThreads), smem, s, g, a_map, b_map);
+    return launch_pdl(mxf4_gemm_kernel<MODE, N>, dim3(grid), dim3(kThreads), smem, s, g, a_map, b_map,
+                      sfa_map, sfb_map);
 }
 
 template <int MODE>
@@ -511,7 +598,74 @@ cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
     }
 }
 
+// out[t, m] = bf16(sum over j ascending of y[m / 128][inv[t * Kt + j]][m % 128])
+// for y blocked as the down epilogue writes it; 4 consecutive m per thread,
+// so a warp reads 512 contiguous bytes per slot.
+__global__ void __launch_bounds__(256) combine_blocked_kernel(const float4* __restrict__ y,
+                                                              const int32_t* __restrict__ inv, int T,
+                                                              int H, int Kt, int cap,
+                                                              uint2* __restrict__ out) {
+    pdl_begin();
+    const int H4 = H / 4;
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < (size_t)T * H4) {
+        const size_t t = i / H4;
+        const int m4 = (int)(i % H4), blk = m4 / 32, r4 = m4 % 32;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < Kt; ++j) {
+            const int p = __ldg(inv + t * Kt + j);
+            if ((unsigned)p >= (unsigned)cap) {
+                flag_index_error();
+                continue;
+            }
+            const float4 v = __ldg(y + ((size_t)blk * cap + p) * 32 + r4);
+            a.x += v.x;
+            a.y += v.y;
+            a.z += v.z;
+            a.w += v.w;
+        }
+        uint2 o;
+        o.x = (uint32_t)f32_to_bf16_bits(a.x) | ((uint32_t)f32_to_bf16_bits(a.y) << 16);
+        o.y = (uint32_t)f32_to_bf16_bits(a.z) | ((uint32_t)f32_to_bf16_bits(a.w) << 16);
+        out[i] = o;
+    }
+    pdl_end();
+}
+
+// w_pos[p] = topk_w[q] for the used positions p holding pair q, else 0.
+__global__ void __launch_bounds__(256) position_weights_kernel(const int32_t* __restrict__ sorted_pairs,
+                                                               const float* __restrict__ topk_w,
+                                                               const int32_t* __restrict__ num_tiles,
+                                                               int tile_m, int cap, int num_pairs,
+                                                               float* __restrict__ w_pos) {
+    pdl_begin();
+    const int rows = min(max(__ldg(num_tiles), 0) * tile_m, cap);
+    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < rows; p += gridDim.x * blockDim.x) {
+        const int q = __ldg(sorted_pairs + p);
+        w_pos[p] = (q >= 0 && q < num_pairs) ? __ldg(topk_w + q) : 0.0f;
+    }
+    pdl_end();
+}
+
 }  // namespace
+
+cudaError_t launch_position_weights(const int32_t* sorted_pairs, const float* topk_w,
+                                    const int32_t* num_tiles, int tile_m, int cap, int num_pairs,
+                                    float* w_pos, cudaStream_t s) {
+    if (cap <= 0) return cudaSuccess;
+    const int blocks = std::min((cap + 255) / 256, num_sms() * 4);
+    return launch_pdl(position_weights_kernel, dim3(blocks), dim3(256), 0, s, sorted_pairs, topk_w,
+                      num_tiles, tile_m, cap, num_pairs, w_pos);
+}
+
+cudaError_t launch_combine_blocked(const float* y, const int32_t* inv, int T, int H, int Kt, int cap,
+                                   uint16_t* out, cudaStream_t s) {
+    const long long n = (long long)T * (H / 4);
+    if (n <= 0) return cudaSuccess;
+    return launch_pdl(combine_blocked_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
+                      reinterpret_cast<const float4*>(y), inv, T, H, Kt, cap,
+                      reinterpret_cast<uint2*>(out));
+}
 
 cudaError_t launch_quantize_mxfp4(const uint16_t* x, int rows, int cols, uint8_t* codes,
                                   uint8_t* scales, cudaStream_t s) {

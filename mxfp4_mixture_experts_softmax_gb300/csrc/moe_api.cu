@@ -547,11 +547,12 @@ moe_status_t moe_ffn(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, 
 }
 
 // ------------------------------------------------ MXFP4-quantised activations
-// Workspace: x codes [T, H/2], x scales [T, H/32], x codes gathered into tile
-// order [cap, H/2], h codes [cap, I/2], h scales [cap, I/32], y fp32 [T*Kt, H];
-// each region starts on a 256-byte boundary.
+// Workspace: x codes [T, H/2], x scales [T, H/32], x codes and scales
+// gathered into tile order [cap, H/2] and [cap, H/32], h codes [cap, I/2], h
+// scales [cap, I/32], routing weight per position fp32 [cap], y fp32 blocked
+// [H/128, cap, 128]; each region starts on a 256-byte boundary.
 struct MxLayoutWs {
-    size_t xc, xs, xg, hc, hs, y, total;
+    size_t xc, xs, xg, xgs, hc, hs, wpos, y, total;
 };
 
 static bool mx_layout(int T, int H, int I, int Et, int Kt, int tile_m, MxLayoutWs* L) {
@@ -560,10 +561,12 @@ static bool mx_layout(int T, int H, int I, int Et, int Kt, int tile_m, MxLayoutW
     L->xc = 0;
     L->xs = L->xc + round_up((size_t)T * (H / 2), 256);
     L->xg = L->xs + round_up((size_t)T * (H / 32), 256);
-    L->hc = L->xg + round_up((size_t)cap * (H / 2), 256);
+    L->xgs = L->xg + round_up((size_t)cap * (H / 2), 256);
+    L->hc = L->xgs + round_up((size_t)cap * (H / 32), 256);
     L->hs = L->hc + round_up((size_t)cap * (I / 2), 256);
-    L->y = L->hs + round_up((size_t)cap * (I / 32), 256);
-    L->total = L->y + round_up((size_t)T * Kt * H * sizeof(float), 256);
+    L->wpos = L->hs + round_up((size_t)cap * (I / 32), 256);
+    L->y = L->wpos + round_up((size_t)cap * sizeof(float), 256);
+    L->total = L->y + round_up((size_t)cap * H * sizeof(float), 256);
     return true;
 }
 
@@ -618,11 +621,20 @@ moe_status_t moe_ffn_mxfp4act_gate_up(const uint16_t* x, const uint8_t* w13, con
                                             reinterpret_cast<uint8_t*>(ws + L.xs), stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     // the GEMM reads each tile's token rows as one box per stage: gather the
-    // code rows (H/2 bytes each) into tile order; the scales stay by token
+    // code rows (H/2 bytes each) into tile order, and the scale rows (H/32
+    // bytes) too when they are whole 16-byte units (then the GEMM loads them
+    // by TMA; otherwise its scale warps read them by token)
     err = launch_gather_rows(reinterpret_cast<const uint16_t*>(ws + L.xc), H / 4, sorted_pairs,
                              num_tiles, tile_m, Kt, (int)cap, T * Kt,
                              reinterpret_cast<uint16_t*>(ws + L.xg), stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
+    const bool sf_tma = H % 512 == 0;
+    if (sf_tma) {
+        err = launch_gather_rows(reinterpret_cast<const uint16_t*>(ws + L.xs), H / 64, sorted_pairs,
+                                 num_tiles, tile_m, Kt, (int)cap, T * Kt,
+                                 reinterpret_cast<uint16_t*>(ws + L.xgs), stream);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+    }
     GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, T, I, Et, Kt, tile_m,
                               (int)(cap / tile_m));
     g.codes = w13;
@@ -631,7 +643,8 @@ moe_status_t moe_ffn_mxfp4act_gate_up(const uint16_t* x, const uint8_t* w13, con
     g.K = H;
     g.act = reinterpret_cast<const uint16_t*>(ws + L.xg);
     g.act_rows = (int)cap;
-    g.act_scales = reinterpret_cast<const uint8_t*>(ws + L.xs);
+    g.act_scales = reinterpret_cast<const uint8_t*>(ws + (sf_tma ? L.xgs : L.xs));
+    g.sf_tma = sf_tma ? 1 : 0;
     g.hq_codes = reinterpret_cast<uint8_t*>(ws + L.hc);
     g.hq_scales = reinterpret_cast<uint8_t*>(ws + L.hs);
     trace("moe_ffn_mxfp4act_gate_up", T, H, I, Et, Kt, tile_m, MOE_PATH_PREFILL);
@@ -639,14 +652,14 @@ moe_status_t moe_ffn_mxfp4act_gate_up(const uint16_t* x, const uint8_t* w13, con
 }
 
 moe_status_t moe_ffn_mxfp4act_down(const uint8_t* w2, const uint8_t* s2, const float* topk_w,
-                                   const int32_t* sorted_pairs, const int32_t* tile_expert,
-                                   const int32_t* num_tiles, int T, int H, int I, int Et, int Kt,
-                                   int tile_m, uint16_t* out, void* workspace, size_t ws_bytes,
-                                   cudaStream_t stream) {
+                                   const int32_t* sorted_pairs, const int32_t* inv_pairs,
+                                   const int32_t* tile_expert, const int32_t* num_tiles, int T,
+                                   int H, int I, int Et, int Kt, int tile_m, uint16_t* out,
+                                   void* workspace, size_t ws_bytes, cudaStream_t stream) {
     moe_status_t st = check_mx_shape(T, H, I, Et, Kt, tile_m);
     if (st != MOE_OK || T == 0) return st;
     if (!ptrs_ok({w2, out, workspace}, 16) ||
-        !ptrs_ok({s2, topk_w, sorted_pairs, tile_expert, num_tiles}, 4))
+        !ptrs_ok({s2, topk_w, sorted_pairs, inv_pairs, tile_expert, num_tiles}, 4))
         return MOE_ERR_INVALID_ARG;
     MxLayoutWs L;
     mx_layout(T, H, I, Et, Kt, tile_m, &L);
@@ -662,12 +675,17 @@ moe_status_t moe_ffn_mxfp4act_down(const uint8_t* w2, const uint8_t* s2, const f
     g.act = reinterpret_cast<const uint16_t*>(ws + L.hc);
     g.act_rows = (int)cap;
     g.act_scales = reinterpret_cast<const uint8_t*>(ws + L.hs);
+    g.sf_tma = I % 512 == 0 ? 1 : 0;
     g.y_out = reinterpret_cast<float*>(ws + L.y);
     g.topk_w = topk_w;
+    g.w_pos = reinterpret_cast<const float*>(ws + L.wpos);
     trace("moe_ffn_mxfp4act_down", T, H, I, Et, Kt, tile_m, MOE_PATH_PREFILL);
-    cudaError_t err = launch_mxfp4act_down(g, stream);
+    cudaError_t err = launch_position_weights(sorted_pairs, topk_w, num_tiles, tile_m, (int)cap,
+                                              T * Kt, reinterpret_cast<float*>(ws + L.wpos), stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    return cuda_status(launch_combine(g.y_out, nullptr, T, H, Kt, out, stream));
+    err = launch_mxfp4act_down(g, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(launch_combine_blocked(g.y_out, inv_pairs, T, H, Kt, (int)cap, out, stream));
 }
 
 moe_status_t moe_ffn_mxfp4act(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
@@ -683,8 +701,8 @@ moe_status_t moe_ffn_mxfp4act(const uint16_t* x, const uint8_t* w13, const uint8
     st = moe_ffn_mxfp4act_gate_up(x, w13, s13, sorted_pairs, tile_expert, num_tiles, T, H, I, Et,
                                   Kt, tile_m, workspace, ws_bytes, stream);
     if (st != MOE_OK) return st;
-    return moe_ffn_mxfp4act_down(w2, s2, topk_w, sorted_pairs, tile_expert, num_tiles, T, H, I, Et,
-                                 Kt, tile_m, out, workspace, ws_bytes, stream);
+    return moe_ffn_mxfp4act_down(w2, s2, topk_w, sorted_pairs, inv_pairs, tile_expert, num_tiles, T,
+                                 H, I, Et, Kt, tile_m, out, workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -70,6 +70,11 @@ struct GroupedGemm {
     const uint8_t* act_scales;
     uint8_t* hq_codes;
     uint8_t* hq_scales;
+    // 1: B scales are tile-ordered rows ([cap][K/32], K % 512 == 0) that the
+    // producer loads by TMA with the codes; 0: scale warps load them (by
+    // token for gate_up, by position for down)
+    int sf_tma;
+    const float* w_pos;          // down: routing weight per sorted position (0 for padding)
     // decode group factor 2^(s-126) as fp32 bits s * exp_one + exp_bias,
     // taken as runtime values so the multiply-add stays one instruction
     uint32_t exp_one = 1u << 23, exp_bias = 1u << 23;
@@ -159,6 +164,14 @@ cudaError_t launch_quantize_mxfp4(const uint16_t* x, int rows, int cols, uint8_t
                                   uint8_t* scales, cudaStream_t s);
 bool mxfp4act_tile_supported(int tile_m);
 bool mxfp4act_shape_supported(int H, int I);
+// w_pos[p] = topk_w[sorted_pairs[p]] for the used positions, 0 for padding
+cudaError_t launch_position_weights(const int32_t* sorted_pairs, const float* topk_w,
+                                    const int32_t* num_tiles, int tile_m, int cap, int num_pairs,
+                                    float* w_pos, cudaStream_t s);
+// out = bf16(sum over the Kt slots of y[m / 128][inv[pair]][m % 128]) (the
+// MXFP4-activation down GEMM's blocked y; H % 128 == 0)
+cudaError_t launch_combine_blocked(const float* y, const int32_t* inv, int T, int H, int Kt, int cap,
+                                   uint16_t* out, cudaStream_t s);
 // block-scaled MXFP4 x MXFP4 grouped GEMMs (tcgen05 kind::mxf4)
 cudaError_t launch_mxfp4act_gate_up(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_mxfp4act_down(const GroupedGemm& g, cudaStream_t s);

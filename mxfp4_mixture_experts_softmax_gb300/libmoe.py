@@ -117,8 +117,8 @@ def load(build: bool = True):
         L.moe_ffn_mxfp4act_gate_up.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, sz,
                                                vp]
         L.moe_ffn_mxfp4act_gate_up.restype = ci
-        L.moe_ffn_mxfp4act_down.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp,
-                                            sz, vp]
+        L.moe_ffn_mxfp4act_down.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp,
+                                            vp, sz, vp]
         L.moe_ffn_mxfp4act_down.restype = ci
         L.moe_ffn_mxfp4act_h_offsets.argtypes = [ci, ci, ci, ci, ci, ci, vp, vp]
         L.moe_ffn_mxfp4act_h_offsets.restype = ci
@@ -460,7 +460,8 @@ def moe_ffn_mxfp4act_gate_up(x, w13, s13, perm: dict, workspace, stream=None):
 def moe_ffn_mxfp4act_down(w2, s2, topk_w, perm: dict, workspace, T: int, out, stream=None):
     Et, H, halfI = w2.shape
     _check(load().moe_ffn_mxfp4act_down(
-        _ptr(w2), _ptr(s2), _ptr(topk_w), _ptr(perm["sorted_pairs"]), _ptr(perm["tile_expert"]),
+        _ptr(w2), _ptr(s2), _ptr(topk_w), _ptr(perm["sorted_pairs"]), _ptr(perm["inv_pairs"]),
+        _ptr(perm["tile_expert"]),
         _ptr(perm["num_tiles"]), T, H, 2 * halfI, Et, perm["Kt"], perm["tile_m"], _ptr(out),
         _ptr(workspace), workspace.numel(), _stream(stream)), "moe_ffn_mxfp4act_down")
     return out
