@@ -632,6 +632,36 @@ __global__ void __launch_bounds__(256) combine_blocked_kernel(const float4* __re
     pdl_end();
 }
 
+// The token rows of the used tiles in tile order, MXFP4 encoded: codes
+// (cb16 16-byte units per row) and, when sb16 > 0, scales (sb16 units per
+// row); zeros for padding positions.  One warp per row, rows grid-strided.
+__global__ void __launch_bounds__(256) gather_mx_rows_kernel(const uint4* __restrict__ xc,
+                                                             const uint4* __restrict__ xs,
+                                                             int cb16, int sb16,
+                                                             const int32_t* __restrict__ sorted_pairs,
+                                                             const int32_t* __restrict__ num_tiles,
+                                                             int tile_m, int Kt, int cap,
+                                                             int num_pairs, uint4* __restrict__ xgc,
+                                                             uint4* __restrict__ xgs) {
+    pdl_begin();
+    const int rows = min(max(__ldg(num_tiles), 0) * tile_m, cap);
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < rows; p += warps) {
+        int q = __ldg(sorted_pairs + p);
+        if (q >= num_pairs) {
+            if (lane == 0) flag_index_error();
+            q = -1;
+        }
+        const size_t t = q < 0 ? 0 : (size_t)(q / Kt);
+        for (int c = lane; c < cb16; c += 32)
+            xgc[(size_t)p * cb16 + c] = q < 0 ? make_uint4(0, 0, 0, 0) : __ldg(xc + t * cb16 + c);
+        for (int c = lane; c < sb16; c += 32)
+            xgs[(size_t)p * sb16 + c] = q < 0 ? make_uint4(0, 0, 0, 0) : __ldg(xs + t * sb16 + c);
+    }
+    pdl_end();
+}
+
 // w_pos[p] = topk_w[q] for the used positions p holding pair q, else 0.
 __global__ void __launch_bounds__(256) position_weights_kernel(const int32_t* __restrict__ sorted_pairs,
                                                                const float* __restrict__ topk_w,
@@ -656,6 +686,18 @@ cudaError_t launch_position_weights(const int32_t* sorted_pairs, const float* to
     const int blocks = std::min((cap + 255) / 256, num_sms() * 4);
     return launch_pdl(position_weights_kernel, dim3(blocks), dim3(256), 0, s, sorted_pairs, topk_w,
                       num_tiles, tile_m, cap, num_pairs, w_pos);
+}
+
+cudaError_t launch_gather_mx_rows(const uint8_t* xc, const uint8_t* xs, int H, bool with_scales,
+                                  const int32_t* sorted_pairs, const int32_t* num_tiles, int tile_m,
+                                  int Kt, int cap, int num_pairs, uint8_t* xgc, uint8_t* xgs,
+                                  cudaStream_t s) {
+    if (cap <= 0) return cudaSuccess;
+    const int blocks = std::min((cap + 7) / 8, num_sms() * 8);
+    return launch_pdl(gather_mx_rows_kernel, dim3(blocks), dim3(256), 0, s,
+                      reinterpret_cast<const uint4*>(xc), reinterpret_cast<const uint4*>(xs), H / 32,
+                      with_scales ? H / 512 : 0, sorted_pairs, num_tiles, tile_m, Kt, cap, num_pairs,
+                      reinterpret_cast<uint4*>(xgc), reinterpret_cast<uint4*>(xgs));
 }
 
 cudaError_t launch_combine_blocked(const float* y, const int32_t* inv, int T, int H, int Kt, int cap,

@@ -624,17 +624,13 @@ moe_status_t moe_ffn_mxfp4act_gate_up(const uint16_t* x, const uint8_t* w13, con
     // code rows (H/2 bytes each) into tile order, and the scale rows (H/32
     // bytes) too when they are whole 16-byte units (then the GEMM loads them
     // by TMA; otherwise its scale warps read them by token)
-    err = launch_gather_rows(reinterpret_cast<const uint16_t*>(ws + L.xc), H / 4, sorted_pairs,
-                             num_tiles, tile_m, Kt, (int)cap, T * Kt,
-                             reinterpret_cast<uint16_t*>(ws + L.xg), stream);
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
     const bool sf_tma = H % 512 == 0;
-    if (sf_tma) {
-        err = launch_gather_rows(reinterpret_cast<const uint16_t*>(ws + L.xs), H / 64, sorted_pairs,
-                                 num_tiles, tile_m, Kt, (int)cap, T * Kt,
-                                 reinterpret_cast<uint16_t*>(ws + L.xgs), stream);
-        if (err != cudaSuccess) return MOE_ERR_CUDA;
-    }
+    err = launch_gather_mx_rows(reinterpret_cast<const uint8_t*>(ws + L.xc),
+                                reinterpret_cast<const uint8_t*>(ws + L.xs), H, sf_tma, sorted_pairs,
+                                num_tiles, tile_m, Kt, (int)cap, T * Kt,
+                                reinterpret_cast<uint8_t*>(ws + L.xg),
+                                reinterpret_cast<uint8_t*>(ws + L.xgs), stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
     GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, T, I, Et, Kt, tile_m,
                               (int)(cap / tile_m));
     g.codes = w13;

@@ -164,6 +164,12 @@ cudaError_t launch_quantize_mxfp4(const uint16_t* x, int rows, int cols, uint8_t
                                   uint8_t* scales, cudaStream_t s);
 bool mxfp4act_tile_supported(int tile_m);
 bool mxfp4act_shape_supported(int H, int I);
+// MXFP4 token rows into tile order: codes [T][H/2] -> [cap][H/2] and, when
+// with_scales (H % 512 == 0), scales [T][H/32] -> [cap][H/32]; zeros for pads
+cudaError_t launch_gather_mx_rows(const uint8_t* xc, const uint8_t* xs, int H, bool with_scales,
+                                  const int32_t* sorted_pairs, const int32_t* num_tiles, int tile_m,
+                                  int Kt, int cap, int num_pairs, uint8_t* xgc, uint8_t* xgs,
+                                  cudaStream_t s);
 // w_pos[p] = topk_w[sorted_pairs[p]] for the used positions, 0 for padding
 cudaError_t launch_position_weights(const int32_t* sorted_pairs, const float* topk_w,
                                     const int32_t* num_tiles, int tile_m, int cap, int num_pairs,

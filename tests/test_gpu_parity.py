@@ -141,6 +141,61 @@ def test_permute_edges(case):
     _permute_check(ids, Et, tm)
 
 
+def _permute_dev(ids, Et, tile_m, multi):
+    import os
+    old = os.environ.get("MOE_PERMUTE_MULTI")
+    os.environ["MOE_PERMUTE_MULTI"] = multi
+    try:
+        got = libmoe.moe_permute(gc.to_dev(ids.astype(np.int32)), Et, tile_m)
+        torch.cuda.synchronize()
+    finally:
+        if old is None:
+            del os.environ["MOE_PERMUTE_MULTI"]
+        else:
+            os.environ["MOE_PERMUTE_MULTI"] = old
+    return {k: got[k].cpu().numpy() for k in ("sorted_pairs", "expert_offsets", "inv_pairs",
+                                              "tile_expert", "num_tiles")}
+
+
+@pytest.mark.parametrize("case", ["workload8192", "workload1536", "one_expert", "experts1025",
+                                  "tile1", "tile256", "bad_ids", "few_pairs_many_blocks"])
+def test_permute_multi_block_equals_single_block(case):
+    """The multi-block sort (large batches) and the single-block kernel give
+    the same bytes, including ids outside [0, Et) (skipped, inv = -1); where
+    every id is valid both equal the oracle."""
+    rng = np.random.default_rng(5)
+    if case.startswith("workload"):
+        w = synth.WORKLOADS["skewed_prefill8192" if case == "workload8192" else "prefill1536"]
+        ids, _ = oracle.route(synth.make_logits(w), w.K, w.with_shared)
+        Et, tm = w.Et, 128
+    elif case == "one_expert":
+        ids, Et, tm = np.full((20000, 1), 3, np.int32), 7, 64
+    elif case == "experts1025":
+        ids = np.stack([rng.permutation(1025)[:20] for _ in range(1000)]).astype(np.int32)
+        Et, tm = 1025, 16
+    elif case == "tile1":
+        ids, Et, tm = rng.integers(0, 9, (9000, 2)).astype(np.int32), 9, 1
+    elif case == "tile256":
+        ids = np.stack([rng.permutation(60)[:6] for _ in range(3000)]).astype(np.int32)
+        Et, tm = 60, 256
+    elif case == "bad_ids":
+        ids = rng.integers(0, 40, (3000, 5)).astype(np.int32)
+        ids[rng.random(ids.shape) < 0.01] = -1
+        ids[rng.random(ids.shape) < 0.01] = 40
+        Et, tm = 40, 32
+    else:  # slices of fewer pairs than blocks * 32: empty warp sub-slices
+        ids, Et, tm = rng.integers(0, 2, (8192, 1)).astype(np.int32), 2, 8
+    single = _permute_dev(ids, Et, tm, "0")
+    multi = _permute_dev(ids, Et, tm, "1")
+    for k in single:
+        np.testing.assert_array_equal(multi[k], single[k], err_msg=k)
+    if case != "bad_ids":
+        _permute_check(ids, Et, tm)
+    else:
+        bad = (ids.reshape(-1) < 0) | (ids.reshape(-1) >= Et)
+        assert (multi["inv_pairs"][bad] == -1).all() and (multi["inv_pairs"][~bad] >= 0).all()
+
+
 # ------------------------------------------------------------------- ffn
 
 def _layer_inputs(w):
