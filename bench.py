@@ -212,8 +212,9 @@ def gpu_id_for(device_index: int) -> str:
 
 def layer_work(w, ids_host, act="bf16"):
     """Algorithmic HBM bytes and flops of one step, from the actual routing.
-    act="mxfp4": x and h move as MXFP4 (codes + scales), and the down step
-    includes the combine (y read, out written)."""
+    The down step includes the combine (y written and read back, out
+    written); act="mxfp4": x and h move as MXFP4 (codes + scales).  The layer
+    counts weights, x, out, h and logits."""
     import numpy as np
     from mxfp4_mixture_experts_softmax_gb300 import synth
     touched = int(np.unique(ids_host).size)
@@ -221,7 +222,7 @@ def layer_work(w, ids_host, act="bf16"):
     w13_b = 2 * I * (H // 2 + H // 32)
     w2_b = H * (I // 2 + I // 32)
     gate_up = touched * w13_b + T * H * 2 + P * I * 2          # weights + x + h write
-    down = touched * w2_b + P * I * 2 + P * H * 4               # weights + h read + y write
+    down = touched * w2_b + P * I * 2 + 2 * P * H * 4 + T * H * 2   # + h read, y out and back, out
     layer = (touched * synth.weight_bytes_per_expert(w) + T * H * 4 + P * I * 4
              + T * w.E * 4)                                     # + x, out, h, logits
     flops = 2 * P * (2 * I * H + H * I)
@@ -229,8 +230,7 @@ def layer_work(w, ids_host, act="bf16"):
         xq, hq = H // 2 + H // 32, I // 2 + I // 32       # MXFP4 bytes per row
         gate_up = touched * w13_b + T * H * 2 + T * xq + 2 * P * xq + P * hq
         down = touched * w2_b + P * hq + 2 * P * H * 4 + T * H * 2
-        layer = touched * synth.weight_bytes_per_expert(w) + T * H * 4 + P * (2 * hq + 2 * xq) \
-            + 2 * P * H * 4 + T * w.E * 4
+        layer = touched * synth.weight_bytes_per_expert(w) + T * H * 4 + 2 * P * hq + T * w.E * 4
     return dict(touched=touched, gate_up_bytes=gate_up, down_bytes=down, layer_bytes=layer,
                 flops=flops, gate_up_flops=2 * P * 2 * I * H)
 
@@ -319,14 +319,13 @@ def run_ours(args, ws, rank, local):
         if mx:  # down GEMM and the combine into out
             libmoe.moe_ffn_mxfp4act_down(W["w2"], W["s2"], tw, perm, bufs["workspace"], w.T,
                                          bufs["out"])
-        else:
-            libmoe.moe_ffn_down(W["w2"], W["s2"], tw, perm, bufs["workspace"], w.T, path)
+        else:  # down GEMM and the combine into out
+            libmoe.moe_ffn_down_combine(W["w2"], W["s2"], tw, perm, bufs["workspace"], w.T,
+                                        bufs["out"], path)
         if ev is not None:
             ev[3].record(stream)
         if gemm_ev is not None:
             gemm_ev[2].record(stream)
-        if not mx:
-            libmoe.moe_combine(y_buf, w.T, w.H, w.Kt, bufs["out"])
         if ev is not None:
             ev[4].record(stream)
 
@@ -417,7 +416,7 @@ def run_ours(args, ws, rank, local):
             os.path.join(ROOT, "mxfp4_mixture_experts_softmax_gb300", "csrc", src))
         gu = roofline_entry(f"{path_name}_gate_up", work["gate_up_bytes"], work["gate_up_flops"],
                             per["gate_up"] / 1e3, traffic, traffic_src, fp4=mx)
-        dn = roofline_entry(f"{path_name}_down" + ("_combine" if mx else ""), work["down_bytes"],
+        dn = roofline_entry(f"{path_name}_down_combine", work["down_bytes"],
                             work["flops"] - work["gate_up_flops"], per["down"] / 1e3, None, None,
                             fp4=mx)
         layer_s = total_ms / K / 1e3  # the whole step, gaps between launches included

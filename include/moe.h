@@ -246,6 +246,21 @@ moe_status_t moe_ffn_down(const uint8_t* w2, const uint8_t* s2, const float* top
                           cudaStream_t stream);
 moe_status_t moe_combine(const float* y, int T, int H, int Kt, uint16_t* out, cudaStream_t stream);
 
+/*
+ * moe_ffn_down_combine -- moe_ffn_down followed by moe_combine, in one call
+ * (moe_ffn runs gate_up and then this).  Same results bit for bit; the
+ * difference is where y lives in between: the prefill path writes y blocked
+ * by 128 output rows ([ceil(H/128)][cap][128], row block, sorted position,
+ * row) so each work item writes one contiguous run, and the combine gathers
+ * each token's Kt positions (inv_pairs) in slot order.  The workspace's y is
+ * therefore not the [T*Kt, H] array of moe_ffn_down after this call.
+ */
+moe_status_t moe_ffn_down_combine(const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                                  const int32_t* sorted_pairs, const int32_t* inv_pairs,
+                                  const int32_t* tile_expert, const int32_t* num_tiles, int T, int H,
+                                  int I, int Et, int Kt, int tile_m, uint16_t* out, void* workspace,
+                                  size_t ws_bytes, moe_path_t path, cudaStream_t stream);
+
 /* moe_combine plus one more fp32 [T, H] term added last (NULL: none). */
 moe_status_t moe_combine_ex(const float* y, const float* y_extra, int T, int H, int Kt,
                             uint16_t* out, cudaStream_t stream);

@@ -374,15 +374,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;  // tensor-memory lanes 32*quad .. 32*quad + 31
         const int r = 32 * quad + lane;
         const bool svec = (K % 512) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 15) == 0);
-        uint32_t it = 0;
-        for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        // Per item: this lane's weight row factor 2^(s_ref - 127) (the part of
+        // the scales the converters left out; accumulator lane r holds A row
+        // r) and the tile's pair indices and column factors (column j in lane
+        // j % 32 of register j / 32; the factor undoes the B row's scaling,
+        // per token for x, per position for h, and in the down GEMM includes
+        // the routing weight).  Loaded one item ahead: frn, qn, cn hold the
+        // values of `item` at the top of the loop.
+        constexpr int kQ = N / 32;
+        int qn[kQ];
+        float cn[kQ];
+        float frn = 0.0f;
+        auto load_item = [&](int item) {
+            if (item >= items) return;
             const int tile = item / row_blocks, block = item % row_blocks;
             const int e = checked_expert(g, tile, false);
-            if (e < 0) continue;
-            const uint32_t b = it % kAccBufs;
-            // this lane's weight row (accumulator lane r holds A row r) and its
-            // factor 2^(s_ref - 127), the part of the scales the converters
-            // left out
+            if (e < 0) return;
             int wrow;
             bool rvalid;
             if (MODE == 0) {
@@ -394,25 +401,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rvalid = wrow < g.rows;
             }
             const uint8_t* sp = g.scales + ((size_t)e * g.rows + (rvalid ? wrow : 0)) * (size_t)(K / 32);
-            const float fr = __uint_as_float(
+            frn = __uint_as_float(
                 (uint32_t)row_scale_ref(rvalid ? row_scale_max_part(sp, K / 32, svec, 0, 1) : 0u) << 23);
-            // the tile's pair indices and column factors once per item:
-            // column j lives in lane j % 32 of register j / 32.  The column
-            // factor undoes the B row's scaling (per token for x, per
-            // position for h) and, in the down GEMM, includes the routing weight.
-            constexpr int kQ = N / 32;
-            int qv[kQ];
-            float cv[kQ];
 #pragma unroll
             for (int u = 0; u < kQ; ++u) {
                 const int p = tile * N + 32 * u + lane;
-                qv[u] = checked_pair(g, p);
-                cv[u] = qv[u] < 0 ? 0.0f
-                        : MODE == 0 ? __ldg(g.act_rscale + qv[u] / g.Kt)
-                                    : __ldg(g.topk_w + qv[u]) * __ldg(g.act_rscale + p);
+                qn[u] = checked_pair(g, p);
+                if (MODE == 0)
+                    cn[u] = qn[u] < 0 ? 0.0f : __ldg(g.act_rscale + qn[u] / g.Kt);
+                else if (g.w_pos)  // both by position: no dependent load
+                    cn[u] = __ldg(g.w_pos + p) * __ldg(g.act_rscale + p);
+                else
+                    cn[u] = qn[u] < 0 ? 0.0f : __ldg(g.topk_w + qn[u]) * __ldg(g.act_rscale + p);
             }
+        };
+        load_item(blockIdx.x);
+        uint32_t it = 0;
+        for (int item = blockIdx.x; item < items; item += gridDim.x) {
+            const int tile = item / row_blocks, block = item % row_blocks;
+            const int e = checked_expert(g, tile, false);
+            if (e < 0) {
+                load_item(item + gridDim.x);
+                continue;
+            }
+            const uint32_t b = it % kAccBufs;
+            const float fr = frn;
+            int qv[kQ];
+            float cv[kQ];
+#pragma unroll
+            for (int u = 0; u < kQ; ++u) qv[u] = qn[u], cv[u] = cn[u];
             if (!mbar_wait(&acc_full[b], (it / kAccBufs) & 1)) break;
             tc_fence_after();
+            load_item(item + gridDim.x);
             // 32 columns per round trip: two loads, one wait
 #pragma unroll
             for (int c0 = 0; c0 < N; c0 += 32) {
@@ -444,12 +464,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     const int m = block * 128 + r;
+                    // blocked y: [rows / 128][position][128], one contiguous
+                    // run per item; else y[pair][m]
+                    float* yb = g.y_out + ((size_t)block * g.act_rows + (size_t)tile * N + c0) * 128 + r;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int q = __shfl_sync(0xFFFFFFFFu, q_lo, i);
                         const float fc = __shfl_sync(0xFFFFFFFFu, c_lo, i);
-                        if (m < g.rows && q >= 0)
-                            g.y_out[(size_t)q * g.rows + m] = fc * (__uint_as_float(v[i]) * fr);
+                        if (m < g.rows && q >= 0) {
+                            const float y = fc * (__uint_as_float(v[i]) * fr);
+                            if (g.y_blocked) yb[(size_t)i * 128] = y;
+                            else g.y_out[(size_t)q * g.rows + m] = y;
+                        }
                     }
                 }
             }

@@ -245,26 +245,39 @@ moe_status_t moe_route_permute(const float* logits, const float* shared_w, int T
 
 static size_t y_offset(int64_t cap, int I) { return round_up((size_t)cap * I * sizeof(uint16_t), 256); }
 
-// After y: x as scaled f16 rows [T, H] (both paths), the prefill path's
-// tile-ordered copy of them [cap, H] (prefill tile heights only), and the
-// fp32 row factors of x [T] and of h [cap].
-static size_t x16_offset(int64_t cap, int T, int H, int I, int Kt) {
-    return y_offset(cap, I) + round_up((size_t)T * Kt * H * sizeof(float), 256);
+// y: fp32 [T*Kt, H] by pair, or, for prefill tile heights, also room for the
+// blocked layout moe_ffn_down_combine writes ([ceil(H/128)][cap][128]).
+static size_t y_bytes(int64_t cap, int T, int H, int Kt, int tile_m) {
+    size_t n = (size_t)T * Kt * H;
+    if (prefill_tile_supported(tile_m)) n = std::max(n, (size_t)((H + 127) / 128) * 128 * (size_t)cap);
+    return round_up(n * sizeof(float), 256);
 }
 
-static size_t xg_offset(int64_t cap, int T, int H, int I, int Kt) {
-    return x16_offset(cap, T, H, I, Kt) + round_up((size_t)T * H * sizeof(uint16_t), 256);
+// After y: x as scaled f16 rows [T, H] (both paths), the prefill path's
+// tile-ordered copy of them [cap, H] (prefill tile heights only), the fp32
+// row factors of x [T] and of h [cap], and the routing weight of each sorted
+// position [cap].
+static size_t x16_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) {
+    return y_offset(cap, I) + y_bytes(cap, T, H, Kt, tile_m);
+}
+
+static size_t xg_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) {
+    return x16_offset(cap, T, H, I, Kt, tile_m) + round_up((size_t)T * H * sizeof(uint16_t), 256);
 }
 
 static size_t rs_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) {
     const size_t xg = prefill_tile_supported(tile_m) ? round_up((size_t)cap * H * sizeof(uint16_t), 256) : 0;
-    return xg_offset(cap, T, H, I, Kt) + xg;
+    return xg_offset(cap, T, H, I, Kt, tile_m) + xg;
+}
+
+static size_t wpos_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) {
+    return rs_offset(cap, T, H, I, Kt, tile_m) + round_up((size_t)(T + cap) * sizeof(float), 256);
 }
 
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m) {
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     if (cap < 0 || H <= 0 || I <= 0) return 0;
-    return rs_offset(cap, T, H, I, Kt, tile_m) + round_up((size_t)(T + cap) * sizeof(float), 256);
+    return wpos_offset(cap, T, H, I, Kt, tile_m) + round_up((size_t)cap * sizeof(float), 256);
 }
 
 moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m) {
@@ -356,7 +369,7 @@ moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_
     // both GEMMs take f16 B rows scaled per row by a power of two: x here,
     // and h (in place) once the GEMM has written it
     char* ws = reinterpret_cast<char*>(workspace);
-    uint16_t* x16 = reinterpret_cast<uint16_t*>(ws + x16_offset(cap, T, H, I, Kt));
+    uint16_t* x16 = reinterpret_cast<uint16_t*>(ws + x16_offset(cap, T, H, I, Kt, tile_m));
     float* rs_x = reinterpret_cast<float*>(ws + rs_offset(cap, T, H, I, Kt, tile_m));
     cudaError_t err = launch_rows_to_f16(x, x16, H, T, nullptr, nullptr, tile_m, rs_x, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
@@ -369,7 +382,7 @@ moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_
     } else {
         // the prefill GEMM reads its token rows as one box per stage: gather
         // them into tile order first
-        uint16_t* xg = reinterpret_cast<uint16_t*>(ws + xg_offset(cap, T, H, I, Kt));
+        uint16_t* xg = reinterpret_cast<uint16_t*>(ws + xg_offset(cap, T, H, I, Kt, tile_m));
         err = launch_gather_rows(x16, H, sorted_pairs, num_tiles, tile_m, Kt, (int)cap, T * Kt, xg,
                                  stream);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
@@ -412,6 +425,52 @@ moe_status_t moe_ffn_down(const uint8_t* w2, const uint8_t* s2, const float* top
     cudaError_t err = path == MOE_PATH_DECODE ? launch_decode_down(g, stream)
                                                : launch_prefill_down(g, stream);
     return cuda_status(err);
+}
+
+moe_status_t moe_ffn_down_combine(const uint8_t* w2, const uint8_t* s2, const float* topk_w,
+                                  const int32_t* sorted_pairs, const int32_t* inv_pairs,
+                                  const int32_t* tile_expert, const int32_t* num_tiles, int T, int H,
+                                  int I, int Et, int Kt, int tile_m, uint16_t* out, void* workspace,
+                                  size_t ws_bytes, moe_path_t path, cudaStream_t stream) {
+    moe_status_t st = check_ffn_shape(T, H, I, Et, Kt, tile_m, &path);
+    if (st != MOE_OK || T == 0) return st;
+    if (!ptrs_ok({w2, out, workspace}, 16) ||
+        !ptrs_ok({s2, topk_w, sorted_pairs, inv_pairs, tile_expert, num_tiles}, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_ffn_workspace_size(T, H, I, Et, Kt, tile_m)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    char* ws = reinterpret_cast<char*>(workspace);
+    float* y = reinterpret_cast<float*>(ws + moe_ffn_y_offset(T, I, Et, Kt, tile_m));
+    if (path == MOE_PATH_DECODE) {  // y by pair, then the slot-ordered combine
+        st = moe_ffn_down(w2, s2, topk_w, sorted_pairs, tile_expert, num_tiles, T, H, I, Et, Kt,
+                          tile_m, workspace, ws_bytes, path, stream);
+        return st != MOE_OK ? st : moe_combine(y, T, H, Kt, out, stream);
+    }
+    // prefill: routing weights by position, y blocked by 128 rows (each work
+    // item writes one contiguous run), the combine gathers each token's
+    // positions in slot order: the same sums in the same order as moe_combine
+    const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    float* w_pos = reinterpret_cast<float*>(ws + wpos_offset(cap, T, H, I, Kt, tile_m));
+    trace("moe_ffn_down_combine", T, H, I, Et, Kt, tile_m, path);
+    cudaError_t err = launch_position_weights(sorted_pairs, topk_w, num_tiles, tile_m, (int)cap,
+                                              T * Kt, w_pos, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, T, I, Et, Kt, tile_m,
+                              (int)(cap / tile_m));
+    g.codes = w2;
+    g.scales = s2;
+    g.rows = H;
+    g.K = I;
+    g.act = reinterpret_cast<const uint16_t*>(workspace);
+    g.act_rscale = reinterpret_cast<const float*>(ws + rs_offset(cap, T, H, I, Kt, tile_m)) + T;
+    g.act_rows = (int)cap;
+    g.act_by_token = 0;
+    g.y_out = y;
+    g.y_blocked = 1;
+    g.topk_w = topk_w;
+    g.w_pos = w_pos;
+    err = launch_prefill_down(g, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(launch_combine_blocked(y, inv_pairs, T, H, Kt, (int)cap, out, stream));
 }
 
 moe_status_t moe_combine_ex(const float* y, const float* y_extra, int T, int H, int Kt,
@@ -527,12 +586,8 @@ moe_status_t moe_ffn_path(const uint16_t* x, const uint8_t* w13, const uint8_t* 
     st = moe_ffn_gate_up(x, w13, s13, sorted_pairs, tile_expert, num_tiles, T, H, I, Et, Kt, tile_m,
                          workspace, ws_bytes, path, stream);
     if (st != MOE_OK) return st;
-    st = moe_ffn_down(w2, s2, topk_w, sorted_pairs, tile_expert, num_tiles, T, H, I, Et, Kt, tile_m,
-                      workspace, ws_bytes, path, stream);
-    if (st != MOE_OK) return st;
-    const float* y = reinterpret_cast<const float*>(reinterpret_cast<const char*>(workspace) +
-                                                    moe_ffn_y_offset(T, I, Et, Kt, tile_m));
-    return moe_combine(y, T, H, Kt, out, stream);
+    return moe_ffn_down_combine(w2, s2, topk_w, sorted_pairs, inv_pairs, tile_expert, num_tiles, T, H,
+                                I, Et, Kt, tile_m, out, workspace, ws_bytes, path, stream);
 }
 
 moe_status_t moe_ffn(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,

@@ -75,6 +75,7 @@ struct GroupedGemm {
     // token for gate_up, by position for down)
     int sf_tma;
     const float* w_pos;          // down: routing weight per sorted position (0 for padding)
+    int y_blocked;               // down: y as [ceil(rows/128)][act_rows][128] instead of [pair][rows]
     // decode group factor 2^(s-126) as fp32 bits s * exp_one + exp_bias,
     // taken as runtime values so the multiply-add stays one instruction
     uint32_t exp_one = 1u << 23, exp_bias = 1u << 23;

@@ -32,7 +32,7 @@ EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_route_ex", "moe
            "moe_ffn_dense_shared_workspace_size", "moe_ffn_dense_shared",
            "moe_selftest_wait_timeout", "moe_quantize_mxfp4", "moe_ffn_mxfp4act_workspace_size",
            "moe_ffn_mxfp4act", "moe_ffn_mxfp4act_gate_up", "moe_ffn_mxfp4act_down",
-           "moe_ffn_mxfp4act_h_offsets")
+           "moe_ffn_mxfp4act_h_offsets", "moe_ffn_down_combine")
 
 # bytes of the fixed device scratch behind moe_ffn_noalloc (include/moe.h)
 MOE_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -108,6 +108,9 @@ def load(build: bool = True):
         L.moe_ffn_dense_shared.restype = ci
         L.moe_selftest_wait_timeout.argtypes = [ci, vp]
         L.moe_selftest_wait_timeout.restype = ci
+        L.moe_ffn_down_combine.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp,
+                                           sz, ci, vp]
+        L.moe_ffn_down_combine.restype = ci
         L.moe_quantize_mxfp4.argtypes = [vp, ci, ci, vp, vp, vp]
         L.moe_quantize_mxfp4.restype = ci
         L.moe_ffn_mxfp4act_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci]
@@ -340,6 +343,18 @@ def moe_ffn_down(w2, s2, topk_w, perm: dict, workspace, T: int, path: int = MOE_
                                Et, perm["Kt"], perm["tile_m"], _ptr(workspace), workspace.numel(),
                                int(path), _stream(stream)), "moe_ffn_down")
     return workspace
+
+
+def moe_ffn_down_combine(w2, s2, topk_w, perm: dict, workspace, T: int, out,
+                         path: int = MOE_PATH_AUTO, stream=None):
+    """down x routing weight and the combine into out (include/moe.h)."""
+    Et, H, halfI = w2.shape
+    _check(load().moe_ffn_down_combine(
+        _ptr(w2), _ptr(s2), _ptr(topk_w), _ptr(perm["sorted_pairs"]), _ptr(perm["inv_pairs"]),
+        _ptr(perm["tile_expert"]), _ptr(perm["num_tiles"]), T, H, 2 * halfI, Et, perm["Kt"],
+        perm["tile_m"], _ptr(out), _ptr(workspace), workspace.numel(), int(path),
+        _stream(stream)), "moe_ffn_down_combine")
+    return out
 
 
 def moe_combine(y, T: int, H: int, Kt: int, out, stream=None):

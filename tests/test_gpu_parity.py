@@ -492,6 +492,34 @@ def test_prefill_full_size(name):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("path,tile_m,name", [(libmoe.MOE_PATH_PREFILL, 32, "ragged37"),
+                                              (libmoe.MOE_PATH_PREFILL, 64, "k_tail"),
+                                              (libmoe.MOE_PATH_PREFILL, 128, "wide_k"),
+                                              (libmoe.MOE_PATH_DECODE, 8, "ragged37")])
+def test_down_combine_equals_down_then_combine(path, tile_m, name):
+    """moe_ffn_down_combine (blocked y on the prefill path) gives the bytes of
+    moe_ffn_down followed by moe_combine (y by pair), and meets the bar."""
+    w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL[name])
+    d, ids, wt = _layer_inputs(w)
+    dw = gc.upload_weights(d)
+    perm = libmoe.moe_permute(gc.to_dev(ids), w.Et, tile_m)
+    ws = libmoe.alloc_workspace(w.T, w.H, w.I, w.Et, ids.shape[1], tile_m)
+    x_d, wt_d = gc.to_dev(d["x"]), gc.to_dev(wt)
+    libmoe.moe_ffn_gate_up(x_d, dw["w13"], dw["s13"], perm, ws, path)
+    a = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+    libmoe.moe_ffn_down(dw["w2"], dw["s2"], wt_d, perm, ws, w.T, path)
+    _, y = libmoe.ffn_views(ws, w.T, w.H, w.I, w.Et, ids.shape[1], tile_m)
+    libmoe.moe_combine(y, w.T, w.H, ids.shape[1], a)
+    b = torch.empty_like(a)
+    libmoe.moe_ffn_down_combine(dw["w2"], dw["s2"], wt_d, perm, ws, w.T, b, path)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(gc.bf16_dev_to_f64(b), gc.bf16_dev_to_f64(a))
+    ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt,
+                                    n_threads=THREADS))
+    gc.ffn_parity(gc.bf16_dev_to_f64(b), ref, f"down_combine {name}")
+    assert libmoe.moe_device_error() == 0
+
+
 # ------------------------------------------- shared expert of another width
 
 def _dense_shared_case(I_s, seed=31, T=37, with_gate=True):
