@@ -222,10 +222,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t* cnt = sh;            // [Et]
     int32_t* off = cnt + Et;      // [Et + 1]
     int32_t* wsum = off + Et + 1; // [kWarps]
+    // Each thread walks its expert's column of nb counts in chunks of 16,
+    // all 16 loads issued before any store that depends on them (a store to
+    // the same array would otherwise order every load behind the previous
+    // store: one L2 round trip per block).
+    constexpr int kChunk = 16;
     for (int e = threadIdx.x; e < Et; e += kThreads) {
         int run = 0;
-#pragma unroll 8
-        for (int b = 0; b < nb; ++b) run += scratch[(size_t)b * Et + e];
+        for (int b0 = 0; b0 < nb; b0 += kChunk) {
+            int c[kChunk];
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) c[j] = b0 + j < nb ? scratch[(size_t)(b0 + j) * Et + e] : 0;
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) run += c[j];
+        }
         cnt[e] = run;
     }
     __syncthreads();
@@ -233,11 +243,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     for (int e = threadIdx.x; e < Et; e += kThreads) {
         int run = off[e];
-#pragma unroll 8
-        for (int b = 0; b < nb; ++b) {
-            const int c = scratch[(size_t)b * Et + e];
-            scratch[(size_t)b * Et + e] = run;
-            run += c;
+        for (int b0 = 0; b0 < nb; b0 += kChunk) {
+            int c[kChunk];
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) c[j] = b0 + j < nb ? scratch[(size_t)(b0 + j) * Et + e] : 0;
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j)
+                if (b0 + j < nb) {
+                    scratch[(size_t)(b0 + j) * Et + e] = run;
+                    run += c[j];
+                }
         }
     }
     write_layout(cnt, off, Et, tile_m, cap, max_tiles, sorted_pairs, offsets_out, tile_expert,
