@@ -142,20 +142,32 @@ __device__ __forceinline__ uint4 codes_to_f16x8(uint32_t w, uint32_t mult) {
 
 template <int N>
 struct PrefillSmem {
+    // 128-row weight blocks per work item.  The blocks share the tile's B
+    // stage, so B crosses L2 once per kRB blocks (the f16 B rows, N * 128
+    // bytes per 64-k stage against 4 KB of codes, make L2 -> shared-memory
+    // traffic a bound).  Two blocks only where both accumulators can still
+    // be double-buffered: at N = 128 the single buffer and the 4-slot ring
+    // cost more than the saved traffic (skewed 8192 prefill 3.1 -> 3.8 ms;
+    // 1536-token prefill with N = 64: 1.86 -> 1.74 ms).
+    static constexpr int kRB = N <= 64 ? 2 : 1;
     static constexpr int kBBytes = N * kBK * 2;
-    static constexpr int kStage = kBBytes + kCodeBytes;            // multiple of 1024
+    static constexpr int kCodeStage = kRB * kCodeBytes;            // codes of the item's blocks
+    static constexpr int kStage = kBBytes + kCodeStage;            // multiple of 1024
     // Converter warp (quadrant, part) owns the stages with gs % 4 == part; with
     // a ring of a multiple of 4 slots each slot belongs to one part, so every
     // barrier's phases are observed in order (a parity wait is unambiguous
     // only one phase ahead).
-    static constexpr int kStages = N <= 128 ? 8 : 4;
+    static constexpr int kStages = (kRB == 1 && N <= 128) ? 8 : 4;
     static_assert(kStages % 4 == 0, "slot ownership");
     static constexpr int kBars = kStages * kStage;
     static constexpr int kTotal = kBars + 256 + 1024;              // + alignment slack
-    // tensor memory (512 columns): the accumulators, then the A stages
-    static constexpr int kAccBufs = 2 * N + kStages * kACols <= 512 ? 2 : 1;
-    static constexpr int kACol0 = kAccBufs * N;
-    static_assert(kACol0 + kStages * kACols <= 512, "tensor memory");
+    // tensor memory (512 columns): the accumulators (one per block, N
+    // columns each), then the A stages (kACols columns per block)
+    static constexpr int kAColsStage = kRB * kACols;
+    static constexpr int kAccCols = kRB * N;
+    static constexpr int kAccBufs = 2 * kAccCols + kStages * kAColsStage <= 512 ? 2 : 1;
+    static constexpr int kACol0 = kAccBufs * kAccCols;
+    static_assert(kACol0 + kStages * kAColsStage <= 512, "tensor memory");
 };
 
 template <int MODE, int N>
@@ -186,8 +198,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int K = g.K;
     // stages per item, rounded up to whole pairs (a padding stage reads zero codes)
     const int nk = ((K + kBK - 1) / kBK + 1) & ~1;
+    // blocks of 64 i (gate_up: 64 gate + 64 up rows) or of 128 rows (down);
+    // an item is one tile x kRB consecutive blocks
+    constexpr int kRB = L::kRB;
     const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
-    const int items = checked_tiles(g) * row_blocks;
+    const int row_groups = (row_blocks + kRB - 1) / kRB;
+    const int items = checked_tiles(g) * row_groups;
     constexpr uint32_t kTmemCols = 512;
 
     if (tid == 0) {
@@ -220,22 +236,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t gs = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
-            const int tile = item / row_blocks, block = item % row_blocks;
-            const int e = checked_expert(g, tile, block == 0);
+            const int tile = item / row_groups, grp = item % row_groups;
+            const int e = checked_expert(g, tile, grp == 0);
             if (e < 0) continue;  // skipped by every role
-            const int crow0 = e * g.rows + (MODE == 0 ? block * 64 : block * 128);
-            const int crow1 = MODE == 0 ? e * g.rows + g.I + block * 64 : crow0 + kCodeBox;
+            // two 64-row code boxes per block: gate and up rows, or the
+            // block's two halves
+            int crow[2 * kRB];
+#pragma unroll
+            for (int j = 0; j < kRB; ++j) {
+                const int block = grp * kRB + j;
+                crow[2 * j] = e * g.rows + (MODE == 0 ? block * 64 : block * 128);
+                crow[2 * j + 1] = MODE == 0 ? e * g.rows + g.I + block * 64 : crow[2 * j] + kCodeBox;
+            }
             if (lane == 0)  // the item's first stages into L2 before the ring asks for them
                 for (int st = 0; st < kPrefetch && st < nk; ++st) {
-                    tma_prefetch_l2_2d(&codes_map, st * (kBK / 2), crow0);
-                    tma_prefetch_l2_2d(&codes_map, st * (kBK / 2), crow1);
+#pragma unroll
+                    for (int c = 0; c < 2 * kRB; ++c) tma_prefetch_l2_2d(&codes_map, st * (kBK / 2), crow[c]);
                     tma_prefetch_l2_2d(&act_map, st * kBK, tile * N);
                 }
             for (int st = 0; st < nk; ++st, ++gs) {
                 const int s = gs % kStages;
                 if (lane == 0 && st + kPrefetch < nk) {
-                    tma_prefetch_l2_2d(&codes_map, (st + kPrefetch) * (kBK / 2), crow0);
-                    tma_prefetch_l2_2d(&codes_map, (st + kPrefetch) * (kBK / 2), crow1);
+#pragma unroll
+                    for (int c = 0; c < 2 * kRB; ++c)
+                        tma_prefetch_l2_2d(&codes_map, (st + kPrefetch) * (kBK / 2), crow[c]);
                     tma_prefetch_l2_2d(&act_map, (st + kPrefetch) * kBK, tile * N);
                 }
                 // both slots of a pair come free with the pair's commit
@@ -245,11 +269,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&raw_full[s], (uint32_t)(kCodeBytes + L::kBBytes));
-                    const uint32_t cdst = smem_u32(stage_c(s));
-                    tma_load_2d(cdst, &codes_map, st * (kBK / 2), crow0, &raw_full[s]);
-                    tma_load_2d(cdst + kCodeBox * (kBK / 2), &codes_map, st * (kBK / 2), crow1,
-                                &raw_full[s]);
+                    mbar_arrive_expect_tx(&raw_full[s], (uint32_t)(L::kCodeStage + L::kBBytes));
+#pragma unroll
+                    for (int j = 0; j < kRB; ++j) {
+                        const uint32_t cdst = smem_u32(stage_c(s)) + j * kCodeBytes;
+                        tma_load_2d(cdst, &codes_map, st * (kBK / 2), crow[2 * j], &raw_full[s]);
+                        tma_load_2d(cdst + kCodeBox * (kBK / 2), &codes_map, st * (kBK / 2),
+                                    crow[2 * j + 1], &raw_full[s]);
+                    }
                     tma_load_2d(smem_u32(stage_b(s)), &act_map, st * kBK, tile * N, &raw_full[s]);
                 }
             }
@@ -267,11 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t gs = 0, it = 0;
             bool ok = true;
             for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
-                if (checked_expert(g, item / row_blocks, false) < 0) continue;
+                if (checked_expert(g, item / row_groups, false) < 0) continue;
                 const uint32_t b = it % kAccBufs;
                 if (it >= (uint32_t)kAccBufs && !mbar_wait(&acc_free[b], ((it / kAccBufs) - 1) & 1)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + b * N;
+                const uint32_t d_tmem = tmem + b * L::kAccCols;
                 for (int st = 0; st < nk; st += 2, gs += 2) {
                     const int pr = (gs >> 1) % kPairs;
                     // both stages' A converted; the converters arrive only after
@@ -284,12 +311,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const int s = (gs + h2) % kStages;
-                        const uint32_t a_tmem = tmem + (uint32_t)(L::kACol0 + s * kACols);
                         const uint64_t bd = sdesc_sw128(smem_u32(stage_b(s)));
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k)  // A: 8 columns per K = 16; B: +32 bytes in the swizzle atom
-                            mma_f16_ts(d_tmem, a_tmem + 8u * k, bd + 2u * k, idesc,
-                                       (st | h2 | k) != 0 ? 1u : 0u);
+                        for (int j = 0; j < kRB; ++j) {  // each block into its own accumulator
+                            const uint32_t a_tmem =
+                                tmem + (uint32_t)(L::kACol0 + s * L::kAColsStage + j * kACols);
+#pragma unroll
+                            for (int k = 0; k < kBK / 16; ++k)  // A: 8 columns per K = 16; B: +32 bytes in the swizzle atom
+                                mma_f16_ts(d_tmem + (uint32_t)(j * N), a_tmem + 8u * k, bd + 2u * k,
+                                           idesc, (st | h2 | k) != 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit(&stage_free[pr]);
                 }
@@ -312,57 +343,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t gs = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
-            const int tile = item / row_blocks, block = item % row_blocks;
+            const int tile = item / row_groups, grp = item % row_groups;
             const int e = checked_expert(g, tile, false);
             if (e < 0) continue;
-            int wrow;
-            bool rvalid;
-            if (MODE == 0) {
-                const int n = block * 64 + (rho >> 1);
-                rvalid = n < g.I;
-                wrow = (rho & 1) ? g.I + n : n;
-            } else {
-                wrow = block * 128 + rho;
-                rvalid = wrow < g.rows;
+            // this lane's weight row in each of the item's blocks
+            const uint8_t* sp[kRB];
+            int s_ref[kRB];
+            bool rvalid[kRB];
+#pragma unroll
+            for (int j = 0; j < kRB; ++j) {
+                const int block = grp * kRB + j;
+                int wrow;
+                if (MODE == 0) {
+                    const int n = block * 64 + (rho >> 1);
+                    rvalid[j] = n < g.I;
+                    wrow = (rho & 1) ? g.I + n : n;
+                } else {
+                    wrow = block * 128 + rho;
+                    rvalid[j] = wrow < g.rows;
+                }
+                sp[j] = g.scales + ((size_t)e * g.rows + (rvalid[j] ? wrow : 0)) * (size_t)ngroups;
+                s_ref[j] = row_scale_ref(rvalid[j] ? row_scale_max_part(sp[j], ngroups, svec, 0, 1) : 0u);
             }
-            const uint8_t* sp = g.scales + ((size_t)e * g.rows + (rvalid ? wrow : 0)) * (size_t)ngroups;
-            const int s_ref = row_scale_ref(rvalid ? row_scale_max_part(sp, ngroups, svec, 0, 1) : 0u);
-            auto scale_at = [&](int gidx) {
-                return (rvalid && gidx < ngroups) ? (uint32_t)__ldg(sp + gidx) : 0u;
+            auto scale_at = [&](int j, int gidx) {
+                return (rvalid[j] && gidx < ngroups) ? (uint32_t)__ldg(sp[j] + gidx) : 0u;
             };
             for (int st = 0; st < nk; ++st, ++gs) {
                 if ((int)(gs & 3u) != part) continue;
                 const int s = gs % kStages;
-                const uint32_t m0 = f16_group_mult(scale_at(2 * st), s_ref);
-                const uint32_t m1 = f16_group_mult(scale_at(2 * st + 1), s_ref);
+                uint32_t m0[kRB], m1[kRB];
+#pragma unroll
+                for (int j = 0; j < kRB; ++j) {
+                    m0[j] = f16_group_mult(scale_at(j, 2 * st), s_ref[j]);
+                    m1[j] = f16_group_mult(scale_at(j, 2 * st + 1), s_ref[j]);
+                }
                 if (!mbar_wait(&raw_full[s], (gs / kStages) & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();  // after the MMAs that last read this A stage
-                uint4 c[2];
-                const uint32_t cs = smem_u32(stage_c(s)) + crow * (kBK / 2);
-                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(c[0].x), "=r"(c[0].y), "=r"(c[0].z), "=r"(c[0].w)
-                             : "r"(cs));
-                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(c[1].x), "=r"(c[1].y), "=r"(c[1].z), "=r"(c[1].w)
-                             : "r"(cs + 16));
-                uint32_t a[32];  // column j of the stage = f16x2 (k 2j, 2j + 1)
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const uint32_t w[4] = {c[hh].x, c[hh].y, c[hh].z, c[hh].w};
-                    const uint32_t m = hh ? m1 : m0;
+                for (int j = 0; j < kRB; ++j) {
+                    uint4 c[2];
+                    const uint32_t cs = smem_u32(stage_c(s)) + j * kCodeBytes + crow * (kBK / 2);
+                    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(c[0].x), "=r"(c[0].y), "=r"(c[0].z), "=r"(c[0].w)
+                                 : "r"(cs));
+                    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(c[1].x), "=r"(c[1].y), "=r"(c[1].z), "=r"(c[1].w)
+                                 : "r"(cs + 16));
+                    uint32_t a[32];  // column i of the block's stage = f16x2 (k 2i, 2i + 1)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint4 v = codes_to_f16x8(w[i], m);
-                        a[16 * hh + 4 * i + 0] = v.x;
-                        a[16 * hh + 4 * i + 1] = v.y;
-                        a[16 * hh + 4 * i + 2] = v.z;
-                        a[16 * hh + 4 * i + 3] = v.w;
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t w[4] = {c[hh].x, c[hh].y, c[hh].z, c[hh].w};
+                        const uint32_t m = hh ? m1[j] : m0[j];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 v = codes_to_f16x8(w[i], m);
+                            a[16 * hh + 4 * i + 0] = v.x;
+                            a[16 * hh + 4 * i + 1] = v.y;
+                            a[16 * hh + 4 * i + 2] = v.z;
+                            a[16 * hh + 4 * i + 3] = v.w;
+                        }
                     }
+                    tmem_st32(lane_base + (uint32_t)(s * L::kAColsStage + j * kACols), a);
                 }
-                tmem_st32(lane_base + (uint32_t)(s * kACols), a);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
@@ -384,25 +429,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kQ = N / 32;
         int qn[kQ];
         float cn[kQ];
-        float frn = 0.0f;
+        float frn[kRB];
         auto load_item = [&](int item) {
             if (item >= items) return;
-            const int tile = item / row_blocks, block = item % row_blocks;
+            const int tile = item / row_groups, grp = item % row_groups;
             const int e = checked_expert(g, tile, false);
             if (e < 0) return;
-            int wrow;
-            bool rvalid;
-            if (MODE == 0) {
-                const int n = block * 64 + (r >> 1);
-                rvalid = n < g.I;
-                wrow = (r & 1) ? g.I + n : n;
-            } else {
-                wrow = block * 128 + r;
-                rvalid = wrow < g.rows;
+#pragma unroll
+            for (int j = 0; j < kRB; ++j) {
+                const int block = grp * kRB + j;
+                int wrow;
+                bool rvalid;
+                if (MODE == 0) {
+                    const int n = block * 64 + (r >> 1);
+                    rvalid = n < g.I;
+                    wrow = (r & 1) ? g.I + n : n;
+                } else {
+                    wrow = block * 128 + r;
+                    rvalid = wrow < g.rows;
+                }
+                const uint8_t* sp = g.scales + ((size_t)e * g.rows + (rvalid ? wrow : 0)) * (size_t)(K / 32);
+                frn[j] = __uint_as_float(
+                    (uint32_t)row_scale_ref(rvalid ? row_scale_max_part(sp, K / 32, svec, 0, 1) : 0u) << 23);
             }
-            const uint8_t* sp = g.scales + ((size_t)e * g.rows + (rvalid ? wrow : 0)) * (size_t)(K / 32);
-            frn = __uint_as_float(
-                (uint32_t)row_scale_ref(rvalid ? row_scale_max_part(sp, K / 32, svec, 0, 1) : 0u) << 23);
 #pragma unroll
             for (int u = 0; u < kQ; ++u) {
                 const int p = tile * N + 32 * u + lane;
@@ -418,14 +467,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_item(blockIdx.x);
         uint32_t it = 0;
         for (int item = blockIdx.x; item < items; item += gridDim.x) {
-            const int tile = item / row_blocks, block = item % row_blocks;
+            const int tile = item / row_groups, grp = item % row_groups;
             const int e = checked_expert(g, tile, false);
             if (e < 0) {
                 load_item(item + gridDim.x);
                 continue;
             }
             const uint32_t b = it % kAccBufs;
-            const float fr = frn;
+            float frs[kRB];
+#pragma unroll
+            for (int j = 0; j < kRB; ++j) frs[j] = frn[j];
             int qv[kQ];
             float cv[kQ];
 #pragma unroll
@@ -433,11 +484,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&acc_full[b], (it / kAccBufs) & 1)) break;
             tc_fence_after();
             load_item(item + gridDim.x);
-            // 32 columns per round trip: two loads, one wait
+            // 32 columns per round trip: two loads, one wait; block by block
+            // (not unrolled across blocks: that doubles the live registers)
+#pragma unroll 1
+            for (int j = 0; j < kRB; ++j) {
+            const int block = grp * kRB + j;
+            const float fr = j == 0 ? frs[0] : frs[kRB - 1];
 #pragma unroll
             for (int c0 = 0; c0 < N; c0 += 32) {
                 uint32_t v[32];
-                const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + b * N + (uint32_t)c0;
+                const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + b * L::kAccCols +
+                                       (uint32_t)(j * N + c0);
                 tmem_ld16_nowait(taddr, v);
                 tmem_ld16_nowait(taddr + 16, v + 16);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -479,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_free[b]);
@@ -512,7 +570,8 @@ cudaError_t launch_n(const GroupedGemm& g, cudaStream_t s) {
                         (uint64_t)g.K * 2, kBK, N, CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
     const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
-    const long long max_items = (long long)g.max_tiles * row_blocks;
+    const int row_groups = (row_blocks + PrefillSmem<N>::kRB - 1) / PrefillSmem<N>::kRB;
+    const long long max_items = (long long)g.max_tiles * row_groups;
     const int grid = (int)std::min<long long>(max_items, (long long)num_sms());
     return launch_pdl(prefill_gemm_kernel<MODE, N>, dim3(grid), dim3(kThreads), smem, s, g,
                       codes_map, act_map);
