@@ -493,9 +493,9 @@ def cpu_baseline(w, host, ids_unused, target_s, act="bf16"):
     n = threads
     dt = _oracle_sample(w, host, ids, wt, n, threads, act=act)
     total_tok, total_s = n, dt
-    while total_s < target_s and total_tok < 4 * w.T:
+    while total_s < target_s and total_tok < 32 * w.T:
         n2 = max(threads, int(n * (target_s - total_s) / max(dt, 1e-3)) // threads * threads)
-        n2 = min(n2, 4 * w.T - total_tok)
+        n2 = min(n2, 32 * w.T - total_tok)
         dt = _oracle_sample(w, host, ids, wt, n2, threads, offset=total_tok, act=act)
         total_tok += n2
         total_s += dt

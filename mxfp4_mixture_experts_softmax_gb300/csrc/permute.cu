@@ -28,14 +28,18 @@
 // stores of sorted_pairs and inv are spread over many SMs instead of one:
 //  1. block b counts the experts of its contiguous slice of pairs into
 //     scratch row b (scratch = inv_pairs, which holds T * Kt >= blocks * Et
-//     ints and is rewritten in step 4);
+//     ints and is rewritten in step 4), and fills its share of sorted_pairs
+//     with -1 (padding and tail stay -1);
 //  2. one block turns the rows into each (block, expert)'s first position:
-//     bucket offset + the counts of earlier blocks; and writes the offsets,
-//     padding, tile map and tails as above;
+//     bucket offset + the counts of earlier blocks; and writes the offsets
+//     and the tile count;
 //  3. block b scatters its slice from its row of positions exactly as the
 //     single-block kernel does (warp sub-slices, lane order within a warp);
 //  4. inv[sorted_pairs[p]] = p for the used positions; -1 for pairs whose id
-//     is outside [0, Et).
+//     is outside [0, Et); the tile -> expert map by binary search in the
+//     offsets.
+// The bulk stores of steps 1 and 4 are spread over the grid: written by the
+// one block of step 2 they took ~30 us at 90k pairs.
 // Slices are contiguous in pair order at every level, so the result is the
 // same stable sort, bit for bit.
 #include <stdlib.h>
@@ -192,12 +196,16 @@ __device__ __forceinline__ void permute_block(const int32_t* ids, int P, int Et,
 
 // ------------------------------------------------- multi-block (large batches)
 
-// 1. scratch[b][e] = pairs of block b's slice with expert e
+// 1. scratch[b][e] = pairs of block b's slice with expert e; sorted_pairs
+//    filled with -1
 __global__ void __launch_bounds__(kThreads) permute_count_kernel(const int32_t* __restrict__ ids,
-                                                                 int P, int Et, int slice,
-                                                                 int32_t* __restrict__ scratch) {
+                                                                 int P, int Et, int slice, int cap,
+                                                                 int32_t* __restrict__ scratch,
+                                                                 int32_t* __restrict__ sorted_pairs) {
     pdl_begin();
     extern __shared__ int32_t sh[];  // [Et]
+    for (int p = blockIdx.x * kThreads + threadIdx.x; p < cap; p += gridDim.x * kThreads)
+        sorted_pairs[p] = -1;
     for (int i = threadIdx.x; i < Et; i += kThreads) sh[i] = 0;
     __syncthreads();
     const int q0 = min(P, blockIdx.x * slice), q1 = min(P, q0 + slice);
@@ -211,12 +219,10 @@ __global__ void __launch_bounds__(kThreads) permute_count_kernel(const int32_t* 
 }
 
 // 2. one block: scratch[b][e] = off[e] + pairs of expert e in blocks < b;
-//    offsets, padding, tile map
+//    offsets and the tile count
 __global__ void __launch_bounds__(kThreads, 1)
-    permute_scan_kernel(int nb, int Et, int tile_m, int cap, int max_tiles,
-                        int32_t* __restrict__ scratch, int32_t* __restrict__ sorted_pairs,
-                        int32_t* __restrict__ offsets_out, int32_t* __restrict__ tile_expert,
-                        int32_t* __restrict__ num_tiles) {
+    permute_scan_kernel(int nb, int Et, int tile_m, int32_t* __restrict__ scratch,
+                        int32_t* __restrict__ offsets_out, int32_t* __restrict__ num_tiles) {
     pdl_begin();
     extern __shared__ int32_t sh[];
     int32_t* cnt = sh;            // [Et]
@@ -255,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
         }
     }
-    write_layout(cnt, off, Et, tile_m, cap, max_tiles, sorted_pairs, offsets_out, tile_expert,
-                 num_tiles);
+    for (int e = threadIdx.x; e <= Et; e += kThreads) offsets_out[e] = off[e];
+    if (threadIdx.x == 0) *num_tiles = off[Et] / tile_m;
     pdl_end();
 }
 
@@ -293,22 +299,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_end();
 }
 
-// 4. the inverse map, and -1 for pairs with an id outside [0, Et)
+// 4. the inverse map, -1 for pairs with an id outside [0, Et), and the tile
+//    -> expert map (the expert whose bucket [off[e], off[e+1]) holds the
+//    tile's first row; -1 past the used tiles)
 __global__ void __launch_bounds__(256) permute_inverse_kernel(const int32_t* __restrict__ ids, int P,
                                                               int Et,
                                                               const int32_t* __restrict__ sorted_pairs,
+                                                              const int32_t* __restrict__ offsets,
                                                               const int32_t* __restrict__ num_tiles,
-                                                              int tile_m, int cap,
-                                                              int32_t* __restrict__ inv) {
+                                                              int tile_m, int cap, int max_tiles,
+                                                              int32_t* __restrict__ inv,
+                                                              int32_t* __restrict__ tile_expert) {
     pdl_begin();
-    const int used = min(max(__ldg(num_tiles), 0) * tile_m, cap);
-    const int n = max(P, used);
+    const int nt = min(max(__ldg(num_tiles), 0), max_tiles);
+    const int used = min(nt * tile_m, cap);
+    const int n = max(max(P, used), max_tiles);
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         if (i < used) {
             const int q = __ldg(sorted_pairs + i);
             if ((unsigned)q < (unsigned)P) inv[q] = i;
         }
         if (i < P && (unsigned)__ldg(ids + i) >= (unsigned)Et) inv[i] = -1;
+        if (i < max_tiles) {
+            int e = -1;
+            if (i < nt) {  // largest e with off[e] <= row (off is non-decreasing, off[0] = 0)
+                const int row = i * tile_m;
+                int lo = 0, hi = Et;  // invariant: off[lo] <= row < off[hi]
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (__ldg(offsets + mid) <= row) lo = mid;
+                    else hi = mid;
+                }
+                e = lo;
+            }
+            tile_expert[i] = e;
+        }
     }
     pdl_end();
 }
@@ -392,10 +417,10 @@ cudaError_t launch_permute(const int32_t* ids, int T, int Kt, int Et, int tile_m
     cudaError_t err = ensure_dynamic_smem((const void*)permute_scatter_kernel, hist_smem);
     if (err == cudaSuccess)
         err = launch_pdl(permute_count_kernel, dim3(nb), dim3(kThreads), sizeof(int32_t) * Et, s,
-                         ids, P, Et, slice, scratch);
+                         ids, P, Et, slice, cap, scratch, sorted_pairs);
     if (err == cudaSuccess)
         err = launch_pdl(permute_scan_kernel, dim3(1), dim3(kThreads), scan_smem, s, nb, Et, tile_m,
-                         cap, max_tiles, scratch, sorted_pairs, offsets, tile_expert, num_tiles);
+                         scratch, offsets, num_tiles);
     if (err == cudaSuccess)
         err = launch_pdl(permute_scatter_kernel, dim3(nb), dim3(kThreads), hist_smem, s, ids, P, Et,
                          slice, (const int32_t*)scratch, sorted_pairs);
@@ -403,7 +428,8 @@ cudaError_t launch_permute(const int32_t* ids, int T, int Kt, int Et, int tile_m
         err = launch_pdl(permute_inverse_kernel, dim3(std::min((std::max(P, cap) + 255) / 256,
                                                                num_sms() * 8)),
                          dim3(256), 0, s, ids, P, Et, (const int32_t*)sorted_pairs,
-                         (const int32_t*)num_tiles, tile_m, cap, inv);
+                         (const int32_t*)offsets, (const int32_t*)num_tiles, tile_m, cap, max_tiles,
+                         inv, tile_expert);
     return err;
 }
 
