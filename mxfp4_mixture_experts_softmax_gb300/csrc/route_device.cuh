@@ -52,30 +52,60 @@ __device__ __forceinline__ void route_token(const float* __restrict__ l, int E, 
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
 
-    uint32_t taken = 0;
     int my_id = 0;
     float my_logit = 0.0f;
-    for (int k = 0; k < K; ++k) {
-        unsigned long long best = 0ull;  // below every valid key
+    if constexpr (VPL <= 16) {
+        // keys built once; a taken key is set to 0 (below every valid key)
+        unsigned long long key[VPL];
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
             const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u)) {
-                unsigned long long key =
-                    ((unsigned long long)order_key(v[i]) << 32) | (0xFFFFFFFFu - (uint32_t)e);
-                best = key > best ? key : best;
+            key[i] = e < E ? ((unsigned long long)order_key(v[i]) << 32) | (0xFFFFFFFFu - (uint32_t)e)
+                           : 0ull;
+        }
+        for (int k = 0; k < K; ++k) {
+            unsigned long long best = key[0];
+#pragma unroll
+            for (int i = 1; i < VPL; ++i) best = key[i] > best ? key[i] : best;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+                best = other > best ? other : best;
+            }
+            const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+#pragma unroll
+            for (int i = 0; i < VPL; ++i)
+                if (lane + 32 * i == e) key[i] = 0ull;
+            if (lane == k) {
+                my_id = e;
+                my_logit = key_to_float((uint32_t)(best >> 32));
             }
         }
+    } else {
+        // many values per lane: keys rebuilt each round (fewer live registers)
+        uint32_t taken = 0;
+        for (int k = 0; k < K; ++k) {
+            unsigned long long best = 0ull;  // below every valid key
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-            best = other > best ? other : best;
-        }
-        const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
-        if ((e & 31) == lane) taken |= 1u << (e >> 5);
-        if (lane == k) {
-            my_id = e;
-            my_logit = key_to_float((uint32_t)(best >> 32));
+            for (int i = 0; i < VPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E && !((taken >> i) & 1u)) {
+                    unsigned long long key =
+                        ((unsigned long long)order_key(v[i]) << 32) | (0xFFFFFFFFu - (uint32_t)e);
+                    best = key > best ? key : best;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+                best = other > best ? other : best;
+            }
+            const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+            if ((e & 31) == lane) taken |= 1u << (e >> 5);
+            if (lane == k) {
+                my_id = e;
+                my_logit = key_to_float((uint32_t)(best >> 32));
+            }
         }
     }
 
