@@ -157,17 +157,23 @@ struct PrefillSmem {
     // a ring of a multiple of 4 slots each slot belongs to one part, so every
     // barrier's phases are observed in order (a parity wait is unambiguous
     // only one phase ahead).
-    static constexpr int kStages = (kRB == 1 && N <= 128) ? 8 : 4;
-    static_assert(kStages % 4 == 0, "slot ownership");
+    // Two rings: kStages shared-memory slots (codes + B, filled by TMA) and
+    // kAStages tensor-memory A slots (filled by the converters).  With two
+    // blocks per item tensor memory holds only 4 A slots, but shared memory
+    // holds 8 stages, so TMA runs further ahead than the conversion.
+    static constexpr int kStages = (N <= 128) ? 8 : 4;
+    static constexpr int kAStages = (kRB == 1 && N <= 128) ? 8 : 4;
+    static_assert(kStages % 4 == 0 && kAStages % 4 == 0, "slot ownership");
+    static_assert(kStages % kAStages == 0, "ring nesting");
     static constexpr int kBars = kStages * kStage;
     static constexpr int kTotal = kBars + 256 + 1024;              // + alignment slack
     // tensor memory (512 columns): the accumulators (one per block, N
     // columns each), then the A stages (kACols columns per block)
     static constexpr int kAColsStage = kRB * kACols;
     static constexpr int kAccCols = kRB * N;
-    static constexpr int kAccBufs = 2 * kAccCols + kStages * kAColsStage <= 512 ? 2 : 1;
+    static constexpr int kAccBufs = 2 * kAccCols + kAStages * kAColsStage <= 512 ? 2 : 1;
     static constexpr int kACol0 = kAccBufs * kAccCols;
-    static_assert(kACol0 + kStages * kAColsStage <= 512, "tensor memory");
+    static_assert(kACol0 + kAStages * kAColsStage <= 512, "tensor memory");
 };
 
 template <int MODE, int N>
@@ -176,17 +182,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap act_map) {
     pdl_begin();
     using L = PrefillSmem<N>;
-    constexpr int kStages = L::kStages;
+    constexpr int kStages = L::kStages, kAStages = L::kAStages;
+    constexpr bool kDecoupled = kAStages != kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     // The MMA thread waits and commits once per pair of stages (stages 2P and
     // 2P + 1 share pair barrier P mod kPairs): its per-stage barrier work,
     // not the tensor pipe, bounds the loop otherwise.
-    constexpr int kPairs = kStages / 2;
+    constexpr int kPairs = kStages / 2, kAPairs = kAStages / 2;
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L::kBars);  // codes + B landed, per slot
-    uint64_t* a_full = raw_full + kStages;                               // A converted, per pair
-    uint64_t* stage_free = a_full + kPairs;                              // MMAs done with a pair
-    uint64_t* acc_full = stage_free + kPairs;                            // [2] accumulator ready
+    uint64_t* a_full = raw_full + kStages;                               // A converted, per A pair
+    uint64_t* stage_free = a_full + kAPairs;                             // MMAs done with a slot pair
+    uint64_t* a_free = stage_free + kPairs;                              // MMAs done with an A pair
+    uint64_t* acc_full = a_free + kAPairs;                               // [2] accumulator ready
     uint64_t* acc_free = acc_full + 2;                                   // [2] accumulator drained
     uint64_t* drain = acc_free + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -208,9 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&raw_full[s], 1);
-        for (int p = 0; p < kPairs; ++p) {
+        for (int p = 0; p < kPairs; ++p) mbar_init(&stage_free[p], 1);
+        for (int p = 0; p < kAPairs; ++p) {
             mbar_init(&a_full[p], 8);  // one converter warp per lane quadrant and stage
-            mbar_init(&stage_free[p], 1);
+            mbar_init(&a_free[p], 1);
         }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -300,22 +309,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + b * L::kAccCols;
                 for (int st = 0; st < nk; st += 2, gs += 2) {
-                    const int pr = (gs >> 1) % kPairs;
+                    const int pr = (gs >> 1) % kPairs, pa = (gs >> 1) % kAPairs;
                     // both stages' A converted; the converters arrive only after
                     // seeing their stage's TMA barrier, so B has landed too
-                    if (!mbar_wait(&a_full[pr], (gs / kStages) & 1)) {
+                    if (!mbar_wait(&a_full[pa], (gs / kAStages) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
-                        const int s = (gs + h2) % kStages;
+                        const int s = (gs + h2) % kStages, sa = (gs + h2) % kAStages;
                         const uint64_t bd = sdesc_sw128(smem_u32(stage_b(s)));
 #pragma unroll
                         for (int j = 0; j < kRB; ++j) {  // each block into its own accumulator
                             const uint32_t a_tmem =
-                                tmem + (uint32_t)(L::kACol0 + s * L::kAColsStage + j * kACols);
+                                tmem + (uint32_t)(L::kACol0 + sa * L::kAColsStage + j * kACols);
 #pragma unroll
                             for (int k = 0; k < kBK / 16; ++k)  // A: 8 columns per K = 16; B: +32 bytes in the swizzle atom
                                 mma_f16_ts(d_tmem + (uint32_t)(j * N), a_tmem + 8u * k, bd + 2u * k,
@@ -323,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     mma_commit(&stage_free[pr]);
+                    if (kDecoupled) mma_commit(&a_free[pa]);
                 }
                 if (ok) mma_commit(&acc_full[b]);
                 ++it;  // items processed (skipped ones use no accumulator)
@@ -370,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             for (int st = 0; st < nk; ++st, ++gs) {
                 if ((int)(gs & 3u) != part) continue;
-                const int s = gs % kStages;
+                const int s = gs % kStages, sa = gs % kAStages;
                 uint32_t m0[kRB], m1[kRB];
 #pragma unroll
                 for (int j = 0; j < kRB; ++j) {
@@ -378,6 +388,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m1[j] = f16_group_mult(scale_at(j, 2 * st + 1), s_ref[j]);
                 }
                 if (!mbar_wait(&raw_full[s], (gs / kStages) & 1)) {
+                    ok = false;
+                    break;
+                }
+                // the A slot comes free with the MMAs of stage gs - kAStages (with
+                // equal rings the TMA barrier already implies it)
+                if (kDecoupled && gs >= (uint32_t)kAStages &&
+                    !mbar_wait(&a_free[(gs >> 1) % kAPairs], ((gs / kAStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -406,12 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             a[16 * hh + 4 * i + 3] = v.w;
                         }
                     }
-                    tmem_st32(lane_base + (uint32_t)(s * L::kAColsStage + j * kACols), a);
+                    tmem_st32(lane_base + (uint32_t)(sa * L::kAColsStage + j * kACols), a);
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[(gs >> 1) % kPairs]);
+                if (lane == 0) mbar_arrive(&a_full[(gs >> 1) % kAPairs]);
             }
         }
     } else {
