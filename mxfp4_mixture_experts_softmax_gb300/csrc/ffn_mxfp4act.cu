@@ -29,11 +29,11 @@
 //     column q), and token column n's at lane 32 q + n % 32, column base +
 //     n / 32 in every quadrant q; byte j of a 32-bit cell is k group j of a
 //     128-k chunk, the MMA's scale id (0 or 2) picks the pair of groups;
-//   * 4 epilogue warps: down scales the fp32 accumulator by the routing
-//     weight and stores it to y blocked as [H/128][cap][128] (row block,
-//     sorted position, row in block), so an item's output is one contiguous
-//     64 KB run of DRAM writes instead of 128-byte pieces 16 KB apart;
-//     the combine gathers each token's positions from it; gate_up passes each 32-column slice of the
+//   * 4 epilogue warps: down stores the fp32 accumulator to y blocked as
+//     [H/128][cap][128] (row block, sorted position, row in block), so an
+//     item's output is one contiguous 64 KB run of DRAM writes; the combine
+//     gathers each token's positions from it and applies the routing weight
+//     there (the same fp32 product the epilogue would form); gate_up passes each 32-column slice of the
 //     accumulator through shared memory (transposed), so each thread holds
 //     16 consecutive i of one token: SwiGLU in fp32, then MXFP4 quantisation
 //     of each 32-block of i (two threads per block), codes and scale stored.
@@ -450,35 +450,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;                        // lanes 32 quad .. 32 quad + 31
         const int et = (warp - kEpiWarp0) * 32 + lane;    // 0..127
         uint32_t it = 0;
-        // down: pair index and routing weight of each column, loaded one item
-        // ahead (qn, wn hold those of `item` at the top of the loop)
-        int qn[kNJ], qv[kNJ];
-        float wn[kNJ], wv[kNJ];
-        auto load_cols = [&](int item) {
+        // down: the tile's pair indices, loaded one item ahead (qn holds those
+        // of `item` at the top of the loop); the positions that hold a pair
+        // are a prefix of the tile (padding follows an expert's pairs), so
+        // their count bounds the stores
+        int qn[kNJ];
+        auto load_pairs = [&](int item) {
             if (MODE == 1 && item < items) {
-                const int tile = item / row_blocks;
 #pragma unroll
-                for (int u = 0; u < kNJ; ++u) {
-                    const int p = tile * N + 32 * u + lane;
-                    qn[u] = checked_pair(g, p);
-                    wn[u] = __ldg(g.w_pos + p);
-                }
+                for (int u = 0; u < kNJ; ++u) qn[u] = checked_pair(g, (item / row_blocks) * N + 32 * u + lane);
             }
         };
-        load_cols(blockIdx.x);
+        load_pairs(blockIdx.x);
         for (int item = blockIdx.x; item < items; item += gridDim.x) {
             const int tile = item / row_blocks, block = item % row_blocks;
             const int e = checked_expert(g, tile, false);
             if (e < 0) {
-                load_cols(item + gridDim.x);
+                load_pairs(item + gridDim.x);
                 continue;
             }
             const uint32_t b = it % kAccBufs;
+            int nvalid = 0;
+            if (MODE == 1) {
 #pragma unroll
-            for (int u = 0; u < kNJ; ++u) qv[u] = qn[u], wv[u] = wn[u];
+                for (int u = 0; u < kNJ; ++u) nvalid += __popc(__ballot_sync(0xFFFFFFFFu, qn[u] >= 0));
+            }
             if (!mbar_wait(&acc_full[b], (it / kAccBufs) & 1)) break;
             tc_fence_after();
-            load_cols(item + gridDim.x);
+            load_pairs(item + gridDim.x);
 #pragma unroll 1
             for (int c0 = 0; c0 < N; c0 += 32) {
                 uint32_t v[32];
@@ -491,23 +490,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&acc_free[b]);
                 }
-                if (MODE == 1) {
+                if (MODE == 1) {  // the raw accumulator of the positions holding a pair
                     float* yb = g.y_out + ((size_t)block * g.act_rows + (size_t)tile * N + c0) * 128 +
                                 32 * quad + lane;
-                    int q_lo = qv[0];
-                    float w_lo = wv[0];
+                    const int nc = nvalid - c0;  // warp-uniform
 #pragma unroll
-                    for (int u = 1; u < kNJ; ++u)  // register select, no local memory
-                        if (u == c0 / 32) {
-                            q_lo = qv[u];
-                            w_lo = wv[u];
-                        }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int q = __shfl_sync(0xFFFFFFFFu, q_lo, i);
-                        const float w = __shfl_sync(0xFFFFFFFFu, w_lo, i);
-                        if (q >= 0) yb[(size_t)i * 128] = w * __uint_as_float(v[i]);
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        if (i < nc) yb[(size_t)i * 128] = __uint_as_float(v[i]);
                 } else {
                     // transpose through shared memory: stg[column][accumulator row]
 #pragma unroll
@@ -598,11 +587,16 @@ cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
     }
 }
 
-// out[t, m] = bf16(sum over j ascending of y[m / 128][inv[t * Kt + j]][m % 128])
-// for y blocked as the down epilogue writes it; 4 consecutive m per thread,
-// so a warp reads 512 contiguous bytes per slot.
+// out[t, m] = bf16(sum over j ascending of f[p] * y[m / 128][p][m % 128]),
+// p = inv[t * Kt + j], f the per-position factor (the routing weight, on the
+// bf16 path times the h row's factor; 1 when f is null), for y blocked as
+// the down epilogues write it.  The product and the sum are rounded apart
+// (no fused multiply-add): the same fp32 values an epilogue applying f would
+// store, summed in the same order.  4 consecutive m per thread, so a warp
+// reads 512 contiguous bytes per slot.
 __global__ void __launch_bounds__(256) combine_blocked_kernel(const float4* __restrict__ y,
-                                                              const int32_t* __restrict__ inv, int T,
+                                                              const int32_t* __restrict__ inv,
+                                                              const float* __restrict__ f, int T,
                                                               int H, int Kt, int cap,
                                                               uint2* __restrict__ out) {
     pdl_begin();
@@ -618,11 +612,18 @@ __global__ void __launch_bounds__(256) combine_blocked_kernel(const float4* __re
                 flag_index_error();
                 continue;
             }
-            const float4 v = __ldg(y + ((size_t)blk * cap + p) * 32 + r4);
-            a.x += v.x;
-            a.y += v.y;
-            a.z += v.z;
-            a.w += v.w;
+            float4 v = __ldg(y + ((size_t)blk * cap + p) * 32 + r4);
+            if (f) {
+                const float c = __ldg(f + p);
+                v.x = __fmul_rn(c, v.x);
+                v.y = __fmul_rn(c, v.y);
+                v.z = __fmul_rn(c, v.z);
+                v.w = __fmul_rn(c, v.w);
+            }
+            a.x = __fadd_rn(a.x, v.x);
+            a.y = __fadd_rn(a.y, v.y);
+            a.z = __fadd_rn(a.z, v.z);
+            a.w = __fadd_rn(a.w, v.w);
         }
         uint2 o;
         o.x = (uint32_t)f32_to_bf16_bits(a.x) | ((uint32_t)f32_to_bf16_bits(a.y) << 16);
@@ -662,9 +663,11 @@ __global__ void __launch_bounds__(256) gather_mx_rows_kernel(const uint4* __rest
     pdl_end();
 }
 
-// w_pos[p] = topk_w[q] for the used positions p holding pair q, else 0.
+// w_pos[p] = topk_w[q] (times rscale[p] when given) for the used positions p
+// holding pair q, else 0.
 __global__ void __launch_bounds__(256) position_weights_kernel(const int32_t* __restrict__ sorted_pairs,
                                                                const float* __restrict__ topk_w,
+                                                               const float* __restrict__ rscale,
                                                                const int32_t* __restrict__ num_tiles,
                                                                int tile_m, int cap, int num_pairs,
                                                                float* __restrict__ w_pos) {
@@ -672,7 +675,9 @@ __global__ void __launch_bounds__(256) position_weights_kernel(const int32_t* __
     const int rows = min(max(__ldg(num_tiles), 0) * tile_m, cap);
     for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < rows; p += gridDim.x * blockDim.x) {
         const int q = __ldg(sorted_pairs + p);
-        w_pos[p] = (q >= 0 && q < num_pairs) ? __ldg(topk_w + q) : 0.0f;
+        float w = (q >= 0 && q < num_pairs) ? __ldg(topk_w + q) : 0.0f;
+        if (rscale) w = __fmul_rn(w, __ldg(rscale + p));
+        w_pos[p] = w;
     }
     pdl_end();
 }
@@ -680,12 +685,12 @@ __global__ void __launch_bounds__(256) position_weights_kernel(const int32_t* __
 }  // namespace
 
 cudaError_t launch_position_weights(const int32_t* sorted_pairs, const float* topk_w,
-                                    const int32_t* num_tiles, int tile_m, int cap, int num_pairs,
-                                    float* w_pos, cudaStream_t s) {
+                                    const float* rscale, const int32_t* num_tiles, int tile_m,
+                                    int cap, int num_pairs, float* w_pos, cudaStream_t s) {
     if (cap <= 0) return cudaSuccess;
     const int blocks = std::min((cap + 255) / 256, num_sms() * 4);
     return launch_pdl(position_weights_kernel, dim3(blocks), dim3(256), 0, s, sorted_pairs, topk_w,
-                      num_tiles, tile_m, cap, num_pairs, w_pos);
+                      rscale, num_tiles, tile_m, cap, num_pairs, w_pos);
 }
 
 cudaError_t launch_gather_mx_rows(const uint8_t* xc, const uint8_t* xs, int H, bool with_scales,
@@ -700,12 +705,12 @@ cudaError_t launch_gather_mx_rows(const uint8_t* xc, const uint8_t* xs, int H, b
                       reinterpret_cast<uint4*>(xgc), reinterpret_cast<uint4*>(xgs));
 }
 
-cudaError_t launch_combine_blocked(const float* y, const int32_t* inv, int T, int H, int Kt, int cap,
-                                   uint16_t* out, cudaStream_t s) {
+cudaError_t launch_combine_blocked(const float* y, const int32_t* inv, const float* f, int T, int H,
+                                   int Kt, int cap, uint16_t* out, cudaStream_t s) {
     const long long n = (long long)T * (H / 4);
     if (n <= 0) return cudaSuccess;
     return launch_pdl(combine_blocked_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
-                      reinterpret_cast<const float4*>(y), inv, T, H, Kt, cap,
+                      reinterpret_cast<const float4*>(y), inv, f, T, H, Kt, cap,
                       reinterpret_cast<uint2*>(out));
 }
 

@@ -475,10 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 qn[u] = checked_pair(g, p);
                 if (MODE == 0)
                     cn[u] = qn[u] < 0 ? 0.0f : __ldg(g.act_rscale + qn[u] / g.Kt);
-                else if (g.w_pos)  // both by position: no dependent load
-                    cn[u] = __ldg(g.w_pos + p) * __ldg(g.act_rscale + p);
-                else
+                else if (!g.y_blocked)  // blocked y leaves the column factor to the combine
                     cn[u] = qn[u] < 0 ? 0.0f : __ldg(g.topk_w + qn[u]) * __ldg(g.act_rscale + p);
+                else
+                    cn[u] = 0.0f;
             }
         };
         load_item(blockIdx.x);
@@ -498,6 +498,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             float cv[kQ];
 #pragma unroll
             for (int u = 0; u < kQ; ++u) qv[u] = qn[u], cv[u] = cn[u];
+            // positions holding a pair: a prefix of the tile (padding follows
+            // an expert's pairs)
+            int nvalid = 0;
+            if (MODE == 1) {
+#pragma unroll
+                for (int u = 0; u < kQ; ++u) nvalid += __popc(__ballot_sync(0xFFFFFFFFu, qv[u] >= 0));
+            }
             if (!mbar_wait(&acc_full[b], (it / kAccBufs) & 1)) break;
             tc_fence_after();
             load_item(item + gridDim.x);
@@ -536,20 +543,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                             g.h_out[(size_t)(tile * N + j) * g.I + n] =
                                 f32_to_bf16_bits(silu(gate * fc) * (up * fc));
                     }
-                } else {
+                } else if (g.y_blocked) {
+                    // blocked y: [rows / 128][position][128], one contiguous run
+                    // per item over the positions holding a pair; the column
+                    // factor (routing weight x h row factor) is applied by the
+                    // combine
                     const int m = block * 128 + r;
-                    // blocked y: [rows / 128][position][128], one contiguous
-                    // run per item; else y[pair][m]
                     float* yb = g.y_out + ((size_t)block * g.act_rows + (size_t)tile * N + c0) * 128 + r;
+                    const int nc = nvalid - c0;  // warp-uniform
+                    if (m < g.rows) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < nc) yb[(size_t)i * 128] = __uint_as_float(v[i]) * fr;
+                    }
+                } else {  // y[pair][m]
+                    const int m = block * 128 + r;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int q = __shfl_sync(0xFFFFFFFFu, q_lo, i);
                         const float fc = __shfl_sync(0xFFFFFFFFu, c_lo, i);
-                        if (m < g.rows && q >= 0) {
-                            const float y = fc * (__uint_as_float(v[i]) * fr);
-                            if (g.y_blocked) yb[(size_t)i * 128] = y;
-                            else g.y_out[(size_t)q * g.rows + m] = y;
-                        }
+                        if (m < g.rows && q >= 0)
+                            g.y_out[(size_t)q * g.rows + m] = fc * (__uint_as_float(v[i]) * fr);
                     }
                 }
             }

@@ -445,14 +445,17 @@ moe_status_t moe_ffn_down_combine(const uint8_t* w2, const uint8_t* s2, const fl
                           tile_m, workspace, ws_bytes, path, stream);
         return st != MOE_OK ? st : moe_combine(y, T, H, Kt, out, stream);
     }
-    // prefill: routing weights by position, y blocked by 128 rows (each work
-    // item writes one contiguous run), the combine gathers each token's
-    // positions in slot order: the same sums in the same order as moe_combine
+    // prefill: y blocked by 128 rows (each work item writes one contiguous
+    // run) without the column factor; the factor per position (routing weight
+    // x h row factor) is applied by the combine, which gathers each token's
+    // positions in slot order: the same products and sums as moe_ffn_down +
+    // moe_combine
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     float* w_pos = reinterpret_cast<float*>(ws + wpos_offset(cap, T, H, I, Kt, tile_m));
+    const float* h_rscale = reinterpret_cast<const float*>(ws + rs_offset(cap, T, H, I, Kt, tile_m)) + T;
     trace("moe_ffn_down_combine", T, H, I, Et, Kt, tile_m, path);
-    cudaError_t err = launch_position_weights(sorted_pairs, topk_w, num_tiles, tile_m, (int)cap,
-                                              T * Kt, w_pos, stream);
+    cudaError_t err = launch_position_weights(sorted_pairs, topk_w, h_rscale, num_tiles, tile_m,
+                                              (int)cap, T * Kt, w_pos, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, T, I, Et, Kt, tile_m,
                               (int)(cap / tile_m));
@@ -461,16 +464,15 @@ moe_status_t moe_ffn_down_combine(const uint8_t* w2, const uint8_t* s2, const fl
     g.rows = H;
     g.K = I;
     g.act = reinterpret_cast<const uint16_t*>(workspace);
-    g.act_rscale = reinterpret_cast<const float*>(ws + rs_offset(cap, T, H, I, Kt, tile_m)) + T;
+    g.act_rscale = h_rscale;
     g.act_rows = (int)cap;
     g.act_by_token = 0;
     g.y_out = y;
     g.y_blocked = 1;
     g.topk_w = topk_w;
-    g.w_pos = w_pos;
     err = launch_prefill_down(g, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    return cuda_status(launch_combine_blocked(y, inv_pairs, T, H, Kt, (int)cap, out, stream));
+    return cuda_status(launch_combine_blocked(y, inv_pairs, w_pos, T, H, Kt, (int)cap, out, stream));
 }
 
 moe_status_t moe_combine_ex(const float* y, const float* y_extra, int T, int H, int Kt,
@@ -729,14 +731,15 @@ moe_status_t moe_ffn_mxfp4act_down(const uint8_t* w2, const uint8_t* s2, const f
     g.sf_tma = I % 512 == 0 ? 1 : 0;
     g.y_out = reinterpret_cast<float*>(ws + L.y);
     g.topk_w = topk_w;
-    g.w_pos = reinterpret_cast<const float*>(ws + L.wpos);
+    float* w_pos = reinterpret_cast<float*>(ws + L.wpos);
     trace("moe_ffn_mxfp4act_down", T, H, I, Et, Kt, tile_m, MOE_PATH_PREFILL);
-    cudaError_t err = launch_position_weights(sorted_pairs, topk_w, num_tiles, tile_m, (int)cap,
-                                              T * Kt, reinterpret_cast<float*>(ws + L.wpos), stream);
+    cudaError_t err = launch_position_weights(sorted_pairs, topk_w, nullptr, num_tiles, tile_m,
+                                              (int)cap, T * Kt, w_pos, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     err = launch_mxfp4act_down(g, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    return cuda_status(launch_combine_blocked(g.y_out, inv_pairs, T, H, Kt, (int)cap, out, stream));
+    return cuda_status(launch_combine_blocked(g.y_out, inv_pairs, w_pos, T, H, Kt, (int)cap, out,
+                                              stream));
 }
 
 moe_status_t moe_ffn_mxfp4act(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,

@@ -74,7 +74,6 @@ struct GroupedGemm {
     // producer loads by TMA with the codes; 0: scale warps load them (by
     // token for gate_up, by position for down)
     int sf_tma;
-    const float* w_pos;          // down: routing weight per sorted position (0 for padding)
     int y_blocked;               // down: y as [ceil(rows/128)][act_rows][128] instead of [pair][rows]
     // decode group factor 2^(s-126) as fp32 bits s * exp_one + exp_bias,
     // taken as runtime values so the multiply-add stays one instruction
@@ -171,14 +170,15 @@ cudaError_t launch_gather_mx_rows(const uint8_t* xc, const uint8_t* xs, int H, b
                                   const int32_t* sorted_pairs, const int32_t* num_tiles, int tile_m,
                                   int Kt, int cap, int num_pairs, uint8_t* xgc, uint8_t* xgs,
                                   cudaStream_t s);
-// w_pos[p] = topk_w[sorted_pairs[p]] for the used positions, 0 for padding
+// w_pos[p] = topk_w[sorted_pairs[p]] (times rscale[p] when given) for the
+// used positions, 0 for padding
 cudaError_t launch_position_weights(const int32_t* sorted_pairs, const float* topk_w,
-                                    const int32_t* num_tiles, int tile_m, int cap, int num_pairs,
-                                    float* w_pos, cudaStream_t s);
-// out = bf16(sum over the Kt slots of y[m / 128][inv[pair]][m % 128]) (the
-// MXFP4-activation down GEMM's blocked y; H % 128 == 0)
-cudaError_t launch_combine_blocked(const float* y, const int32_t* inv, int T, int H, int Kt, int cap,
-                                   uint16_t* out, cudaStream_t s);
+                                    const float* rscale, const int32_t* num_tiles, int tile_m,
+                                    int cap, int num_pairs, float* w_pos, cudaStream_t s);
+// out = bf16(sum over the Kt slots of f[p] * y[m / 128][p][m % 128], p =
+// inv[pair]) for the down GEMMs' blocked y (f null: factor 1)
+cudaError_t launch_combine_blocked(const float* y, const int32_t* inv, const float* f, int T, int H,
+                                   int Kt, int cap, uint16_t* out, cudaStream_t s);
 // block-scaled MXFP4 x MXFP4 grouped GEMMs (tcgen05 kind::mxf4)
 cudaError_t launch_mxfp4act_gate_up(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_mxfp4act_down(const GroupedGemm& g, cudaStream_t s);
