@@ -40,8 +40,8 @@ def parse_args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="decode64")
     p.add_argument("--tile-m", type=int, default=0,
-                   help="rows per expert tile (default: 8 for bf16; for mxfp4 32 below 16 mean "
-                        "rows per expert, else 128)")
+                   help="rows per expert tile (default: 8 for bf16; for mxfp4 by the mean rows "
+                        "per expert: 32 below 16, 64 below 64, else 128)")
     p.add_argument("--E", type=int, default=0,
                    help="routed experts override (smaller cases for profiler captures)")
     p.add_argument("--path", default="auto", choices=["auto", "decode", "prefill"])
@@ -271,7 +271,8 @@ def run_ours(args, ws, rank, local):
             "prefill": libmoe.MOE_PATH_PREFILL}[args.path]
     tm = args.tile_m
     if not tm:
-        tm = 8 if args.act == "bf16" else (32 if w.T * w.Kt < 16 * w.Et else 128)
+        rows = w.T * w.Kt / w.Et
+        tm = 8 if args.act == "bf16" else (32 if rows < 16 else 64 if rows < 64 else 128)
     host = synth.make_inputs(w)
 
     def up(a):
