@@ -86,3 +86,32 @@ def test_out_of_range_indices_are_flagged_not_followed(corrupt, path, tile_m):
     # the context and the library are intact: a valid call matches the oracle
     gc.ffn_parity(_run(w, d, ids, wt, tile_m, path), ref, "after the index error")
     assert libmoe.moe_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("corrupt", [_bad_expert, _bad_pair, _bad_tile_count])
+@pytest.mark.parametrize("tile_m", [32, 64])
+def test_mxfp4act_out_of_range_indices_are_flagged_not_followed(corrupt, tile_m):
+    """The MXFP4-activation path (gather, both GEMMs with their scale warps,
+    the position weights, the blocked combine) under the same corruptions: the
+    index checks flag them, nothing faults, and the next valid call gives the
+    bytes of the valid call before it."""
+    w, d, ids, wt, _ = _case()
+    dev_w = gc.upload_weights(d)
+    x_d, wt_d = gc.to_dev(d["x"]), gc.to_dev(wt)
+
+    def run(corrupt_fn=None):
+        perm = libmoe.moe_permute(gc.to_dev(ids), w.Et, tile_m)
+        if corrupt_fn is not None:
+            corrupt_fn(perm)
+        out = libmoe.moe_ffn_mxfp4act(x_d, dev_w["w13"], dev_w["s13"], dev_w["w2"], dev_w["s2"],
+                                      wt_d, perm)
+        torch.cuda.synchronize()
+        return gc.bf16_dev_to_f64(out)
+
+    assert libmoe.moe_device_error(clear=True) in (0, 1, 2, 3)
+    before = run()
+    assert libmoe.moe_device_error(clear=True) == 0
+    run(corrupt)  # outputs of the skipped work are unspecified
+    assert libmoe.moe_device_error(clear=True) & 2
+    np.testing.assert_array_equal(run(), before)
+    assert libmoe.moe_device_error(clear=True) == 0
