@@ -71,3 +71,55 @@ def test_host_validation_rejects_before_launch(lib):
     assert ffn(x=ctypes.c_void_p(0x1008)) == m.MOE_ERR_INVALID_ARG
     assert ffn(path=7) == m.MOE_ERR_INVALID_ARG
     assert ffn(T=-2) == m.MOE_ERR_INVALID_ARG
+
+
+def test_mxfp4act_host_validation_and_layout(lib):
+    """The MXFP4-activation entries: shape and argument checks before any
+    launch; workspace regions 256-byte aligned and large enough."""
+    from mxfp4_mixture_experts_softmax_gb300 import libmoe as m
+    nul = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x1000)
+
+    def mx(T=4, H=256, I=128, Et=8, Kt=2, tile_m=32, ws=1 << 30, x=fake):
+        return lib.moe_ffn_mxfp4act(x, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                                    T, H, I, Et, Kt, tile_m, fake, fake, ws, nul)
+    assert mx(H=160) == m.MOE_ERR_UNSUPPORTED_SHAPE       # H % 128
+    assert mx(I=96) == m.MOE_ERR_UNSUPPORTED_SHAPE        # I % 128
+    for tm in (8, 16, 48, 512):
+        assert mx(tile_m=tm) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert mx(T=-1) == m.MOE_ERR_INVALID_ARG
+    assert mx(ws=64) == m.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert mx(x=nul) == m.MOE_ERR_INVALID_ARG
+    assert mx(x=ctypes.c_void_p(0x1004)) == m.MOE_ERR_INVALID_ARG  # not 16-byte aligned
+    assert mx(T=0) == m.MOE_OK
+    # quantiser: columns not a multiple of 32, negative rows, NULL pointers
+    assert lib.moe_quantize_mxfp4(fake, 4, 48, fake, fake, nul) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_quantize_mxfp4(fake, -1, 64, fake, fake, nul) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_mxfp4(nul, 4, 64, fake, fake, nul) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_mxfp4(nul, 0, 64, nul, nul, nul) == m.MOE_OK
+    # workspace layout: h regions aligned, inside the workspace, sized for cap rows
+    for T, tm in ((64, 32), (1536, 64), (8192, 128)):
+        H, I, Et, Kt = 4096, 1024, 513, 11
+        ws = m.moe_ffn_mxfp4act_workspace_size(T, H, I, Et, Kt, tm)
+        cap = m.moe_permute_capacity(T, Kt, Et, tm)
+        co, so = ctypes.c_size_t(), ctypes.c_size_t()
+        assert lib.moe_ffn_mxfp4act_h_offsets(T, H, I, Et, Kt, tm, ctypes.byref(co),
+                                              ctypes.byref(so)) == m.MOE_OK
+        assert co.value % 256 == 0 and so.value % 256 == 0
+        assert so.value >= co.value + cap * (I // 2)
+        # y (blocked, fp32 [H/128, cap, 128]) and the rest follow the scales
+        assert ws >= so.value + cap * (I // 32) + cap * H * 4
+    assert lib.moe_ffn_mxfp4act_h_offsets(4, 256, 128, 8, 2, 32, None, None) == m.MOE_ERR_INVALID_ARG
+
+
+def test_bf16_workspace_holds_blocked_y_for_prefill_tiles(lib):
+    """moe_ffn_down_combine's prefill path writes y blocked over cap
+    positions: the workspace reserves that much for prefill tile heights."""
+    from mxfp4_mixture_experts_softmax_gb300 import libmoe as m
+    H, I, Et, Kt = 4096, 1024, 513, 11
+    for T, tm in ((1536, 64), (8192, 128)):
+        cap = m.moe_permute_capacity(T, Kt, Et, tm)
+        ws = m.moe_ffn_workspace_size(T, H, I, Et, Kt, tm)
+        y_off = m.moe_ffn_y_offset(T, I, Et, Kt, tm)
+        assert y_off % 256 == 0 and y_off >= cap * I * 2
+        assert ws >= y_off + cap * H * 4
