@@ -235,6 +235,26 @@ def layer_work(w, ids_host, act="bf16"):
                 flops=flops, gate_up_flops=2 * P * 2 * I * H)
 
 
+def launches_per_step(w, path_name: str) -> int:
+    """Kernel launches of one step: route + permute (one fused launch up to
+    MOE_ROUTE_PERMUTE_FUSED_MAX_T tokens; else the routing kernel and the
+    permutation, one launch or, for large batches, the four-launch multi-block
+    sort), then per path:
+      decode   x -> f16 rows, gate_up, h -> f16 rows | down, combine
+      prefill  x -> f16 rows, gather, gate_up, h -> f16 rows | position
+               weights, down, blocked combine
+      mxfp4act quantise x, gather, gate_up | position weights, down, blocked
+               combine"""
+    from mxfp4_mixture_experts_softmax_gb300 import libmoe
+    P = w.T * w.Kt
+    if w.T <= libmoe.MOE_ROUTE_PERMUTE_FUSED_MAX_T:
+        rp = 1
+    else:
+        nb = min(P // max(w.Et, 1), 160)
+        rp = 1 + (4 if (nb >= 8 and P >= 8192) else 1)
+    return rp + {"decode": 3 + 2, "prefill": 4 + 3, "mxfp4act": 3 + 3}[path_name]
+
+
 # ------------------------------------------------------------ ranks
 
 def max_over_ranks(values, device):
@@ -453,12 +473,7 @@ def run_ours(args, ws, rank, local):
                     "h2d_bytes_per_step": int(host["logits"].nbytes + host["x"].nbytes),
                     "d2h_bytes_per_step": int(w.T * w.H * 2),
                     "ms_per_step": e2e_ms / K},
-            # route + permute (one launch up to MOE_ROUTE_PERMUTE_FUSED_MAX_T
-            # tokens, else two), then bf16: x -> f16 rows, [prefill: gather rows
-            # by tile], gate_up, h -> f16 rows, down, combine; mxfp4: quantise
-            # x, gather code rows, gate_up, down, combine
-            "gpu_launches": ((1 if w.T <= libmoe.MOE_ROUTE_PERMUTE_FUSED_MAX_T else 2)
-                             + (6 if path_name == "prefill" else 5)) * K,
+            "gpu_launches": launches_per_step(w, path_name) * K,
             "clocks": clocks,
         }
         if ws == 1 and not args.no_cpu_baseline:
