@@ -19,6 +19,10 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
 _LIB = os.path.join(_HERE, "libmoe_oracle.so")
+# A prebuilt oracle library to load instead of building this one: the
+# mutation test points it at copies of moe_oracle.c with planted mistakes to
+# show that the pins catch them.
+_LIB_OVERRIDE = os.environ.get("MOE_ORACLE_LIB")
 _lock = threading.Lock()
 _lib = None
 
@@ -26,6 +30,8 @@ GCC_FLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", 
 
 
 def build(force: bool = False) -> str:
+    if _LIB_OVERRIDE:
+        return _LIB_OVERRIDE
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", *GCC_FLAGS, _SRC, "-o", tmp, "-lm"])
@@ -37,8 +43,7 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB)
+            lib = ctypes.CDLL(build())
             vp, ci = ctypes.c_void_p, ctypes.c_int
             lib.moe_ref_route.argtypes = [vp, vp, ci, ci, ci, ci, ci, vp, vp]
             lib.moe_ref_route.restype = ci
