@@ -83,6 +83,32 @@ MUTANTS = [
     ("mx_negative_zero_dropped",
      "return best | (signbit(v) ? 8 : 0);",
      "return best | (signbit(v) && best != 0 ? 8 : 0);"),
+    ("selects_smallest_logits",
+     "if (best < 0 || l[e] > l[best]) best = e;",
+     "if (best < 0 || l[e] < l[best]) best = e;"),
+    ("shared_weight_ignored",
+     "w[K] = shared_w ? shared_w[t] : 1.0f;",
+     "w[K] = 1.0f;"),
+    ("tile_map_off_by_one",
+     "int64_t row = i * tile_m;",
+     "int64_t row = i > 0 ? i * tile_m - 1 : 0;"),
+    ("inverse_map_shifted",
+     "inv[q] = (int32_t)pos;",
+     "inv[q] = (int32_t)(pos + 1);"),
+    ("padding_not_minus_one",
+     "for (int64_t i = 0; i < cap; ++i) sorted_pairs[i] = -1;",
+     "for (int64_t i = 0; i < cap; ++i) sorted_pairs[i] = 0;"),
+    ("silu_sign",
+     "float moe_ref_silu(float g) { return g / (1.0f + expf(-g)); }",
+     "float moe_ref_silu(float g) { return g / (1.0f + expf(g)); }"),
+    ("routing_weight_not_applied",
+     "s2 + e * s2_e, H, I, h, y);\n"
+     "            for (int m = 0; m < H; ++m) acc[m] += wj * y[m];",
+     "s2 + e * s2_e, H, I, h, y);\n"
+     "            for (int m = 0; m < H; ++m) acc[m] += y[m];"),
+    ("bf16_ties_away_from_zero",
+     "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1u;",
+     "if (rest >= 0x8000u) keep += 1u;"),
     ("mx_swiglu_rounded_before_quantisation",
      "a[n] = moe_ref_silu(g) * u;",
      "a[n] = moe_ref_bf16_to_f32(moe_ref_f32_to_bf16(moe_ref_silu(g) * u));"),
