@@ -1,5 +1,6 @@
-"""Randomised pins of the oracle (CPU only): routing, permutation and MXFP4
-quantisation against the independent brute-force forms in bruteforce.py on
+"""Randomised pins of the oracle (CPU only): routing, permutation, MXFP4
+quantisation and the expert FFN against the independent brute-force forms in
+bruteforce.py on
 shapes and value mixes drawn by hypothesis -- exact ties, -inf logits, empty
 batches, tile heights of 1 and tiles larger than the batch, zero blocks,
 signed zeros, rounding midpoints and exponents across the E8M0 range."""
@@ -98,3 +99,39 @@ def test_quantize_mxfp4_matches_bruteforce(oracle_mod, v):
 @given(st.floats(min_value=-40.0, max_value=40.0, allow_nan=False, width=64))
 def test_e2m1_round_matches_binade_rounding(oracle_mod, x):
     assert oracle_mod.e2m1_round(x) == bf.e2m1_round_binade(x)
+
+
+@st.composite
+def ffn_cases(draw):
+    T = draw(st.integers(1, 4))
+    H = draw(st.sampled_from([32, 64, 96, 128]))
+    I = draw(st.sampled_from([32, 64, 96]))
+    E = draw(st.integers(1, 6))
+    K = draw(st.integers(1, E))
+    shared = draw(st.booleans())
+    rng = np.random.default_rng(draw(st.integers(0, 2**32 - 1)))
+    lo = draw(st.integers(100, 130))
+    Et = E + int(shared)
+    w13 = rng.integers(0, 256, (Et, 2 * I, H // 2), dtype=np.uint8)
+    s13 = rng.integers(lo, lo + 6, (Et, 2 * I, H // 32), dtype=np.uint8)
+    w2 = rng.integers(0, 256, (Et, H, I // 2), dtype=np.uint8)
+    s2 = rng.integers(lo, lo + 6, (Et, H, I // 32), dtype=np.uint8)
+    xf = rng.standard_normal((T, H)).astype(np.float32)
+    x = (xf.view(np.uint32) >> 16).astype(np.uint16)  # bf16 bits (truncated: any bf16 will do)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    return x, w13, s13, w2, s2, logits, K, shared
+
+
+@SETTINGS
+@given(ffn_cases())
+def test_ffn_matches_double_bruteforce(oracle_mod, case):
+    """The per-token fp32 loop against float64 products of the closed-form
+    decode (h rounded to bf16 in both): only fp32 rounding separates them."""
+    x, w13, s13, w2, s2, logits, K, shared = case
+    ids, wt = oracle_mod.route(logits, K, shared)
+    got = bf.bf16_bits_to_f64(oracle_mod.ffn(x, w13, s13, w2, s2, ids, wt))
+    with np.errstate(over="ignore"):  # silu of a large negative g is -0 in both
+        ref = bf.bf16_round(bf.ffn(x, w13, s13, w2, s2, ids, wt))
+    rms = np.sqrt(np.mean(ref**2))
+    assert (np.abs(got - ref) <= 2.0**-6 * np.abs(ref) + 1e-4 * rms).all()
+    assert np.linalg.norm(got - ref) <= 2e-3 * np.linalg.norm(ref)
