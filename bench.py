@@ -235,6 +235,14 @@ def layer_work(w, ids_host, act="bf16"):
                 flops=flops, gate_up_flops=2 * P * 2 * I * H)
 
 
+def workload_config(w, act: str, ws: int) -> dict:
+    """The keys that name the workload, shared by both arms' config."""
+    return {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K,
+            "shared_expert": w.with_shared, "Et": w.Et, "Kt": w.Kt,
+            "activations": "mxfp4 (OCP MX quantisation of x and h)" if act == "mxfp4" else "bf16",
+            "parallelism": f"replicas x{ws} (weak scaling, tokens per GPU fixed)"}
+
+
 def launches_per_step(w, path_name: str) -> int:
     """Kernel launches of one step: route + permute (one fused launch up to
     MOE_ROUTE_PERMUTE_FUSED_MAX_T tokens; else the routing kernel and the
@@ -456,11 +464,8 @@ def run_ours(args, ws, rank, local):
             "dtype": "e2m1" if mx else "f16",
             "data": "synthetic (seeded; random MXFP4 weights, N(0,1) activations and logits)",
             "config": {
-                "workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K,
-                "shared_expert": w.with_shared, "Et": w.Et, "Kt": w.Kt, "tile_m": tm,
-                "path": path_name, "experts_touched": work["touched"],
-                "activations": "mxfp4 (OCP MX quantisation of x and h)" if mx else "bf16",
-                "parallelism": f"replicas x{ws} (weak scaling, tokens per GPU fixed)",
+                **workload_config(w, args.act, ws), "tile_m": tm, "path": path_name,
+                "experts_touched": work["touched"],
                 "l2": f"inputs larger than L2: {work['layer_bytes'] / 1e9:.2f} GB touched per "
                       f"step, {R} weight replicas rotated per step",
             },
@@ -552,8 +557,7 @@ def run_reference(args, ws, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K,
-                   "shared_expert": w.with_shared, "activations": args.act},
+        "config": workload_config(w, args.act, ws),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,

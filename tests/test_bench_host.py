@@ -120,3 +120,25 @@ def test_traffic_lookup_is_keyed_to_the_kernel_source(tmp_path, monkeypatch):
 def test_weak_scaling_value_counts_all_ranks():
     # 64 tokens per rank-step, 30 steps, 4 ranks, slowest rank 15 ms
     assert bench.weak_scaling_value(64, 30, 4, 15.0) == pytest.approx(64 * 30 * 4 / 0.015)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """--impl reference times the CPU oracle and prints one JSON line with the
+    same metric, unit and workload keys as the GPU arm."""
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny16",
+                        "--steps", "2", "--warmup", "1"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["higher_is_better"] is True and d["steps"] == 2 and d["warmup"] == 1
+    assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"] == bench.workload_config(synth.WORKLOADS["tiny16"], "bf16", 1)
