@@ -1,6 +1,6 @@
 """Randomised pins of the oracle (CPU only): routing, permutation, MXFP4
-quantisation and the expert FFN against the independent brute-force forms in
-bruteforce.py on
+quantisation, the expert FFN and the MXFP4-activation layer against the
+independent brute-force forms in bruteforce.py on
 shapes and value mixes drawn by hypothesis -- exact ties, -inf logits, empty
 batches, tile heights of 1 and tiles larger than the batch, zero blocks,
 signed zeros, rounding midpoints and exponents across the E8M0 range."""
@@ -140,3 +140,37 @@ def test_ffn_matches_double_bruteforce(oracle_mod, case):
     rms = np.sqrt(np.mean(ref**2))
     assert (np.abs(got - ref) <= 5e-2 * (np.abs(ref) + rms)).all()
     assert np.linalg.norm(got - ref) <= 1e-2 * np.linalg.norm(ref)
+
+
+@SETTINGS
+@given(ffn_cases())
+def test_ffn_mxfp4act_stage_by_stage(oracle_mod, case):
+    """The MXFP4-activation layer on drawn shapes, stage by stage against
+    float64: x's encoding exactly, the SwiGLU output a to fp32 accuracy, h's
+    encoding exactly when decided on the oracle's own a (as the oracle does),
+    and the output from float64 products of the decoded h."""
+    x, w13, s13, w2, s2, logits, K, shared = case
+    ids, wt = oracle_mod.route(logits, K, shared)
+    out, acc, h = oracle_mod.ffn_mxfp4act(x, w13, s13, w2, s2, ids, wt, want_f32=True, want_h=True)
+    T, H = x.shape
+    I = w13.shape[1] // 2
+    Kt = ids.shape[1]
+    xc, xs = bf.quantize_mxfp4(bf.bf16_bits_to_f64(x))
+    xq = bf.decode_mxfp4(xc, xs)
+    W13 = bf.decode_mxfp4(w13, s13)
+    W2 = bf.decode_mxfp4(w2, s2)
+    ref = np.zeros((T, H))
+    for t in range(T):
+        for j in range(Kt):
+            e, r = ids[t, j], t * Kt + j
+            g = W13[e, :I] @ xq[t]
+            u = W13[e, I:] @ xq[t]
+            with np.errstate(over="ignore"):
+                a64 = g / (1 + np.exp(-g)) * u
+            scale = np.abs(a64).max()
+            assert (np.abs(h["a"][r] - a64) <= 1e-3 * np.abs(a64) + 1e-4 * scale).all()
+            hc, hs = bf.quantize_mxfp4(h["a"][r])
+            np.testing.assert_array_equal(h["codes"][r], hc)
+            np.testing.assert_array_equal(h["scales"][r], hs)
+            ref[t] += wt[t, j] * (W2[e] @ bf.decode_mxfp4(hc, hs))
+    np.testing.assert_allclose(acc, ref, rtol=1e-4, atol=1e-5 * np.abs(ref).max())
