@@ -28,8 +28,12 @@
  *
  * Conventions for every call:
  *   - Every pointer is a caller-owned DEVICE pointer (cudaMalloc or
- *     equivalent) unless stated.  The library allocates nothing, keeps no
- *     state between calls and never synchronises the host with the device.
+ *     equivalent) unless stated.  No call allocates memory or synchronises
+ *     the host with the device.  The library's only state is: two device
+ *     error words per kernel file (read and cleared by moe_device_error),
+ *     the fixed scratch array of moe_ffn_noalloc, and host-side caches (the
+ *     per-device SM count and per-kernel shared-memory limits, the scratch
+ *     address per CUDA context).  Results never depend on that state.
  *   - Work is enqueued on `stream` (0 = legacy default stream).  Calls are
  *     asynchronous; read outputs only after the stream has completed.
  *   - Arguments and shapes are checked on the host before any launch.  A
@@ -136,7 +140,10 @@ size_t moe_permute_max_tiles(int T, int Kt, int Et, int tile_m);
  * Limits: 1 <= Kt <= 33, 1 <= Et <= 1025, 1 <= tile_m <= 256, cap < 2^31.
  * Output is bit-exact (a deterministic function of topk_ids).  Ids outside
  * [0, Et) are a precondition violation: such pairs are dropped and their
- * inv_pairs entry is -1.  One CTA does the whole sort.
+ * inv_pairs entry is -1.  Small batches sort in one CTA; batches of at least
+ * 8192 pairs with at least 8 pairs per expert use a four-launch multi-block
+ * version of the same stable sort (count, scan, scatter, inverse map), with
+ * identical output.
  */
 moe_status_t moe_permute(const int32_t* topk_ids, int T, int Kt, int Et, int tile_m,
                          int32_t* sorted_pairs, int32_t* expert_offsets, int32_t* inv_pairs,
@@ -196,9 +203,9 @@ size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
  * path stores each weight row in f16 relative to its largest scale, exact
  * for every group whose scale is within 2^36 of that largest (groups further
  * below are rounded, at most 2^-37 of the row's largest weight).
- * Limits: H % 32 == 0, I % 32 == 0, H, I <= 65536, tile_m % 8 == 0 and
- * tile_m <= 64 for the decode path; the prefill path needs tile_m in
- * {32, 64, 128}.  Pointers 16-byte aligned.
+ * Limits: H % 32 == 0, I % 32 == 0, H, I <= 65536; the decode path needs
+ * tile_m in {8, 16, 32, 64}, the prefill path tile_m in {32, 64, 128, 256}.
+ * Pointers 16-byte aligned.
  */
 moe_status_t moe_ffn(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,
                      const uint8_t* s2, const float* topk_w, const int32_t* sorted_pairs,
@@ -328,6 +335,23 @@ moe_status_t moe_device_error(int* flag, int clear);
 moe_status_t moe_selftest_wait_timeout(int limit_us, cudaStream_t stream);
 
 /*
+ * moe_selftest_wait_split -- diagnostic: one block of two warps whose bounded
+ * waits end differently.  Warp 0 waits on an mbarrier nothing arrives at
+ * (limit_us microseconds, 1..10^6), warp 1 on one that has already
+ * completed.  Each warp makes its outcome uniform across its lanes, the two
+ * warps reduce it with AND at a named barrier, and they meet at that barrier
+ * again only if both succeeded -- the pattern the GEMM epilogues use before
+ * their own named barriers, so a failure seen by one warp cannot leave
+ * another waiting there without a limit.
+ *   outcome  device int32 [2], 4-byte aligned: written with the outcome each
+ *            warp acted on (0 = stopped; both are 0 after a correct run).
+ * Raises device error bit 1 (moe_device_error) like moe_selftest_wait_timeout.
+ * MOE_ERR_INVALID_ARG for a limit outside 1..10^6 or a null/misaligned
+ * outcome.  The pages have no counterpart.
+ */
+moe_status_t moe_selftest_wait_split(int limit_us, int32_t* outcome, cudaStream_t stream);
+
+/*
  * moe_ffn_noalloc -- moe_ffn for callers that cannot allocate device memory
  * (no cudaMalloc allowed where they run: inside a stream capture that must
  * not allocate, or in a runtime or plugin that only owns fixed, pre-assigned
@@ -335,7 +359,7 @@ moe_status_t moe_selftest_wait_timeout(int limit_us, cudaStream_t stream);
  * convenience.
  *
  * Same arguments, results and limits as moe_ffn, minus the workspace: the
- * scratch (the bf16 SwiGLU intermediate and the fp32 per-pair outputs) lives
+ * scratch (the whole moe_ffn workspace, moe_ffn_workspace_size() bytes) lives
  * in a fixed device array of MOE_NOALLOC_SCRATCH_BYTES inside the library,
  * which every GPU that loads libmoe holds until the process exits.  The call
  * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
@@ -343,8 +367,11 @@ moe_status_t moe_selftest_wait_timeout(int limit_us, cudaStream_t stream);
  *     are rejected with MOE_ERR_UNSUPPORTED_SHAPE before any launch (the
  *     64-token decode step of a 4096/1024, 513-expert, top-10+1 layer needs
  *     about 20 MiB with tile_m = 8).
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *   - The first call in each CUDA context looks up the array's device
+ *     address there (cudaGetSymbolAddress) and caches it under the context's
+ *     ID (cuCtxGetId, never reused within a process), so a context created
+ *     again after cudaDeviceReset, or a caller's own non-primary context,
+ *     gets its own lookup.  Make the first call in a context before any
  *     stream capture.
  *   - Every call on a device shares the one array, and it keeps the last
  *     call's contents.  Nothing in it needs to start at zero.  Calls whose

@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int c = 0; c < nchunks; ++c, ++gc) {
                 const int b = gc & 1;
-                if (gc >= 2 && !mbar_wait(&xempty[b], ((gc >> 1) - 1) & 1)) return;
+                if (gc >= 2 && !mbar_wait_warp(&xempty[b], ((gc >> 1) - 1) & 1)) return;
                 const int kc = c * KC;
                 const uint32_t bytes = (uint32_t)min(KC, K - kc) * 2u;
                 if (lane == 0) mbar_arrive_expect_tx(&xfull[b], valid * bytes);
@@ -259,12 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kst = st * kStageK;
             if (kst % KC == 0) {  // first stage of a staged chunk
                 xbuf = (gc & 1) * L::kXBuf;
-                if (!failed && !mbar_wait(&xfull[gc & 1], (gc >> 1) & 1)) failed = true;
+                if (!failed && !mbar_wait_warp(&xfull[gc & 1], (gc >> 1) & 1)) failed = true;
             }
             const int s = gs % kStages;
             const uint2 sc0 = nsc0, sc1 = nsc1;
             if (st + 1 < nsteps) load_scales(st + 1, nsc0, nsc1);
-            if (!failed && !mbar_wait(&full[s], (gs / kStages) & 1)) failed = true;
+            if (!failed && !mbar_wait_warp(&full[s], (gs / kStages) & 1)) failed = true;
             if (!failed) {
                 const uint32_t soff = s * kStageBytes;
                 const uint32_t xoff = xbuf + (uint32_t)(kst % KC) * 2u;  // bytes into the staged rows
@@ -485,6 +485,37 @@ static __global__ void wait_selftest_kernel(unsigned long long limit_ns) {
 
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s) {
     return launch_pdl(wait_selftest_kernel, dim3(1), dim3(32), 0, s, limit_ns);
+}
+
+// Two warps whose waits end differently: warp 0 waits on a barrier nothing
+// arrives at (gives up after limit_ns), warp 1 on one whose phase has already
+// completed.  Each warp makes its outcome uniform, the two reduce it at named
+// barrier 1, and only if both succeeded do they meet there again -- the
+// pattern of the GEMM epilogues, whose warps meet at a named barrier after
+// their accumulator wait.  outcome[w] = the outcome warp w acted on (0: both
+// stop; warp 1 is not left waiting at the barrier for warp 0).
+static __global__ void wait_split_selftest_kernel(unsigned long long limit_ns, int32_t* outcome) {
+    pdl_begin();
+    __shared__ uint64_t bar[2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive(&bar[1]);  // phase 0 of bar[1] completes
+    }
+    __syncthreads();
+    bool ok = mbar_wait_for(&bar[warp], 0, warp == 0 ? limit_ns : kWaitLimitNs);
+    ok = __all_sync(0xFFFFFFFFu, ok) != 0;
+    ok = all_at_barrier(ok, 1, 64);
+    if (ok) asm volatile("bar.sync 1, 64;" ::: "memory");
+    if (lane == 0) outcome[warp] = ok ? 1 : 0;
+    pdl_end();
+}
+
+cudaError_t launch_wait_split_selftest(unsigned long long limit_ns, int32_t* outcome,
+                                       cudaStream_t s) {
+    return launch_pdl(wait_split_selftest_kernel, dim3(1), dim3(64), 0, s, limit_ns, outcome);
 }
 
 cudaError_t read_device_error_decode(int* flag, int clear) {

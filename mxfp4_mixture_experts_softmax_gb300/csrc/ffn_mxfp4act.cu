@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (sf_tma) {
                     // the pair's slot is filled once the producer saw the MMAs
                     // that last read these tensor-memory columns complete
-                    if (!mbar_wait(&tma_full[pr], (gs / kStages) & 1)) {
+                    if (!mbar_wait_warp(&tma_full[pr], (gs / kStages) & 1)) {
                         ok = false;
                         break;
                     }
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             ? __ldg(reinterpret_cast<const uint32_t*>(sb[j] + grp))
                                             : 0u;
                     }
-                    if (gs >= kStages && !mbar_wait(&stage_free[pr], ((gs / kStages) - 1) & 1)) {
+                    if (gs >= kStages && !mbar_wait_warp(&stage_free[pr], ((gs / kStages) - 1) & 1)) {
                         ok = false;
                         break;
                     }
@@ -475,7 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < kNJ; ++u) nvalid += __popc(__ballot_sync(0xFFFFFFFFu, qn[u] >= 0));
             }
-            if (!mbar_wait(&acc_full[b], (it / kAccBufs) & 1)) break;
+            // one outcome for the warp, and in gate_up for all four epilogue
+            // warps, which meet at named barrier 1 below: none may go on to
+            // that barrier while another stopped
+            bool acc_ok = mbar_wait_warp(&acc_full[b], (it / kAccBufs) & 1);
+            if (MODE == 0) acc_ok = all_at_barrier(acc_ok, 1, kEpiThreads);
+            if (!acc_ok) break;
             tc_fence_after();
             load_pairs(item + gridDim.x);
 #pragma unroll 1

@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // both slots of a pair come free with the pair's commit
                 if (gs >= kStages && (gs & 1) == 0 &&
-                    !mbar_wait(&stage_free[(gs >> 1) % kPairs], ((gs / kStages) - 1) & 1)) {
+                    !mbar_wait_warp(&stage_free[(gs >> 1) % kPairs], ((gs / kStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -387,14 +387,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m0[j] = f16_group_mult(scale_at(j, 2 * st), s_ref[j]);
                     m1[j] = f16_group_mult(scale_at(j, 2 * st + 1), s_ref[j]);
                 }
-                if (!mbar_wait(&raw_full[s], (gs / kStages) & 1)) {
+                if (!mbar_wait_warp(&raw_full[s], (gs / kStages) & 1)) {
                     ok = false;
                     break;
                 }
                 // the A slot comes free with the MMAs of stage gs - kAStages (with
                 // equal rings the TMA barrier already implies it)
                 if (kDecoupled && gs >= (uint32_t)kAStages &&
-                    !mbar_wait(&a_free[(gs >> 1) % kAPairs], ((gs / kAStages) - 1) & 1)) {
+                    !mbar_wait_warp(&a_free[(gs >> 1) % kAPairs], ((gs / kAStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < kQ; ++u) nvalid += __popc(__ballot_sync(0xFFFFFFFFu, qv[u] >= 0));
             }
-            if (!mbar_wait(&acc_full[b], (it / kAccBufs) & 1)) break;
+            if (!mbar_wait_warp(&acc_full[b], (it / kAccBufs) & 1)) break;
             tc_fence_after();
             load_item(item + gridDim.x);
             // 32 columns per round trip: two loads, one wait; block by block

@@ -150,6 +150,13 @@ moe_status_t moe_selftest_wait_timeout(int limit_us, cudaStream_t stream) {
     return cuda_status(launch_wait_selftest((unsigned long long)limit_us * 1000ull, stream));
 }
 
+moe_status_t moe_selftest_wait_split(int limit_us, int32_t* outcome, cudaStream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000 || !outcome || !aligned(outcome, 4))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_status(
+        launch_wait_split_selftest((unsigned long long)limit_us * 1000ull, outcome, stream));
+}
+
 static moe_status_t check_route(const float* logits, const float* shared_w, int T, int E, int K,
                                 int with_shared, const int32_t* topk_ids, const float* topk_w) {
     if (T < 0 || E < 1 || K < 1) return MOE_ERR_INVALID_ARG;

@@ -109,6 +109,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
+// A bounded wait whose outcome is the same on every lane of the warp: if one
+// lane gave up, all of them do.  A wait's result is otherwise taken per
+// thread, and a lane that stopped while the others went on would leave them
+// in a warp-collective instruction (a shuffle, tcgen05.ld / st, ldmatrix,
+// mma.sync) that it never reaches.  All 32 lanes must call it.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xFFFFFFFFu, ok) != 0;
+}
+
+// `ok` reduced with AND over the `nthreads` threads (whole warps) that meet
+// at named barrier `id`; every one of them must call it.  Threads that then
+// synchronise at that barrier again act on the same outcome, so none is left
+// waiting there for threads that stopped.
+__device__ __forceinline__ bool all_at_barrier(bool ok, int id, int nthreads) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // Prefetch one 2D box of a tensor map into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int c0, int c1) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap),

@@ -123,6 +123,10 @@ cudaError_t launch_prefill_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t read_device_error_prefill(int* flag, int clear);
 // one block waiting on a barrier that never completes, for limit_ns
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
+// two warps, one wait giving up and one completing; outcome[2] (device) gets
+// the outcome each warp acted on
+cudaError_t launch_wait_split_selftest(unsigned long long limit_ns, int32_t* outcome,
+                                       cudaStream_t s);
 cudaError_t read_device_error_decode(int* flag, int clear);
 // out = bf16(sum of the Kt slot rows of y, then + y2's row when y2 is not null)
 cudaError_t launch_combine(const float* y, const float* y2, int T, int H, int Kt, uint16_t* out,

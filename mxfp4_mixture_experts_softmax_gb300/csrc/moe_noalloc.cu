@@ -3,10 +3,10 @@
 // Some callers cannot call cudaMalloc at the point where they run the layer:
 // code running under a CUDA stream capture that must not allocate, runtimes
 // that hand out only fixed, pre-registered device memory, or plugins that do
-// not own an allocator.  For them moe_ffn_noalloc runs the same three FFN
-// kernels as moe_ffn with its workspace (the bf16 SwiGLU intermediate and the
-// fp32 per-pair outputs) in the fixed device array below instead of a
-// caller-provided buffer.  Inputs and outputs are still the caller's.
+// not own an allocator.  For them moe_ffn_noalloc runs the same FFN kernels
+// as moe_ffn with the whole moe_ffn workspace (moe_ffn_workspace_size bytes)
+// in the fixed device array below instead of a caller-provided buffer.
+// Inputs and outputs are still the caller's.
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -18,27 +18,70 @@ namespace {
 // until the process exits.
 __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device.  The host-side
-// name g_noalloc_scratch is only a stand-in for the symbol; the address a
-// kernel may use is looked up once per device (the first call on a device
-// does this set-up) and cached.
-cudaError_t scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+template <typename Fn>
+Fn driver_fn(const char* name) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+
+// A __device__ array has one address per CUDA context (the module is loaded
+// into each context), so the cache is keyed by the current context's ID,
+// which the driver never reuses within a process: a context destroyed and
+// created again (cudaDeviceReset) or a caller's own non-primary context gets
+// its own lookup.
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void* addr;
+};
+constexpr int kMaxContexts = 64;
+std::mutex g_scratch_mu;
+ScratchEntry g_scratch_cache[kMaxContexts] = {};
+int g_scratch_next = 0;
+
+cudaError_t current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (!get_current || !get_id) return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorContextIsDestroyed;
+    if (!ctx) {
+        // no context bound to this thread yet: the runtime binds the current
+        // device's primary context on its first call that needs one
         void* p = nullptr;
-        err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (err != cudaSuccess) return err;
-        g_scratch_addr[dev] = p;
+        if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorContextIsDestroyed;
     }
-    *out = g_scratch_addr[dev];
+    return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorContextIsDestroyed;
+}
+
+// Device address of the scratch array in the current context.  The host-side
+// name g_noalloc_scratch is only a stand-in for the symbol; the address a
+// kernel may use is looked up by the first call in each context (with that
+// context current) and cached.
+cudaError_t scratch_address(void** out) {
+    unsigned long long id = 0;
+    cudaError_t err = current_context_id(&id);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    for (const ScratchEntry& e : g_scratch_cache)
+        if (e.addr && e.ctx_id == id) {
+            *out = e.addr;
+            return cudaSuccess;
+        }
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (err != cudaSuccess) return err;
+    g_scratch_cache[g_scratch_next] = ScratchEntry{id, p};
+    g_scratch_next = (g_scratch_next + 1) % kMaxContexts;
+    *out = p;
     return cudaSuccess;
 }
 

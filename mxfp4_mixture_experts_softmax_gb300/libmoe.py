@@ -30,7 +30,7 @@ EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_route_ex", "moe
            "moe_ffn_path", "moe_ffn_auto_path", "moe_ffn_gate_up", "moe_ffn_down", "moe_combine",
            "moe_ffn_y_offset", "moe_device_error", "moe_ffn_noalloc", "moe_combine_ex",
            "moe_ffn_dense_shared_workspace_size", "moe_ffn_dense_shared",
-           "moe_selftest_wait_timeout", "moe_quantize_mxfp4", "moe_ffn_mxfp4act_workspace_size",
+           "moe_selftest_wait_timeout", "moe_selftest_wait_split", "moe_quantize_mxfp4", "moe_ffn_mxfp4act_workspace_size",
            "moe_ffn_mxfp4act", "moe_ffn_mxfp4act_gate_up", "moe_ffn_mxfp4act_down",
            "moe_ffn_mxfp4act_h_offsets", "moe_ffn_down_combine")
 
@@ -108,6 +108,8 @@ def load(build: bool = True):
         L.moe_ffn_dense_shared.restype = ci
         L.moe_selftest_wait_timeout.argtypes = [ci, vp]
         L.moe_selftest_wait_timeout.restype = ci
+        L.moe_selftest_wait_split.argtypes = [ci, vp, vp]
+        L.moe_selftest_wait_split.restype = ci
         L.moe_ffn_down_combine.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp,
                                            sz, ci, vp]
         L.moe_ffn_down_combine.restype = ci
@@ -289,6 +291,17 @@ def moe_selftest_wait_timeout(limit_us: int = 2000, stream=None):
     """Diagnostic: a bounded wait that runs out (include/moe.h)."""
     _check(load().moe_selftest_wait_timeout(int(limit_us), _stream(stream)),
            "moe_selftest_wait_timeout")
+
+
+def moe_selftest_wait_split(limit_us: int = 2000, stream=None):
+    """Diagnostic: two warps whose bounded waits end differently must stop
+    together (include/moe.h).  Returns the device tensor of the two warps'
+    outcomes (int32 [2]; 0 = stopped)."""
+    import torch
+    out = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    _check(load().moe_selftest_wait_split(int(limit_us), _ptr(out), _stream(stream)),
+           "moe_selftest_wait_split")
+    return out
 
 
 def moe_ffn_noalloc(x, w13, s13, w2, s2, topk_w, perm: dict, out=None, stream=None):

@@ -58,10 +58,26 @@ def test_wait_timeout_raises_flag_and_context_survives():
     assert libmoe.moe_device_error(clear=True) == 0
 
 
+def test_split_wait_outcomes_stop_both_warps():
+    """One warp's wait runs out while the other's completes: both act on the
+    failed outcome (neither is left at the named barrier that follows), the
+    kernel returns, the flag is raised and the context stays usable."""
+    assert libmoe.moe_device_error(clear=True) in (0, 1, 2, 3)
+    outcome = libmoe.moe_selftest_wait_split(2000)
+    torch.cuda.synchronize()
+    assert outcome.cpu().tolist() == [0, 0]
+    assert libmoe.moe_device_error(clear=True) == 1
+    w, d, ids, wt, ref = _case()
+    gc.ffn_parity(_run(w, d, ids, wt, 32, libmoe.MOE_PATH_PREFILL), ref, "after the split wait")
+    assert libmoe.moe_device_error(clear=True) == 0
+
+
 def test_selftest_rejects_bad_limits():
     for bad in (0, -5, 2_000_000):
         with pytest.raises(libmoe.MoeError):
             libmoe.moe_selftest_wait_timeout(bad)
+        with pytest.raises(libmoe.MoeError):
+            libmoe.moe_selftest_wait_split(bad)
 
 
 def _bad_expert(perm):
