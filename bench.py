@@ -4,8 +4,16 @@
 One step = one pass of the whole layer over one batch of the workload's
 tokens, every kernel from libmoe.  Prints ONE JSON line on rank 0.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode64]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload skewed_prefill8192]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+The headline workload (default: the 8192-token skewed prefill, the largest
+single-GPU configuration) is timed over exactly K steps.  On rank 0 the line
+also carries `per_config`: every other full-size workload (the 64-token
+decode step, the 288-token MTP verify step, the 1536-token prefill chunk and
+the calibrated skewed prefill) and the headline workload again, each timed
+over a region of at least --config-seconds with its own clock record and
+binding roofline.
 
 Under torchrun every rank runs its own replica of the layer on its own batch
 (the layer is data parallel over tokens; no collective on the data path);
@@ -28,6 +36,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MXFP4 MoE layer tokens/s; % of HBM roofline (decode) / tensor peak (prefill)"
+DEFAULT_WORKLOAD = "skewed_prefill8192"
+# the full-size workloads; each is timed in per_config
+PER_CONFIG = ("decode64", "mtp_verify288", "prefill1536", "skewed_prefill8192",
+              "skewed_prefill8192_cal")
+# bf16 layer: the tile height each full-size workload runs with (decode path
+# with 8-row tiles while most experts see a few rows; prefill path above)
+BENCH_TILE_M = {"decode64": 8, "mtp_verify288": 8, "prefill1536": 64,
+                "skewed_prefill8192": 128, "skewed_prefill8192_cal": 128}
+CLOCK_PERIOD_MS = 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -38,10 +55,10 @@ def parse_args():
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="decode64")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--tile-m", type=int, default=0,
-                   help="rows per expert tile (default: 8 for bf16; for mxfp4 by the mean rows "
-                        "per expert: 32 below 16, 64 below 64, else 128)")
+                   help="rows per expert tile (default: bf16 by BENCH_TILE_M, else 8; mxfp4 by "
+                        "the mean rows per expert: 32 below 16, 64 below 64, else 128)")
     p.add_argument("--E", type=int, default=0,
                    help="routed experts override (smaller cases for profiler captures)")
     p.add_argument("--path", default="auto", choices=["auto", "decode", "prefill"])
@@ -53,6 +70,9 @@ def parse_args():
     p.add_argument("--act", default="bf16", choices=["bf16", "mxfp4"],
                    help="activations: bf16 (the layer as specified) or MXFP4-quantised "
                         "(moe_ffn_mxfp4act, block-scaled MXFP4 x MXFP4 GEMMs)")
+    p.add_argument("--config-seconds", type=float, default=2.0,
+                   help="minimum timed region of each per_config entry")
+    p.add_argument("--no-per-config", action="store_true")
     return p.parse_args()
 
 
@@ -148,7 +168,7 @@ def traffic_from_profiles(kernel: str, workload: str, src_file: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every CLOCK_PERIOD_MS."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -159,7 +179,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(CLOCK_PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -167,7 +187,7 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(2 * CLOCK_PERIOD_MS / 1e3)
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
@@ -211,26 +231,25 @@ def gpu_id_for(device_index: int) -> str:
 # ------------------------------------------------------- algorithmic work
 
 def layer_work(w, ids_host, act="bf16"):
-    """Algorithmic HBM bytes and flops of one step, from the actual routing.
-    The down step includes the combine (y written and read back, out
-    written); act="mxfp4": x and h move as MXFP4 (codes + scales).  The layer
-    counts weights, x, out, h and logits."""
+    """Algorithmic HBM bytes and flops of one step, from the actual routing
+    (the per-unit figures of the layer: each touched expert's packed weights
+    once, x read, h written once and read once, out written, logits read).
+      gate_up step: W13 of the touched experts + x read + h write
+      down step:    W2 of the touched experts + h read + out write
+    Intermediate buffers an implementation adds (f16 copies of rows, the
+    per-pair fp32 outputs before the combine) are not algorithmic and are not
+    counted.  act="mxfp4": h moves as MXFP4 (codes + scales)."""
     import numpy as np
     from mxfp4_mixture_experts_softmax_gb300 import synth
     touched = int(np.unique(ids_host).size)
     H, I, T, P = w.H, w.I, w.T, w.pairs
     w13_b = 2 * I * (H // 2 + H // 32)
     w2_b = H * (I // 2 + I // 32)
-    gate_up = touched * w13_b + T * H * 2 + P * I * 2          # weights + x + h write
-    down = touched * w2_b + P * I * 2 + 2 * P * H * 4 + T * H * 2   # + h read, y out and back, out
-    layer = (touched * synth.weight_bytes_per_expert(w) + T * H * 4 + P * I * 4
-             + T * w.E * 4)                                     # + x, out, h, logits
+    hb = I // 2 + I // 32 if act == "mxfp4" else 2 * I   # bytes of one h row
+    gate_up = touched * w13_b + T * H * 2 + P * hb
+    down = touched * w2_b + P * hb + T * H * 2
+    layer = touched * synth.weight_bytes_per_expert(w) + T * H * 4 + 2 * P * hb + T * w.E * 4
     flops = 2 * P * (2 * I * H + H * I)
-    if act == "mxfp4":
-        xq, hq = H // 2 + H // 32, I // 2 + I // 32       # MXFP4 bytes per row
-        gate_up = touched * w13_b + T * H * 2 + T * xq + 2 * P * xq + P * hq
-        down = touched * w2_b + P * hq + 2 * P * H * 4 + T * H * 2
-        layer = touched * synth.weight_bytes_per_expert(w) + T * H * 4 + 2 * P * hq + T * w.E * 4
     return dict(touched=touched, gate_up_bytes=gate_up, down_bytes=down, layer_bytes=layer,
                 flops=flops, gate_up_flops=2 * P * 2 * I * H)
 
@@ -281,10 +300,229 @@ def weak_scaling_value(tokens_per_rank_step: int, steps: int, world: int, max_ms
 
 # ------------------------------------------------------------ our arm
 
-def run_ours(args, ws, rank, local):
-    import numpy as np
+def default_tile_m(w, act: str) -> int:
+    if act == "bf16":
+        return BENCH_TILE_M.get(w.name, 8)
+    rows = w.T * w.Kt / w.Et
+    return 32 if rows < 16 else 64 if rows < 64 else 128
+
+
+class Layer:
+    """One workload resident on the device: R weight / input replicas rotated
+    per step (the touched weights of one step are far larger than L2, and a
+    step never finds the previous step's weights there), the routing and
+    workspace buffers, and the step itself."""
+
+    def __init__(self, w, act: str, tm: int, path_arg: str, replicas: int, dev):
+        import numpy as np
+        import torch
+        from mxfp4_mixture_experts_softmax_gb300 import libmoe, synth
+        self.w, self.act, self.tm, self.dev = w, act, tm, dev
+        self.mx = act == "mxfp4"
+        self.path = {"auto": libmoe.MOE_PATH_AUTO, "decode": libmoe.MOE_PATH_DECODE,
+                     "prefill": libmoe.MOE_PATH_PREFILL}[path_arg]
+        if self.mx:
+            self.path_name = "mxfp4act"
+        elif path_arg == "prefill" or (path_arg == "auto" and libmoe.moe_ffn_auto_path(
+                w.T, w.Kt, w.Et, tm) == libmoe.MOE_PATH_PREFILL):
+            self.path_name = "prefill"
+        else:
+            self.path_name = "decode"
+        self.host = synth.make_inputs(w)
+
+        def up(a):
+            t = torch.from_numpy(np.ascontiguousarray(a))
+            if a.dtype == np.uint16:
+                t = t.view(torch.int16).view(torch.bfloat16)
+            return t.to(dev)
+
+        self.R = max(1, replicas)
+        self.weights = [{k: up(self.host[k]) for k in ("w13", "s13", "w2", "s2")}]
+        for _ in range(self.R - 1):
+            self.weights.append({k: v.clone() for k, v in self.weights[0].items()})
+        self.logits = [up(self.host["logits"]) for _ in range(self.R)]
+        self.xs = [up(self.host["x"]) for _ in range(self.R)]
+        self.bufs = libmoe.alloc_layer(w.T, w.E, w.K, w.with_shared, w.H, w.I, w.Et, tm, dev)
+        if self.mx:  # the MXFP4-activation workspace replaces the bf16 one
+            self.bufs["workspace"] = libmoe.alloc_workspace_mxfp4act(w.T, w.H, w.I, w.Et, w.Kt,
+                                                                     tm, dev)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def step(self, i, ev=None, gemm_ev=None):
+        """One pass of the layer.  ev: events between all calls (breakdown);
+        gemm_ev: events only around the two GEMM steps, so the programmatic
+        launches still overlap at the other kernel boundaries."""
+        from mxfp4_mixture_experts_softmax_gb300 import libmoe
+        w, b, r = self.w, self.bufs, i % self.R
+        W = self.weights[r]
+        if ev is not None:
+            ev[0].record(self.stream)
+        # routing + permutation: one launch up to MOE_ROUTE_PERMUTE_FUSED_MAX_T tokens
+        _, tw, perm = libmoe.moe_route_permute(self.logits[r], w.K, self.tm, w.with_shared,
+                                               w.renormalize, b["topk_ids"], b["topk_w"],
+                                               b["perm"])
+        if ev is not None:
+            ev[1].record(self.stream)
+        if gemm_ev is not None:
+            gemm_ev[0].record(self.stream)
+        if self.mx:
+            libmoe.moe_ffn_mxfp4act_gate_up(self.xs[r], W["w13"], W["s13"], perm, b["workspace"])
+        else:
+            libmoe.moe_ffn_gate_up(self.xs[r], W["w13"], W["s13"], perm, b["workspace"],
+                                   self.path)
+        if ev is not None:
+            ev[2].record(self.stream)
+        if gemm_ev is not None:
+            gemm_ev[1].record(self.stream)
+        if self.mx:  # down GEMM and the combine into out
+            libmoe.moe_ffn_mxfp4act_down(W["w2"], W["s2"], tw, perm, b["workspace"], w.T, b["out"])
+        else:
+            libmoe.moe_ffn_down_combine(W["w2"], W["s2"], tw, perm, b["workspace"], w.T, b["out"],
+                                        self.path)
+        if ev is not None:
+            ev[3].record(self.stream)
+        if gemm_ev is not None:
+            gemm_ev[2].record(self.stream)
+
+    def timed(self, steps: int, gpu_index: int, ws: int = 1):
+        """Exactly `steps` steps between two events, barrier + synchronize on
+        both sides, clocks sampled during the region; returns the region's
+        milliseconds, the mean GEMM-step times and the clock record."""
+        import torch
+        dev = self.dev
+        gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler = ClockSampler(gpu_id_for(gpu_index))
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        t0.record(self.stream)
+        for i in range(steps):
+            self.step(i, gemm_ev=gevs[i])
+        t1.record(self.stream)
+        torch.cuda.synchronize(dev)
+        if ws > 1:
+            torch.distributed.barrier()
+        clocks = sampler.stop()
+        gemm = {"gate_up": statistics.mean(g[0].elapsed_time(g[1]) for g in gevs),
+                "down": statistics.mean(g[1].elapsed_time(g[2]) for g in gevs)}
+        return t0.elapsed_time(t1), gemm, clocks
+
+    def breakdown(self, n: int = 10) -> dict:
+        """Per-call times (events between every call; after the timed region)."""
+        import torch
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+        for i in range(n):
+            self.step(i, ev=evs[i])
+        torch.cuda.synchronize(self.dev)
+        names = ["route_permute", "gate_up", "down_combine"]
+        return {nm: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
+                for j, nm in enumerate(names)}
+
+    def e2e(self, steps: int, warmup: int) -> float:
+        """The layer through the public API with host buffers: per step H2D of
+        logits + x from pinned host memory and D2H of the output; returns ms."""
+        import torch
+        from mxfp4_mixture_experts_softmax_gb300 import libmoe
+        w, b = self.w, self.bufs
+        pin_logits = torch.from_numpy(self.host["logits"]).pin_memory()
+        pin_x = torch.from_numpy(self.host["x"]).view(torch.int16).view(torch.bfloat16).pin_memory()
+        pin_out = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+        W = self.weights[0]
+
+        def one():
+            self.logits[0].copy_(pin_logits, non_blocking=True)
+            self.xs[0].copy_(pin_x, non_blocking=True)
+            if self.mx:
+                _, tw, perm = libmoe.moe_route_permute(self.logits[0], w.K, self.tm, w.with_shared,
+                                                       w.renormalize, b["topk_ids"], b["topk_w"],
+                                                       b["perm"])
+                libmoe.moe_ffn_mxfp4act(self.xs[0], W["w13"], W["s13"], W["w2"], W["s2"], tw, perm,
+                                        b["out"], b["workspace"])
+            else:
+                libmoe.moe_layer(self.logits[0], self.xs[0], W["w13"], W["s13"], W["w2"], W["s2"],
+                                 w.K, w.with_shared, w.renormalize, tile_m=self.tm, path=self.path,
+                                 bufs=b)
+            pin_out.copy_(b["out"], non_blocking=True)
+
+        for _ in range(max(3, warmup)):
+            one()
+        torch.cuda.synchronize(self.dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for _ in range(steps):
+            one()
+        e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return e0.elapsed_time(e1)
+
+    def check_output(self):
+        import numpy as np
+        if not np.isfinite(self.bufs["out"].float().cpu().numpy()).all():
+            raise RuntimeError(f"non-finite layer output on {self.w.name}")
+
+    def rooflines(self, work, gemm_ms: dict, total_ms: float, steps: int):
+        """gate_up, down + combine and the whole step against their binding roofline."""
+        src = {"prefill": "ffn_prefill.cu", "decode": "ffn_decode.cu",
+               "mxfp4act": "ffn_mxfp4act.cu"}[self.path_name]
+        traffic, traffic_src = traffic_from_profiles(
+            f"{self.path_name}_gate_up", self.w.name,
+            os.path.join(ROOT, "mxfp4_mixture_experts_softmax_gb300", "csrc", src))
+        gu = roofline_entry(f"{self.path_name}_gate_up", work["gate_up_bytes"],
+                            work["gate_up_flops"], gemm_ms["gate_up"] / 1e3, traffic, traffic_src,
+                            fp4=self.mx)
+        dn = roofline_entry(f"{self.path_name}_down_combine", work["down_bytes"],
+                            work["flops"] - work["gate_up_flops"], gemm_ms["down"] / 1e3, None,
+                            None, fp4=self.mx)
+        layer = roofline_entry("layer", work["layer_bytes"], work["flops"], total_ms / steps / 1e3,
+                               None, None, fp4=self.mx)
+        return gu, dn, layer
+
+    def free(self):
+        import torch
+        self.weights = self.logits = self.xs = self.bufs = self.host = None
+        torch.cuda.empty_cache()
+
+
+def config_entry(lay, total_ms, steps, gemm, clocks, per, work):
+    gu, dn, layer = lay.rooflines(work, gemm, total_ms, steps)
+    return {"workload": lay.w.name, "T": lay.w.T, "tile_m": lay.tm, "path": lay.path_name,
+            "steps": steps, "timed_s": total_ms / 1e3, "ms_per_step": total_ms / steps,
+            "tokens_per_s": lay.w.T * steps / (total_ms / 1e3),
+            "experts_touched": work["touched"], "roofline": layer,
+            "gate_up": gu, "down_combine": dn,
+            "kernels_us": {n: v * 1e3 for n, v in {**per, **gemm}.items()}, "clocks": clocks}
+
+
+def measure_per_config(args, local, dev, skip=()):
+    """Every full-size workload, each timed over at least --config-seconds."""
     import torch
-    from mxfp4_mixture_experts_softmax_gb300 import libmoe, synth
+    from mxfp4_mixture_experts_softmax_gb300 import synth
+    out = {}
+    for name in PER_CONFIG:
+        if name in skip:
+            continue
+        w = synth.WORKLOADS[name]
+        lay = Layer(w, args.act, default_tile_m(w, args.act), "auto", args.replicas, dev)
+        for i in range(3):
+            lay.step(i)
+        torch.cuda.synchronize(dev)
+        ms, _, _ = lay.timed(5, local)
+        steps = int(min(20000, max(20, -(-args.config_seconds * 1e3 // (ms / 5)))))
+        ids_host = lay.bufs["topk_ids"].cpu().numpy()
+        work = layer_work(w, ids_host, args.act)
+        total_ms, gemm, clocks = lay.timed(steps, local)
+        per = lay.breakdown()
+        lay.check_output()
+        out[name] = config_entry(lay, total_ms, steps, gemm, clocks, per, work)
+        lay.free()
+        del lay
+    return out
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    from mxfp4_mixture_experts_softmax_gb300 import synth
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -295,160 +533,26 @@ def run_ours(args, ws, rank, local):
     w = synth.WORKLOADS[args.workload]
     if args.E:
         w = synth.scaled(w, E=args.E, name=f"{w.name}_E{args.E}")
-    path = {"auto": libmoe.MOE_PATH_AUTO, "decode": libmoe.MOE_PATH_DECODE,
-            "prefill": libmoe.MOE_PATH_PREFILL}[args.path]
-    tm = args.tile_m
-    if not tm:
-        rows = w.T * w.Kt / w.Et
-        tm = 8 if args.act == "bf16" else (32 if rows < 16 else 64 if rows < 64 else 128)
-    host = synth.make_inputs(w)
-
-    def up(a):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        if a.dtype == np.uint16:
-            t = t.view(torch.int16).view(torch.bfloat16)
-        return t.to(dev)
-
-    R = max(1, args.replicas)
-    weights = [{k: up(host[k]) for k in ("w13", "s13", "w2", "s2")}]
-    for _ in range(R - 1):
-        weights.append({k: v.clone() for k, v in weights[0].items()})
-    logits = [up(host["logits"]) for _ in range(R)]
-    xs = [up(host["x"]) for _ in range(R)]
-    mx = args.act == "mxfp4"
-    bufs = libmoe.alloc_layer(w.T, w.E, w.K, w.with_shared, w.H, w.I, w.Et, tm, dev)
-    h_buf, y_buf = libmoe.ffn_views(bufs["workspace"], w.T, w.H, w.I, w.Et, w.Kt, tm)
-    if mx:  # the MXFP4-activation workspace replaces the bf16 one
-        bufs["workspace"] = libmoe.alloc_workspace_mxfp4act(w.T, w.H, w.I, w.Et, w.Kt, tm, dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step(i, ev=None, gemm_ev=None):
-        # ev: events between all five calls (breakdown); gemm_ev: events only
-        # around the two GEMM steps (timed region), so that the programmatic
-        # launches overlap at the other kernel boundaries
-        r = i % R
-        W = weights[r]
-        if ev is not None:
-            ev[0].record(stream)
-        # routing + permutation: one launch up to MOE_ROUTE_PERMUTE_FUSED_MAX_T tokens
-        ids, tw, perm = libmoe.moe_route_permute(logits[r], w.K, tm, w.with_shared, w.renormalize,
-                                                 bufs["topk_ids"], bufs["topk_w"], bufs["perm"])
-        if ev is not None:
-            ev[1].record(stream)
-        if gemm_ev is not None:
-            gemm_ev[0].record(stream)
-        if mx:
-            libmoe.moe_ffn_mxfp4act_gate_up(xs[r], W["w13"], W["s13"], perm, bufs["workspace"])
-        else:
-            libmoe.moe_ffn_gate_up(xs[r], W["w13"], W["s13"], perm, bufs["workspace"], path)
-        if ev is not None:
-            ev[2].record(stream)
-        if gemm_ev is not None:
-            gemm_ev[1].record(stream)
-        if mx:  # down GEMM and the combine into out
-            libmoe.moe_ffn_mxfp4act_down(W["w2"], W["s2"], tw, perm, bufs["workspace"], w.T,
-                                         bufs["out"])
-        else:  # down GEMM and the combine into out
-            libmoe.moe_ffn_down_combine(W["w2"], W["s2"], tw, perm, bufs["workspace"], w.T,
-                                        bufs["out"], path)
-        if ev is not None:
-            ev[3].record(stream)
-        if gemm_ev is not None:
-            gemm_ev[2].record(stream)
-        if ev is not None:
-            ev[4].record(stream)
+    tm = args.tile_m or default_tile_m(w, args.act)
+    lay = Layer(w, args.act, tm, args.path, args.replicas, dev)
 
     for i in range(args.warmup):
-        step(i)
+        lay.step(i)
     torch.cuda.synchronize(dev)
-    ids_host = bufs["topk_ids"].cpu().numpy()
+    ids_host = lay.bufs["topk_ids"].cpu().numpy()
     work = layer_work(w, ids_host, args.act)
 
     K = args.steps
-    gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(gpu_id_for(local))
-    if ws > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    t_start.record(stream)
-    for i in range(K):
-        step(i, gemm_ev=gevs[i])
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    if ws > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    gemm = {"gate_up": statistics.mean(g[0].elapsed_time(g[1]) for g in gevs),
-            "down": statistics.mean(g[1].elapsed_time(g[2]) for g in gevs)}
-    # per-call breakdown (after the timed region: events between every call)
-    KB = min(K, 10)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(KB)]
-    for i in range(KB):
-        step(i, ev=evs[i])
-    torch.cuda.synchronize(dev)
-    names = ["route_permute", "gate_up", "down", "combine"]
-    per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(KB))
-           for j, n in enumerate(names)}
-    per.update(gemm)  # the GEMM steps as timed inside the timed region
-    if not np.isfinite(bufs["out"].float().cpu().numpy()).all():
-        raise RuntimeError("non-finite layer output")
-
-    # end to end: per step H2D of logits + x from pinned host memory, the layer,
-    # D2H of the output into pinned host memory
-    pin_logits = torch.from_numpy(host["logits"]).pin_memory()
-    pin_x = torch.from_numpy(host["x"]).view(torch.int16).view(torch.bfloat16).pin_memory()
-    pin_out = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
-
-    def e2e_step():
-        logits[0].copy_(pin_logits, non_blocking=True)
-        xs[0].copy_(pin_x, non_blocking=True)
-        if mx:
-            _, tw, perm = libmoe.moe_route_permute(logits[0], w.K, tm, w.with_shared,
-                                                   w.renormalize, bufs["topk_ids"],
-                                                   bufs["topk_w"], bufs["perm"])
-            libmoe.moe_ffn_mxfp4act(xs[0], weights[0]["w13"], weights[0]["s13"],
-                                    weights[0]["w2"], weights[0]["s2"], tw, perm, bufs["out"],
-                                    bufs["workspace"])
-        else:
-            libmoe.moe_layer(logits[0], xs[0], weights[0]["w13"], weights[0]["s13"],
-                             weights[0]["w2"], weights[0]["s2"], w.K, w.with_shared,
-                             w.renormalize, tile_m=tm, path=path, bufs=bufs)
-        pin_out.copy_(bufs["out"], non_blocking=True)
-
-    for _ in range(max(3, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-
+    total_ms, gemm, clocks = lay.timed(K, local, ws)
+    per = lay.breakdown(min(K, 10))
+    lay.check_output()
+    e2e_ms = lay.e2e(K, args.warmup)
     if ws > 1:
         total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dev)
 
     result = None
     if rank == 0:
-        path_name = "prefill" if (args.path == "prefill" or (
-            args.path == "auto" and libmoe.moe_ffn_auto_path(w.T, w.Kt, w.Et, tm)
-            == libmoe.MOE_PATH_PREFILL)) else "decode"
-        if mx:
-            path_name = "mxfp4act"
-        src = {"prefill": "ffn_prefill.cu", "decode": "ffn_decode.cu",
-               "mxfp4act": "ffn_mxfp4act.cu"}[path_name]
-        traffic, traffic_src = traffic_from_profiles(
-            f"{path_name}_gate_up", w.name,
-            os.path.join(ROOT, "mxfp4_mixture_experts_softmax_gb300", "csrc", src))
-        gu = roofline_entry(f"{path_name}_gate_up", work["gate_up_bytes"], work["gate_up_flops"],
-                            per["gate_up"] / 1e3, traffic, traffic_src, fp4=mx)
-        dn = roofline_entry(f"{path_name}_down_combine", work["down_bytes"],
-                            work["flops"] - work["gate_up_flops"], per["down"] / 1e3, None, None,
-                            fp4=mx)
-        layer_s = total_ms / K / 1e3  # the whole step, gaps between launches included
+        gu, dn, layer = lay.rooflines(work, gemm, total_ms, K)
         result = {
             "metric": METRIC,
             "value": weak_scaling_value(w.T, K, ws, total_ms),
@@ -460,29 +564,33 @@ def run_ours(args, ws, rank, local):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            # MMA operand type (bf16 in and out, fp32 accumulation)
-            "dtype": "e2m1" if mx else "f16",
+            # MMA operand type (f16 rows scaled per row, fp32 accumulation)
+            "dtype": "e2m1" if lay.mx else "f16",
             "data": "synthetic (seeded; random MXFP4 weights, N(0,1) activations and logits)",
             "config": {
-                **workload_config(w, args.act, ws), "tile_m": tm, "path": path_name,
+                **workload_config(w, args.act, ws), "tile_m": tm, "path": lay.path_name,
                 "experts_touched": work["touched"],
                 "l2": f"inputs larger than L2: {work['layer_bytes'] / 1e9:.2f} GB touched per "
-                      f"step, {R} weight replicas rotated per step",
+                      f"step, {lay.R} weight replicas rotated per step",
             },
             "roofline": gu,
             "roofline_down": dn,
-            "layer_roofline": roofline_entry("layer", work["layer_bytes"], work["flops"],
-                                             layer_s, None, None, fp4=mx),
-            "kernels_us": {n: v * 1e3 for n, v in per.items()},
+            "layer_roofline": layer,
+            "kernels_us": {n: v * 1e3 for n, v in {**per, **gemm}.items()},
             "e2e": {"value": w.T * K * ws / (e2e_ms / 1e3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": int(host["logits"].nbytes + host["x"].nbytes),
+                    "h2d_bytes_per_step": int(lay.host["logits"].nbytes + lay.host["x"].nbytes),
                     "d2h_bytes_per_step": int(w.T * w.H * 2),
                     "ms_per_step": e2e_ms / K},
-            "gpu_launches": launches_per_step(w, path_name) * K,
+            "gpu_launches": launches_per_step(w, lay.path_name) * K,
             "clocks": clocks,
         }
-        if ws == 1 and not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(w, host, ids_host, args.cpu_seconds, args.act)
+    host = lay.host
+    lay.free()
+    del lay
+    if rank == 0 and ws == 1 and not args.no_per_config and not args.E:
+        result["per_config"] = measure_per_config(args, local, dev)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, host, None, args.cpu_seconds, args.act)
     if ws > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()

@@ -51,3 +51,29 @@ def ffn_parity(gpu: np.ndarray, ref: np.ndarray, what: str = "") -> dict:
 
 def upload_weights(d: dict) -> dict:
     return {k: to_dev(d[k]) for k in ("w13", "s13", "w2", "s2")}
+
+
+def edge_tokens(ids: np.ndarray, tile_m: int, n_total: int, seed: int) -> np.ndarray:
+    """Tokens whose pairs sit at the edges of the grouped GEMMs' tiles, for a
+    sampled comparison at full size: the first and last row in use (the
+    first and last work items), then, expert by expert in descending order of
+    load, the first and last row of the expert's last (usually partial) tile,
+    until three quarters of the budget; random tokens fill the rest.  Rows
+    follow the stable grouping by expert, as moe_permute lays them out."""
+    T, Kt = ids.shape
+    flat = ids.ravel()
+    order = np.argsort(flat, kind="stable")  # pair indices grouped by expert, ascending within
+    _, starts, counts = np.unique(flat[order], return_index=True, return_counts=True)
+    picks = {int(order[0]) // Kt, int(order[-1]) // Kt}
+    for i in np.argsort(-counts, kind="stable"):
+        if len(picks) >= max(2, n_total * 3 // 4):
+            break
+        c, s0 = int(counts[i]), int(starts[i])
+        last0 = s0 + ((c - 1) // tile_m) * tile_m
+        picks.add(int(order[last0]) // Kt)
+        picks.add(int(order[s0 + c - 1]) // Kt)
+    rng = np.random.default_rng(seed)
+    rest = np.setdiff1d(np.arange(T), np.fromiter(picks, int))
+    n_more = max(0, min(n_total - len(picks), rest.size))
+    tokens = np.concatenate([np.fromiter(picks, int), rng.choice(rest, n_more, replace=False)])
+    return np.unique(tokens).astype(np.int32)

@@ -42,7 +42,8 @@ def test_layer_work_matches_the_closed_forms(name, synth_mod, oracle_mod):
     w13 = 2 * I * (H // 2 + H // 32)
     w2 = H * (I // 2 + I // 32)
     assert work["gate_up_bytes"] == touched * w13 + 2 * T * H + 2 * P * I
-    assert work["down_bytes"] == touched * w2 + 2 * P * I + 8 * P * H + 2 * T * H
+    # algorithmic only: no per-pair fp32 outputs written and read back
+    assert work["down_bytes"] == touched * w2 + 2 * P * I + 2 * T * H
     assert work["layer_bytes"] == touched * (w13 + w2) + 4 * T * H + 4 * P * I + 4 * T * w.E
 
 
@@ -55,6 +56,16 @@ def test_layer_work_mxfp4_moves_encoded_rows(synth_mod, oracle_mod):
     # h crosses HBM as 0.53 bytes per value instead of 2 (written once, read once)
     hq = w.I // 2 + w.I // 32
     assert bf["layer_bytes"] - mx["layer_bytes"] == 4 * w.pairs * w.I - 2 * w.pairs * hq
+
+
+def test_per_config_covers_every_full_size_workload():
+    full = [n for n, w in synth.WORKLOADS.items() if w.H == 4096]
+    assert sorted(bench.PER_CONFIG) == sorted(full)
+    assert bench.DEFAULT_WORKLOAD in bench.PER_CONFIG
+    for n in bench.PER_CONFIG:  # the bf16 tile height gives the path the pages' regime names
+        w = synth.WORKLOADS[n]
+        path = libmoe.moe_ffn_auto_path(w.T, w.Kt, w.Et, bench.default_tile_m(w, "bf16"))
+        assert path == (libmoe.MOE_PATH_DECODE if w.T <= 288 else libmoe.MOE_PATH_PREFILL), n
 
 
 def test_launch_counts_per_path():

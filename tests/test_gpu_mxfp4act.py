@@ -233,8 +233,8 @@ def test_ffn_mxfp4act_rejections_and_empty_batch():
     assert out0.shape == (0, w.H)
 
 
-FULL = {"decode64": (32, 8), "prefill1536": (64, 8), "skewed_prefill8192": (128, 6),
-        "skewed_prefill8192_cal": (128, 6)}
+FULL = {"decode64": (32, None), "prefill1536": (64, 64), "skewed_prefill8192": (128, 64),
+        "skewed_prefill8192_cal": (128, 64)}
 
 
 @pytest.mark.parametrize("name", list(FULL))
@@ -247,9 +247,8 @@ def test_ffn_mxfp4act_full_size(name):
     ids, wt = oracle.route(d["logits"], w.K, w.with_shared)
     T, H = d["x"].shape
     I, Et, Kt = w.I, w.Et, ids.shape[1]
-    rng = np.random.default_rng(97)
-    tokens = np.unique(np.concatenate([[0, T - 1], rng.choice(T, n_tok - 2, replace=False)]))
-    tokens = tokens.astype(np.int32)
+    tokens = (np.arange(T, dtype=np.int32) if n_tok is None
+              else gc.edge_tokens(ids, tile_m, n_tok, 97))
     out_ref, ref = oracle.ffn_mxfp4act(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt,
                                        tokens=tokens, want_h=True, n_threads=THREADS)
     dw = gc.upload_weights(d)
@@ -263,7 +262,7 @@ def test_ffn_mxfp4act_full_size(name):
     gpu_hd, _, _ = _h_by_pair(ws, perm, T, H, I, Et, Kt, tile_m, pairs)
     mism = _compare_h(gpu_hd, ref, np.arange(pairs.size))
     bad_tok = mism.reshape(tokens.size, Kt, I).any(axis=(1, 2))
-    assert bad_tok.sum() <= 1
+    assert bad_tok.sum() <= max(1, tokens.size // 32)
     got = gc.bf16_dev_to_f64(out)[tokens]
     stats = gc.ffn_parity(got[~bad_tok], gc.bits_to_f64(out_ref)[~bad_tok], name)
     print(name, "mxfp4act", stats, "h flips", int(mism.sum()))

@@ -2,9 +2,10 @@
 
 Routing ids and the permutation bit for bit; moe_ffn within the stated
 floating-point bar (gpu_common.ffn_parity).  Small shapes compare every
-output element; the full-size workloads compare every token of the 64-token
-decode step and a sample of tokens elsewhere, in the launch configuration the
-bench times.
+output element; the full-size workloads compare every token of the 64-, 288-
+and 1536-token workloads and, at 8192 tokens, a sample chosen at the tiles'
+edges plus a cross-check of the two GEMM paths on every token, in the launch
+configuration the bench times.
 """
 import numpy as np
 import pytest
@@ -329,13 +330,19 @@ def test_ffn_empty_batch():
 
 # ------------------------------------------------- full-size workloads
 
-FULL = {  # workload -> (tile_m as the bench runs it, tokens compared)
+FULL = {  # workload -> (tile_m, tokens compared: None = all), on the decode path
     "decode64": (8, None),
-    "mtp_verify288": (8, 24),
-    "prefill1536": (8, 12),
-    "skewed_prefill8192": (8, 8),
-    "skewed_prefill8192_cal": (8, 8),
+    "mtp_verify288": (8, None),
+    "prefill1536": (8, 96),
+    "skewed_prefill8192": (8, 64),
+    "skewed_prefill8192_cal": (8, 64),
 }
+
+
+def _tokens_for(w, ids, tile_m, n_tok, seed):
+    if n_tok is None:
+        return np.arange(w.T, dtype=np.int32)
+    return gc.edge_tokens(ids, tile_m, n_tok, seed)
 
 
 @pytest.mark.parametrize("name", list(FULL))
@@ -343,23 +350,19 @@ def test_ffn_full_size(name):
     w = synth.WORKLOADS[name]
     tile_m, n_tok = FULL[name]
     d, ids, wt = _layer_inputs(w)
-    if n_tok is None:
-        tokens = np.arange(w.T, dtype=np.int32)
-    else:
-        rng = np.random.default_rng(99)
-        tokens = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, n_tok - 2, replace=False)]))
-        tokens = tokens.astype(np.int32)
+    tokens = _tokens_for(w, ids, tile_m, n_tok, 99)
     ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt,
                                     tokens=tokens, n_threads=THREADS))
     dev_w = gc.upload_weights(d)
-    # the whole layer as the bench runs it: route -> permute -> ffn on the device
+    # the whole layer: route -> permute -> ffn on the device
     out = libmoe.moe_layer(gc.to_dev(d["logits"]), gc.to_dev(d["x"]), dev_w["w13"], dev_w["s13"],
                            dev_w["w2"], dev_w["s2"], w.K, w.with_shared, tile_m=tile_m,
                            path=libmoe.MOE_PATH_DECODE)
     torch.cuda.synchronize()
+    assert libmoe.moe_device_error() == 0
     got = gc.bf16_dev_to_f64(out)[tokens]
     stats = gc.ffn_parity(got, ref, name)
-    print(name, stats)
+    print(name, tokens.size, "tokens", stats)
     del dev_w
     torch.cuda.empty_cache()
 
@@ -466,18 +469,24 @@ def test_prefill_tile_m_and_permutation_invariance():
                                   2 * outs[0])
 
 
-PREFILL_FULL = {"prefill1536": (32, 12), "mtp_verify288": (32, 12),
-                "skewed_prefill8192": (128, 8), "skewed_prefill8192_cal": (128, 8)}
+PREFILL_FULL = {  # workload -> (tile_m as the bench runs it, tokens compared: None = all)
+    "mtp_verify288": (32, None),
+    "prefill1536": (64, None),
+    "skewed_prefill8192": (128, 256),
+    "skewed_prefill8192_cal": (128, 256),
+}
 
 
 @pytest.mark.parametrize("name", list(PREFILL_FULL))
 def test_prefill_full_size(name):
+    """The prefill path at full size in the bench's launch configuration:
+    every token of the 288- and 1536-token workloads; on the 8192-token
+    ones 256 tokens that include the first and last row of each hot
+    expert's last partial tile and of the first and last work items."""
     w = synth.WORKLOADS[name]
     tile_m, n_tok = PREFILL_FULL[name]
     d, ids, wt = _layer_inputs(w)
-    rng = np.random.default_rng(98)
-    tokens = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, n_tok - 2, replace=False)]))
-    tokens = tokens.astype(np.int32)
+    tokens = _tokens_for(w, ids, tile_m, n_tok, 98)
     ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt,
                                     tokens=tokens, n_threads=THREADS))
     dev_w = gc.upload_weights(d)
@@ -487,7 +496,31 @@ def test_prefill_full_size(name):
     torch.cuda.synchronize()
     assert libmoe.moe_device_error() == 0
     stats = gc.ffn_parity(gc.bf16_dev_to_f64(out)[tokens], ref, name)
-    print(name, "prefill", stats)
+    print(name, "prefill", tokens.size, "tokens", stats)
+    del dev_w
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["skewed_prefill8192", "skewed_prefill8192_cal"])
+def test_decode_and_prefill_paths_agree_on_every_token(name):
+    """All 8192 tokens: the prefill path (128-row tiles, tcgen05) against the
+    decode path (8-row tiles, warp MMA) -- two independent kernel families
+    held to the parity bar against each other, so a broken tile that the
+    oracle's token sample misses still shows."""
+    w = synth.WORKLOADS[name]
+    d, ids, wt = _layer_inputs(w)
+    dev_w = gc.upload_weights(d)
+    logits, x = gc.to_dev(d["logits"]), gc.to_dev(d["x"])
+    outs = {}
+    for path, tile_m in ((libmoe.MOE_PATH_DECODE, 8), (libmoe.MOE_PATH_PREFILL, 128)):
+        outs[path] = gc.bf16_dev_to_f64(libmoe.moe_layer(
+            logits, x, dev_w["w13"], dev_w["s13"], dev_w["w2"], dev_w["s2"], w.K, w.with_shared,
+            tile_m=tile_m, path=path))
+    torch.cuda.synchronize()
+    assert libmoe.moe_device_error() == 0
+    stats = gc.ffn_parity(outs[libmoe.MOE_PATH_PREFILL], outs[libmoe.MOE_PATH_DECODE],
+                          f"{name} prefill vs decode")
+    print(name, "prefill vs decode", stats)
     del dev_w
     torch.cuda.empty_cache()
 
