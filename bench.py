@@ -531,9 +531,9 @@ def run_ours(args, ws, rank, local):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo",
                                 device_id=dev if torch.cuda.is_available() else None)
     w = synth.WORKLOADS[args.workload]
-    if args.E:
+    tm = args.tile_m or default_tile_m(w, args.act)  # the full workload's tile height
+    if args.E:  # fewer routed experts (profiler captures): same tile height
         w = synth.scaled(w, E=args.E, name=f"{w.name}_E{args.E}")
-    tm = args.tile_m or default_tile_m(w, args.act)
     lay = Layer(w, args.act, tm, args.path, args.replicas, dev)
 
     for i in range(args.warmup):

@@ -36,6 +36,8 @@
 //     overlaps the next item's MMAs.
 // Every wait is bounded (see mbar_wait); after a timeout each role stops, the
 // MMA thread drains its own MMAs (bounded), and tensor memory is freed.
+#include <stdlib.h>
+
 #include <algorithm>
 
 #include "moe_internal.h"
@@ -57,6 +59,7 @@ constexpr int kACols = kBK / 2;                           // tensor-memory colum
 constexpr int kCodeBytes = 128 * (kBK / 2);               // 4 KB packed codes stage
 constexpr int kCodeBox = 64;                              // rows per codes box
 constexpr int kPrefetch = 12;                             // code stages prefetched into L2 ahead
+constexpr int kPairPrefetch = 12;                         // the same for the CTA-pair kernel
 
 // Instruction descriptor: f16 x f16 -> fp32 (a and b format fields 0), both
 // operands K-major, M x N.
@@ -71,6 +74,20 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The pair form, issued by the even CTA of a CTA pair: M = 256, A rows 0..127
+// from this CTA's tensor memory and 128..255 from the other CTA's at the same
+// address, B's N rows split between the two CTAs' shared memory at the same
+// offset (rows 0..N/2-1 here), D rows likewise split by CTA.
+__device__ __forceinline__ void mma_f16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -140,19 +157,23 @@ __device__ __forceinline__ uint4 codes_to_f16x8(uint32_t w, uint32_t mult) {
     return v;
 }
 
-template <int N>
+template <int N, bool PAIR>
 struct PrefillSmem {
-    // 128-row weight blocks per work item.  The blocks share the tile's B
-    // stage, so B crosses L2 once per kRB blocks (the f16 B rows, N * 128
-    // bytes per 64-k stage against 4 KB of codes, make L2 -> shared-memory
-    // traffic a bound).  Two blocks only where both accumulators can still
-    // be double-buffered: at N = 128 the single buffer and the 4-slot ring
-    // cost more than the saved traffic (skewed 8192 prefill 3.1 -> 3.8 ms;
-    // 1536-token prefill with N = 64: 1.86 -> 1.74 ms).
-    static constexpr int kRB = N <= 64 ? 2 : 1;
-    static constexpr int kBBytes = N * kBK * 2;
-    static constexpr int kCodeStage = kRB * kCodeBytes;            // codes of the item's blocks
+    // 128-row weight blocks per work item and CTA.  The blocks share the
+    // tile's B stage, so B crosses L2 once per kRB blocks (the f16 B rows,
+    // N * 128 bytes per 64-k stage against 4 KB of codes, make L2 ->
+    // shared-memory traffic a bound).  Two blocks only where both
+    // accumulators can still be double-buffered: at N = 128 the single buffer
+    // and the 4-slot ring cost more than the saved traffic (skewed 8192
+    // prefill 3.1 -> 3.8 ms; 1536-token prefill with N = 64: 1.86 -> 1.74 ms).
+    // A CTA pair (PAIR) shares B instead: each CTA holds one block and loads
+    // half of the tile's B rows, and one pair MMA (M = 256) reads both halves.
+    static constexpr int kRB = (!PAIR && N <= 64) ? 2 : 1;
+    static constexpr int kBRows = PAIR ? N / 2 : N;                // B rows this CTA loads
+    static constexpr int kBBytes = kBRows * kBK * 2;
+    static constexpr int kCodeStage = kRB * kCodeBytes;            // codes of the CTA's blocks
     static constexpr int kStage = kBBytes + kCodeStage;            // multiple of 1024
+    static_assert(kStage % 1024 == 0, "swizzle atoms");
     // Converter warp (quadrant, part) owns the stages with gs % 4 == part; with
     // a ring of a multiple of 4 slots each slot belongs to one part, so every
     // barrier's phases are observed in order (a parity wait is unambiguous
@@ -161,7 +182,7 @@ struct PrefillSmem {
     // kAStages tensor-memory A slots (filled by the converters).  With two
     // blocks per item tensor memory holds only 4 A slots, but shared memory
     // holds 8 stages, so TMA runs further ahead than the conversion.
-    static constexpr int kStages = (N <= 128) ? 8 : 4;
+    static constexpr int kStages = 8 * kStage <= 170 * 1024 ? 8 : 4;
     static constexpr int kAStages = (kRB == 1 && N <= 128) ? 8 : 4;
     static_assert(kStages % 4 == 0 && kAStages % 4 == 0, "slot ownership");
     static_assert(kStages % kAStages == 0, "ring nesting");
@@ -181,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_gemm_kernel(const GroupedGemm g, const __grid_constant__ CUtensorMap codes_map,
                         const __grid_constant__ CUtensorMap act_map) {
     pdl_begin();
-    using L = PrefillSmem<N>;
+    using L = PrefillSmem<N, false>;
     constexpr int kStages = L::kStages, kAStages = L::kAStages;
     constexpr bool kDecoupled = kAStages != kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -586,36 +607,451 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_end();
 }
 
+// The CTA-pair form of the kernel above (launched as clusters of 2): a work
+// item is one tile x two adjacent 128-row weight blocks, block 2 grp + rank
+// in CTA `rank` of the pair.  Each CTA loads its block's codes and half of the
+// tile's B rows (N / 2 rows, at the same shared-memory offset in both CTAs)
+// and converts its block into its own tensor memory; the even CTA's MMA
+// thread issues one M = 256 MMA per K = 16 for both (tcgen05 cta_group::2),
+// which reads both CTAs' A and B halves, and commits to the barriers of both
+// CTAs.  B crosses L2 -> shared memory once per 256 weight rows instead of
+// once per 128.  The odd CTA's converter and epilogue warps arrive on the
+// even CTA's barriers; its MMA warp only allocates and frees tensor memory.
 template <int MODE, int N>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_pair_kernel(const GroupedGemm g, const __grid_constant__ CUtensorMap codes_map,
+                        const __grid_constant__ CUtensorMap act_map) {
+    pdl_begin();
+    using L = PrefillSmem<N, true>;
+    constexpr int kStages = L::kStages, kAStages = L::kAStages;
+    constexpr bool kDecoupled = kAStages != kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    constexpr int kPairs = kStages / 2, kAPairs = kAStages / 2;
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L::kBars);  // codes + B landed, per slot
+    uint64_t* a_full = raw_full + kStages;      // A converted in both CTAs, per A pair (even CTA)
+    uint64_t* stage_free = a_full + kAPairs;    // MMAs done with a slot pair
+    uint64_t* a_free = stage_free + kPairs;     // MMAs done with an A pair
+    uint64_t* acc_full = a_free + kAPairs;      // [2] accumulator ready
+    uint64_t* acc_free = acc_full + 2;          // [2] drained by both CTAs (even CTA)
+    uint64_t* drain = acc_free + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    constexpr int kAccBufs = L::kAccBufs;
+    auto stage_b = [&](int s) { return smem + s * L::kStage; };
+    auto stage_c = [&](int s) { return smem + s * L::kStage + L::kBBytes; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // clusters of 2 along x: the rank in the pair is the low bit of the CTA index
+    const int rank = (int)(blockIdx.x & 1u);
+    const int K = g.K;
+    const int nk = ((K + kBK - 1) / kBK + 1) & ~1;  // stages per item, whole pairs
+    const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
+    const int row_groups = row_blocks / 2;          // even (checked by the launcher)
+    const int items = checked_tiles(g) * row_groups;
+    constexpr uint32_t kTmemCols = 512;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&raw_full[s], 1);
+        for (int p = 0; p < kPairs; ++p) mbar_init(&stage_free[p], 1);
+        for (int p = 0; p < kAPairs; ++p) {
+            mbar_init(&a_full[p], 8);  // per stage pair one converter warp per lane quadrant, both CTAs
+            mbar_init(&a_free[p], 1);
+        }
+        for (int b = 0; b < kAccBufs; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_free[b], 2 * kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) tmem_alloc<true>(tmem_slot, kTmemCols);
+    tc_fence_before();
+    // the other CTA's barriers are initialised and its tensor memory
+    // allocated before anything arrives there or an MMA writes it
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------- producer
+        uint32_t gs = 0;
+        bool ok = true;
+        for (int item = blockIdx.x >> 1; item < items && ok; item += gridDim.x >> 1) {
+            const int tile = item / row_groups, block = 2 * (item % row_groups) + rank;
+            const int e = checked_expert(g, tile, block == 0);
+            if (e < 0) continue;  // skipped by every role of both CTAs
+            const int crow0 = e * g.rows + (MODE == 0 ? block * 64 : block * 128);
+            const int crow1 = MODE == 0 ? e * g.rows + g.I + block * 64 : crow0 + kCodeBox;
+            const int brow = tile * N + rank * L::kBRows;
+            if (lane == 0)
+                for (int st = 0; st < kPairPrefetch && st < nk; ++st) {
+                    tma_prefetch_l2_2d(&codes_map, st * (kBK / 2), crow0);
+                    tma_prefetch_l2_2d(&codes_map, st * (kBK / 2), crow1);
+                    tma_prefetch_l2_2d(&act_map, st * kBK, brow);
+                }
+            for (int st = 0; st < nk; ++st, ++gs) {
+                const int s = gs % kStages;
+                if (lane == 0 && st + kPairPrefetch < nk) {
+                    tma_prefetch_l2_2d(&codes_map, (st + kPairPrefetch) * (kBK / 2), crow0);
+                    tma_prefetch_l2_2d(&codes_map, (st + kPairPrefetch) * (kBK / 2), crow1);
+                    tma_prefetch_l2_2d(&act_map, (st + kPairPrefetch) * kBK, brow);
+                }
+                if (gs >= kStages && (gs & 1) == 0 &&
+                    !mbar_wait_warp(&stage_free[(gs >> 1) % kPairs], ((gs / kStages) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&raw_full[s], (uint32_t)(L::kCodeStage + L::kBBytes));
+                    const uint32_t cdst = smem_u32(stage_c(s));
+                    tma_load_2d(cdst, &codes_map, st * (kBK / 2), crow0, &raw_full[s]);
+                    tma_load_2d(cdst + kCodeBox * (kBK / 2), &codes_map, st * (kBK / 2), crow1,
+                                &raw_full[s]);
+                    tma_load_2d(smem_u32(stage_b(s)), &act_map, st * kBK, brow, &raw_full[s]);
+                }
+            }
+        }
+        if (lane == 0)  // the last loads landed before the CTA can exit (bounded)
+            for (int d = 0; d < kStages && d < (int)gs; ++d) {
+                const uint32_t u = gs - 1 - d;
+                if (!mbar_wait(&raw_full[u % kStages], (u / kStages) & 1)) break;
+            }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_f16(256, N);
+            uint32_t gs = 0, it = 0;
+            bool ok = true;
+            for (int item = blockIdx.x >> 1; item < items && ok; item += gridDim.x >> 1) {
+                if (checked_expert(g, item / row_groups, false) < 0) continue;
+                const uint32_t b = it % kAccBufs;
+                if (it >= (uint32_t)kAccBufs && !mbar_wait(&acc_free[b], ((it / kAccBufs) - 1) & 1)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + b * L::kAccCols;
+                for (int st = 0; st < nk; st += 2, gs += 2) {
+                    const int pr = (gs >> 1) % kPairs, pa = (gs >> 1) % kAPairs;
+                    // both stages' A converted in both CTAs (the converters
+                    // arrive after their stage's TMA barrier: B has landed)
+                    if (!mbar_wait(&a_full[pa], (gs / kAStages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int s = (gs + h2) % kStages, sa = (gs + h2) % kAStages;
+                        const uint64_t bd = sdesc_sw128(smem_u32(stage_b(s)));
+                        const uint32_t a_tmem = tmem + (uint32_t)(L::kACol0 + sa * kACols);
+#pragma unroll
+                        for (int k = 0; k < kBK / 16; ++k)
+                            mma_f16_ts_pair(d_tmem, a_tmem + 8u * k, bd + 2u * k, idesc,
+                                            (st | h2 | k) != 0 ? 1u : 0u);
+                    }
+                    mma_commit_pair(&stage_free[pr]);
+                    if (kDecoupled) mma_commit_pair(&a_free[pa]);
+                }
+                if (ok) mma_commit_pair(&acc_full[b]);
+                ++it;
+            }
+            mma_commit_pair(drain);  // both CTAs: every MMA of the pair has completed
+            mbar_wait(drain, 0);
+        } else if (lane == 0) {
+            // the odd CTA: the pair's MMAs, and the commits arriving on this
+            // CTA's barriers as they complete, are done before it exits
+            mbar_wait(drain, 0);
+        }
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------------ converters
+        // warp (quadrant, part) converts its quadrant's 32 weight rows for the
+        // stage pairs P (stages 2P, 2P + 1, counted over all items) with
+        // P % kParts == part; the pair's four scale groups of a row are one
+        // 32-bit load.  kParts = the A-slot pairs (at most 4): every slot, its
+        // TMA barrier and its A-slot barrier then belong to one part, which
+        // waits on each of their phases in order (a parity wait is unambiguous
+        // only one phase ahead).  With 4 A slots (256-row tiles) half the
+        // converter warps stay idle; the MMAs take twice as long per stage.
+        constexpr int kParts = kAPairs < 4 ? kAPairs : 4;
+        static_assert((kStages / 2) % kParts == 0, "slot ownership");
+        const int quad = warp & 3, part = (warp - kConvWarp0) >> 2;
+        const int rho = 32 * quad + lane;
+        const int crow = MODE == 0 ? ((rho & 1) ? kCodeBox + (rho >> 1) : rho >> 1) : rho;
+        const bool svec = (K % 512) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 15) == 0);
+        const int ngroups = K / 32;
+        const bool s4 = (ngroups % 4) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 3) == 0);
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)L::kACol0;
+        uint32_t gs = 0;  // the item's first stage, counted over all items (even)
+        bool ok = true;
+        for (int item = blockIdx.x >> 1; item < items && ok; item += gridDim.x >> 1) {
+            const int tile = item / row_groups, block = 2 * (item % row_groups) + rank;
+            const int e = checked_expert(g, tile, false);
+            if (e < 0) continue;
+            int wrow;
+            bool rvalid;
+            if (MODE == 0) {
+                const int n = block * 64 + (rho >> 1);
+                rvalid = n < g.I;
+                wrow = (rho & 1) ? g.I + n : n;
+            } else {
+                wrow = block * 128 + rho;
+                rvalid = wrow < g.rows;
+            }
+            const uint8_t* sp = g.scales + ((size_t)e * g.rows + (rvalid ? wrow : 0)) * (size_t)ngroups;
+            const int s_ref = row_scale_ref(rvalid ? row_scale_max_part(sp, ngroups, svec, 0, 1) : 0u);
+            // scale bytes of groups 4p .. 4p + 3 (stage pair p of the item), 0 past the row
+            auto scales4 = [&](int p) -> uint32_t {
+                if (!rvalid) return 0u;
+                if (s4 && 4 * p + 3 < ngroups) return __ldg(reinterpret_cast<const uint32_t*>(sp) + p);
+                uint32_t v = 0;
+                for (int i = 0; i < 4; ++i)
+                    if (4 * p + i < ngroups) v |= (uint32_t)__ldg(sp + 4 * p + i) << (8 * i);
+                return v;
+            };
+            const int np = nk / 2;
+            // this warp's first pair of the item (np when the part is idle)
+            const int p0 = part < kParts
+                               ? (int)((uint32_t)(part - (int)(gs >> 1)) % (uint32_t)kParts)
+                               : np;
+            uint32_t sc = p0 < np ? scales4(p0) : 0u;  // loaded one of this warp's pairs ahead
+            for (int p = p0; p < np; p += kParts) {
+                const uint32_t g0 = gs + 2u * (uint32_t)p;  // first stage of the pair
+                const uint32_t scv = sc;
+                if (p + kParts < np) sc = scales4(p + kParts);
+                if (kDecoupled && g0 >= (uint32_t)kAStages &&
+                    !mbar_wait_warp(&a_free[(g0 >> 1) % kAPairs], ((g0 / kAStages) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll 1
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const uint32_t g_s = g0 + (uint32_t)h2;
+                    const int s = g_s % kStages, sa = g_s % kAStages;
+                    const uint32_t m0 = f16_group_mult((scv >> (16 * h2)) & 0xFFu, s_ref);
+                    const uint32_t m1 = f16_group_mult((scv >> (16 * h2 + 8)) & 0xFFu, s_ref);
+                    if (!mbar_wait_warp(&raw_full[s], (g_s / kStages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();  // after the MMAs that last read this A stage
+                    uint4 c[2];
+                    const uint32_t cs = smem_u32(stage_c(s)) + crow * (kBK / 2);
+                    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(c[0].x), "=r"(c[0].y), "=r"(c[0].z), "=r"(c[0].w)
+                                 : "r"(cs));
+                    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(c[1].x), "=r"(c[1].y), "=r"(c[1].z), "=r"(c[1].w)
+                                 : "r"(cs + 16));
+                    uint32_t a[32];  // column i of the stage = f16x2 (k 2i, 2i + 1)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t w[4] = {c[hh].x, c[hh].y, c[hh].z, c[hh].w};
+                        const uint32_t m = hh ? m1 : m0;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 v = codes_to_f16x8(w[i], m);
+                            a[16 * hh + 4 * i + 0] = v.x;
+                            a[16 * hh + 4 * i + 1] = v.y;
+                            a[16 * hh + 4 * i + 2] = v.z;
+                            a[16 * hh + 4 * i + 3] = v.w;
+                        }
+                    }
+                    tmem_st32(lane_base + (uint32_t)(sa * kACols), a);
+                }
+                if (!ok) break;
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(&a_full[(g0 >> 1) % kAPairs], 0);
+            }
+            gs += (uint32_t)nk;
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int r = 32 * quad + lane;
+        const bool svec = (K % 512) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 15) == 0);
+        constexpr int kQ = N / 32;
+        int qn[kQ];
+        float cn[kQ];
+        float frn = 0.0f;
+        auto load_item = [&](int item) {
+            if (item >= items) return;
+            const int tile = item / row_groups, block = 2 * (item % row_groups) + rank;
+            const int e = checked_expert(g, tile, false);
+            if (e < 0) return;
+            int wrow;
+            bool rvalid;
+            if (MODE == 0) {
+                const int n = block * 64 + (r >> 1);
+                rvalid = n < g.I;
+                wrow = (r & 1) ? g.I + n : n;
+            } else {
+                wrow = block * 128 + r;
+                rvalid = wrow < g.rows;
+            }
+            const uint8_t* sp = g.scales + ((size_t)e * g.rows + (rvalid ? wrow : 0)) * (size_t)(K / 32);
+            frn = __uint_as_float(
+                (uint32_t)row_scale_ref(rvalid ? row_scale_max_part(sp, K / 32, svec, 0, 1) : 0u) << 23);
+#pragma unroll
+            for (int u = 0; u < kQ; ++u) {
+                const int p = tile * N + 32 * u + lane;
+                qn[u] = checked_pair(g, p);
+                if (MODE == 0)
+                    cn[u] = qn[u] < 0 ? 0.0f : __ldg(g.act_rscale + qn[u] / g.Kt);
+                else if (!g.y_blocked)
+                    cn[u] = qn[u] < 0 ? 0.0f : __ldg(g.topk_w + qn[u]) * __ldg(g.act_rscale + p);
+                else
+                    cn[u] = 0.0f;
+            }
+        };
+        load_item(blockIdx.x >> 1);
+        uint32_t it = 0;
+        for (int item = blockIdx.x >> 1; item < items; item += gridDim.x >> 1) {
+            const int tile = item / row_groups, block = 2 * (item % row_groups) + rank;
+            const int e = checked_expert(g, tile, false);
+            if (e < 0) {
+                load_item(item + (gridDim.x >> 1));
+                continue;
+            }
+            const uint32_t b = it % kAccBufs;
+            const float fr = frn;
+            int qv[kQ];
+            float cv[kQ];
+#pragma unroll
+            for (int u = 0; u < kQ; ++u) qv[u] = qn[u], cv[u] = cn[u];
+            int nvalid = 0;
+            if (MODE == 1) {
+#pragma unroll
+                for (int u = 0; u < kQ; ++u) nvalid += __popc(__ballot_sync(0xFFFFFFFFu, qv[u] >= 0));
+            }
+            if (!mbar_wait_warp(&acc_full[b], (it / kAccBufs) & 1)) break;
+            tc_fence_after();
+            load_item(item + (gridDim.x >> 1));
+#pragma unroll
+            for (int c0 = 0; c0 < N; c0 += 32) {
+                uint32_t v[32];
+                const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + b * L::kAccCols + (uint32_t)c0;
+                tmem_ld16_nowait(taddr, v);
+                tmem_ld16_nowait(taddr + 16, v + 16);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                const int q_lo = qv[c0 / 32];
+                const float c_lo = cv[c0 / 32];
+                if (MODE == 0) {
+                    const int n = block * 64 + (r >> 1);
+                    const bool odd = lane & 1;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float a0 = __uint_as_float(v[i]) * fr, a1 = __uint_as_float(v[i + 1]) * fr;
+                        const float other = __shfl_xor_sync(0xFFFFFFFFu, odd ? a0 : a1, 1);
+                        const int j = c0 + i + (odd ? 1 : 0);
+                        const float gate = odd ? other : a0;
+                        const float up = odd ? a1 : other;
+                        const int q = __shfl_sync(0xFFFFFFFFu, q_lo, j & 31);
+                        const float fc = __shfl_sync(0xFFFFFFFFu, c_lo, j & 31);
+                        if (n < g.I && q >= 0)
+                            g.h_out[(size_t)(tile * N + j) * g.I + n] =
+                                f32_to_bf16_bits(silu(gate * fc) * (up * fc));
+                    }
+                } else if (g.y_blocked) {
+                    const int m = block * 128 + r;
+                    float* yb = g.y_out + ((size_t)block * g.act_rows + (size_t)tile * N + c0) * 128 + r;
+                    const int nc = nvalid - c0;
+                    if (m < g.rows) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < nc) yb[(size_t)i * 128] = __uint_as_float(v[i]) * fr;
+                    }
+                } else {
+                    const int m = block * 128 + r;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int q = __shfl_sync(0xFFFFFFFFu, q_lo, i);
+                        const float fc = __shfl_sync(0xFFFFFFFFu, c_lo, i);
+                        if (m < g.rows && q >= 0)
+                            g.y_out[(size_t)q * g.rows + m] = fc * (__uint_as_float(v[i]) * fr);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(&acc_free[b], 0);  // the even CTA's MMA thread waits
+            ++it;
+        }
+    }
+
+    tc_fence_before();
+    // neither CTA releases its tensor memory or shared memory while the other
+    // may still arrive there or the pair's MMAs may still run
+    cluster_sync_all();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc<true>(tmem, kTmemCols);
+    }
+    pdl_end();
+}
+
+template <int MODE, int N, bool PAIR>
 cudaError_t launch_n(const GroupedGemm& g, cudaStream_t s) {
-    const size_t smem = PrefillSmem<N>::kTotal;
-    cudaError_t err = ensure_dynamic_smem((const void*)prefill_gemm_kernel<MODE, N>, smem);
+    using L = PrefillSmem<N, PAIR>;
+    const size_t smem = L::kTotal;
+    const void* fn;
+    if constexpr (PAIR)
+        fn = (const void*)prefill_pair_kernel<MODE, N>;
+    else
+        fn = (const void*)prefill_gemm_kernel<MODE, N>;
+    cudaError_t err = ensure_dynamic_smem(fn, smem);
     if (err != cudaSuccess) return err;
     CUtensorMap codes_map, act_map;
     err = encode_2d_map(&codes_map, g.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K / 2,
                         (uint64_t)g.num_experts * g.rows, g.K / 2, kBK / 2, kCodeBox,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
-    // activations in tile order (gathered x for gate_up, h for down): N rows per box
+    // activations in tile order (gathered x for gate_up, h for down): the
+    // CTA's B rows of a tile per box (all N, or its half of a pair's tile)
     err = encode_2d_map(&act_map, g.act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g.K, (uint64_t)g.act_rows,
-                        (uint64_t)g.K * 2, kBK, N, CU_TENSOR_MAP_SWIZZLE_128B);
+                        (uint64_t)g.K * 2, kBK, L::kBRows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
     const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
-    const int row_groups = (row_blocks + PrefillSmem<N>::kRB - 1) / PrefillSmem<N>::kRB;
+    const int row_groups = PAIR ? row_blocks / 2 : (row_blocks + L::kRB - 1) / L::kRB;
     const long long max_items = (long long)g.max_tiles * row_groups;
-    const int grid = (int)std::min<long long>(max_items, (long long)num_sms());
-    return launch_pdl(prefill_gemm_kernel<MODE, N>, dim3(grid), dim3(kThreads), smem, s, g,
-                      codes_map, act_map);
+    if constexpr (PAIR) {
+        // one wave of pairs: as many as can be resident at once (a pair needs
+        // two SMs of one GPC), one item per pair at least
+        int resident = 0;
+        err = max_active_pairs(fn, kThreads, smem, &resident);
+        if (err != cudaSuccess) return err;
+        const int pairs = (int)std::min<long long>(max_items, (long long)std::max(resident, 1));
+        return launch_pdl_cluster(prefill_pair_kernel<MODE, N>, dim3(2 * pairs),
+                                  dim3(kThreads), smem, s, 2u, g, codes_map, act_map);
+    } else {
+        const int grid = (int)std::min<long long>(max_items, (long long)num_sms());
+        return launch_pdl(prefill_gemm_kernel<MODE, N>, dim3(grid), dim3(kThreads), smem, s, g,
+                          codes_map, act_map);
+    }
+}
+
+// CTA pairs (two 128-row weight blocks sharing each B stage, one per CTA)
+// for tiles of 128 or more rows whenever the blocks pair up evenly (with
+// 64-row tiles the single-CTA kernel, two blocks per CTA, is faster);
+// MOE_PREFILL_PAIR=0 selects the single-CTA kernel (for comparisons).
+static bool use_pairs(const GroupedGemm& g, int mode) {
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("MOE_PREFILL_PAIR");
+        env = (v && v[0] == '0') ? 0 : 1;
+    }
+    const int row_blocks = mode == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
+    return env == 1 && g.tile_m >= 128 && row_blocks % 2 == 0;
 }
 
 template <int MODE>
 cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
     if (g.max_tiles == 0) return cudaSuccess;
+    const bool pair = use_pairs(g, MODE);
     switch (g.tile_m) {
-        case 32: return launch_n<MODE, 32>(g, s);
-        case 64: return launch_n<MODE, 64>(g, s);
-        case 128: return launch_n<MODE, 128>(g, s);
-        case 256: return launch_n<MODE, 256>(g, s);
+        case 32: return launch_n<MODE, 32, false>(g, s);
+        case 64: return pair ? launch_n<MODE, 64, true>(g, s) : launch_n<MODE, 64, false>(g, s);
+        case 128: return pair ? launch_n<MODE, 128, true>(g, s) : launch_n<MODE, 128, false>(g, s);
+        case 256: return pair ? launch_n<MODE, 256, true>(g, s) : launch_n<MODE, 256, false>(g, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -94,6 +94,44 @@ int num_sms() {
     return cached[dev];
 }
 
+cudaError_t max_active_pairs(const void* func, int threads, size_t smem, int* pairs) {
+    struct Entry {
+        const void* func;
+        int device;
+        size_t smem;
+        int pairs;
+    };
+    static std::mutex mu;
+    static Entry seen[64];
+    static int n_seen = 0;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_seen; ++i)
+        if (seen[i].func == func && seen[i].device == dev && seen[i].smem == smem) {
+            *pairs = seen[i].pairs;
+            return cudaSuccess;
+        }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 1024);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    err = cudaOccupancyMaxActiveClusters(&n, func, &cfg);
+    if (err != cudaSuccess) return err;
+    *pairs = n;
+    if (n_seen < 64) seen[n_seen++] = Entry{func, dev, smem, n};
+    return cudaSuccess;
+}
+
 static bool trace_enabled() {
     static int v = -1;
     if (v < 0) {

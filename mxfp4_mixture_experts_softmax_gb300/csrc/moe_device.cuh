@@ -136,6 +136,34 @@ __device__ __forceinline__ bool all_at_barrier(bool ok, int id, int nthreads) {
     return r != 0;
 }
 
+// ------------------------------------------------- CTA pairs (clusters of 2)
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster; orders the threads' earlier
+// shared-memory writes (barrier inits among them) before the other CTAs'
+// later accesses.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// Arrive on the mbarrier at the same shared-memory offset in CTA `rank` of
+// the cluster, with the arrive's default semantics (release at CTA scope): no
+// cluster-scope fence, which stalled every arriving warp for microseconds.
+// The data the arrival announces is either ordered by the tensor-core fences
+// around it (tensor-memory stores) or was itself announced to this thread by
+// an mbarrier phase (TMA writes).
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t* bar, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(rank));
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
 // Prefetch one 2D box of a tensor map into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int c0, int c1) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap),

@@ -34,6 +34,47 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
+// The same for MMAs issued with cta_group::2 by the pair's even CTA: arrives
+// on the mbarrier at this offset in each CTA of cta_mask (bit = rank in the
+// cluster; 3 = both CTAs of the pair).
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask = 3) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Tensor-memory allocation of `cols` columns (a power of two >= 32); the
+// address lands in *slot.  Pair form: one warp of each CTA of the pair
+// executes it, and both CTAs get the same columns.
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t cols) {
+    if (PAIR) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(slot)),
+                     "r"(cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(slot)),
+                     "r"(cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+    if (PAIR)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+                     : "memory");
+}
+
 // 16 consecutive 32-bit tensor-memory columns of this thread's lane (the
 // caller waits with tcgen05.wait::ld before using them).
 __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t* r) {
