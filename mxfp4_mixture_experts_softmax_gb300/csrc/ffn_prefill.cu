@@ -58,8 +58,6 @@ constexpr int kBK = 64;                                   // k per stage (one 12
 constexpr int kACols = kBK / 2;                           // tensor-memory columns of one A stage
 constexpr int kCodeBytes = 128 * (kBK / 2);               // 4 KB packed codes stage
 constexpr int kCodeBox = 64;                              // rows per codes box
-constexpr int kPrefetch = 12;                             // code stages prefetched into L2 ahead
-constexpr int kPairPrefetch = 12;                         // the same for the CTA-pair kernel
 
 // Instruction descriptor: f16 x f16 -> fp32 (a and b format fields 0), both
 // operands K-major, M x N.
@@ -182,7 +180,12 @@ struct PrefillSmem {
     // kAStages tensor-memory A slots (filled by the converters).  With two
     // blocks per item tensor memory holds only 4 A slots, but shared memory
     // holds 8 stages, so TMA runs further ahead than the conversion.
-    static constexpr int kStages = 8 * kStage <= 170 * 1024 ? 8 : 4;
+    // a pair's stages (half the B rows, no second block) are small enough
+    // for 16 slots at 128-row tiles: 2.77 -> 2.71 ms on the skewed 8192-token
+    // prefill; the A slots in tensor memory stay 8 (the rings decouple)
+    static constexpr int kStages = (PAIR && 16 * kStage <= 200 * 1024) ? 16
+                                   : 8 * kStage <= 170 * 1024       ? 8
+                                                                    : 4;
     static constexpr int kAStages = (kRB == 1 && N <= 128) ? 8 : 4;
     static_assert(kStages % 4 == 0 && kAStages % 4 == 0, "slot ownership");
     static_assert(kStages % kAStages == 0, "ring nesting");
@@ -278,20 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 crow[2 * j] = e * g.rows + (MODE == 0 ? block * 64 : block * 128);
                 crow[2 * j + 1] = MODE == 0 ? e * g.rows + g.I + block * 64 : crow[2 * j] + kCodeBox;
             }
-            if (lane == 0)  // the item's first stages into L2 before the ring asks for them
-                for (int st = 0; st < kPrefetch && st < nk; ++st) {
-#pragma unroll
-                    for (int c = 0; c < 2 * kRB; ++c) tma_prefetch_l2_2d(&codes_map, st * (kBK / 2), crow[c]);
-                    tma_prefetch_l2_2d(&act_map, st * kBK, tile * N);
-                }
+            // no L2 prefetches ahead of the ring (1536-token prefill: 1.62 -> 1.57 ms
+            // without them)
             for (int st = 0; st < nk; ++st, ++gs) {
                 const int s = gs % kStages;
-                if (lane == 0 && st + kPrefetch < nk) {
-#pragma unroll
-                    for (int c = 0; c < 2 * kRB; ++c)
-                        tma_prefetch_l2_2d(&codes_map, (st + kPrefetch) * (kBK / 2), crow[c]);
-                    tma_prefetch_l2_2d(&act_map, (st + kPrefetch) * kBK, tile * N);
-                }
                 // both slots of a pair come free with the pair's commit
                 if (gs >= kStages && (gs & 1) == 0 &&
                     !mbar_wait_warp(&stage_free[(gs >> 1) % kPairs], ((gs / kStages) - 1) & 1)) {
@@ -683,19 +676,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int crow0 = e * g.rows + (MODE == 0 ? block * 64 : block * 128);
             const int crow1 = MODE == 0 ? e * g.rows + g.I + block * 64 : crow0 + kCodeBox;
             const int brow = tile * N + rank * L::kBRows;
-            if (lane == 0)
-                for (int st = 0; st < kPairPrefetch && st < nk; ++st) {
-                    tma_prefetch_l2_2d(&codes_map, st * (kBK / 2), crow0);
-                    tma_prefetch_l2_2d(&codes_map, st * (kBK / 2), crow1);
-                    tma_prefetch_l2_2d(&act_map, st * kBK, brow);
-                }
+            // no L2 prefetches ahead of the ring: on the skewed 8192-token
+            // prefill they cost 11% of the layer (3.11 -> 2.77 ms without)
             for (int st = 0; st < nk; ++st, ++gs) {
                 const int s = gs % kStages;
-                if (lane == 0 && st + kPairPrefetch < nk) {
-                    tma_prefetch_l2_2d(&codes_map, (st + kPairPrefetch) * (kBK / 2), crow0);
-                    tma_prefetch_l2_2d(&codes_map, (st + kPairPrefetch) * (kBK / 2), crow1);
-                    tma_prefetch_l2_2d(&act_map, (st + kPairPrefetch) * kBK, brow);
-                }
                 if (gs >= kStages && (gs & 1) == 0 &&
                     !mbar_wait_warp(&stage_free[(gs >> 1) % kPairs], ((gs / kStages) - 1) & 1)) {
                     ok = false;
