@@ -620,12 +620,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kDecoupled = kAStages != kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    // The MMA thread waits once per pair of stages (on the converters) and
+    // releases slots once per group of four (stage_free, a_free): each
+    // commit costs the issuing thread about as much as two MMAs.
     constexpr int kPairs = kStages / 2, kAPairs = kAStages / 2;
+    constexpr int kGroups = kStages / 4, kAGroups = kAStages / 4;
+    static_assert(kStages % 4 == 0 && kAStages % 4 == 0, "groups of four stages");
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L::kBars);  // codes + B landed, per slot
     uint64_t* a_full = raw_full + kStages;      // A converted in both CTAs, per A pair (even CTA)
-    uint64_t* stage_free = a_full + kAPairs;    // MMAs done with a slot pair
-    uint64_t* a_free = stage_free + kPairs;     // MMAs done with an A pair
-    uint64_t* acc_full = a_free + kAPairs;      // [2] accumulator ready
+    uint64_t* stage_free = a_full + kAPairs;    // MMAs done with a group of four slots
+    uint64_t* a_free = stage_free + kGroups;    // MMAs done with a group of four A slots
+    uint64_t* acc_full = a_free + kAGroups;     // [2] accumulator ready
     uint64_t* acc_free = acc_full + 2;          // [2] drained by both CTAs (even CTA)
     uint64_t* drain = acc_free + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -637,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // clusters of 2 along x: the rank in the pair is the low bit of the CTA index
     const int rank = (int)(blockIdx.x & 1u);
     const int K = g.K;
-    const int nk = ((K + kBK - 1) / kBK + 1) & ~1;  // stages per item, whole pairs
+    const int nk = ((K + kBK - 1) / kBK + 3) & ~3;  // stages per item, whole groups of four
     const int row_blocks = MODE == 0 ? (g.I + 63) / 64 : (g.rows + 127) / 128;
     const int row_groups = row_blocks / 2;          // even (checked by the launcher)
     const int items = checked_tiles(g) * row_groups;
@@ -645,11 +650,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&raw_full[s], 1);
-        for (int p = 0; p < kPairs; ++p) mbar_init(&stage_free[p], 1);
-        for (int p = 0; p < kAPairs; ++p) {
+        for (int p = 0; p < kGroups; ++p) mbar_init(&stage_free[p], 1);
+        for (int p = 0; p < kAGroups; ++p) mbar_init(&a_free[p], 1);
+        for (int p = 0; p < kAPairs; ++p)
             mbar_init(&a_full[p], 8);  // per stage pair one converter warp per lane quadrant, both CTAs
-            mbar_init(&a_free[p], 1);
-        }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_free[b], 2 * kEpiWarps);
@@ -680,8 +684,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // prefill they cost 11% of the layer (3.11 -> 2.77 ms without)
             for (int st = 0; st < nk; ++st, ++gs) {
                 const int s = gs % kStages;
-                if (gs >= kStages && (gs & 1) == 0 &&
-                    !mbar_wait_warp(&stage_free[(gs >> 1) % kPairs], ((gs / kStages) - 1) & 1)) {
+                // four slots come free with their group's commit
+                if (gs >= kStages && (gs & 3) == 0 &&
+                    !mbar_wait_warp(&stage_free[(gs >> 2) % kGroups], ((gs / kStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -713,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + b * L::kAccCols;
                 for (int st = 0; st < nk; st += 2, gs += 2) {
-                    const int pr = (gs >> 1) % kPairs, pa = (gs >> 1) % kAPairs;
+                    const int pa = (gs >> 1) % kAPairs;
                     // both stages' A converted in both CTAs (the converters
                     // arrive after their stage's TMA barrier: B has landed)
                     if (!mbar_wait(&a_full[pa], (gs / kAStages) & 1)) {
@@ -731,8 +736,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_f16_ts_pair(d_tmem, a_tmem + 8u * k, bd + 2u * k, idesc,
                                             (st | h2 | k) != 0 ? 1u : 0u);
                     }
-                    mma_commit_pair(&stage_free[pr]);
-                    if (kDecoupled) mma_commit_pair(&a_free[pa]);
+                    if (gs & 2) {  // the group's second pair: release its four slots
+                        mma_commit_pair(&stage_free[(gs >> 2) % kGroups]);
+                        if (kDecoupled) mma_commit_pair(&a_free[(gs >> 2) % kAGroups]);
+                    }
                 }
                 if (ok) mma_commit_pair(&acc_full[b]);
                 ++it;
@@ -801,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t scv = sc;
                 if (p + kParts < np) sc = scales4(p + kParts);
                 if (kDecoupled && g0 >= (uint32_t)kAStages &&
-                    !mbar_wait_warp(&a_free[(g0 >> 1) % kAPairs], ((g0 / kAStages) - 1) & 1)) {
+                    !mbar_wait_warp(&a_free[(g0 >> 2) % kAGroups], ((g0 / kAStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
