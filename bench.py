@@ -348,10 +348,10 @@ class Layer:
                                                                      tm, dev)
         self.stream = torch.cuda.current_stream(dev)
 
-    def step(self, i, ev=None, gemm_ev=None):
+    def step(self, i, ev=None, kern_ev=None):
         """One pass of the layer.  ev: events between all calls (breakdown);
-        gemm_ev: events only around the two GEMM steps, so the programmatic
-        launches still overlap at the other kernel boundaries."""
+        kern_ev: four events the library records around the gate_up and the
+        down GEMM kernel launches themselves (moe_set_gemm_events)."""
         from mxfp4_mixture_experts_softmax_gb300 import libmoe
         w, b, r = self.w, self.bufs, i % self.R
         W = self.weights[r]
@@ -363,8 +363,8 @@ class Layer:
                                                b["perm"])
         if ev is not None:
             ev[1].record(self.stream)
-        if gemm_ev is not None:
-            gemm_ev[0].record(self.stream)
+        if kern_ev is not None:
+            libmoe.moe_set_gemm_events(kern_ev[0], kern_ev[1])
         if self.mx:
             libmoe.moe_ffn_mxfp4act_gate_up(self.xs[r], W["w13"], W["s13"], perm, b["workspace"])
         else:
@@ -372,8 +372,8 @@ class Layer:
                                    self.path)
         if ev is not None:
             ev[2].record(self.stream)
-        if gemm_ev is not None:
-            gemm_ev[1].record(self.stream)
+        if kern_ev is not None:
+            libmoe.moe_set_gemm_events(kern_ev[2], kern_ev[3])
         if self.mx:  # down GEMM and the combine into out
             libmoe.moe_ffn_mxfp4act_down(W["w2"], W["s2"], tw, perm, b["workspace"], w.T, b["out"])
         else:
@@ -381,16 +381,23 @@ class Layer:
                                         self.path)
         if ev is not None:
             ev[3].record(self.stream)
-        if gemm_ev is not None:
-            gemm_ev[2].record(self.stream)
+        if kern_ev is not None:
+            libmoe.moe_set_gemm_events(None, None)
 
-    def timed(self, steps: int, gpu_index: int, ws: int = 1):
+    def timed(self, steps: int, gpu_index: int, ws: int = 1, kernel_events: bool = True):
         """Exactly `steps` steps between two events, barrier + synchronize on
         both sides, clocks sampled during the region; returns the region's
-        milliseconds, the mean GEMM-step times and the clock record."""
+        milliseconds, the mean GEMM kernel times (kernel_events: the library
+        records a pair of events around each of the two GEMM kernel launches
+        of every step, on the launching stream; otherwise nothing is recorded
+        inside the region) and the clock record."""
         import torch
         dev = self.dev
-        gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        if kernel_events:
+            for kv in kevs:  # created before the region (torch creates events on first record)
+                for e in kv:
+                    e.record(self.stream)
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         sampler = ClockSampler(gpu_id_for(gpu_index))
         if ws > 1:
@@ -398,14 +405,16 @@ class Layer:
         torch.cuda.synchronize(dev)
         t0.record(self.stream)
         for i in range(steps):
-            self.step(i, gemm_ev=gevs[i])
+            self.step(i, kern_ev=kevs[i] if kernel_events else None)
         t1.record(self.stream)
         torch.cuda.synchronize(dev)
         if ws > 1:
             torch.distributed.barrier()
         clocks = sampler.stop()
-        gemm = {"gate_up": statistics.mean(g[0].elapsed_time(g[1]) for g in gevs),
-                "down": statistics.mean(g[1].elapsed_time(g[2]) for g in gevs)}
+        gemm = {}
+        if kernel_events:
+            gemm = {"gate_up_gemm": statistics.mean(k[0].elapsed_time(k[1]) for k in kevs),
+                    "down_gemm": statistics.mean(k[2].elapsed_time(k[3]) for k in kevs)}
         return t0.elapsed_time(t1), gemm, clocks
 
     def breakdown(self, n: int = 10) -> dict:
@@ -415,7 +424,7 @@ class Layer:
         for i in range(n):
             self.step(i, ev=evs[i])
         torch.cuda.synchronize(self.dev)
-        names = ["route_permute", "gate_up", "down_combine"]
+        names = ["route_permute", "gate_up", "down"]
         return {nm: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
                 for j, nm in enumerate(names)}
 
@@ -462,21 +471,33 @@ class Layer:
             raise RuntimeError(f"non-finite layer output on {self.w.name}")
 
     def rooflines(self, work, gemm_ms: dict, total_ms: float, steps: int):
-        """gate_up, down + combine and the whole step against their binding roofline."""
+        """The gate_up and down GEMM kernels (each timed alone by the events
+        the library records around its launch), the gate_up and down +
+        combine steps (every launch of each call) and the whole step, each
+        against its binding roofline.  The work is the algorithmic work of the
+        step either way: the steps' other launches (f16 row copies, the
+        combine) add no algorithmic bytes."""
         src = {"prefill": "ffn_prefill.cu", "decode": "ffn_decode.cu",
                "mxfp4act": "ffn_mxfp4act.cu"}[self.path_name]
         traffic, traffic_src = traffic_from_profiles(
             f"{self.path_name}_gate_up", self.w.name,
             os.path.join(ROOT, "mxfp4_mixture_experts_softmax_gb300", "csrc", src))
-        gu = roofline_entry(f"{self.path_name}_gate_up", work["gate_up_bytes"],
-                            work["gate_up_flops"], gemm_ms["gate_up"] / 1e3, traffic, traffic_src,
-                            fp4=self.mx)
-        dn = roofline_entry(f"{self.path_name}_down_combine", work["down_bytes"],
-                            work["flops"] - work["gate_up_flops"], gemm_ms["down"] / 1e3, None,
-                            None, fp4=self.mx)
+        down_flops = work["flops"] - work["gate_up_flops"]
+        gu = roofline_entry(f"{self.path_name}_gate_up_gemm", work["gate_up_bytes"],
+                            work["gate_up_flops"], gemm_ms["gate_up_gemm"] / 1e3, traffic,
+                            traffic_src, fp4=self.mx)
+        dn = roofline_entry(f"{self.path_name}_down_gemm", work["down_bytes"], down_flops,
+                            gemm_ms["down_gemm"] / 1e3, None, None, fp4=self.mx)
+        steps_rl = {
+            "gate_up_step": roofline_entry(f"{self.path_name}_gate_up_step", work["gate_up_bytes"],
+                                           work["gate_up_flops"], gemm_ms["gate_up"] / 1e3, None,
+                                           None, fp4=self.mx),
+            "down_combine_step": roofline_entry(f"{self.path_name}_down_combine_step",
+                                                work["down_bytes"], down_flops,
+                                                gemm_ms["down"] / 1e3, None, None, fp4=self.mx)}
         layer = roofline_entry("layer", work["layer_bytes"], work["flops"], total_ms / steps / 1e3,
                                None, None, fp4=self.mx)
-        return gu, dn, layer
+        return gu, dn, layer, steps_rl
 
     def free(self):
         import torch
@@ -485,12 +506,12 @@ class Layer:
 
 
 def config_entry(lay, total_ms, steps, gemm, clocks, per, work):
-    gu, dn, layer = lay.rooflines(work, gemm, total_ms, steps)
+    gu, dn, layer, steps_rl = lay.rooflines(work, gemm, total_ms, steps)
     return {"workload": lay.w.name, "T": lay.w.T, "tile_m": lay.tm, "path": lay.path_name,
             "steps": steps, "timed_s": total_ms / 1e3, "ms_per_step": total_ms / steps,
             "tokens_per_s": lay.w.T * steps / (total_ms / 1e3),
             "experts_touched": work["touched"], "roofline": layer,
-            "gate_up": gu, "down_combine": dn,
+            "gate_up_gemm": gu, "down_gemm": dn, **steps_rl,
             "kernels_us": {n: v * 1e3 for n, v in {**per, **gemm}.items()}, "clocks": clocks}
 
 
@@ -507,12 +528,16 @@ def measure_per_config(args, local, dev, skip=()):
         for i in range(3):
             lay.step(i)
         torch.cuda.synchronize(dev)
-        ms, _, _ = lay.timed(5, local)
+        ms, _, _ = lay.timed(5, local, kernel_events=False)
         steps = int(min(20000, max(20, -(-args.config_seconds * 1e3 // (ms / 5)))))
         ids_host = lay.bufs["topk_ids"].cpu().numpy()
         work = layer_work(w, ids_host, args.act)
-        total_ms, gemm, clocks = lay.timed(steps, local)
+        # throughput over a region with nothing recorded inside it; the GEMM
+        # kernel times over a second, shorter region with the kernel events
+        total_ms, _, clocks = lay.timed(steps, local, kernel_events=False)
+        _, gemm, _ = lay.timed(max(20, steps // 4), local, kernel_events=True)
         per = lay.breakdown()
+        gemm.update(per)
         lay.check_output()
         out[name] = config_entry(lay, total_ms, steps, gemm, clocks, per, work)
         lay.free()
@@ -545,6 +570,7 @@ def run_ours(args, ws, rank, local):
     K = args.steps
     total_ms, gemm, clocks = lay.timed(K, local, ws)
     per = lay.breakdown(min(K, 10))
+    gemm.update(per)  # the gate_up and down steps (every launch of each call)
     lay.check_output()
     e2e_ms = lay.e2e(K, args.warmup)
     if ws > 1:
@@ -552,7 +578,7 @@ def run_ours(args, ws, rank, local):
 
     result = None
     if rank == 0:
-        gu, dn, layer = lay.rooflines(work, gemm, total_ms, K)
+        gu, dn, layer, steps_rl = lay.rooflines(work, gemm, total_ms, K)
         result = {
             "metric": METRIC,
             "value": weak_scaling_value(w.T, K, ws, total_ms),
@@ -575,6 +601,7 @@ def run_ours(args, ws, rank, local):
             },
             "roofline": gu,
             "roofline_down": dn,
+            "roofline_steps": steps_rl,
             "layer_roofline": layer,
             "kernels_us": {n: v * 1e3 for n, v in {**per, **gemm}.items()},
             "e2e": {"value": w.T * K * ws / (e2e_ms / 1e3), "unit": "tokens/s",

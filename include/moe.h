@@ -335,6 +335,20 @@ moe_status_t moe_device_error(int* flag, int clear);
 moe_status_t moe_selftest_wait_timeout(int limit_us, cudaStream_t stream);
 
 /*
+ * moe_set_gemm_events -- profiling hook: from this call on (process-wide,
+ * until changed), every FFN call (moe_ffn*, moe_ffn_gate_up, moe_ffn_down,
+ * moe_ffn_down_combine, moe_ffn_mxfp4act*) records `before` on its stream
+ * right before launching its grouped GEMM kernel and `after` right after,
+ * so cudaEventElapsedTime(before, after) is that kernel's duration (each call
+ * re-records the pair; set a fresh pair per call to time several).  Both
+ * events are caller-created CUDA events of the current device; pass two
+ * nulls to switch the hook off.  MOE_ERR_INVALID_ARG when only one is null.
+ * A failed record returns MOE_ERR_CUDA from the FFN call.  The pages have no
+ * counterpart.
+ */
+moe_status_t moe_set_gemm_events(cudaEvent_t before, cudaEvent_t after);
+
+/*
  * moe_selftest_wait_split -- diagnostic: one block of two warps whose bounded
  * waits end differently.  Warp 0 waits on an mbarrier nothing arrives at
  * (limit_us microseconds, 1..10^6), warp 1 on one that has already

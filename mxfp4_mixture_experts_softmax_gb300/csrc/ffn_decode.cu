@@ -393,27 +393,12 @@ __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* src, u
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    int sigma = 0;
-    if (mx != 0) {
-        // floor(log2) of a bf16 magnitude: its exponent field, or for a
-        // subnormal the position of its top mantissa bit
-        const int ef = (int)(mx >> 7);
-        const int e = ef > 0 ? ef - 127 : (31 - __clz((int)mx)) - 133;
-        sigma = min(max(14 - e, -113), 112);
-    }
+    const int sigma = row_f16_shift(mx);
     const float up = __uint_as_float((uint32_t)(127 + sigma) << 23);
     for (int i = lane; i < n16; i += 32) {
         const uint4 v = s4[i];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float lo = __uint_as_float(w[k] << 16) * up;
-            const float hi = __uint_as_float(w[k] & 0xFFFF0000u) * up;
-            const __half2 hv = __floats2half2_rn(lo, hi);
-            o[k] = *reinterpret_cast<const uint32_t*>(&hv);
-        }
-        d4[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        d4[i] = make_uint4(bf16x2_to_f16x2_scaled(v.x, up), bf16x2_to_f16x2_scaled(v.y, up),
+                           bf16x2_to_f16x2_scaled(v.z, up), bf16x2_to_f16x2_scaled(v.w, up));
     }
     if (lane == 0) rscale[row] = __uint_as_float((uint32_t)(127 - sigma) << 23);
     pdl_end();

@@ -12,7 +12,7 @@
 //   * producer warp: 2D TMA loads of the block's packed codes (64 k per
 //     stage, prefetched into L2 ahead of the ring) and of the tile's token
 //     rows as one box in the 128-byte swizzled K-major layout the MMA reads
-//     (gate_up reads x gathered into tile order by gather_rows_kernel, down
+//     (gate_up reads x gathered into tile order by gather_rows_f16_kernel, down
 //     reads h, which is already in tile order); both are f16 rows scaled per
 //     row by a power of two (rows_to_f16_kernel), the factor undone in the
 //     epilogue;
@@ -940,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float fc = __shfl_sync(0xFFFFFFFFu, c_lo, j & 31);
                         if (n < g.I && q >= 0)
                             g.h_out[(size_t)(tile * N + j) * g.I + n] =
-                                f32_to_bf16_bits(silu(gate * fc) * (up * fc));
+                                f32_to_bf16_bits(silu_fast(gate * fc) * (up * fc));
                     }
                 } else if (g.y_blocked) {
                     const int m = block * 128 + r;
@@ -1047,27 +1047,78 @@ cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
     }
 }
 
-// xg[p] = x[token of sorted position p] for the rows of the used tiles, zero
-// for padding; one block per row (grid-stride over rows), 16 bytes per thread.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int H8,
-                                                          const int32_t* __restrict__ sorted_pairs,
-                                                          const int32_t* __restrict__ num_tiles,
-                                                          int tile_m, int Kt, int cap, int num_pairs,
-                                                          uint4* __restrict__ xg) {
+// xg[p] = f16(x[t] * 2^sigma_t), t the token of sorted position p's pair, for
+// the rows of the used tiles (zero rows for padding), and rscale[t] =
+// 2^-sigma_t: rows_to_f16_kernel's conversion of x applied while gathering
+// into tile order, so x never exists as a separate f16 copy.  One warp per
+// position (grid-stride).  Rows of up to 32 * NPL 16-byte pieces stay in
+// registers (one pass over the token's bf16 row, read from L2); longer rows
+// (NPL = 0) take a pass for the largest magnitude and one to convert.  Every
+// position of a token writes the same rscale value.
+template <int NPL>
+__global__ void __launch_bounds__(256) gather_rows_f16_kernel(const uint4* __restrict__ x, int H8,
+                                                              const int32_t* __restrict__ sorted_pairs,
+                                                              const int32_t* __restrict__ num_tiles,
+                                                              int tile_m, int Kt, int cap, int num_pairs,
+                                                              uint4* __restrict__ xg,
+                                                              float* __restrict__ rscale) {
     pdl_begin();
     const int rows = min(max(__ldg(num_tiles), 0) * tile_m, cap);  // clamped like checked_tiles
-    for (int p = blockIdx.x; p < rows; p += gridDim.x) {
+    const int lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
+    for (int p = blockIdx.x * wpb + (threadIdx.x >> 5); p < rows; p += gridDim.x * wpb) {
         int q = __ldg(sorted_pairs + p);
         if (q >= num_pairs) {
-            if (threadIdx.x == 0) flag_index_error();
+            if (lane == 0) flag_index_error();
             q = -1;
         }
         uint4* dst = xg + (size_t)p * H8;
         if (q < 0) {
-            for (int c = threadIdx.x; c < H8; c += blockDim.x) dst[c] = make_uint4(0, 0, 0, 0);
+            for (int c = lane; c < H8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+            continue;
+        }
+        const int t = q / Kt;
+        const uint4* src = x + (size_t)t * H8;
+        uint32_t mx = 0;  // max |bf16| bit pattern (orders like the magnitude)
+        auto row_max = [&](const uint4& v) {
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+        };
+        if constexpr (NPL > 0) {
+            uint4 v[NPL];
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) {
+                const int c = lane + 32 * i;
+                v[i] = c < H8 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) row_max(v[i]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+            const int sigma = row_f16_shift(mx);
+            const float up = __uint_as_float((uint32_t)(127 + sigma) << 23);
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) {
+                const int c = lane + 32 * i;
+                if (c < H8)
+                    dst[c] = make_uint4(bf16x2_to_f16x2_scaled(v[i].x, up), bf16x2_to_f16x2_scaled(v[i].y, up),
+                                        bf16x2_to_f16x2_scaled(v[i].z, up), bf16x2_to_f16x2_scaled(v[i].w, up));
+            }
+            if (lane == 0) rscale[t] = __uint_as_float((uint32_t)(127 - sigma) << 23);
         } else {
-            const uint4* src = x + (size_t)(q / Kt) * H8;
-            for (int c = threadIdx.x; c < H8; c += blockDim.x) dst[c] = __ldg(src + c);
+#pragma unroll 4
+            for (int c = lane; c < H8; c += 32) row_max(__ldg(src + c));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+            const int sigma = row_f16_shift(mx);
+            const float up = __uint_as_float((uint32_t)(127 + sigma) << 23);
+#pragma unroll 4
+            for (int c = lane; c < H8; c += 32) {
+                const uint4 v = __ldg(src + c);
+                dst[c] = make_uint4(bf16x2_to_f16x2_scaled(v.x, up), bf16x2_to_f16x2_scaled(v.y, up),
+                                    bf16x2_to_f16x2_scaled(v.z, up), bf16x2_to_f16x2_scaled(v.w, up));
+            }
+            if (lane == 0) rscale[t] = __uint_as_float((uint32_t)(127 - sigma) << 23);
         }
     }
     pdl_end();
@@ -1075,14 +1126,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 
 }  // namespace
 
-cudaError_t launch_gather_rows(const uint16_t* x, int H, const int32_t* sorted_pairs,
-                               const int32_t* num_tiles, int tile_m, int Kt, int cap, int num_pairs,
-                               uint16_t* xg, cudaStream_t s) {
+cudaError_t launch_gather_rows_f16(const uint16_t* x, int H, const int32_t* sorted_pairs,
+                                   const int32_t* num_tiles, int tile_m, int Kt, int cap,
+                                   int num_pairs, uint16_t* xg, float* rscale, cudaStream_t s) {
     if (cap <= 0) return cudaSuccess;
-    const int blocks = std::min(cap, num_sms() * 16);
-    return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s,
-                      reinterpret_cast<const uint4*>(x), H / 8, sorted_pairs, num_tiles, tile_m,
-                      Kt, cap, num_pairs, reinterpret_cast<uint4*>(xg));
+    const int blocks = std::min((cap + 7) / 8, num_sms() * 8);
+    // rows of up to 4096 values in registers (16 pieces of 16 bytes per lane)
+    auto kernel = H / 8 <= 32 * 16 ? gather_rows_f16_kernel<16> : gather_rows_f16_kernel<0>;
+    return launch_pdl(kernel, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const uint4*>(x),
+                      H / 8, sorted_pairs, num_tiles, tile_m, Kt, cap, num_pairs,
+                      reinterpret_cast<uint4*>(xg), rscale);
 }
 
 bool prefill_tile_supported(int tile_m) {

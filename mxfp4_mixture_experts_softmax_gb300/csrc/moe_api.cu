@@ -143,6 +143,26 @@ static bool trace_enabled() {
 
 static moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Profiling hook (moe_set_gemm_events): events recorded on the caller's stream
+// right before and right after the GEMM kernel launch of each FFN call.
+static std::mutex g_gemm_ev_mu;
+static cudaEvent_t g_gemm_ev_before = nullptr, g_gemm_ev_after = nullptr;
+
+template <typename F>
+static cudaError_t launch_gemm_timed(F launch, cudaStream_t stream) {
+    cudaEvent_t before, after;
+    {
+        std::lock_guard<std::mutex> lock(g_gemm_ev_mu);
+        before = g_gemm_ev_before;
+        after = g_gemm_ev_after;
+    }
+    cudaError_t err = before ? cudaEventRecord(before, stream) : cudaSuccess;
+    if (err != cudaSuccess) return err;
+    err = launch();
+    if (err == cudaSuccess && after) err = cudaEventRecord(after, stream);
+    return err;
+}
+
 static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -181,6 +201,14 @@ moe_status_t moe_device_error(int* flag, int clear) {
     if (err == cudaSuccess) err = read_device_error_mxfp4act(&c, clear);
     *flag = a | b | c;
     return cuda_status(err);
+}
+
+moe_status_t moe_set_gemm_events(cudaEvent_t before, cudaEvent_t after) {
+    if ((before == nullptr) != (after == nullptr)) return MOE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_gemm_ev_mu);
+    g_gemm_ev_before = before;
+    g_gemm_ev_after = after;
+    return MOE_OK;
 }
 
 moe_status_t moe_selftest_wait_timeout(int limit_us, cudaStream_t stream) {
@@ -416,25 +444,26 @@ moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_
     char* ws = reinterpret_cast<char*>(workspace);
     uint16_t* x16 = reinterpret_cast<uint16_t*>(ws + x16_offset(cap, T, H, I, Kt, tile_m));
     float* rs_x = reinterpret_cast<float*>(ws + rs_offset(cap, T, H, I, Kt, tile_m));
-    cudaError_t err = launch_rows_to_f16(x, x16, H, T, nullptr, nullptr, tile_m, rs_x, stream);
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
     g.act_rscale = rs_x;  // indexed by token
+    cudaError_t err;
     if (path == MOE_PATH_DECODE) {
+        err = launch_rows_to_f16(x, x16, H, T, nullptr, nullptr, tile_m, rs_x, stream);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
         g.act = x16;
         g.act_rows = T;
         g.act_by_token = 1;
-        err = launch_decode_gate_up(g, stream);
+        err = launch_gemm_timed([&] { return launch_decode_gate_up(g, stream); }, stream);
     } else {
         // the prefill GEMM reads its token rows as one box per stage: gather
-        // them into tile order first
+        // them into tile order, converted to scaled f16 on the way
         uint16_t* xg = reinterpret_cast<uint16_t*>(ws + xg_offset(cap, T, H, I, Kt, tile_m));
-        err = launch_gather_rows(x16, H, sorted_pairs, num_tiles, tile_m, Kt, (int)cap, T * Kt, xg,
-                                 stream);
+        err = launch_gather_rows_f16(x, H, sorted_pairs, num_tiles, tile_m, Kt, (int)cap, T * Kt, xg,
+                                     rs_x, stream);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         g.act = xg;
         g.act_rows = (int)cap;
         g.act_by_token = 0;
-        err = launch_prefill_gate_up(g, stream);
+        err = launch_gemm_timed([&] { return launch_prefill_gate_up(g, stream); }, stream);
     }
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     err = launch_rows_to_f16(g.h_out, g.h_out, I, (int)cap, sorted_pairs, num_tiles, tile_m,
@@ -467,8 +496,9 @@ moe_status_t moe_ffn_down(const uint8_t* w2, const uint8_t* s2, const float* top
     g.act_by_token = 0;
     g.y_out = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + y_offset(cap, I));
     g.topk_w = topk_w;
-    cudaError_t err = path == MOE_PATH_DECODE ? launch_decode_down(g, stream)
-                                               : launch_prefill_down(g, stream);
+    cudaError_t err = launch_gemm_timed(
+        [&] { return path == MOE_PATH_DECODE ? launch_decode_down(g, stream) : launch_prefill_down(g, stream); },
+        stream);
     return cuda_status(err);
 }
 
@@ -515,7 +545,7 @@ moe_status_t moe_ffn_down_combine(const uint8_t* w2, const uint8_t* s2, const fl
     g.y_out = y;
     g.y_blocked = 1;
     g.topk_w = topk_w;
-    err = launch_prefill_down(g, stream);
+    err = launch_gemm_timed([&] { return launch_prefill_down(g, stream); }, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     return cuda_status(launch_combine_blocked(y, inv_pairs, w_pos, T, H, Kt, (int)cap, out, stream));
 }
@@ -746,7 +776,7 @@ moe_status_t moe_ffn_mxfp4act_gate_up(const uint16_t* x, const uint8_t* w13, con
     g.hq_codes = reinterpret_cast<uint8_t*>(ws + L.hc);
     g.hq_scales = reinterpret_cast<uint8_t*>(ws + L.hs);
     trace("moe_ffn_mxfp4act_gate_up", T, H, I, Et, Kt, tile_m, MOE_PATH_PREFILL);
-    return cuda_status(launch_mxfp4act_gate_up(g, stream));
+    return cuda_status(launch_gemm_timed([&] { return launch_mxfp4act_gate_up(g, stream); }, stream));
 }
 
 moe_status_t moe_ffn_mxfp4act_down(const uint8_t* w2, const uint8_t* s2, const float* topk_w,
@@ -781,7 +811,7 @@ moe_status_t moe_ffn_mxfp4act_down(const uint8_t* w2, const uint8_t* s2, const f
     cudaError_t err = launch_position_weights(sorted_pairs, topk_w, nullptr, num_tiles, tile_m,
                                               (int)cap, T * Kt, w_pos, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    err = launch_mxfp4act_down(g, stream);
+    err = launch_gemm_timed([&] { return launch_mxfp4act_down(g, stream); }, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     return cuda_status(launch_combine_blocked(g.y_out, inv_pairs, w_pos, T, H, Kt, (int)cap, out,
                                               stream));

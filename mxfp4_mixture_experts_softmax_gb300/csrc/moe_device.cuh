@@ -38,9 +38,40 @@ __device__ __forceinline__ void pdl_end() {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// silu with the fast exponential and division: a few fp32 ulp from silu(),
+// so a product rounded to bf16 afterwards differs from the correctly rounded
+// one only where it lies within those ulps of a bf16 rounding boundary (one
+// bf16 ulp then).  For g below about -88 the exponential overflows and the
+// quotient is 0, as silu's limit is.
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
     __nv_bfloat16 b = __float2bfloat16_rn(f);
     return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// ------------------------------------------- bf16 rows as scaled f16 rows
+
+// The power-of-two shift sigma that moves a bf16 row's largest magnitude into
+// [2^14, 2^15), from the largest |bf16| bit pattern mx of the row (0 for an
+// all-zero row), clamped to [-113, 112].  bf16 has fewer significant bits
+// than f16, so every element that stays in the f16 normal range converts
+// exactly.
+__device__ __forceinline__ int row_f16_shift(uint32_t mx) {
+    if (mx == 0) return 0;
+    // floor(log2) of a bf16 magnitude: its exponent field, or for a subnormal
+    // the position of its top mantissa bit
+    const int ef = (int)(mx >> 7);
+    const int e = ef > 0 ? ef - 127 : (31 - __clz((int)mx)) - 133;
+    return min(max(14 - e, -113), 112);
+}
+
+// Two bf16 (low half first) times `up` (= 2^sigma) as an f16x2.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float up) {
+    const float lo = __uint_as_float(w << 16) * up;
+    const float hi = __uint_as_float(w & 0xFFFF0000u) * up;
+    const __half2 hv = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&hv);
 }
 
 // ------------------------------------------------ async copies, mbarriers

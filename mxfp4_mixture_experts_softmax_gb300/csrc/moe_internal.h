@@ -142,10 +142,12 @@ cudaError_t launch_rows_to_f16(const uint16_t* src, uint16_t* dst, int cols, int
                                float* rscale, cudaStream_t s);
 cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_prefill_gate_up(const GroupedGemm& g, cudaStream_t s);
-// xg[p] = x[sorted_pairs[p] / Kt] for the rows of the used tiles (0 for pads).
-cudaError_t launch_gather_rows(const uint16_t* x, int H, const int32_t* sorted_pairs,
-                               const int32_t* num_tiles, int tile_m, int Kt, int cap, int num_pairs,
-                               uint16_t* xg, cudaStream_t s);
+// xg[p] = f16(x[t] * 2^sigma_t), t = sorted_pairs[p] / Kt, for the rows of
+// the used tiles (0 for pads), rscale[t] = 2^-sigma_t (the conversion of
+// launch_rows_to_f16, applied while gathering x (bf16) into tile order)
+cudaError_t launch_gather_rows_f16(const uint16_t* x, int H, const int32_t* sorted_pairs,
+                                   const int32_t* num_tiles, int tile_m, int Kt, int cap,
+                                   int num_pairs, uint16_t* xg, float* rscale, cudaStream_t s);
 cudaError_t launch_prefill_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t read_device_error_prefill(int* flag, int clear);
 // one block waiting on a barrier that never completes, for limit_ns

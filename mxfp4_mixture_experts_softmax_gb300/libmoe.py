@@ -30,7 +30,8 @@ EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_route_ex", "moe
            "moe_ffn_path", "moe_ffn_auto_path", "moe_ffn_gate_up", "moe_ffn_down", "moe_combine",
            "moe_ffn_y_offset", "moe_device_error", "moe_ffn_noalloc", "moe_combine_ex",
            "moe_ffn_dense_shared_workspace_size", "moe_ffn_dense_shared",
-           "moe_selftest_wait_timeout", "moe_selftest_wait_split", "moe_quantize_mxfp4", "moe_ffn_mxfp4act_workspace_size",
+           "moe_selftest_wait_timeout", "moe_selftest_wait_split", "moe_set_gemm_events",
+           "moe_quantize_mxfp4", "moe_ffn_mxfp4act_workspace_size",
            "moe_ffn_mxfp4act", "moe_ffn_mxfp4act_gate_up", "moe_ffn_mxfp4act_down",
            "moe_ffn_mxfp4act_h_offsets", "moe_ffn_down_combine")
 
@@ -110,6 +111,8 @@ def load(build: bool = True):
         L.moe_selftest_wait_timeout.restype = ci
         L.moe_selftest_wait_split.argtypes = [ci, vp, vp]
         L.moe_selftest_wait_split.restype = ci
+        L.moe_set_gemm_events.argtypes = [vp, vp]
+        L.moe_set_gemm_events.restype = ci
         L.moe_ffn_down_combine.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp,
                                            sz, ci, vp]
         L.moe_ffn_down_combine.restype = ci
@@ -291,6 +294,22 @@ def moe_selftest_wait_timeout(limit_us: int = 2000, stream=None):
     """Diagnostic: a bounded wait that runs out (include/moe.h)."""
     _check(load().moe_selftest_wait_timeout(int(limit_us), _stream(stream)),
            "moe_selftest_wait_timeout")
+
+
+def moe_set_gemm_events(before=None, after=None):
+    """Profiling hook (include/moe.h): record the torch.cuda.Event pair around
+    the grouped GEMM kernel of each following FFN call; None, None switches it
+    off.  The events are created here if they have not been recorded yet."""
+    import torch
+    handles = []
+    for ev in (before, after):
+        if ev is None:
+            handles.append(None)
+            continue
+        if ev.cuda_event == 0:  # torch creates an event lazily, on its first record
+            ev.record(torch.cuda.current_stream())
+        handles.append(ctypes.c_void_p(ev.cuda_event))
+    _check(load().moe_set_gemm_events(*handles), "moe_set_gemm_events")
 
 
 def moe_selftest_wait_split(limit_us: int = 2000, stream=None):

@@ -123,3 +123,12 @@ def test_bf16_workspace_holds_blocked_y_for_prefill_tiles(lib):
         y_off = m.moe_ffn_y_offset(T, I, Et, Kt, tm)
         assert y_off % 256 == 0 and y_off >= cap * I * 2
         assert ws >= y_off + cap * H * 4
+
+
+def test_gemm_events_hook_argument_rule(lib):
+    """moe_set_gemm_events takes both events or neither (host-side check only)."""
+    from mxfp4_mixture_experts_softmax_gb300 import libmoe as m
+    nul, fake = ctypes.c_void_p(0), ctypes.c_void_p(0x1000)
+    assert lib.moe_set_gemm_events(fake, nul) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_gemm_events(nul, fake) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_gemm_events(nul, nul) == m.MOE_OK

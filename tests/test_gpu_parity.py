@@ -367,6 +367,37 @@ def test_ffn_full_size(name):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("path,tile_m", [(libmoe.MOE_PATH_DECODE, 8), (libmoe.MOE_PATH_PREFILL, 128)])
+def test_gemm_events_bracket_the_gemm_kernel(path, tile_m):
+    """The profiling hook records its events around the GEMM kernel alone: the
+    interval is positive and shorter than the whole call's; switched off, the
+    events are not recorded again and the result is unchanged."""
+    w = synth.scaled(synth.WORKLOADS["tiny16"], T=300, H=512, I=256, E=16, K=4, with_shared=True,
+                     seed=17)
+    d, ids, wt = _layer_inputs(w)
+    dw = gc.upload_weights(d)
+    x, wt_d = gc.to_dev(d["x"]), gc.to_dev(wt)
+    perm = libmoe.moe_permute(gc.to_dev(ids), w.Et, tile_m)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev[0].record()
+    libmoe.moe_set_gemm_events(ev[1], ev[2])
+    try:
+        out = libmoe.moe_ffn_gate_up(x, dw["w13"], dw["s13"], perm,
+                                     libmoe.alloc_workspace(w.T, w.H, w.I, w.Et, w.Kt, tile_m), path)
+    finally:
+        libmoe.moe_set_gemm_events(None, None)
+    ev[3].record()
+    torch.cuda.synchronize()
+    gemm_ms, call_ms = ev[1].elapsed_time(ev[2]), ev[0].elapsed_time(ev[3])
+    assert 0.0 < gemm_ms < call_ms
+    before = ev[2].elapsed_time(ev[3])
+    ref = libmoe.moe_ffn(x, dw["w13"], dw["s13"], dw["w2"], dw["s2"], wt_d, perm, path=path)
+    torch.cuda.synchronize()
+    assert ev[2].elapsed_time(ev[3]) == before  # not re-recorded once switched off
+    gc.ffn_parity(gc.bf16_dev_to_f64(ref), gc.bits_to_f64(
+        oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt)), "after the hook")
+
+
 def test_layer_graph_capture_replays_identically():
     w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL["ragged37"])
     d = synth.make_inputs(w)
