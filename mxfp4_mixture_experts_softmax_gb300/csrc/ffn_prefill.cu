@@ -652,8 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) mbar_init(&raw_full[s], 1);
         for (int p = 0; p < kGroups; ++p) mbar_init(&stage_free[p], 1);
         for (int p = 0; p < kAGroups; ++p) mbar_init(&a_free[p], 1);
-        for (int p = 0; p < kAPairs; ++p)
-            mbar_init(&a_full[p], 8);  // per stage pair one converter warp per lane quadrant, both CTAs
+        for (int p = 0; p < kAGroups; ++p)
+            mbar_init(&a_full[p], 16);  // per stage pair one converter warp per lane quadrant: 2 pairs, 2 CTAs
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_free[b], 2 * kEpiWarps);
@@ -717,17 +717,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it >= (uint32_t)kAccBufs && !mbar_wait(&acc_free[b], ((it / kAccBufs) - 1) & 1)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + b * L::kAccCols;
-                for (int st = 0; st < nk; st += 2, gs += 2) {
-                    const int pa = (gs >> 1) % kAPairs;
-                    // both stages' A converted in both CTAs (the converters
-                    // arrive after their stage's TMA barrier: B has landed)
-                    if (!mbar_wait(&a_full[pa], (gs / kAStages) & 1)) {
+                for (int st = 0; st < nk; st += 4, gs += 4) {
+                    // the group's four stages converted in both CTAs (the
+                    // converters arrive after their stage's TMA barrier: B has
+                    // landed)
+                    if (!mbar_wait(&a_full[(gs >> 2) % kAGroups], (gs / kAStages) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
+                    for (int h2 = 0; h2 < 4; ++h2) {
                         const int s = (gs + h2) % kStages, sa = (gs + h2) % kAStages;
                         const uint64_t bd = sdesc_sw128(smem_u32(stage_b(s)));
                         const uint32_t a_tmem = tmem + (uint32_t)(L::kACol0 + sa * kACols);
@@ -736,10 +736,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_f16_ts_pair(d_tmem, a_tmem + 8u * k, bd + 2u * k, idesc,
                                             (st | h2 | k) != 0 ? 1u : 0u);
                     }
-                    if (gs & 2) {  // the group's second pair: release its four slots
-                        mma_commit_pair(&stage_free[(gs >> 2) % kGroups]);
-                        if (kDecoupled) mma_commit_pair(&a_free[(gs >> 2) % kAGroups]);
-                    }
+                    mma_commit_pair(&stage_free[(gs >> 2) % kGroups]);  // release the group's slots
+                    if (kDecoupled) mma_commit_pair(&a_free[(gs >> 2) % kAGroups]);
                 }
                 if (ok) mma_commit_pair(&acc_full[b]);
                 ++it;
@@ -851,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_remote(&a_full[(g0 >> 1) % kAPairs], 0);
+                if (lane == 0) mbar_arrive_remote(&a_full[(g0 >> 2) % kAGroups], 0);
             }
             gs += (uint32_t)nk;
         }
