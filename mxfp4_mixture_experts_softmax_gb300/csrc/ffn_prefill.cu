@@ -363,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int crow = MODE == 0 ? ((rho & 1) ? kCodeBox + (rho >> 1) : rho >> 1) : rho;
         const bool svec = (K % 512) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 15) == 0);
         const int ngroups = K / 32;
+        const bool s2 = (ngroups % 2) == 0 && ((reinterpret_cast<uintptr_t>(g.scales) & 1) == 0);
         const uint32_t lane_base = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)L::kACol0;
         uint32_t gs = 0;
         bool ok = true;
@@ -389,8 +390,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sp[j] = g.scales + ((size_t)e * g.rows + (rvalid[j] ? wrow : 0)) * (size_t)ngroups;
                 s_ref[j] = row_scale_ref(rvalid[j] ? row_scale_max_part(sp[j], ngroups, svec, 0, 1) : 0u);
             }
-            auto scale_at = [&](int j, int gidx) {
-                return (rvalid[j] && gidx < ngroups) ? (uint32_t)__ldg(sp[j] + gidx) : 0u;
+            // the stage's two scale groups of a row (bytes 2st, 2st + 1): one
+            // 16-bit load where aligned (a 32-sector load per warp either way,
+            // so one load instead of two halves the L1 wavefronts)
+            auto scales2 = [&](int j, int st) -> uint32_t {
+                if (!rvalid[j]) return 0u;
+                if (s2 && 2 * st + 1 < ngroups)
+                    return (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(sp[j]) + st);
+                uint32_t v = 0;
+                if (2 * st < ngroups) v = (uint32_t)__ldg(sp[j] + 2 * st);
+                if (2 * st + 1 < ngroups) v |= (uint32_t)__ldg(sp[j] + 2 * st + 1) << 8;
+                return v;
             };
             for (int st = 0; st < nk; ++st, ++gs) {
                 if ((int)(gs & 3u) != part) continue;
@@ -398,8 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t m0[kRB], m1[kRB];
 #pragma unroll
                 for (int j = 0; j < kRB; ++j) {
-                    m0[j] = f16_group_mult(scale_at(j, 2 * st), s_ref[j]);
-                    m1[j] = f16_group_mult(scale_at(j, 2 * st + 1), s_ref[j]);
+                    const uint32_t sc = scales2(j, st);
+                    m0[j] = f16_group_mult(sc & 0xFFu, s_ref[j]);
+                    m1[j] = f16_group_mult(sc >> 8, s_ref[j]);
                 }
                 if (!mbar_wait_warp(&raw_full[s], (gs / kStages) & 1)) {
                     ok = false;
