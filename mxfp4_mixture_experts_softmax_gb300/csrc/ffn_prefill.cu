@@ -631,17 +631,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kDecoupled = kAStages != kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    // The MMA thread waits once per pair of stages (on the converters) and
-    // releases slots once per group of four (stage_free, a_free): each
-    // commit costs the issuing thread about as much as two MMAs.
-    constexpr int kPairs = kStages / 2, kAPairs = kAStages / 2;
+    // The MMA thread waits on the converters once per group of four stages
+    // and releases the group's slots with one commit: each wait and commit
+    // costs the issuing thread about as much as two MMAs.
+    constexpr int kAPairs = kAStages / 2;
     constexpr int kGroups = kStages / 4, kAGroups = kAStages / 4;
     static_assert(kStages % 4 == 0 && kAStages % 4 == 0, "groups of four stages");
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L::kBars);  // codes + B landed, per slot
     uint64_t* a_full = raw_full + kStages;      // A converted in both CTAs, per A pair (even CTA)
-    uint64_t* stage_free = a_full + kAPairs;    // MMAs done with a group of four slots
-    uint64_t* a_free = stage_free + kGroups;    // MMAs done with a group of four A slots
-    uint64_t* acc_full = a_free + kAGroups;     // [2] accumulator ready
+    // MMAs of a group of four stages completed: frees the group's shared-
+    // memory slots (waited by the producer, kGroups groups later) and its A
+    // slots (waited by the converters, kAGroups groups later) with one commit
+    uint64_t* grp_done = a_full + kAPairs;
+    uint64_t* acc_full = grp_done + kGroups;    // [2] accumulator ready
     uint64_t* acc_free = acc_full + 2;          // [2] drained by both CTAs (even CTA)
     uint64_t* drain = acc_free + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -661,8 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&raw_full[s], 1);
-        for (int p = 0; p < kGroups; ++p) mbar_init(&stage_free[p], 1);
-        for (int p = 0; p < kAGroups; ++p) mbar_init(&a_free[p], 1);
+        for (int p = 0; p < kGroups; ++p) mbar_init(&grp_done[p], 1);
         for (int p = 0; p < kAGroups; ++p)
             mbar_init(&a_full[p], 16);  // per stage pair one converter warp per lane quadrant: 2 pairs, 2 CTAs
         for (int b = 0; b < kAccBufs; ++b) {
@@ -697,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = gs % kStages;
                 // four slots come free with their group's commit
                 if (gs >= kStages && (gs & 3) == 0 &&
-                    !mbar_wait_warp(&stage_free[(gs >> 2) % kGroups], ((gs / kStages) - 1) & 1)) {
+                    !mbar_wait_warp(&grp_done[(gs >> 2) % kGroups], ((gs / kStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -747,8 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_f16_ts_pair(d_tmem, a_tmem + 8u * k, bd + 2u * k, idesc,
                                             (st | h2 | k) != 0 ? 1u : 0u);
                     }
-                    mma_commit_pair(&stage_free[(gs >> 2) % kGroups]);  // release the group's slots
-                    if (kDecoupled) mma_commit_pair(&a_free[(gs >> 2) % kAGroups]);
+                    mma_commit_pair(&grp_done[(gs >> 2) % kGroups]);  // release the group's slots
                 }
                 if (ok) mma_commit_pair(&acc_full[b]);
                 ++it;
@@ -817,7 +817,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t scv = sc;
                 if (p + kParts < np) sc = scales4(p + kParts);
                 if (kDecoupled && g0 >= (uint32_t)kAStages &&
-                    !mbar_wait_warp(&a_free[(g0 >> 2) % kAGroups], ((g0 / kAStages) - 1) & 1)) {
+                    !mbar_wait_warp(&grp_done[((g0 >> 2) - kAGroups) % kGroups],
+                                    (((g0 >> 2) - kAGroups) / kGroups) & 1)) {
                     ok = false;
                     break;
                 }
