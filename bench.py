@@ -268,8 +268,8 @@ def launches_per_step(w, path_name: str) -> int:
     permutation, one launch or, for large batches, the four-launch multi-block
     sort), then per path:
       decode   x -> f16 rows, gate_up, h -> f16 rows | down, combine
-      prefill  x -> f16 rows, gather, gate_up, h -> f16 rows | position
-               weights, down, blocked combine
+      prefill  gather of x into tile order as f16 rows, gate_up, h -> f16
+               rows | position weights, down, blocked combine
       mxfp4act quantise x, gather, gate_up | position weights, down, blocked
                combine"""
     from mxfp4_mixture_experts_softmax_gb300 import libmoe
@@ -279,7 +279,7 @@ def launches_per_step(w, path_name: str) -> int:
     else:
         nb = min(P // max(w.Et, 1), 160)
         rp = 1 + (4 if (nb >= 8 and P >= 8192) else 1)
-    return rp + {"decode": 3 + 2, "prefill": 4 + 3, "mxfp4act": 3 + 3}[path_name]
+    return rp + {"decode": 3 + 2, "prefill": 3 + 3, "mxfp4act": 3 + 3}[path_name]
 
 
 # ------------------------------------------------------------ ranks

@@ -169,8 +169,10 @@ moe_status_t moe_route_permute(const float* logits, const float* shared_w, int T
  * moe_ffn_workspace_size -- bytes of device workspace moe_ffn needs:
  * the 16-bit SwiGLU intermediate [cap, I], the weighted fp32 per-pair expert
  * outputs [T*Kt, H], x as f16 rows [T, H], when tile_m is a prefill tile
- * height (32, 64, 128, 256) their tile-ordered copy [cap, H], and T + cap
- * fp32 row factors; each 256-byte aligned.
+ * height (32, 64, 128, 256) their tile-ordered copy [cap, H], T + cap fp32
+ * row factors, cap fp32 position weights and, for prefill tile heights, the
+ * shift bytes of the staged y [ceil(cap/32), H rounded up to 128]; each
+ * 256-byte aligned.
  */
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
 
@@ -194,7 +196,10 @@ size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
  * Both paths carry x and h into the MMAs as f16 scaled per row by a power
  * of two (largest magnitude in [2^14, 2^15)): elements at least 2^-29 of
  * their row's largest magnitude stay exact, smaller ones move by less than
- * 2^-39 of it.
+ * 2^-39 of it.  The prefill path hands y from the down GEMM to the combine
+ * as f16 scaled by a power of two per (output row, 32 sorted positions):
+ * relative error at most 2^-11 per element (elements more than 2^28 below
+ * their group's largest move by less than 2^-38 of it).
  * Result tolerance against the plain fp32 definition: per element
  * |out - ref| <= 1e-2 * (|ref| + rms(ref)) and relative L2 error <= 2e-3
  * (the GEMM summation order differs; SwiGLU bf16 roundings may flip by 1 ulp).
@@ -255,12 +260,16 @@ moe_status_t moe_combine(const float* y, int T, int H, int Kt, uint16_t* out, cu
 
 /*
  * moe_ffn_down_combine -- moe_ffn_down followed by moe_combine, in one call
- * (moe_ffn runs gate_up and then this).  Same results bit for bit; the
- * difference is where y lives in between: the prefill path writes y blocked
- * by 128 output rows ([ceil(H/128)][cap][128], row block, sorted position,
- * row) so each work item writes one contiguous run, and the combine gathers
- * each token's Kt positions (inv_pairs) in slot order.  The workspace's y is
- * therefore not the [T*Kt, H] array of moe_ffn_down after this call.
+ * (moe_ffn runs gate_up and then this).  The decode path gives the same
+ * results bit for bit.  The prefill path writes y blocked by 128 output rows
+ * ([ceil(H/128)][cap][128], row block, sorted position, row) so each work
+ * item writes one contiguous run, stored as f16 times a power of two per
+ * (output row, 32 sorted positions) with the shift bytes after the position
+ * weights; the combine undoes the shift exactly, multiplies by the routing
+ * weight and sums each token's Kt positions (inv_pairs) in slot order.  The
+ * one rounding to f16 (at most 2^-11 relative) is the only difference from
+ * moe_ffn_down + moe_combine; the result meets moe_ffn's tolerance.  The
+ * workspace's y is not the [T*Kt, H] array of moe_ffn_down after this call.
  */
 moe_status_t moe_ffn_down_combine(const uint8_t* w2, const uint8_t* s2, const float* topk_w,
                                   const int32_t* sorted_pairs, const int32_t* inv_pairs,

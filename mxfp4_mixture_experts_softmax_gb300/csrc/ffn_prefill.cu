@@ -155,6 +155,39 @@ __device__ __forceinline__ uint4 codes_to_f16x8(uint32_t w, uint32_t mult) {
     return v;
 }
 
+// One 32-column chunk of a down item's blocked y, staged as f16 scaled by a
+// power of two per (output row, 32 positions): lane `lane` of quadrant `quad`
+// holds output row 32 quad + lane of the block, v[i] the accumulator of column
+// col0 + i (col0 = the chunk's first sorted position, a multiple of 32), fr
+// the row factor.  The lane's largest |y| over the chunk's nc columns that
+// hold a pair sets the shift that moves it into [2^14, 2^15); each element is
+// stored as f16(y * 2^shift) (relative error at most 2^-11 for every element
+// within 2^28 of that largest) and the shift as one byte at
+// y_shift[col0 / 32][block * 128 + row].  row_ok = the output row exists.
+__device__ __forceinline__ void store_y16_chunk(const GroupedGemm& g, const uint32_t v[32], float fr,
+                                                int block, int quad, int lane, int col0, int nc,
+                                                bool row_ok) {
+    if (!row_ok) return;
+    float y[32];
+    float mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        y[i] = __uint_as_float(v[i]) * fr;
+        if (i < nc) mx = fmaxf(mx, fabsf(y[i]));
+    }
+    const int sh = f32_f16_shift(__float_as_uint(mx));
+    const float up = __uint_as_float((uint32_t)(127 + sh) << 23);
+    const int row = block * 128 + 32 * quad + lane;
+    uint16_t* yb = g.y16_out + ((size_t)block * g.act_rows + col0) * 128 + 32 * quad + lane;
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const __half2 h = __floats2half2_rn(y[i] * up, y[i + 1] * up);
+        if (i < nc) yb[(size_t)i * 128] = __half_as_ushort(__low2half(h));
+        if (i + 1 < nc) yb[(size_t)(i + 1) * 128] = __half_as_ushort(__high2half(h));
+    }
+    g.y_shift[(size_t)(col0 / 32) * g.y_rows_pad + row] = (int8_t)sh;
+}
+
 template <int N, bool PAIR>
 struct PrefillSmem {
     // 128-row weight blocks per work item and CTA.  The blocks share the
@@ -574,12 +607,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // factor (routing weight x h row factor) is applied by the
                     // combine
                     const int m = block * 128 + r;
-                    float* yb = g.y_out + ((size_t)block * g.act_rows + (size_t)tile * N + c0) * 128 + r;
                     const int nc = nvalid - c0;  // warp-uniform
-                    if (m < g.rows) {
+                    if (g.y16_out) {
+                        store_y16_chunk(g, v, fr, block, quad, lane, tile * N + c0, nc, m < g.rows);
+                    } else {
+                        float* yb = g.y_out + ((size_t)block * g.act_rows + (size_t)tile * N + c0) * 128 + r;
+                        if (m < g.rows) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (i < nc) yb[(size_t)i * 128] = __uint_as_float(v[i]) * fr;
+                            for (int i = 0; i < 32; ++i)
+                                if (i < nc) yb[(size_t)i * 128] = __uint_as_float(v[i]) * fr;
+                        }
                     }
                 } else {  // y[pair][m]
                     const int m = block * 128 + r;
@@ -954,12 +991,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else if (g.y_blocked) {
                     const int m = block * 128 + r;
-                    float* yb = g.y_out + ((size_t)block * g.act_rows + (size_t)tile * N + c0) * 128 + r;
                     const int nc = nvalid - c0;
-                    if (m < g.rows) {
+                    if (g.y16_out) {
+                        store_y16_chunk(g, v, fr, block, quad, lane, tile * N + c0, nc, m < g.rows);
+                    } else {
+                        float* yb = g.y_out + ((size_t)block * g.act_rows + (size_t)tile * N + c0) * 128 + r;
+                        if (m < g.rows) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (i < nc) yb[(size_t)i * 128] = __uint_as_float(v[i]) * fr;
+                            for (int i = 0; i < 32; ++i)
+                                if (i < nc) yb[(size_t)i * 128] = __uint_as_float(v[i]) * fr;
+                        }
                     }
                 } else {
                     const int m = block * 128 + r;
@@ -1134,7 +1175,86 @@ __global__ void __launch_bounds__(256) gather_rows_f16_kernel(const uint4* __res
     pdl_end();
 }
 
+// out[t, m] = bf16(sum over j ascending of f[p] * (y16 * 2^-shift)), p =
+// inv[t * Kt + j], for y staged by the down epilogues as f16 with a shift per
+// (output row, 32 positions) ([H/128][cap][128] halves, [cap/32][Hpad]
+// shift bytes, Hpad = H rounded up to 128).  Undoing the shift is exact; the
+// product and the sum are rounded apart, in slot order, like
+// combine_blocked_kernel's.  8 consecutive m per thread.
+// 2^-s for the signed shift byte s in the low 8 bits of b (|s| <= 120).
+__device__ __forceinline__ float pow2_neg_byte(uint32_t b) {
+    return __uint_as_float((uint32_t)(127 - (int)(int8_t)(b & 0xFFu)) << 23);
+}
+
+__global__ void __launch_bounds__(256) combine_blocked_f16_kernel(const uint4* __restrict__ y16,
+                                                                  const int8_t* __restrict__ shift,
+                                                                  const int32_t* __restrict__ inv,
+                                                                  const float* __restrict__ f, int T,
+                                                                  int H, int Kt, int cap,
+                                                                  uint4* __restrict__ out) {
+    pdl_begin();
+    const int H8 = H / 8, Hpad8 = (H + 127) / 128 * 16;
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < (size_t)T * H8) {
+        const size_t t = i / H8;
+        const int m8 = (int)(i % H8), blk = m8 / 16, r8 = m8 % 16;
+        const uint2* sh8 = reinterpret_cast<const uint2*>(shift) + m8;
+        float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // four slots' loads in flight at a time; the sums stay in slot order
+        for (int j0 = 0; j0 < Kt; j0 += 4) {
+            int p[4];
+            uint4 h[4];
+            uint2 sh[4];
+            float c[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) p[u] = j0 + u < Kt ? __ldg(inv + t * Kt + j0 + u) : -1;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if ((unsigned)p[u] < (unsigned)cap) {
+                    h[u] = __ldg(y16 + ((size_t)blk * cap + p[u]) * 16 + r8);
+                    sh[u] = __ldg(sh8 + (size_t)(p[u] / 32) * Hpad8);
+                    c[u] = f ? __ldg(f + p[u]) : 1.0f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (j0 + u >= Kt) break;
+                if ((unsigned)p[u] >= (unsigned)cap) {
+                    flag_index_error();
+                    continue;
+                }
+                const uint32_t hw[4] = {h[u].x, h[u].y, h[u].z, h[u].w};
+                const uint32_t sw[2] = {sh[u].x, sh[u].y};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const __half2 hh = *reinterpret_cast<const __half2*>(&hw[k / 2]);
+                    const float y = __half2float((k & 1) ? __high2half(hh) : __low2half(hh)) *
+                                    pow2_neg_byte(sw[k / 4] >> (8 * (k % 4)));
+                    a[k] = __fadd_rn(a[k], __fmul_rn(c[u], y));
+                }
+            }
+        }
+        uint4 o;
+        o.x = (uint32_t)f32_to_bf16_bits(a[0]) | ((uint32_t)f32_to_bf16_bits(a[1]) << 16);
+        o.y = (uint32_t)f32_to_bf16_bits(a[2]) | ((uint32_t)f32_to_bf16_bits(a[3]) << 16);
+        o.z = (uint32_t)f32_to_bf16_bits(a[4]) | ((uint32_t)f32_to_bf16_bits(a[5]) << 16);
+        o.w = (uint32_t)f32_to_bf16_bits(a[6]) | ((uint32_t)f32_to_bf16_bits(a[7]) << 16);
+        out[i] = o;
+    }
+    pdl_end();
+}
+
 }  // namespace
+
+cudaError_t launch_combine_blocked_f16(const uint16_t* y16, const int8_t* shift, const int32_t* inv,
+                                       const float* f, int T, int H, int Kt, int cap, uint16_t* out,
+                                       cudaStream_t s) {
+    const long long n = (long long)T * (H / 8);
+    if (n <= 0) return cudaSuccess;
+    return launch_pdl(combine_blocked_f16_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
+                      reinterpret_cast<const uint4*>(y16), shift, inv, f, T, H, Kt, cap,
+                      reinterpret_cast<uint4*>(out));
+}
 
 cudaError_t launch_gather_rows_f16(const uint16_t* x, int H, const int32_t* sorted_pairs,
                                    const int32_t* num_tiles, int tile_m, int Kt, int cap,

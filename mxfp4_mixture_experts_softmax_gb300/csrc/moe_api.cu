@@ -319,11 +319,12 @@ moe_status_t moe_route_permute(const float* logits, const float* shared_w, int T
 static size_t y_offset(int64_t cap, int I) { return round_up((size_t)cap * I * sizeof(uint16_t), 256); }
 
 // y: fp32 [T*Kt, H] by pair, or, for prefill tile heights, also room for the
-// blocked layout moe_ffn_down_combine writes ([ceil(H/128)][cap][128]).
+// blocked f16 layout moe_ffn_down_combine writes ([ceil(H/128)][cap][128]).
 static size_t y_bytes(int64_t cap, int T, int H, int Kt, int tile_m) {
-    size_t n = (size_t)T * Kt * H;
-    if (prefill_tile_supported(tile_m)) n = std::max(n, (size_t)((H + 127) / 128) * 128 * (size_t)cap);
-    return round_up(n * sizeof(float), 256);
+    size_t n = (size_t)T * Kt * H * sizeof(float);
+    if (prefill_tile_supported(tile_m))
+        n = std::max(n, (size_t)((H + 127) / 128) * 128 * (size_t)cap * sizeof(uint16_t));
+    return round_up(n, 256);
 }
 
 // After y: x as scaled f16 rows [T, H] (both paths), the prefill path's
@@ -347,10 +348,19 @@ static size_t wpos_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) 
     return rs_offset(cap, T, H, I, Kt, tile_m) + round_up((size_t)(T + cap) * sizeof(float), 256);
 }
 
+// After the position weights: the shifts of y staged as f16 by the prefill
+// down GEMMs, one byte per (output row, 32 positions) [ceil(cap/32)][H
+// rounded up to 128].
+static size_t yshift_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) {
+    return wpos_offset(cap, T, H, I, Kt, tile_m) + round_up((size_t)cap * sizeof(float), 256);
+}
+
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m) {
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     if (cap < 0 || H <= 0 || I <= 0) return 0;
-    return wpos_offset(cap, T, H, I, Kt, tile_m) + round_up((size_t)cap * sizeof(float), 256);
+    const size_t shifts =
+        prefill_tile_supported(tile_m) ? (size_t)((cap + 31) / 32) * (size_t)((H + 127) / 128 * 128) : 0;
+    return yshift_offset(cap, T, H, I, Kt, tile_m) + round_up(shifts, 256);
 }
 
 moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m) {
@@ -521,10 +531,10 @@ moe_status_t moe_ffn_down_combine(const uint8_t* w2, const uint8_t* s2, const fl
         return st != MOE_OK ? st : moe_combine(y, T, H, Kt, out, stream);
     }
     // prefill: y blocked by 128 rows (each work item writes one contiguous
-    // run) without the column factor; the factor per position (routing weight
-    // x h row factor) is applied by the combine, which gathers each token's
-    // positions in slot order: the same products and sums as moe_ffn_down +
-    // moe_combine
+    // run), staged as f16 with a power-of-two shift per (32 output rows,
+    // position), without the column factor; the factor per position (routing
+    // weight x h row factor) is applied by the combine, which gathers each
+    // token's positions in slot order
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     float* w_pos = reinterpret_cast<float*>(ws + wpos_offset(cap, T, H, I, Kt, tile_m));
     const float* h_rscale = reinterpret_cast<const float*>(ws + rs_offset(cap, T, H, I, Kt, tile_m)) + T;
@@ -544,10 +554,14 @@ moe_status_t moe_ffn_down_combine(const uint8_t* w2, const uint8_t* s2, const fl
     g.act_by_token = 0;
     g.y_out = y;
     g.y_blocked = 1;
+    g.y16_out = reinterpret_cast<uint16_t*>(y);
+    g.y_shift = reinterpret_cast<int8_t*>(ws + yshift_offset(cap, T, H, I, Kt, tile_m));
+    g.y_rows_pad = (H + 127) / 128 * 128;
     g.topk_w = topk_w;
     err = launch_gemm_timed([&] { return launch_prefill_down(g, stream); }, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    return cuda_status(launch_combine_blocked(y, inv_pairs, w_pos, T, H, Kt, (int)cap, out, stream));
+    return cuda_status(launch_combine_blocked_f16(g.y16_out, g.y_shift, inv_pairs, w_pos, T, H, Kt,
+                                                  (int)cap, out, stream));
 }
 
 moe_status_t moe_combine_ex(const float* y, const float* y_extra, int T, int H, int Kt,

@@ -66,6 +66,15 @@ __device__ __forceinline__ int row_f16_shift(uint32_t mx) {
     return min(max(14 - e, -113), 112);
 }
 
+// The power-of-two shift that moves an fp32 magnitude with bit pattern mx
+// (the largest |value| of a group) into [2^14, 2^15), clamped to [-120, 120]
+// so that 2^shift and 2^-shift are normal fp32 values; 0 for mx == 0.
+__device__ __forceinline__ int f32_f16_shift(uint32_t mx) {
+    if (mx == 0) return 0;
+    const int e = (mx >> 23) ? (int)(mx >> 23) - 127 : (31 - __clz((int)mx)) - 149;
+    return min(max(14 - e, -120), 120);
+}
+
 // Two bf16 (low half first) times `up` (= 2^sigma) as an f16x2.
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float up) {
     const float lo = __uint_as_float(w << 16) * up;

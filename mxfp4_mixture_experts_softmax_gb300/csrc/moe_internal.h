@@ -75,6 +75,13 @@ struct GroupedGemm {
     // token for gate_up, by position for down)
     int sf_tma;
     int y_blocked;               // down: y as [ceil(rows/128)][act_rows][128] instead of [pair][rows]
+    // blocked y staged as f16 (prefill path): y16_out [ceil(rows/128)][act_rows][128]
+    // holds f16(y * 2^shift), y_shift [act_rows/32][y_rows_pad] the shift of each
+    // (output row, 32 positions) group, y_rows_pad = rows rounded up to 128;
+    // null: fp32 y_out
+    uint16_t* y16_out = nullptr;
+    int8_t* y_shift = nullptr;
+    int y_rows_pad = 0;
     // decode group factor 2^(s-126) as fp32 bits s * exp_one + exp_bias,
     // taken as runtime values so the multiply-add stays one instruction
     uint32_t exp_one = 1u << 23, exp_bias = 1u << 23;
@@ -208,6 +215,11 @@ cudaError_t launch_gather_mx_rows(const uint8_t* xc, const uint8_t* xs, int H, b
 cudaError_t launch_position_weights(const int32_t* sorted_pairs, const float* topk_w,
                                     const float* rscale, const int32_t* num_tiles, int tile_m,
                                     int cap, int num_pairs, float* w_pos, cudaStream_t s);
+// the same for y staged as f16 with a power-of-two shift per (output row,
+// 32 positions): y = y16 * 2^-shift (exact), then as above
+cudaError_t launch_combine_blocked_f16(const uint16_t* y16, const int8_t* shift, const int32_t* inv,
+                                       const float* f, int T, int H, int Kt, int cap, uint16_t* out,
+                                       cudaStream_t s);
 // out = bf16(sum over the Kt slots of f[p] * y[m / 128][p][m % 128], p =
 // inv[pair]) for the down GEMMs' blocked y (f null: factor 1)
 cudaError_t launch_combine_blocked(const float* y, const int32_t* inv, const float* f, int T, int H,

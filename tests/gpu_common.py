@@ -49,6 +49,21 @@ def ffn_parity(gpu: np.ndarray, ref: np.ndarray, what: str = "") -> dict:
     return stats
 
 
+def staged_close(a: np.ndarray, b: np.ndarray, what: str = "") -> float:
+    """Two GPU results that differ only in the prefill combine's f16 staging
+    of y (each term rounded to 11 significant bits before the fp32 sum, then
+    both sums rounded to bf16): per element |a - b| <= 2^-7 * (|a| + rms(a)),
+    with 2^-11 per term and two bf16 roundings (2^-9 each) well inside.
+    Returns the worst ratio."""
+    assert a.shape == b.shape and np.isfinite(a).all() and np.isfinite(b).all(), what
+    bound = 2.0 ** -7 * (np.abs(a) + float(np.sqrt(np.mean(a ** 2))))
+    err = np.abs(a - b)
+    ratio = np.divide(err, bound, out=np.where(err > 0, np.inf, 0.0), where=bound > 0)
+    worst = float(ratio.max()) if err.size else 0.0
+    assert worst <= 1.0, f"{what}: {worst:.3g} x bound"
+    return worst
+
+
 def upload_weights(d: dict) -> dict:
     return {k: to_dev(d[k]) for k in ("w13", "s13", "w2", "s2")}
 

@@ -76,8 +76,8 @@ def test_launch_counts_per_path():
     assert bench.launches_per_step(W["decode64"], "decode") == 7
     assert bench.launches_per_step(W["decode64"], "mxfp4act") == 8
     # 16,896 and 90,112 pairs: the four-launch multi-block sort
-    assert bench.launches_per_step(W["prefill1536"], "prefill") == 12
-    assert bench.launches_per_step(W["skewed_prefill8192"], "prefill") == 12
+    assert bench.launches_per_step(W["prefill1536"], "prefill") == 11
+    assert bench.launches_per_step(W["skewed_prefill8192"], "prefill") == 11
     assert bench.launches_per_step(W["skewed_prefill8192"], "mxfp4act") == 11
 
 

@@ -424,7 +424,10 @@ def test_layer_graph_capture_replays_identically():
                                          (libmoe.MOE_PATH_DECODE, 64),
                                          (libmoe.MOE_PATH_PREFILL, 64)])
 def test_split_steps_equal_moe_ffn(path, tile_m):
-    """gate_up, down and combine as separate calls reproduce moe_ffn bit for bit."""
+    """gate_up, down and combine as separate calls reproduce moe_ffn: bit for
+    bit on the decode path; on the prefill path moe_ffn's combine reads y
+    staged as scaled f16, so the two agree to the staging bound and both
+    meet the bar against the oracle."""
     w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL["ragged37"])
     d, ids, wt = _layer_inputs(w)
     dev_w = gc.upload_weights(d)
@@ -440,8 +443,16 @@ def test_split_steps_equal_moe_ffn(path, tile_m):
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
     libmoe.moe_combine(y, w.T, w.H, w.Kt, out)
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(gc.bf16_dev_to_f64(out), gc.bf16_dev_to_f64(whole))
-    assert np.isfinite(gc.bf16_dev_to_f64(out)).all()
+    a, b = gc.bf16_dev_to_f64(out), gc.bf16_dev_to_f64(whole)
+    assert np.isfinite(a).all()
+    if path == libmoe.MOE_PATH_DECODE:
+        np.testing.assert_array_equal(a, b)
+    else:
+        gc.staged_close(a, b, "split steps vs moe_ffn")
+        ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt,
+                                        n_threads=THREADS))
+        gc.ffn_parity(a, ref, "split steps")
+        gc.ffn_parity(b, ref, "moe_ffn")
 
 
 # ------------------------------------------------------ prefill (tcgen05)
@@ -561,8 +572,10 @@ def test_decode_and_prefill_paths_agree_on_every_token(name):
                                               (libmoe.MOE_PATH_PREFILL, 128, "wide_k"),
                                               (libmoe.MOE_PATH_DECODE, 8, "ragged37")])
 def test_down_combine_equals_down_then_combine(path, tile_m, name):
-    """moe_ffn_down_combine (blocked y on the prefill path) gives the bytes of
-    moe_ffn_down followed by moe_combine (y by pair), and meets the bar."""
+    """moe_ffn_down_combine gives the bytes of moe_ffn_down followed by
+    moe_combine (y by pair) on the decode path; on the prefill path (y blocked
+    and staged as scaled f16) it agrees with them to the staging bound; both
+    meet the bar."""
     w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL[name])
     d, ids, wt = _layer_inputs(w)
     dw = gc.upload_weights(d)
@@ -577,9 +590,13 @@ def test_down_combine_equals_down_then_combine(path, tile_m, name):
     b = torch.empty_like(a)
     libmoe.moe_ffn_down_combine(dw["w2"], dw["s2"], wt_d, perm, ws, w.T, b, path)
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(gc.bf16_dev_to_f64(b), gc.bf16_dev_to_f64(a))
+    if path == libmoe.MOE_PATH_DECODE:
+        np.testing.assert_array_equal(gc.bf16_dev_to_f64(b), gc.bf16_dev_to_f64(a))
+    else:
+        gc.staged_close(gc.bf16_dev_to_f64(a), gc.bf16_dev_to_f64(b), f"down_combine {name}")
     ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt,
                                     n_threads=THREADS))
+    gc.ffn_parity(gc.bf16_dev_to_f64(a), ref, f"down then combine {name}")
     gc.ffn_parity(gc.bf16_dev_to_f64(b), ref, f"down_combine {name}")
     assert libmoe.moe_device_error() == 0
 
