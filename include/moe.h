@@ -171,8 +171,8 @@ moe_status_t moe_route_permute(const float* logits, const float* shared_w, int T
  * outputs [T*Kt, H], x as f16 rows [T, H], when tile_m is a prefill tile
  * height (32, 64, 128, 256) their tile-ordered copy [cap, H], T + cap fp32
  * row factors, cap fp32 position weights and, for prefill tile heights, the
- * shift bytes of the staged y [ceil(cap/32), H rounded up to 128]; each
- * 256-byte aligned.
+ * shift bytes of the staged y [ceil(cap/32), (H rounded up to 128) / 8];
+ * each 256-byte aligned.
  */
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
 
@@ -197,7 +197,7 @@ size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
  * of two (largest magnitude in [2^14, 2^15)): elements at least 2^-29 of
  * their row's largest magnitude stay exact, smaller ones move by less than
  * 2^-39 of it.  The prefill path hands y from the down GEMM to the combine
- * as f16 scaled by a power of two per (output row, 32 sorted positions):
+ * as f16 scaled by a power of two per (8 output rows, 32 sorted positions):
  * relative error at most 2^-11 per element (elements more than 2^28 below
  * their group's largest move by less than 2^-38 of it).
  * Result tolerance against the plain fp32 definition: per element
@@ -261,10 +261,9 @@ moe_status_t moe_combine(const float* y, int T, int H, int Kt, uint16_t* out, cu
 /*
  * moe_ffn_down_combine -- moe_ffn_down followed by moe_combine, in one call
  * (moe_ffn runs gate_up and then this).  The decode path gives the same
- * results bit for bit.  The prefill path writes y blocked by 128 output rows
- * ([ceil(H/128)][cap][128], row block, sorted position, row) so each work
- * item writes one contiguous run, stored as f16 times a power of two per
- * (output row, 32 sorted positions) with the shift bytes after the position
+ * results bit for bit.  The prefill path writes y by sorted position
+ * ([cap][H rounded up to 128]) as f16 times a power of two per (8 output
+ * rows, 32 sorted positions), with the shift bytes after the position
  * weights; the combine undoes the shift exactly, multiplies by the routing
  * weight and sums each token's Kt positions (inv_pairs) in slot order.  The
  * one rounding to f16 (at most 2^-11 relative) is the only difference from

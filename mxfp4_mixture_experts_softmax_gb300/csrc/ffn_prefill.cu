@@ -155,19 +155,21 @@ __device__ __forceinline__ uint4 codes_to_f16x8(uint32_t w, uint32_t mult) {
     return v;
 }
 
-// One 32-column chunk of a down item's blocked y, staged as f16 scaled by a
-// power of two per (output row, 32 positions): lane `lane` of quadrant `quad`
-// holds output row 32 quad + lane of the block, v[i] the accumulator of column
-// col0 + i (col0 = the chunk's first sorted position, a multiple of 32), fr
-// the row factor.  The lane's largest |y| over the chunk's nc columns that
-// hold a pair sets the shift that moves it into [2^14, 2^15); each element is
-// stored as f16(y * 2^shift) (relative error at most 2^-11 for every element
-// within 2^28 of that largest) and the shift as one byte at
-// y_shift[col0 / 32][block * 128 + row].  row_ok = the output row exists.
+// One 32-column chunk of a down item's y, staged as f16 rows by sorted
+// position (y16_out [act_rows][y_rows_pad]) scaled by a power of two per
+// (8 output rows, 32 positions): lane `lane` of quadrant
+// `quad` holds output row 32 quad + lane of the block, v[i] the accumulator of
+// column col0 + i (col0 = the chunk's first sorted position, a multiple of 32), fr
+// the row factor.  The largest |y| over the chunk's nc columns that hold a
+// pair and the 8 rows of the lane's group (three exchanges) sets the shift
+// that moves it into [2^14, 2^15); each element is stored as f16(y * 2^shift)
+// (relative error at most 2^-11 for every element within 2^28 of that
+// largest) and the group's shift as one byte at
+// y_shift[col0 / 32][(block * 128 + row) / 8].  row_ok = the output row
+// exists.  All 32 lanes call it.
 __device__ __forceinline__ void store_y16_chunk(const GroupedGemm& g, const uint32_t v[32], float fr,
                                                 int block, int quad, int lane, int col0, int nc,
                                                 bool row_ok) {
-    if (!row_ok) return;
     float y[32];
     float mx = 0.0f;
 #pragma unroll
@@ -175,17 +177,21 @@ __device__ __forceinline__ void store_y16_chunk(const GroupedGemm& g, const uint
         y[i] = __uint_as_float(v[i]) * fr;
         if (i < nc) mx = fmaxf(mx, fabsf(y[i]));
     }
+    if (!row_ok) mx = 0.0f;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    if (!row_ok) return;
     const int sh = f32_f16_shift(__float_as_uint(mx));
     const float up = __uint_as_float((uint32_t)(127 + sh) << 23);
     const int row = block * 128 + 32 * quad + lane;
-    uint16_t* yb = g.y16_out + ((size_t)block * g.act_rows + col0) * 128 + 32 * quad + lane;
+    uint16_t* yb = g.y16_out + (size_t)col0 * g.y_rows_pad + row;
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
         const __half2 h = __floats2half2_rn(y[i] * up, y[i + 1] * up);
-        if (i < nc) yb[(size_t)i * 128] = __half_as_ushort(__low2half(h));
-        if (i + 1 < nc) yb[(size_t)(i + 1) * 128] = __half_as_ushort(__high2half(h));
+        if (i < nc) yb[(size_t)i * g.y_rows_pad] = __half_as_ushort(__low2half(h));
+        if (i + 1 < nc) yb[(size_t)(i + 1) * g.y_rows_pad] = __half_as_ushort(__high2half(h));
     }
-    g.y_shift[(size_t)(col0 / 32) * g.y_rows_pad + row] = (int8_t)sh;
+    if ((lane & 7) == 0) g.y_shift[(size_t)(col0 / 32) * (g.y_rows_pad / 8) + row / 8] = (int8_t)sh;
 }
 
 template <int N, bool PAIR>
@@ -602,22 +608,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 f32_to_bf16_bits(silu(gate * fc) * (up * fc));
                     }
                 } else if (g.y_blocked) {
-                    // blocked y: [rows / 128][position][128], one contiguous run
-                    // per item over the positions holding a pair; the column
-                    // factor (routing weight x h row factor) is applied by the
-                    // combine
+                    // y staged as scaled f16 rows by position, written for the
+                    // positions holding a pair; the column factor (routing
+                    // weight x h row factor) is applied by the combine
                     const int m = block * 128 + r;
                     const int nc = nvalid - c0;  // warp-uniform
-                    if (g.y16_out) {
-                        store_y16_chunk(g, v, fr, block, quad, lane, tile * N + c0, nc, m < g.rows);
-                    } else {
-                        float* yb = g.y_out + ((size_t)block * g.act_rows + (size_t)tile * N + c0) * 128 + r;
-                        if (m < g.rows) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (i < nc) yb[(size_t)i * 128] = __uint_as_float(v[i]) * fr;
-                        }
-                    }
+                    store_y16_chunk(g, v, fr, block, quad, lane, tile * N + c0, nc, m < g.rows);
                 } else {  // y[pair][m]
                     const int m = block * 128 + r;
 #pragma unroll
@@ -992,16 +988,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else if (g.y_blocked) {
                     const int m = block * 128 + r;
                     const int nc = nvalid - c0;
-                    if (g.y16_out) {
-                        store_y16_chunk(g, v, fr, block, quad, lane, tile * N + c0, nc, m < g.rows);
-                    } else {
-                        float* yb = g.y_out + ((size_t)block * g.act_rows + (size_t)tile * N + c0) * 128 + r;
-                        if (m < g.rows) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (i < nc) yb[(size_t)i * 128] = __uint_as_float(v[i]) * fr;
-                        }
-                    }
+                    store_y16_chunk(g, v, fr, block, quad, lane, tile * N + c0, nc, m < g.rows);
                 } else {
                     const int m = block * 128 + r;
 #pragma unroll
@@ -1104,8 +1091,10 @@ cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
 // into tile order, so x never exists as a separate f16 copy.  One warp per
 // position (grid-stride).  Rows of up to 32 * NPL 16-byte pieces stay in
 // registers (one pass over the token's bf16 row, read from L2); longer rows
-// (NPL = 0) take a pass for the largest magnitude and one to convert.  Every
-// position of a token writes the same rscale value.
+// (NPL = 0) take a pass for the largest magnitude and one to convert.  The
+// copy is written with streaming (evict-first) stores, so the far larger
+// stream of gathered rows does not push x out of L2 while its Kt positions
+// are read.  Every position of a token writes the same rscale value.
 template <int NPL>
 __global__ void __launch_bounds__(256) gather_rows_f16_kernel(const uint4* __restrict__ x, int H8,
                                                               const int32_t* __restrict__ sorted_pairs,
@@ -1124,7 +1113,7 @@ __global__ void __launch_bounds__(256) gather_rows_f16_kernel(const uint4* __res
         }
         uint4* dst = xg + (size_t)p * H8;
         if (q < 0) {
-            for (int c = lane; c < H8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+            for (int c = lane; c < H8; c += 32) __stcs(dst + c, make_uint4(0, 0, 0, 0));
             continue;
         }
         const int t = q / Kt;
@@ -1152,8 +1141,8 @@ __global__ void __launch_bounds__(256) gather_rows_f16_kernel(const uint4* __res
             for (int i = 0; i < NPL; ++i) {
                 const int c = lane + 32 * i;
                 if (c < H8)
-                    dst[c] = make_uint4(bf16x2_to_f16x2_scaled(v[i].x, up), bf16x2_to_f16x2_scaled(v[i].y, up),
-                                        bf16x2_to_f16x2_scaled(v[i].z, up), bf16x2_to_f16x2_scaled(v[i].w, up));
+                    __stcs(dst + c, make_uint4(bf16x2_to_f16x2_scaled(v[i].x, up), bf16x2_to_f16x2_scaled(v[i].y, up),
+                                               bf16x2_to_f16x2_scaled(v[i].z, up), bf16x2_to_f16x2_scaled(v[i].w, up)));
             }
             if (lane == 0) rscale[t] = __uint_as_float((uint32_t)(127 - sigma) << 23);
         } else {
@@ -1166,8 +1155,8 @@ __global__ void __launch_bounds__(256) gather_rows_f16_kernel(const uint4* __res
 #pragma unroll 4
             for (int c = lane; c < H8; c += 32) {
                 const uint4 v = __ldg(src + c);
-                dst[c] = make_uint4(bf16x2_to_f16x2_scaled(v.x, up), bf16x2_to_f16x2_scaled(v.y, up),
-                                    bf16x2_to_f16x2_scaled(v.z, up), bf16x2_to_f16x2_scaled(v.w, up));
+                __stcs(dst + c, make_uint4(bf16x2_to_f16x2_scaled(v.x, up), bf16x2_to_f16x2_scaled(v.y, up),
+                                           bf16x2_to_f16x2_scaled(v.z, up), bf16x2_to_f16x2_scaled(v.w, up)));
             }
             if (lane == 0) rscale[t] = __uint_as_float((uint32_t)(127 - sigma) << 23);
         }
@@ -1176,16 +1165,17 @@ __global__ void __launch_bounds__(256) gather_rows_f16_kernel(const uint4* __res
 }
 
 // out[t, m] = bf16(sum over j ascending of f[p] * (y16 * 2^-shift)), p =
-// inv[t * Kt + j], for y staged by the down epilogues as f16 with a shift per
-// (output row, 32 positions) ([H/128][cap][128] halves, [cap/32][Hpad]
-// shift bytes, Hpad = H rounded up to 128).  Undoing the shift is exact; the
-// product and the sum are rounded apart, in slot order, like
-// combine_blocked_kernel's.  8 consecutive m per thread.
-// 2^-s for the signed shift byte s in the low 8 bits of b (|s| <= 120).
-__device__ __forceinline__ float pow2_neg_byte(uint32_t b) {
-    return __uint_as_float((uint32_t)(127 - (int)(int8_t)(b & 0xFFu)) << 23);
-}
-
+// inv[t * Kt + j], for y staged by the down epilogues as f16 rows by sorted
+// position ([cap][Hpad] halves, Hpad = H rounded up to 128) with a shift per
+// (8 output rows, 32 positions) ([cap/32][Hpad/8] bytes).  8 consecutive m per
+// thread, so one shift per slot: the slot's factor f[p] * 2^-shift is exact
+// (a power of two times f[p]; the products it could push below the normal
+// range are below 2^-110) and each term f[p] * y is rounded once, then added
+// in slot order, like combine_blocked_kernel's.  S slots' loads are in flight
+// at a time: their index loads first, then their y loads.  S = 2 measured
+// fastest on the 8192-token prefill (155 µs; 173 µs with 1, ~190 µs with 4,
+// ~355 µs with 12, where the register count halves the resident warps).
+template <int S>
 __global__ void __launch_bounds__(256) combine_blocked_f16_kernel(const uint4* __restrict__ y16,
                                                                   const int8_t* __restrict__ shift,
                                                                   const int32_t* __restrict__ inv,
@@ -1197,40 +1187,35 @@ __global__ void __launch_bounds__(256) combine_blocked_f16_kernel(const uint4* _
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < (size_t)T * H8) {
         const size_t t = i / H8;
-        const int m8 = (int)(i % H8), blk = m8 / 16, r8 = m8 % 16;
-        const uint2* sh8 = reinterpret_cast<const uint2*>(shift) + m8;
+        const int m8 = (int)(i % H8);
         float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        // four slots' loads in flight at a time; the sums stay in slot order
-        for (int j0 = 0; j0 < Kt; j0 += 4) {
-            int p[4];
-            uint4 h[4];
-            uint2 sh[4];
-            float c[4];
+        for (int j0 = 0; j0 < Kt; j0 += S) {
+            int p[S];
+            uint4 h[S];
+            float c[S];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) p[u] = j0 + u < Kt ? __ldg(inv + t * Kt + j0 + u) : -1;
+            for (int u = 0; u < S; ++u) p[u] = j0 + u < Kt ? __ldg(inv + t * Kt + j0 + u) : -1;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < S; ++u) {
                 if ((unsigned)p[u] < (unsigned)cap) {
-                    h[u] = __ldg(y16 + ((size_t)blk * cap + p[u]) * 16 + r8);
-                    sh[u] = __ldg(sh8 + (size_t)(p[u] / 32) * Hpad8);
-                    c[u] = f ? __ldg(f + p[u]) : 1.0f;
+                    h[u] = __ldg(y16 + (size_t)p[u] * Hpad8 + m8);
+                    const int sh = __ldg(shift + (size_t)(p[u] / 32) * Hpad8 + m8);
+                    c[u] = (f ? __ldg(f + p[u]) : 1.0f) * __uint_as_float((uint32_t)(127 - sh) << 23);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < S; ++u) {
                 if (j0 + u >= Kt) break;
                 if ((unsigned)p[u] >= (unsigned)cap) {
                     flag_index_error();
                     continue;
                 }
                 const uint32_t hw[4] = {h[u].x, h[u].y, h[u].z, h[u].w};
-                const uint32_t sw[2] = {sh[u].x, sh[u].y};
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const __half2 hh = *reinterpret_cast<const __half2*>(&hw[k / 2]);
-                    const float y = __half2float((k & 1) ? __high2half(hh) : __low2half(hh)) *
-                                    pow2_neg_byte(sw[k / 4] >> (8 * (k % 4)));
-                    a[k] = __fadd_rn(a[k], __fmul_rn(c[u], y));
+                for (int k = 0; k < 4; ++k) {
+                    const float2 yy = __half22float2(*reinterpret_cast<const __half2*>(&hw[k]));
+                    a[2 * k] = __fadd_rn(a[2 * k], __fmul_rn(yy.x, c[u]));
+                    a[2 * k + 1] = __fadd_rn(a[2 * k + 1], __fmul_rn(yy.y, c[u]));
                 }
             }
         }
@@ -1251,9 +1236,10 @@ cudaError_t launch_combine_blocked_f16(const uint16_t* y16, const int8_t* shift,
                                        cudaStream_t s) {
     const long long n = (long long)T * (H / 8);
     if (n <= 0) return cudaSuccess;
-    return launch_pdl(combine_blocked_f16_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
-                      reinterpret_cast<const uint4*>(y16), shift, inv, f, T, H, Kt, cap,
-                      reinterpret_cast<uint4*>(out));
+    const dim3 grid((unsigned)((n + 255) / 256)), block(256);
+    const uint4* y = reinterpret_cast<const uint4*>(y16);
+    uint4* o = reinterpret_cast<uint4*>(out);
+    return launch_pdl(combine_blocked_f16_kernel<2>, grid, block, 0, s, y, shift, inv, f, T, H, Kt, cap, o);
 }
 
 cudaError_t launch_gather_rows_f16(const uint16_t* x, int H, const int32_t* sorted_pairs,

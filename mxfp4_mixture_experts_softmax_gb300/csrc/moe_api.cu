@@ -319,7 +319,7 @@ moe_status_t moe_route_permute(const float* logits, const float* shared_w, int T
 static size_t y_offset(int64_t cap, int I) { return round_up((size_t)cap * I * sizeof(uint16_t), 256); }
 
 // y: fp32 [T*Kt, H] by pair, or, for prefill tile heights, also room for the
-// blocked f16 layout moe_ffn_down_combine writes ([ceil(H/128)][cap][128]).
+// f16 rows by position moe_ffn_down_combine writes ([cap][H rounded up to 128]).
 static size_t y_bytes(int64_t cap, int T, int H, int Kt, int tile_m) {
     size_t n = (size_t)T * Kt * H * sizeof(float);
     if (prefill_tile_supported(tile_m))
@@ -349,8 +349,8 @@ static size_t wpos_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) 
 }
 
 // After the position weights: the shifts of y staged as f16 by the prefill
-// down GEMMs, one byte per (output row, 32 positions) [ceil(cap/32)][H
-// rounded up to 128].
+// down GEMMs, one byte per (8 output rows, 32 positions) [ceil(cap/32)][H
+// rounded up to 128, / 8].
 static size_t yshift_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) {
     return wpos_offset(cap, T, H, I, Kt, tile_m) + round_up((size_t)cap * sizeof(float), 256);
 }
@@ -359,7 +359,7 @@ size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m) {
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     if (cap < 0 || H <= 0 || I <= 0) return 0;
     const size_t shifts =
-        prefill_tile_supported(tile_m) ? (size_t)((cap + 31) / 32) * (size_t)((H + 127) / 128 * 128) : 0;
+        prefill_tile_supported(tile_m) ? (size_t)((cap + 31) / 32) * (size_t)((H + 127) / 128 * 16) : 0;
     return yshift_offset(cap, T, H, I, Kt, tile_m) + round_up(shifts, 256);
 }
 
@@ -530,11 +530,10 @@ moe_status_t moe_ffn_down_combine(const uint8_t* w2, const uint8_t* s2, const fl
                           tile_m, workspace, ws_bytes, path, stream);
         return st != MOE_OK ? st : moe_combine(y, T, H, Kt, out, stream);
     }
-    // prefill: y blocked by 128 rows (each work item writes one contiguous
-    // run), staged as f16 with a power-of-two shift per (32 output rows,
-    // position), without the column factor; the factor per position (routing
-    // weight x h row factor) is applied by the combine, which gathers each
-    // token's positions in slot order
+    // prefill: y by sorted position, staged as f16 with a power-of-two shift
+    // per (8 output rows, 32 positions), without the column factor; the
+    // factor per position (routing weight x h row factor) is applied by the
+    // combine, which gathers each token's positions in slot order
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     float* w_pos = reinterpret_cast<float*>(ws + wpos_offset(cap, T, H, I, Kt, tile_m));
     const float* h_rscale = reinterpret_cast<const float*>(ws + rs_offset(cap, T, H, I, Kt, tile_m)) + T;

@@ -74,11 +74,12 @@ struct GroupedGemm {
     // producer loads by TMA with the codes; 0: scale warps load them (by
     // token for gate_up, by position for down)
     int sf_tma;
-    int y_blocked;               // down: y as [ceil(rows/128)][act_rows][128] instead of [pair][rows]
-    // blocked y staged as f16 (prefill path): y16_out [ceil(rows/128)][act_rows][128]
-    // holds f16(y * 2^shift), y_shift [act_rows/32][y_rows_pad] the shift of each
-    // (output row, 32 positions) group, y_rows_pad = rows rounded up to 128;
-    // null: fp32 y_out
+    int y_blocked;               // down: y by sorted position instead of [pair][rows], without
+                                 // the column factor (MXFP4 path: fp32 [ceil(rows/128)][act_rows][128];
+                                 // prefill path: the staged f16 rows below)
+    // prefill path: y16_out [act_rows][y_rows_pad] holds f16(y * 2^shift),
+    // y_shift [ceil(act_rows/32)][y_rows_pad/8] the shift of each (8 output
+    // rows, 32 positions) group, y_rows_pad = rows rounded up to 128
     uint16_t* y16_out = nullptr;
     int8_t* y_shift = nullptr;
     int y_rows_pad = 0;
@@ -215,8 +216,8 @@ cudaError_t launch_gather_mx_rows(const uint8_t* xc, const uint8_t* xs, int H, b
 cudaError_t launch_position_weights(const int32_t* sorted_pairs, const float* topk_w,
                                     const float* rscale, const int32_t* num_tiles, int tile_m,
                                     int cap, int num_pairs, float* w_pos, cudaStream_t s);
-// the same for y staged as f16 with a power-of-two shift per (output row,
-// 32 positions): y = y16 * 2^-shift (exact), then as above
+// the same for y staged as f16 with a power-of-two shift per (8 output
+// rows, 32 positions): y = y16 * 2^-shift (exact), then as above
 cudaError_t launch_combine_blocked_f16(const uint16_t* y16, const int8_t* shift, const int32_t* inv,
                                        const float* f, int T, int H, int Kt, int cap, uint16_t* out,
                                        cudaStream_t s);
