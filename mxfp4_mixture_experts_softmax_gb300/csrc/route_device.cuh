@@ -5,10 +5,9 @@
 // blog, optimisations section, PR #21421), with the shared expert appended as
 // slot K (same blog, PR #20736).  Lane l holds logits l, l+32, ... in
 // registers (coalesced 128-byte loads); the softmax max and denominator are
-// warp reductions; the K winners come from K rounds of a warp arg-max on a
-// 64-bit key (order-preserving logit bits, then the complemented expert
-// index), so equal logits resolve to the lower index and the selection is
-// exact.  Lane k keeps the k-th winner and writes it.
+// warp reductions; the K winners come from K rounds of a warp arg-max on the
+// order-preserving logit bits, ties going to the lower expert index, so the
+// selection is exact.  Lane k keeps the k-th winner and writes it.
 #pragma once
 
 #include "moe_device.cuh"
@@ -55,30 +54,29 @@ __device__ __forceinline__ void route_token(const float* __restrict__ l, int E, 
     int my_id = 0;
     float my_logit = 0.0f;
     if constexpr (VPL <= 16) {
-        // keys built once; a taken key is set to 0 (below every valid key)
-        unsigned long long key[VPL];
+        // 32-bit order keys built once; a taken key is set to 0 (below every
+        // valid key).  Each round: the warp's largest key (one max reduction),
+        // then the lowest expert index holding it (one min reduction) -- the
+        // same winner as an arg-max on (key, lower index first).
+        uint32_t key[VPL];
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int e = lane + 32 * i;
-            key[i] = e < E ? ((unsigned long long)order_key(v[i]) << 32) | (0xFFFFFFFFu - (uint32_t)e)
-                           : 0ull;
-        }
+        for (int i = 0; i < VPL; ++i) key[i] = lane + 32 * i < E ? order_key(v[i]) : 0u;
         for (int k = 0; k < K; ++k) {
-            unsigned long long best = key[0];
+            uint32_t lm = 0u;
 #pragma unroll
-            for (int i = 1; i < VPL; ++i) best = key[i] > best ? key[i] : best;
+            for (int i = 0; i < VPL; ++i) lm = max(lm, key[i]);
+            const uint32_t best = __reduce_max_sync(0xFFFFFFFFu, lm);
+            uint32_t le = 0xFFFFFFFFu;  // this lane's lowest expert holding `best`
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-                best = other > best ? other : best;
-            }
-            const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+            for (int i = VPL - 1; i >= 0; --i)
+                if (best != 0u && key[i] == best) le = (uint32_t)(lane + 32 * i);
+            const int e = (int)__reduce_min_sync(0xFFFFFFFFu, le);  // -1 if none is left
 #pragma unroll
             for (int i = 0; i < VPL; ++i)
-                if (lane + 32 * i == e) key[i] = 0ull;
+                if (lane + 32 * i == e) key[i] = 0u;
             if (lane == k) {
                 my_id = e;
-                my_logit = key_to_float((uint32_t)(best >> 32));
+                my_logit = key_to_float(best);
             }
         }
     } else {
