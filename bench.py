@@ -440,6 +440,7 @@ class Layer:
         import torch
         from mxfp4_mixture_experts_softmax_gb300 import libmoe
         w, dev = self.w, self.dev
+        ref_out = self.bufs["out"].cpu()  # the device-timed loop's output
         pin_logits = torch.from_numpy(self.host["logits"]).pin_memory()
         pin_x = torch.from_numpy(self.host["x"]).view(torch.int16).view(torch.bfloat16).pin_memory()
         pin_out = [torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
@@ -494,6 +495,11 @@ class Layer:
         cs.wait_stream(down_s)
         e1.record(cs)
         torch.cuda.synchronize(dev)
+        # the deterministic layer gives the device-timed loop's bytes: a
+        # buffer reused too early would show here
+        last = pin_out[(steps - 1) % 2]
+        if not torch.equal(last.view(torch.int16), ref_out.view(torch.int16)):
+            raise RuntimeError(f"end-to-end output differs from the device-timed output on {w.name}")
         return e0.elapsed_time(e1)
 
     def e2e_serial(self, steps: int, warmup: int) -> float:
