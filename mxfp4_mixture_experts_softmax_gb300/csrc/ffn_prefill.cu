@@ -842,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int np = nk / 2;
             // this warp's first pair of the item (np when the part is idle)
             const int p0 = part < kParts
-                               ? (int)((uint32_t)(part - (int)(gs >> 1)) % (uint32_t)kParts)
+                               ? (part - (int)((gs >> 1) % (uint32_t)kParts) + kParts) % kParts
                                : np;
             uint32_t sc = p0 < np ? scales4(p0) : 0u;  // loaded one of this warp's pairs ahead
             for (int p = p0; p < np; p += kParts) {
