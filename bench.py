@@ -52,7 +52,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=0,
+                   help="timed steps (default 0: as many as fill about 2 s, at least 50; the "
+                        "reference arm takes 50)")
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -643,6 +645,11 @@ def run_ours(args, ws, rank, local):
     work = layer_work(w, ids_host, args.act)
 
     K = args.steps
+    if K <= 0:  # enough steps for a region of about 2 s (the clock sampler's record)
+        ms, _, _ = lay.timed(5, local, ws, kernel_events=False)
+        K = int(min(20000, max(50, -(-2000.0 // (ms / 5)))))
+        if ws > 1:
+            K = int(max_over_ranks([K], dev)[0])
     total_ms, gemm, clocks = lay.timed(K, local, ws)
     per = lay.breakdown(min(K, 10))
     gemm.update(per)  # the gate_up and down steps (every launch of each call)
@@ -751,6 +758,8 @@ def run_reference(args, ws, rank):
         return None
     import oracle
     from mxfp4_mixture_experts_softmax_gb300 import synth
+    if args.steps <= 0:
+        args.steps = 50
     w = synth.WORKLOADS[args.workload]
     host = synth.make_inputs(w)
     threads = synth.cpu_threads()
