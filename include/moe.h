@@ -438,9 +438,10 @@ moe_status_t moe_quantize_mxfp4(const uint16_t* x, int rows, int cols, uint8_t* 
  * moe_ffn_mxfp4act_workspace_size -- bytes of device workspace the calls
  * below need: x codes [T, H/2] and scales [T, H/32], both again in tile
  * order [cap, ...], h codes [cap, I/2] and scales [cap, I/32], the routing
- * weight of each sorted position fp32 [cap], and y fp32 blocked by 128
- * output rows [H/128, cap, 128] (row block, sorted position, row), so each
- * down-GEMM work item writes one contiguous run.
+ * weight of each sorted position fp32 [cap], y as f16 rows by sorted
+ * position [cap, H] and its shift bytes [ceil(cap/32), H/8] (one power of
+ * two per 8 output rows and 32 positions), as moe_ffn_down_combine's
+ * prefill path stages it.
  */
 size_t moe_ffn_mxfp4act_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
 
@@ -451,7 +452,9 @@ size_t moe_ffn_mxfp4act_workspace_size(int T, int H, int I, int Et, int Kt, int 
  *   xq  = decode(quantise(x_t))                  (blocks of 32 along H)
  *   g_n = W13[e][n] . xq,  u_n = W13[e][I+n] . xq (fp32 accumulation)
  *   h   = decode(quantise(silu(g) * u))          (fp32 SwiGLU, blocks of 32 along I)
- *   y   = topk_w[t, j] * (W2[e] . h)             (fp32)
+ *   y   = topk_w[t, j] * (W2[e] . h)             (fp32; W2[e] . h passes to the
+ *                                                 combine as f16 scaled by a power
+ *                                                 of two, at most 2^-11 relative)
  *   out_t = bf16(sum over j ascending of y)
  * Both GEMMs are tcgen05 block-scaled MXFP4 x MXFP4 contractions; the scales
  * of weights and activations are applied inside the MMA.

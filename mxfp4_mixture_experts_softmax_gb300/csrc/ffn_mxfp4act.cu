@@ -495,13 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&acc_free[b]);
                 }
-                if (MODE == 1) {  // the raw accumulator of the positions holding a pair
-                    float* yb = g.y_out + ((size_t)block * g.act_rows + (size_t)tile * N + c0) * 128 +
-                                32 * quad + lane;
+                if (MODE == 1) {  // the raw accumulator of the positions holding a pair, staged as f16
                     const int nc = nvalid - c0;  // warp-uniform
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (i < nc) yb[(size_t)i * 128] = __uint_as_float(v[i]);
+                    store_y16_chunk(g, v, 1.0f, block, quad, lane, tile * N + c0, nc,
+                                    block * 128 + 32 * quad + lane < g.rows);
                 } else {
                     // transpose through shared memory: stg[column][accumulator row]
 #pragma unroll
@@ -592,52 +589,6 @@ cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
     }
 }
 
-// out[t, m] = bf16(sum over j ascending of f[p] * y[m / 128][p][m % 128]),
-// p = inv[t * Kt + j], f the per-position factor (the routing weight, on the
-// bf16 path times the h row's factor; 1 when f is null), for y blocked as
-// the down epilogues write it.  The product and the sum are rounded apart
-// (no fused multiply-add): the same fp32 values an epilogue applying f would
-// store, summed in the same order.  4 consecutive m per thread, so a warp
-// reads 512 contiguous bytes per slot.
-__global__ void __launch_bounds__(256) combine_blocked_kernel(const float4* __restrict__ y,
-                                                              const int32_t* __restrict__ inv,
-                                                              const float* __restrict__ f, int T,
-                                                              int H, int Kt, int cap,
-                                                              uint2* __restrict__ out) {
-    pdl_begin();
-    const int H4 = H / 4;
-    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < (size_t)T * H4) {
-        const size_t t = i / H4;
-        const int m4 = (int)(i % H4), blk = m4 / 32, r4 = m4 % 32;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < Kt; ++j) {
-            const int p = __ldg(inv + t * Kt + j);
-            if ((unsigned)p >= (unsigned)cap) {
-                flag_index_error();
-                continue;
-            }
-            float4 v = __ldg(y + ((size_t)blk * cap + p) * 32 + r4);
-            if (f) {
-                const float c = __ldg(f + p);
-                v.x = __fmul_rn(c, v.x);
-                v.y = __fmul_rn(c, v.y);
-                v.z = __fmul_rn(c, v.z);
-                v.w = __fmul_rn(c, v.w);
-            }
-            a.x = __fadd_rn(a.x, v.x);
-            a.y = __fadd_rn(a.y, v.y);
-            a.z = __fadd_rn(a.z, v.z);
-            a.w = __fadd_rn(a.w, v.w);
-        }
-        uint2 o;
-        o.x = (uint32_t)f32_to_bf16_bits(a.x) | ((uint32_t)f32_to_bf16_bits(a.y) << 16);
-        o.y = (uint32_t)f32_to_bf16_bits(a.z) | ((uint32_t)f32_to_bf16_bits(a.w) << 16);
-        out[i] = o;
-    }
-    pdl_end();
-}
-
 // The token rows of the used tiles in tile order, MXFP4 encoded: codes
 // (cb16 16-byte units per row) and, when sb16 > 0, scales (sb16 units per
 // row); zeros for padding positions.  One warp per row, rows grid-strided.
@@ -708,15 +659,6 @@ cudaError_t launch_gather_mx_rows(const uint8_t* xc, const uint8_t* xs, int H, b
                       reinterpret_cast<const uint4*>(xc), reinterpret_cast<const uint4*>(xs), H / 32,
                       with_scales ? H / 512 : 0, sorted_pairs, num_tiles, tile_m, Kt, cap, num_pairs,
                       reinterpret_cast<uint4*>(xgc), reinterpret_cast<uint4*>(xgs));
-}
-
-cudaError_t launch_combine_blocked(const float* y, const int32_t* inv, const float* f, int T, int H,
-                                   int Kt, int cap, uint16_t* out, cudaStream_t s) {
-    const long long n = (long long)T * (H / 4);
-    if (n <= 0) return cudaSuccess;
-    return launch_pdl(combine_blocked_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
-                      reinterpret_cast<const float4*>(y), inv, f, T, H, Kt, cap,
-                      reinterpret_cast<uint2*>(out));
 }
 
 cudaError_t launch_quantize_mxfp4(const uint16_t* x, int rows, int cols, uint8_t* codes,

@@ -155,45 +155,6 @@ __device__ __forceinline__ uint4 codes_to_f16x8(uint32_t w, uint32_t mult) {
     return v;
 }
 
-// One 32-column chunk of a down item's y, staged as f16 rows by sorted
-// position (y16_out [act_rows][y_rows_pad]) scaled by a power of two per
-// (8 output rows, 32 positions): lane `lane` of quadrant
-// `quad` holds output row 32 quad + lane of the block, v[i] the accumulator of
-// column col0 + i (col0 = the chunk's first sorted position, a multiple of 32), fr
-// the row factor.  The largest |y| over the chunk's nc columns that hold a
-// pair and the 8 rows of the lane's group (three exchanges) sets the shift
-// that moves it into [2^14, 2^15); each element is stored as f16(y * 2^shift)
-// (relative error at most 2^-11 for every element within 2^28 of that
-// largest) and the group's shift as one byte at
-// y_shift[col0 / 32][(block * 128 + row) / 8].  row_ok = the output row
-// exists.  All 32 lanes call it.
-__device__ __forceinline__ void store_y16_chunk(const GroupedGemm& g, const uint32_t v[32], float fr,
-                                                int block, int quad, int lane, int col0, int nc,
-                                                bool row_ok) {
-    float y[32];
-    float mx = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        y[i] = __uint_as_float(v[i]) * fr;
-        if (i < nc) mx = fmaxf(mx, fabsf(y[i]));
-    }
-    if (!row_ok) mx = 0.0f;
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    if (!row_ok) return;
-    const int sh = f32_f16_shift(__float_as_uint(mx));
-    const float up = __uint_as_float((uint32_t)(127 + sh) << 23);
-    const int row = block * 128 + 32 * quad + lane;
-    uint16_t* yb = g.y16_out + (size_t)col0 * g.y_rows_pad + row;
-#pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-        const __half2 h = __floats2half2_rn(y[i] * up, y[i + 1] * up);
-        if (i < nc) yb[(size_t)i * g.y_rows_pad] = __half_as_ushort(__low2half(h));
-        if (i + 1 < nc) yb[(size_t)(i + 1) * g.y_rows_pad] = __half_as_ushort(__high2half(h));
-    }
-    if ((lane & 7) == 0) g.y_shift[(size_t)(col0 / 32) * (g.y_rows_pad / 8) + row / 8] = (int8_t)sh;
-}
-
 template <int N, bool PAIR>
 struct PrefillSmem {
     // 128-row weight blocks per work item and CTA.  The blocks share the

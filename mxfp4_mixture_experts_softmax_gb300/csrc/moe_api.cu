@@ -697,7 +697,7 @@ moe_status_t moe_ffn(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, 
 // scales [cap, I/32], routing weight per position fp32 [cap], y fp32 blocked
 // [H/128, cap, 128]; each region starts on a 256-byte boundary.
 struct MxLayoutWs {
-    size_t xc, xs, xg, xgs, hc, hs, wpos, y, total;
+    size_t xc, xs, xg, xgs, hc, hs, wpos, y, ysh, total;
 };
 
 static bool mx_layout(int T, int H, int I, int Et, int Kt, int tile_m, MxLayoutWs* L) {
@@ -711,7 +711,9 @@ static bool mx_layout(int T, int H, int I, int Et, int Kt, int tile_m, MxLayoutW
     L->hs = L->hc + round_up((size_t)cap * (I / 2), 256);
     L->wpos = L->hs + round_up((size_t)cap * (I / 32), 256);
     L->y = L->wpos + round_up((size_t)cap * sizeof(float), 256);
-    L->total = L->y + round_up((size_t)cap * H * sizeof(float), 256);
+    const size_t hpad = (size_t)(H + 127) / 128 * 128;
+    L->ysh = L->y + round_up((size_t)cap * hpad * sizeof(uint16_t), 256);
+    L->total = L->ysh + round_up((size_t)((cap + 31) / 32) * (hpad / 8), 256);
     return true;
 }
 
@@ -817,7 +819,10 @@ moe_status_t moe_ffn_mxfp4act_down(const uint8_t* w2, const uint8_t* s2, const f
     g.act_rows = (int)cap;
     g.act_scales = reinterpret_cast<const uint8_t*>(ws + L.hs);
     g.sf_tma = I % 512 == 0 ? 1 : 0;
-    g.y_out = reinterpret_cast<float*>(ws + L.y);
+    g.y_blocked = 1;
+    g.y16_out = reinterpret_cast<uint16_t*>(ws + L.y);
+    g.y_shift = reinterpret_cast<int8_t*>(ws + L.ysh);
+    g.y_rows_pad = (H + 127) / 128 * 128;
     g.topk_w = topk_w;
     float* w_pos = reinterpret_cast<float*>(ws + L.wpos);
     trace("moe_ffn_mxfp4act_down", T, H, I, Et, Kt, tile_m, MOE_PATH_PREFILL);
@@ -826,8 +831,8 @@ moe_status_t moe_ffn_mxfp4act_down(const uint8_t* w2, const uint8_t* s2, const f
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     err = launch_gemm_timed([&] { return launch_mxfp4act_down(g, stream); }, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    return cuda_status(launch_combine_blocked(g.y_out, inv_pairs, w_pos, T, H, Kt, (int)cap, out,
-                                              stream));
+    return cuda_status(launch_combine_blocked_f16(g.y16_out, g.y_shift, inv_pairs, w_pos, T, H, Kt,
+                                                  (int)cap, out, stream));
 }
 
 moe_status_t moe_ffn_mxfp4act(const uint16_t* x, const uint8_t* w13, const uint8_t* s13,

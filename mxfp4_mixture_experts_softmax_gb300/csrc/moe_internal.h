@@ -75,9 +75,8 @@ struct GroupedGemm {
     // token for gate_up, by position for down)
     int sf_tma;
     int y_blocked;               // down: y by sorted position instead of [pair][rows], without
-                                 // the column factor (MXFP4 path: fp32 [ceil(rows/128)][act_rows][128];
-                                 // prefill path: the staged f16 rows below)
-    // prefill path: y16_out [act_rows][y_rows_pad] holds f16(y * 2^shift),
+                                 // the column factor, staged as the f16 rows below
+    // y16_out [act_rows][y_rows_pad] holds f16(y * 2^shift),
     // y_shift [ceil(act_rows/32)][y_rows_pad/8] the shift of each (8 output
     // rows, 32 positions) group, y_rows_pad = rows rounded up to 128
     uint16_t* y16_out = nullptr;
@@ -199,6 +198,45 @@ __device__ __forceinline__ int checked_pair(const GroupedGemm& g, int pos) {
     return q;
 }
 
+// One 32-column chunk of a down item's y (the prefill and MXFP4-activation
+// down GEMMs), staged as f16 rows by sorted position (y16_out [act_rows][y_rows_pad]) scaled by a power of two per
+// (8 output rows, 32 positions): lane `lane` of quadrant
+// `quad` holds output row 32 quad + lane of the block, v[i] the accumulator of
+// column col0 + i (col0 = the chunk's first sorted position, a multiple of 32), fr
+// the row factor.  The largest |y| over the chunk's nc columns that hold a
+// pair and the 8 rows of the lane's group (three exchanges) sets the shift
+// that moves it into [2^14, 2^15); each element is stored as f16(y * 2^shift)
+// (relative error at most 2^-11 for every element within 2^28 of that
+// largest) and the group's shift as one byte at
+// y_shift[col0 / 32][(block * 128 + row) / 8].  row_ok = the output row
+// exists.  All 32 lanes call it.
+__device__ __forceinline__ void store_y16_chunk(const GroupedGemm& g, const uint32_t v[32], float fr,
+                                                int block, int quad, int lane, int col0, int nc,
+                                                bool row_ok) {
+    float y[32];
+    float mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        y[i] = __uint_as_float(v[i]) * fr;
+        if (i < nc) mx = fmaxf(mx, fabsf(y[i]));
+    }
+    if (!row_ok) mx = 0.0f;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    if (!row_ok) return;
+    const int sh = f32_f16_shift(__float_as_uint(mx));
+    const float up = __uint_as_float((uint32_t)(127 + sh) << 23);
+    const int row = block * 128 + 32 * quad + lane;
+    uint16_t* yb = g.y16_out + (size_t)col0 * g.y_rows_pad + row;
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const __half2 h = __floats2half2_rn(y[i] * up, y[i + 1] * up);
+        if (i < nc) yb[(size_t)i * g.y_rows_pad] = __half_as_ushort(__low2half(h));
+        if (i + 1 < nc) yb[(size_t)(i + 1) * g.y_rows_pad] = __half_as_ushort(__high2half(h));
+    }
+    if ((lane & 7) == 0) g.y_shift[(size_t)(col0 / 32) * (g.y_rows_pad / 8) + row / 8] = (int8_t)sh;
+}
+
 // MXFP4 activations: codes [rows][cols/2] and scales [rows][cols/32] of bf16
 // rows (cols a multiple of 32), OCP MX rounding (see ffn_mxfp4act.cu).
 cudaError_t launch_quantize_mxfp4(const uint16_t* x, int rows, int cols, uint8_t* codes,
@@ -216,15 +254,13 @@ cudaError_t launch_gather_mx_rows(const uint8_t* xc, const uint8_t* xs, int H, b
 cudaError_t launch_position_weights(const int32_t* sorted_pairs, const float* topk_w,
                                     const float* rscale, const int32_t* num_tiles, int tile_m,
                                     int cap, int num_pairs, float* w_pos, cudaStream_t s);
-// the same for y staged as f16 with a power-of-two shift per (8 output
-// rows, 32 positions): y = y16 * 2^-shift (exact), then as above
+// out[t, m] = bf16(sum over the Kt slots j ascending of f[p] * y[p][m]), p =
+// inv[t * Kt + j], for y staged by the down epilogues (store_y16_chunk) as f16
+// rows by position with a power-of-two shift per (8 output rows, 32
+// positions): y = y16 * 2^-shift (exact); f null: factor 1
 cudaError_t launch_combine_blocked_f16(const uint16_t* y16, const int8_t* shift, const int32_t* inv,
                                        const float* f, int T, int H, int Kt, int cap, uint16_t* out,
                                        cudaStream_t s);
-// out = bf16(sum over the Kt slots of f[p] * y[m / 128][p][m % 128], p =
-// inv[pair]) for the down GEMMs' blocked y (f null: factor 1)
-cudaError_t launch_combine_blocked(const float* y, const int32_t* inv, const float* f, int T, int H,
-                                   int Kt, int cap, uint16_t* out, cudaStream_t s);
 // block-scaled MXFP4 x MXFP4 grouped GEMMs (tcgen05 kind::mxf4)
 cudaError_t launch_mxfp4act_gate_up(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_mxfp4act_down(const GroupedGemm& g, cudaStream_t s);

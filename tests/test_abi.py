@@ -107,13 +107,14 @@ def test_mxfp4act_host_validation_and_layout(lib):
                                               ctypes.byref(so)) == m.MOE_OK
         assert co.value % 256 == 0 and so.value % 256 == 0
         assert so.value >= co.value + cap * (I // 2)
-        # y (blocked, fp32 [H/128, cap, 128]) and the rest follow the scales
-        assert ws >= so.value + cap * (I // 32) + cap * H * 4
+        # the position weights, y (staged f16 rows by position [cap, H]) and its
+        # shift bytes ([ceil(cap/32), H/8]) follow the scales
+        assert ws >= so.value + cap * (I // 32) + cap * 4 + cap * H * 2 + (cap + 31) // 32 * (H // 8)
     assert lib.moe_ffn_mxfp4act_h_offsets(4, 256, 128, 8, 2, 32, None, None) == m.MOE_ERR_INVALID_ARG
 
 
-def test_bf16_workspace_holds_blocked_y_for_prefill_tiles(lib):
-    """moe_ffn_down_combine's prefill path writes y blocked over cap
+def test_bf16_workspace_holds_staged_y_for_prefill_tiles(lib):
+    """moe_ffn_down_combine's prefill path writes y as f16 rows over cap
     positions: the workspace reserves that much for prefill tile heights."""
     from mxfp4_mixture_experts_softmax_gb300 import libmoe as m
     H, I, Et, Kt = 4096, 1024, 513, 11
@@ -122,7 +123,7 @@ def test_bf16_workspace_holds_blocked_y_for_prefill_tiles(lib):
         ws = m.moe_ffn_workspace_size(T, H, I, Et, Kt, tm)
         y_off = m.moe_ffn_y_offset(T, I, Et, Kt, tm)
         assert y_off % 256 == 0 and y_off >= cap * I * 2
-        assert ws >= y_off + cap * H * 4
+        assert ws >= y_off + max(T * Kt * H * 4, cap * H * 2)
 
 
 def test_gemm_events_hook_argument_rule(lib):
