@@ -51,9 +51,16 @@ namespace {
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kScaleWarp0 = 2;   // 2..5: warp % 4 covers every lane quadrant
-constexpr int kEpiWarp0 = 6;     // 6..9
-constexpr int kEpiThreads = 128;
-constexpr int kThreads = (kEpiWarp0 + 4) * 32;  // 320
+constexpr int kEpiWarp0 = 6;     // 6..9 (gate_up), 6.. (down)
+constexpr int kEpiThreads = 128;  // gate_up's epilogue warps, which meet at named barrier 1
+// the down epilogue (staging y as f16, store-bound) has one warp per lane
+// quadrant and 32-column chunk (two per quadrant at N = 256, where registers
+// allow no more), warp h of a quadrant draining chunks h, h + 2, ...
+// (skewed 8192-token MXFP4 step, down GEMM: 4 warps 422 us, 8: 366, 16: 349)
+template <int MODE, int N>
+constexpr int mx_epi_warps() { return MODE == 1 ? (N == 256 ? 8 : 4 * (N / 32)) : 4; }
+template <int MODE, int N>
+constexpr int mx_threads() { return (kEpiWarp0 + mx_epi_warps<MODE, N>()) * 32; }
 constexpr int kBK = 256;                         // k per stage: one 128-byte row of packed codes
 constexpr int kRowBytes = kBK / 2;
 constexpr int kABytes = 128 * kRowBytes;         // 16 KB weight stage
@@ -224,7 +231,7 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
 __device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 template <int MODE, int N>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(mx_threads<MODE, N>(), 1)
     mxf4_gemm_kernel(const GroupedGemm g, const __grid_constant__ CUtensorMap a_map,
                      const __grid_constant__ CUtensorMap b_map,
                      const __grid_constant__ CUtensorMap sfa_map,
@@ -263,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_free[b], 4);
+            mbar_init(&acc_free[b], mx_epi_warps<MODE, N>());
         }
         mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -483,14 +490,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!acc_ok) break;
             tc_fence_after();
             load_pairs(item + gridDim.x);
+            // down: warp h of a quadrant drains chunks 32 h, 32 (h + kPerQuad), ...
+            constexpr int kPerQuad = mx_epi_warps<MODE, N>() / 4;
+            const int half = MODE == 1 ? (warp - kEpiWarp0) >> 2 : 0;
+            constexpr int kCStep = 32 * kPerQuad;
+            if (32 * half >= N) {  // no chunk for this warp (narrow tiles)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_free[b]);
+            }
 #pragma unroll 1
-            for (int c0 = 0; c0 < N; c0 += 32) {
+            for (int c0 = 32 * half; c0 < N; c0 += kCStep) {
                 uint32_t v[32];
                 const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + b * N + (uint32_t)c0;
                 tmem_ld16_nowait(taddr, v);
                 tmem_ld16_nowait(taddr + 16, v + 16);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (c0 + 32 == N) {  // the accumulator is drained: the next item may use it
+                if (c0 + kCStep >= N) {  // this warp's part is drained: the next item may use it
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&acc_free[b]);
@@ -573,8 +589,8 @@ cudaError_t launch_n(const GroupedGemm& g, cudaStream_t s) {
     const int row_blocks = MODE == 0 ? g.I / 64 : g.rows / 128;
     const long long max_items = (long long)g.max_tiles * row_blocks;
     const int grid = (int)std::min<long long>(max_items, (long long)num_sms());
-    return launch_pdl(mxf4_gemm_kernel<MODE, N>, dim3(grid), dim3(kThreads), smem, s, g, a_map, b_map,
-                      sfa_map, sfb_map);
+    return launch_pdl(mxf4_gemm_kernel<MODE, N>, dim3(grid), dim3(mx_threads<MODE, N>()), smem, s, g, a_map,
+                      b_map, sfa_map, sfb_map);
 }
 
 template <int MODE>
