@@ -29,14 +29,15 @@
 //     column q), and token column n's at lane 32 q + n % 32, column base +
 //     n / 32 in every quadrant q; byte j of a 32-bit cell is k group j of a
 //     128-k chunk, the MMA's scale id (0 or 2) picks the pair of groups;
-//   * 4 epilogue warps: down stores the fp32 accumulator to y blocked as
-//     [H/128][cap][128] (row block, sorted position, row in block), so an
-//     item's output is one contiguous 64 KB run of DRAM writes; the combine
-//     gathers each token's positions from it and applies the routing weight
-//     there (the same fp32 product the epilogue would form); gate_up passes each 32-column slice of the
-//     accumulator through shared memory (transposed), so each thread holds
-//     16 consecutive i of one token: SwiGLU in fp32, then MXFP4 quantisation
-//     of each 32-block of i (two threads per block), codes and scale stored.
+//   * epilogue warps: down (one warp per lane quadrant and 32-column chunk)
+//     stages the accumulator of the positions holding a pair as f16 rows by
+//     sorted position, scaled by a power of two per (8 rows, 32 positions)
+//     (store_y16_chunk); the combine gathers each token's positions from it
+//     and applies the routing weight there; gate_up (4 warps) passes each
+//     32-column slice of the accumulator through shared memory (transposed),
+//     so each thread holds 16 consecutive i of one token: SwiGLU in fp32, then
+//     MXFP4 quantisation of each 32-block of i (two threads per block), codes
+//     and scale stored.
 // Every wait is bounded (see mbar_wait); after a timeout each role stops, the
 // MMA thread drains its own MMAs (bounded), and tensor memory is freed.
 #include <algorithm>

@@ -1131,8 +1131,9 @@ __global__ void __launch_bounds__(256) gather_rows_f16_kernel(const uint4* __res
 // (8 output rows, 32 positions) ([cap/32][Hpad/8] bytes).  8 consecutive m per
 // thread, so one shift per slot: the slot's factor f[p] * 2^-shift is exact
 // (a power of two times f[p]; the products it could push below the normal
-// range are below 2^-110) and each term f[p] * y is rounded once, then added
-// in slot order, like combine_blocked_kernel's.  S slots' loads are in flight
+// range are below 2^-110) and each term f[p] * y is rounded once (no fused
+// multiply-add), then added in slot order, as moe_combine sums.  S slots'
+// loads are in flight
 // at a time: their index loads first, then their y loads.  S = 2 measured
 // fastest on the 8192-token prefill (155 µs; 173 µs with 1, ~190 µs with 4,
 // ~355 µs with 12, where the register count halves the resident warps).

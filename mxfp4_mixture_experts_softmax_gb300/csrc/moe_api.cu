@@ -694,8 +694,9 @@ moe_status_t moe_ffn(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, 
 // ------------------------------------------------ MXFP4-quantised activations
 // Workspace: x codes [T, H/2], x scales [T, H/32], x codes and scales
 // gathered into tile order [cap, H/2] and [cap, H/32], h codes [cap, I/2], h
-// scales [cap, I/32], routing weight per position fp32 [cap], y fp32 blocked
-// [H/128, cap, 128]; each region starts on a 256-byte boundary.
+// scales [cap, I/32], routing weight per position fp32 [cap], y staged as f16
+// rows by position [cap, Hpad] and its shift bytes [ceil(cap/32), Hpad/8]
+// (Hpad = H rounded up to 128); each region starts on a 256-byte boundary.
 struct MxLayoutWs {
     size_t xc, xs, xg, xgs, hc, hs, wpos, y, ysh, total;
 };

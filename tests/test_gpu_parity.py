@@ -573,9 +573,9 @@ def test_decode_and_prefill_paths_agree_on_every_token(name):
                                               (libmoe.MOE_PATH_DECODE, 8, "ragged37")])
 def test_down_combine_equals_down_then_combine(path, tile_m, name):
     """moe_ffn_down_combine gives the bytes of moe_ffn_down followed by
-    moe_combine (y by pair) on the decode path; on the prefill path (y blocked
-    and staged as scaled f16) it agrees with them to the staging bound; both
-    meet the bar."""
+    moe_combine (y by pair) on the decode path; on the prefill path (y staged
+    as scaled f16 rows by position) it agrees with them to the staging bound;
+    both meet the bar."""
     w = synth.scaled(synth.WORKLOADS["tiny16"], **SMALL[name])
     d, ids, wt = _layer_inputs(w)
     dw = gc.upload_weights(d)
