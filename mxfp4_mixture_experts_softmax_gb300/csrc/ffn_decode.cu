@@ -406,7 +406,9 @@ __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* src, u
 
 // out[t][m] = bf16(sum over j ascending of y[t*Kt + j][m], then + y2[t][m] when
 // y2 is given: a shared expert run as a separate dense MLP comes last, where
-// the fused shared slot K would be); four columns per thread.
+// the fused shared slot K would be); four columns per thread.  Four slots'
+// loads are issued before their adds (the sum keeps slot order): a thread
+// then waits on about Kt / 4 load round trips instead of Kt.
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y,
                                                       const float4* __restrict__ y2, int T, int H4,
                                                       int Kt, uint2* __restrict__ out) {
@@ -416,12 +418,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
     const size_t t = i / H4, m = i % H4;
     const float4* yt = y + t * Kt * H4 + m;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < Kt; ++j) {
-        const float4 v = __ldg(yt + (size_t)j * H4);
-        a.x += v.x;
-        a.y += v.y;
-        a.z += v.z;
-        a.w += v.w;
+    for (int j0 = 0; j0 < Kt; j0 += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (j0 + u < Kt) v[u] = __ldg(yt + (size_t)(j0 + u) * H4);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (j0 + u >= Kt) break;
+            a.x += v[u].x;
+            a.y += v[u].y;
+            a.z += v[u].z;
+            a.w += v[u].w;
+        }
     }
     if (y2) {
         const float4 v = __ldg(y2 + t * H4 + m);
