@@ -219,47 +219,59 @@ __global__ void __launch_bounds__(kThreads) permute_count_kernel(const int32_t* 
 }
 
 // 2. one block: scratch[b][e] = off[e] + pairs of expert e in blocks < b;
-//    offsets and the tile count
+//    offsets and the tile count.  The work is split into units of one
+//    expert's counts in 16 consecutive blocks (a chunk), spread over all the
+//    block's threads (all 16 loads of a unit issued before any store that
+//    depends on them: a store to the same array would otherwise order every
+//    later load behind it).  csum holds each unit's sum, then its first
+//    position within the expert.
 __global__ void __launch_bounds__(kThreads, 1)
     permute_scan_kernel(int nb, int Et, int tile_m, int32_t* __restrict__ scratch,
                         int32_t* __restrict__ offsets_out, int32_t* __restrict__ num_tiles) {
     pdl_begin();
     extern __shared__ int32_t sh[];
-    int32_t* cnt = sh;            // [Et]
-    int32_t* off = cnt + Et;      // [Et + 1]
-    int32_t* wsum = off + Et + 1; // [kWarps]
-    // Each thread walks its expert's column of nb counts in chunks of 16,
-    // all 16 loads issued before any store that depends on them (a store to
-    // the same array would otherwise order every load behind the previous
-    // store: one L2 round trip per block).
+    int32_t* cnt = sh;              // [Et]
+    int32_t* off = cnt + Et;        // [Et + 1]
+    int32_t* wsum = off + Et + 1;   // [kWarps]
+    int32_t* csum = wsum + kWarps;  // [chunks][Et]
     constexpr int kChunk = 16;
+    const int nch = (nb + kChunk - 1) / kChunk;
+    const int units = nch * Et;  // unit u: expert u % Et, chunk u / Et
+    for (int u = threadIdx.x; u < units; u += kThreads) {
+        const int e = u % Et, b0 = (u / Et) * kChunk;
+        int c[kChunk];
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) c[j] = b0 + j < nb ? scratch[(size_t)(b0 + j) * Et + e] : 0;
+        int sum = 0;
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) sum += c[j];
+        csum[u] = sum;
+    }
+    __syncthreads();
     for (int e = threadIdx.x; e < Et; e += kThreads) {
         int run = 0;
-        for (int b0 = 0; b0 < nb; b0 += kChunk) {
-            int c[kChunk];
-#pragma unroll
-            for (int j = 0; j < kChunk; ++j) c[j] = b0 + j < nb ? scratch[(size_t)(b0 + j) * Et + e] : 0;
-#pragma unroll
-            for (int j = 0; j < kChunk; ++j) run += c[j];
+        for (int k = 0; k < nch; ++k) {
+            const int v = csum[k * Et + e];
+            csum[k * Et + e] = run;
+            run += v;
         }
         cnt[e] = run;
     }
     __syncthreads();
     padded_offsets(cnt, Et, tile_m, off, wsum);
     __syncthreads();
-    for (int e = threadIdx.x; e < Et; e += kThreads) {
-        int run = off[e];
-        for (int b0 = 0; b0 < nb; b0 += kChunk) {
-            int c[kChunk];
+    for (int u = threadIdx.x; u < units; u += kThreads) {
+        const int e = u % Et, b0 = (u / Et) * kChunk;
+        int c[kChunk];
 #pragma unroll
-            for (int j = 0; j < kChunk; ++j) c[j] = b0 + j < nb ? scratch[(size_t)(b0 + j) * Et + e] : 0;
+        for (int j = 0; j < kChunk; ++j) c[j] = b0 + j < nb ? scratch[(size_t)(b0 + j) * Et + e] : 0;
+        int run = off[e] + csum[u];
 #pragma unroll
-            for (int j = 0; j < kChunk; ++j)
-                if (b0 + j < nb) {
-                    scratch[(size_t)(b0 + j) * Et + e] = run;
-                    run += c[j];
-                }
-        }
+        for (int j = 0; j < kChunk; ++j)
+            if (b0 + j < nb) {
+                scratch[(size_t)(b0 + j) * Et + e] = run;
+                run += c[j];
+            }
     }
     for (int e = threadIdx.x; e <= Et; e += kThreads) offsets_out[e] = off[e];
     if (threadIdx.x == 0) *num_tiles = off[Et] / tile_m;
@@ -413,8 +425,10 @@ cudaError_t launch_permute(const int32_t* ids, int T, int Kt, int Et, int tile_m
     const int slice = (P + nb - 1) / nb;
     int32_t* scratch = inv;  // nb * Et <= P ints, rewritten by the last step
     const size_t hist_smem = sizeof(int32_t) * (size_t)kWarps * Et;
-    const size_t scan_smem = sizeof(int32_t) * (2 * (size_t)Et + 1 + kWarps);
+    const size_t scan_smem =
+        sizeof(int32_t) * (2 * (size_t)Et + 1 + kWarps + (size_t)((nb + 15) / 16) * Et);
     cudaError_t err = ensure_dynamic_smem((const void*)permute_scatter_kernel, hist_smem);
+    if (err == cudaSuccess) err = ensure_dynamic_smem((const void*)permute_scan_kernel, scan_smem);
     if (err == cudaSuccess)
         err = launch_pdl(permute_count_kernel, dim3(nb), dim3(kThreads), sizeof(int32_t) * Et, s,
                          ids, P, Et, slice, cap, scratch, sorted_pairs);
