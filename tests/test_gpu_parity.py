@@ -511,6 +511,24 @@ def test_prefill_tile_m_and_permutation_invariance():
                                   2 * outs[0])
 
 
+@pytest.mark.parametrize("path,tile_m", [(libmoe.MOE_PATH_DECODE, 8), (libmoe.MOE_PATH_PREFILL, 32),
+                                         (libmoe.MOE_PATH_PREFILL, 128)])
+def test_many_slots_per_token(path, tile_m):
+    """Top-16 plus the shared expert (17 slots, an odd count above the
+    combines' groups of loads) over 40 experts: every output element meets
+    the bar on the decode path, the single-CTA prefill kernel and the CTA
+    pairs."""
+    w = synth.scaled(synth.WORKLOADS["tiny16"], T=40, H=256, I=128, E=40, K=16, with_shared=True,
+                     seed=17)
+    d, ids, wt = _layer_inputs(w)
+    assert ids.shape[1] == 17
+    ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt,
+                                    n_threads=THREADS))
+    got = _gpu_ffn(d, ids, wt, w.Et, tile_m, path)
+    gc.ffn_parity(got, ref, f"17 slots path={path} tile_m={tile_m}")
+    assert libmoe.moe_device_error() == 0
+
+
 PREFILL_FULL = {  # workload -> (tile_m as the bench runs it, tokens compared: None = all)
     "mtp_verify288": (32, None),
     "prefill1536": (64, None),
