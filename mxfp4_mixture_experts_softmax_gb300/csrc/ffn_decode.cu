@@ -371,36 +371,46 @@ cudaError_t launch_mode(const GroupedGemm& g, cudaStream_t s) {
 // element that stays in the f16 normal range converts exactly.  Rows are
 // either all `rows` rows, or (sorted_pairs given) the positions of the used
 // tiles that hold a pair.  src may equal dst: each lane reads its elements
-// before it writes them.
+// before it writes them.  independent: the rows are the caller's input (x),
+// read and written by no kernel between the last one that waited on its
+// predecessors and this one, so the work runs before the wait on the
+// previous kernel and overlaps it (the permutation, which signals its
+// dependents as soon as its own wait is over); every thread still waits
+// before it exits, so this grid completes only after its predecessor has.
 __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* src, uint16_t* dst,
                                                           int cols, int rows,
                                                           const int32_t* __restrict__ sorted_pairs,
                                                           const int32_t* __restrict__ num_tiles,
-                                                          int tile_m, float* __restrict__ rscale) {
-    pdl_begin();
+                                                          int tile_m, float* __restrict__ rscale,
+                                                          int independent) {
+    if (!independent) pdl_begin();
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    if (sorted_pairs && (row >= __ldg(num_tiles) * tile_m || __ldg(sorted_pairs + row) < 0)) return;
-    const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)row * cols);
-    uint4* d4 = reinterpret_cast<uint4*>(dst + (size_t)row * cols);
-    const int n16 = cols / 8;
-    uint32_t mx = 0;  // max |bf16| bit pattern (orders like the magnitude)
-    for (int i = lane; i < n16; i += 32) {
-        const uint4 v = s4[i];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    bool active = row < rows;
+    if (active && sorted_pairs)
+        active = row < __ldg(num_tiles) * tile_m && __ldg(sorted_pairs + row) >= 0;
+    if (active) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)row * cols);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + (size_t)row * cols);
+        const int n16 = cols / 8;
+        uint32_t mx = 0;  // max |bf16| bit pattern (orders like the magnitude)
+        for (int i = lane; i < n16; i += 32) {
+            const uint4 v = s4[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
-    }
+            for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+        }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    const int sigma = row_f16_shift(mx);
-    const float up = __uint_as_float((uint32_t)(127 + sigma) << 23);
-    for (int i = lane; i < n16; i += 32) {
-        const uint4 v = s4[i];
-        d4[i] = make_uint4(bf16x2_to_f16x2_scaled(v.x, up), bf16x2_to_f16x2_scaled(v.y, up),
-                           bf16x2_to_f16x2_scaled(v.z, up), bf16x2_to_f16x2_scaled(v.w, up));
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        const int sigma = row_f16_shift(mx);
+        const float up = __uint_as_float((uint32_t)(127 + sigma) << 23);
+        for (int i = lane; i < n16; i += 32) {
+            const uint4 v = s4[i];
+            d4[i] = make_uint4(bf16x2_to_f16x2_scaled(v.x, up), bf16x2_to_f16x2_scaled(v.y, up),
+                               bf16x2_to_f16x2_scaled(v.z, up), bf16x2_to_f16x2_scaled(v.w, up));
+        }
+        if (lane == 0) rscale[row] = __uint_as_float((uint32_t)(127 - sigma) << 23);
     }
-    if (lane == 0) rscale[row] = __uint_as_float((uint32_t)(127 - sigma) << 23);
+    if (independent) pdl_begin();
     pdl_end();
 }
 
@@ -457,10 +467,10 @@ cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s) { return la
 
 cudaError_t launch_rows_to_f16(const uint16_t* src, uint16_t* dst, int cols, int rows,
                                const int32_t* sorted_pairs, const int32_t* num_tiles, int tile_m,
-                               float* rscale, cudaStream_t s) {
+                               float* rscale, cudaStream_t s, bool independent) {
     if (rows <= 0) return cudaSuccess;
     return launch_pdl(rows_to_f16_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, src, dst, cols,
-                      rows, sorted_pairs, num_tiles, tile_m, rscale);
+                      rows, sorted_pairs, num_tiles, tile_m, rscale, independent ? 1 : 0);
 }
 
 // Waits on a barrier that nothing arrives at: the bounded wait gives up after

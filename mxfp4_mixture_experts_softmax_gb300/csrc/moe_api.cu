@@ -457,7 +457,8 @@ moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_
     g.act_rscale = rs_x;  // indexed by token
     cudaError_t err;
     if (path == MOE_PATH_DECODE) {
-        err = launch_rows_to_f16(x, x16, H, T, nullptr, nullptr, tile_m, rs_x, stream);
+        err = launch_rows_to_f16(x, x16, H, T, nullptr, nullptr, tile_m, rs_x, stream,
+                                 /*independent=*/true);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         g.act = x16;
         g.act_rows = T;

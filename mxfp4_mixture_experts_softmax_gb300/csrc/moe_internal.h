@@ -143,10 +143,12 @@ bool prefill_shape_supported(int H, int I);
 cudaError_t launch_decode_gate_up(const GroupedGemm& g, cudaStream_t s);
 // dst[row] = f16(src[row] * 2^sigma_row), rscale[row] = 2^-sigma_row (the
 // decode GEMMs' B rows); every row, or with sorted_pairs the used positions
-// that hold a pair.  src may equal dst.
+// that hold a pair.  src may equal dst.  independent: src is the layer's
+// input, touched by no kernel since the last one that waited on all before
+// it, so the conversion may overlap its predecessor (see rows_to_f16_kernel).
 cudaError_t launch_rows_to_f16(const uint16_t* src, uint16_t* dst, int cols, int rows,
                                const int32_t* sorted_pairs, const int32_t* num_tiles, int tile_m,
-                               float* rscale, cudaStream_t s);
+                               float* rscale, cudaStream_t s, bool independent = false);
 cudaError_t launch_decode_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_prefill_gate_up(const GroupedGemm& g, cudaStream_t s);
 // xg[p] = f16(x[t] * 2^sigma_t), t = sorted_pairs[p] / Kt, for the rows of

@@ -356,9 +356,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                    int32_t* __restrict__ offsets_out, int32_t* __restrict__ inv,
                    int32_t* __restrict__ tile_expert, int32_t* __restrict__ num_tiles) {
     pdl_begin();
+    // one block on one SM: the next kernel may start right away (every kernel
+    // of the layer waits on this one before it reads what it writes; one that
+    // needs none of it overlaps it, see rows_to_f16_kernel)
+    pdl_end();
     permute_block<false>(ids, P, Et, tile_m, cap, max_tiles, sorted_pairs, offsets_out, inv,
                          tile_expert, num_tiles);
-    pdl_end();
 }
 
 template <int VPL>
