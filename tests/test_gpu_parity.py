@@ -529,6 +529,42 @@ def test_many_slots_per_token(path, tile_m):
     assert libmoe.moe_device_error() == 0
 
 
+def _random_case(seed):
+    """A seeded random layer shape and launch configuration: widths multiples
+    of 32 (H of 128 for an even number of 128-row blocks only some of the
+    time, so the CTA-pair launcher also falls back to the single-CTA kernel),
+    1-40 experts, top-1 to top-12, with or without the shared expert, and a
+    tile height and path the shape allows."""
+    rng = np.random.default_rng(1000 + seed)
+    H = int(rng.choice([128, 256, 384, 512, 640, 1024]))
+    I = int(rng.choice([64, 96, 128, 192, 256, 384]))
+    E = int(rng.integers(1, 41))
+    K = int(rng.integers(1, min(E, 12) + 1))
+    T = int(rng.integers(1, 260))
+    shared = bool(rng.integers(0, 2))
+    path, tile_m = [(libmoe.MOE_PATH_DECODE, 8), (libmoe.MOE_PATH_DECODE, 16),
+                    (libmoe.MOE_PATH_DECODE, 64), (libmoe.MOE_PATH_PREFILL, 32),
+                    (libmoe.MOE_PATH_PREFILL, 64), (libmoe.MOE_PATH_PREFILL, 128),
+                    (libmoe.MOE_PATH_PREFILL, 256)][int(rng.integers(0, 7))]
+    w = synth.scaled(synth.WORKLOADS["tiny16"], T=T, H=H, I=I, E=E, K=K, with_shared=shared,
+                     seed=50 + seed)
+    return w, path, tile_m
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes_every_path(seed):
+    """Seeded random shapes and launch configurations, every output element
+    against the oracle at the bar."""
+    w, path, tile_m = _random_case(seed)
+    d, ids, wt = _layer_inputs(w)
+    ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt,
+                                    n_threads=THREADS))
+    got = _gpu_ffn(d, ids, wt, w.Et, tile_m, path)
+    gc.ffn_parity(got, ref, f"seed {seed}: T={w.T} H={w.H} I={w.I} E={w.E} K={w.K} "
+                            f"shared={w.with_shared} path={path} tile_m={tile_m}")
+    assert libmoe.moe_device_error() == 0
+
+
 PREFILL_FULL = {  # workload -> (tile_m as the bench runs it, tokens compared: None = all)
     "mtp_verify288": (32, None),
     "prefill1536": (64, None),
