@@ -63,7 +63,7 @@ def parse_args():
                         "the mean rows per expert: 32 below 16, 64 below 64, else 128)")
     p.add_argument("--E", type=int, default=0,
                    help="routed experts override (smaller cases for profiler captures)")
-    p.add_argument("--path", default="auto", choices=["auto", "decode", "prefill"])
+    p.add_argument("--path", default="auto", choices=["auto", "decode", "prefill", "prefill_fp8x2"])
     p.add_argument("--replicas", type=int, default=2,
                    help="weight/input replicas rotated per step (keeps L2 cold)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -272,6 +272,8 @@ def launches_per_step(w, path_name: str) -> int:
       decode   x -> f16 rows, gate_up, h -> f16 rows | down, combine
       prefill  gather of x into tile order as f16 rows, gate_up, h -> f16
                rows | position weights, down, blocked combine
+      prefill_fp8x2  gather of x into tile order as two E4M3 terms, gate_up |
+               position weights, down, blocked combine
       mxfp4act quantise x, gather, gate_up | position weights, down, blocked
                combine"""
     from mxfp4_mixture_experts_softmax_gb300 import libmoe
@@ -281,7 +283,7 @@ def launches_per_step(w, path_name: str) -> int:
     else:
         nb = min(P // max(w.Et, 1), 160)
         rp = 1 + (4 if (nb >= 8 and P >= 8192) else 1)
-    return rp + {"decode": 3 + 2, "prefill": 3 + 3, "mxfp4act": 3 + 3}[path_name]
+    return rp + {"decode": 3 + 2, "prefill": 3 + 3, "prefill_fp8x2": 2 + 3, "mxfp4act": 3 + 3}[path_name]
 
 
 # ------------------------------------------------------------ ranks
@@ -322,14 +324,15 @@ class Layer:
         self.w, self.act, self.tm, self.dev = w, act, tm, dev
         self.mx = act == "mxfp4"
         self.path = {"auto": libmoe.MOE_PATH_AUTO, "decode": libmoe.MOE_PATH_DECODE,
-                     "prefill": libmoe.MOE_PATH_PREFILL}[path_arg]
+                     "prefill": libmoe.MOE_PATH_PREFILL,
+                     "prefill_fp8x2": libmoe.MOE_PATH_PREFILL_FP8X2}[path_arg]
+        resolved = (libmoe.moe_ffn_auto_path(w.T, w.Kt, w.Et, tm) if self.path == libmoe.MOE_PATH_AUTO
+                    else self.path)
         if self.mx:
             self.path_name = "mxfp4act"
-        elif path_arg == "prefill" or (path_arg == "auto" and libmoe.moe_ffn_auto_path(
-                w.T, w.Kt, w.Et, tm) == libmoe.MOE_PATH_PREFILL):
-            self.path_name = "prefill"
         else:
-            self.path_name = "decode"
+            self.path_name = {libmoe.MOE_PATH_DECODE: "decode", libmoe.MOE_PATH_PREFILL: "prefill",
+                              libmoe.MOE_PATH_PREFILL_FP8X2: "prefill_fp8x2"}[resolved]
         self.host = synth.make_inputs(w)
 
         def up(a):
@@ -555,7 +558,7 @@ class Layer:
         step either way: the steps' other launches (f16 row copies, the
         combine) add no algorithmic bytes."""
         src = {"prefill": "ffn_prefill.cu", "decode": "ffn_decode.cu",
-               "mxfp4act": "ffn_mxfp4act.cu"}[self.path_name]
+               "prefill_fp8x2": "ffn_fp8x2.cu", "mxfp4act": "ffn_mxfp4act.cu"}[self.path_name]
         traffic, traffic_src = traffic_from_profiles(
             f"{self.path_name}_gate_up", self.w.name,
             os.path.join(ROOT, "mxfp4_mixture_experts_softmax_gb300", "csrc", src))

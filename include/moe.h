@@ -69,7 +69,10 @@ typedef enum {
 typedef enum {
     MOE_PATH_AUTO = 0,
     MOE_PATH_DECODE = 1, /* small M: weights streamed through registers, mma.sync */
-    MOE_PATH_PREFILL = 2 /* large M: TMA + tcgen05 MMA with TMEM accumulators */
+    MOE_PATH_PREFILL = 2, /* large M: TMA + tcgen05 MMA with TMEM accumulators */
+    /* large M on the block-scaled tensor cores (tcgen05.mma kind::mxf8f6f4):
+     * the E2M1 weights as stored, each bf16 activation as two E4M3 terms */
+    MOE_PATH_PREFILL_FP8X2 = 3
 } moe_path_t;
 
 /* Static string for a status code (never NULL). */
@@ -169,9 +172,10 @@ moe_status_t moe_route_permute(const float* logits, const float* shared_w, int T
  * moe_ffn_workspace_size -- bytes of device workspace moe_ffn needs:
  * the 16-bit SwiGLU intermediate [cap, I], the weighted fp32 per-pair expert
  * outputs [T*Kt, H], x as f16 rows [T, H], when tile_m is a prefill tile
- * height (32, 64, 128, 256) their tile-ordered copy [cap, H], T + cap fp32
+ * height (32, 64, 96, 128, 256) their tile-ordered copy [cap, H], T + cap fp32
  * row factors, cap fp32 position weights and, for prefill tile heights, the
- * shift bytes of the staged y [ceil(cap/32), (H rounded up to 128) / 8];
+ * shift bytes of the staged y [ceil(cap/32), (H rounded up to 128) / 8] and
+ * the scale bytes of h's two E4M3 terms [2 cap, I/32] (MOE_PATH_PREFILL_FP8X2);
  * each 256-byte aligned.
  */
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
@@ -208,8 +212,16 @@ size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m);
  * path stores each weight row in f16 relative to its largest scale, exact
  * for every group whose scale is within 2^36 of that largest (groups further
  * below are rounded, at most 2^-37 of the row's largest weight).
+ * MOE_PATH_PREFILL_FP8X2 carries x and h instead as two E4M3 terms per
+ * value with an E8M0 scale per 32 values and term: per block of 32 with
+ * largest magnitude amax (biased fp32 exponent b), s_hi = max(b - 7, 0),
+ * s_lo = max(s_hi - 5, 0), u = v * 2^(127 - s_hi), hi = E4M3(u) and
+ * lo = E4M3((u - hi) * 2^(s_hi - s_lo)), nearest even (moe_split_e4m3x2):
+ * exact for every element within 2^14 of amax, smaller ones move by less
+ * than 2^-21 amax.  Its y goes to the combine as on the prefill path.
  * Limits: H % 32 == 0, I % 32 == 0, H, I <= 65536; the decode path needs
- * tile_m in {8, 16, 32, 64}, the prefill path tile_m in {32, 64, 128, 256}.
+ * tile_m in {8, 16, 32, 64}, the prefill path tile_m in {32, 64, 128, 256},
+ * MOE_PATH_PREFILL_FP8X2 tile_m in {32, 64, 96, 128} and H % 512 == I % 512 == 0.
  * Pointers 16-byte aligned.
  */
 moe_status_t moe_ffn(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,
@@ -424,6 +436,19 @@ moe_status_t moe_ffn_noalloc(const uint16_t* x, const uint8_t* w13, const uint8_
  *            above 6 saturating to 6, the sign of v_k kept
  * codes packed two per byte, element 2i in the low nibble.
  */
+
+/*
+ * moe_split_e4m3x2 -- the two-term E4M3 encoding MOE_PATH_PREFILL_FP8X2 gives
+ * its activations, of a bf16 matrix row by row (see moe_ffn):
+ *   x      bf16 [rows, cols] in (cols a multiple of 32).
+ *   q_hi, q_lo  uint8 [rows, cols] out: the E4M3 bytes of the two terms.
+ *   s_hi, s_lo  uint8 [rows, cols/32] out: their E8M0 scale bytes.
+ * x[r, c] == e4m3(q_hi) * 2^(s_hi - 127) + e4m3(q_lo) * 2^(s_lo - 127)
+ * exactly whenever |x[r, c]| >= 2^-14 of its block's largest magnitude.
+ * Device pointers; x, q_hi and q_lo 16-byte aligned.  Asynchronous on stream.
+ */
+moe_status_t moe_split_e4m3x2(const uint16_t* x, int rows, int cols, uint8_t* q_hi, uint8_t* q_lo,
+                              uint8_t* s_hi, uint8_t* s_lo, cudaStream_t stream);
 
 /*
  * moe_quantize_mxfp4 -- MXFP4 encoding of a bf16 matrix, row by row.

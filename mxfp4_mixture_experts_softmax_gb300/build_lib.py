@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "lib", "libmoe.so")
 SOURCES = ["moe_api.cu", "route.cu", "permute.cu", "ffn_decode.cu", "ffn_prefill.cu",
-           "ffn_mxfp4act.cu", "moe_noalloc.cu"]
+           "ffn_mxfp4act.cu", "ffn_fp8x2.cu", "moe_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I", os.path.join(ROOT, "include")]

@@ -195,11 +195,12 @@ int moe_version(void) { return 100; }
 moe_status_t moe_device_error(int* flag, int clear) {
     if (!flag) return MOE_ERR_INVALID_ARG;
     int a = 0, b = 0;
-    int c = 0;
+    int c = 0, d = 0;
     cudaError_t err = read_device_error_prefill(&a, clear);
     if (err == cudaSuccess) err = read_device_error_decode(&b, clear);
     if (err == cudaSuccess) err = read_device_error_mxfp4act(&c, clear);
-    *flag = a | b | c;
+    if (err == cudaSuccess) err = read_device_error_fp8x2(&d, clear);
+    *flag = a | b | c | d;
     return cuda_status(err);
 }
 
@@ -316,13 +317,17 @@ moe_status_t moe_route_permute(const float* logits, const float* shared_w, int T
                                             stream));
 }
 
+// Tile heights of the paths that gather B rows into tile order and stage y
+// by sorted position (prefill, and the two-term path's 96).
+static bool staged_tile(int tile_m) { return prefill_tile_supported(tile_m) || fp8x2_tile_supported(tile_m); }
+
 static size_t y_offset(int64_t cap, int I) { return round_up((size_t)cap * I * sizeof(uint16_t), 256); }
 
 // y: fp32 [T*Kt, H] by pair, or, for prefill tile heights, also room for the
 // f16 rows by position moe_ffn_down_combine writes ([cap][H rounded up to 128]).
 static size_t y_bytes(int64_t cap, int T, int H, int Kt, int tile_m) {
     size_t n = (size_t)T * Kt * H * sizeof(float);
-    if (prefill_tile_supported(tile_m))
+    if (staged_tile(tile_m))
         n = std::max(n, (size_t)((H + 127) / 128) * 128 * (size_t)cap * sizeof(uint16_t));
     return round_up(n, 256);
 }
@@ -340,7 +345,7 @@ static size_t xg_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) {
 }
 
 static size_t rs_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) {
-    const size_t xg = prefill_tile_supported(tile_m) ? round_up((size_t)cap * H * sizeof(uint16_t), 256) : 0;
+    const size_t xg = staged_tile(tile_m) ? round_up((size_t)cap * H * sizeof(uint16_t), 256) : 0;
     return xg_offset(cap, T, H, I, Kt, tile_m) + xg;
 }
 
@@ -355,12 +360,19 @@ static size_t yshift_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m
     return wpos_offset(cap, T, H, I, Kt, tile_m) + round_up((size_t)cap * sizeof(float), 256);
 }
 
+// After the shifts: the scale bytes of h's two E4M3 terms on the
+// MOE_PATH_PREFILL_FP8X2 path [2 cap][I/32] (its tile heights only).
+static size_t x2s_offset(int64_t cap, int T, int H, int I, int Kt, int tile_m) {
+    const size_t shifts =
+        staged_tile(tile_m) ? (size_t)((cap + 31) / 32) * (size_t)((H + 127) / 128 * 16) : 0;
+    return yshift_offset(cap, T, H, I, Kt, tile_m) + round_up(shifts, 256);
+}
+
 size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m) {
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
     if (cap < 0 || H <= 0 || I <= 0) return 0;
-    const size_t shifts =
-        prefill_tile_supported(tile_m) ? (size_t)((cap + 31) / 32) * (size_t)((H + 127) / 128 * 16) : 0;
-    return yshift_offset(cap, T, H, I, Kt, tile_m) + round_up(shifts, 256);
+    const size_t x2s = fp8x2_tile_supported(tile_m) ? (size_t)cap * 2 * (size_t)(I / 32) : 0;
+    return x2s_offset(cap, T, H, I, Kt, tile_m) + round_up(x2s, 256);
 }
 
 moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m) {
@@ -382,15 +394,20 @@ static moe_status_t check_ffn_shape(int T, int H, int I, int Et, int Kt, int til
         cap >= ((int64_t)1 << 31))
         return MOE_ERR_UNSUPPORTED_SHAPE;
     moe_path_t p = *path;
-    if (p != MOE_PATH_AUTO && p != MOE_PATH_DECODE && p != MOE_PATH_PREFILL) return MOE_ERR_INVALID_ARG;
+    if (p != MOE_PATH_AUTO && p != MOE_PATH_DECODE && p != MOE_PATH_PREFILL &&
+        p != MOE_PATH_PREFILL_FP8X2)
+        return MOE_ERR_INVALID_ARG;
     if (p == MOE_PATH_AUTO) {
         const char* f = getenv("MOE_FORCE_PATH");
         if (f && !strcmp(f, "decode")) p = MOE_PATH_DECODE;
         else if (f && !strcmp(f, "prefill")) p = MOE_PATH_PREFILL;
+        else if (f && !strcmp(f, "prefill_fp8x2")) p = MOE_PATH_PREFILL_FP8X2;
         else p = moe_ffn_auto_path(T, Kt, Et, tile_m);
     }
     if (p == MOE_PATH_DECODE && !decode_tile_supported(tile_m)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (p == MOE_PATH_PREFILL && (!prefill_tile_supported(tile_m) || !prefill_shape_supported(H, I)))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (p == MOE_PATH_PREFILL_FP8X2 && (!fp8x2_tile_supported(tile_m) || !fp8x2_shape_supported(H, I)))
         return MOE_ERR_UNSUPPORTED_SHAPE;
     *path = p;
     return MOE_OK;
@@ -421,7 +438,8 @@ static GroupedGemm base_gemm(const int32_t* sorted_pairs, const int32_t* tile_ex
 static void trace(const char* step, int T, int H, int I, int Et, int Kt, int tile_m, moe_path_t p) {
     if (trace_enabled())
         fprintf(stderr, "[libmoe] %s T=%d H=%d I=%d Et=%d Kt=%d tile_m=%d path=%s\n", step, T, H, I,
-                Et, Kt, tile_m, p == MOE_PATH_DECODE ? "decode" : "prefill");
+                Et, Kt, tile_m,
+                p == MOE_PATH_DECODE ? "decode" : (p == MOE_PATH_PREFILL_FP8X2 ? "prefill_fp8x2" : "prefill"));
 }
 
 size_t moe_ffn_y_offset(int T, int I, int Et, int Kt, int tile_m) {
@@ -449,6 +467,26 @@ moe_status_t moe_ffn_gate_up(const uint16_t* x, const uint8_t* w13, const uint8_
     g.rows = 2 * I;
     g.K = H;
     g.h_out = reinterpret_cast<uint16_t*>(workspace);
+    if (path == MOE_PATH_PREFILL_FP8X2) {
+        if (!aligned(w13, 32)) return MOE_ERR_INVALID_ARG;  // unpacking TMA loads
+        // x as two E4M3 terms in tile order, 2 tile_m rows per tile (in the
+        // area of the tile-ordered copy), their scale bytes in the y area
+        // (free until the down GEMM); h comes out in the same form (the h
+        // area, and its scale bytes after the shifts)
+        char* ws = reinterpret_cast<char*>(workspace);
+        uint8_t* xq = reinterpret_cast<uint8_t*>(ws + xg_offset(cap, T, H, I, Kt, tile_m));
+        uint8_t* xs = reinterpret_cast<uint8_t*>(ws + y_offset(cap, I));
+        cudaError_t err = launch_split_rows(x, H, 0, sorted_pairs, num_tiles, tile_m, Kt, (int)cap,
+                                            T * Kt, xq, xq + (size_t)tile_m * H, xs,
+                                            xs + (size_t)tile_m * (H / 32), stream);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        g.act = reinterpret_cast<const uint16_t*>(xq);
+        g.act_rows = max_tiles * 2 * tile_m;
+        g.act_scales = xs;
+        g.hq_codes = reinterpret_cast<uint8_t*>(ws);
+        g.hq_scales = reinterpret_cast<uint8_t*>(ws + x2s_offset(cap, T, H, I, Kt, tile_m));
+        return cuda_status(launch_gemm_timed([&] { return launch_fp8x2_gate_up(g, stream); }, stream));
+    }
     // both GEMMs take f16 B rows scaled per row by a power of two: x here,
     // and h (in place) once the GEMM has written it
     char* ws = reinterpret_cast<char*>(workspace);
@@ -507,6 +545,13 @@ moe_status_t moe_ffn_down(const uint8_t* w2, const uint8_t* s2, const float* top
     g.act_by_token = 0;
     g.y_out = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + y_offset(cap, I));
     g.topk_w = topk_w;
+    if (path == MOE_PATH_PREFILL_FP8X2) {  // h as two E4M3 terms, y by pair
+        if (!aligned(w2, 32)) return MOE_ERR_INVALID_ARG;
+        g.act_rows = max_tiles * 2 * tile_m;
+        g.act_scales = reinterpret_cast<const uint8_t*>(workspace) + x2s_offset(cap, T, H, I, Kt, tile_m);
+        g.act_rscale = nullptr;
+        return cuda_status(launch_gemm_timed([&] { return launch_fp8x2_down(g, stream); }, stream));
+    }
     cudaError_t err = launch_gemm_timed(
         [&] { return path == MOE_PATH_DECODE ? launch_decode_down(g, stream) : launch_prefill_down(g, stream); },
         stream);
@@ -536,11 +581,14 @@ moe_status_t moe_ffn_down_combine(const uint8_t* w2, const uint8_t* s2, const fl
     // factor per position (routing weight x h row factor) is applied by the
     // combine, which gathers each token's positions in slot order
     const int64_t cap = capacity64(T, Kt, Et, tile_m);
+    const bool x2 = path == MOE_PATH_PREFILL_FP8X2;
+    if (x2 && !aligned(w2, 32)) return MOE_ERR_INVALID_ARG;  // unpacking TMA loads
     float* w_pos = reinterpret_cast<float*>(ws + wpos_offset(cap, T, H, I, Kt, tile_m));
     const float* h_rscale = reinterpret_cast<const float*>(ws + rs_offset(cap, T, H, I, Kt, tile_m)) + T;
     trace("moe_ffn_down_combine", T, H, I, Et, Kt, tile_m, path);
-    cudaError_t err = launch_position_weights(sorted_pairs, topk_w, h_rscale, num_tiles, tile_m,
-                                              (int)cap, T * Kt, w_pos, stream);
+    // the two-term path's h needs no row factor
+    cudaError_t err = launch_position_weights(sorted_pairs, topk_w, x2 ? nullptr : h_rscale, num_tiles,
+                                              tile_m, (int)cap, T * Kt, w_pos, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     GroupedGemm g = base_gemm(sorted_pairs, tile_expert, num_tiles, T, I, Et, Kt, tile_m,
                               (int)(cap / tile_m));
@@ -558,7 +606,13 @@ moe_status_t moe_ffn_down_combine(const uint8_t* w2, const uint8_t* s2, const fl
     g.y_shift = reinterpret_cast<int8_t*>(ws + yshift_offset(cap, T, H, I, Kt, tile_m));
     g.y_rows_pad = (H + 127) / 128 * 128;
     g.topk_w = topk_w;
-    err = launch_gemm_timed([&] { return launch_prefill_down(g, stream); }, stream);
+    if (x2) {
+        g.act_rows = (int)(cap / tile_m) * 2 * tile_m;
+        g.act_scales = reinterpret_cast<const uint8_t*>(ws + x2s_offset(cap, T, H, I, Kt, tile_m));
+        g.act_rscale = nullptr;
+    }
+    err = launch_gemm_timed(
+        [&] { return x2 ? launch_fp8x2_down(g, stream) : launch_prefill_down(g, stream); }, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     return cuda_status(launch_combine_blocked_f16(g.y16_out, g.y_shift, inv_pairs, w_pos, T, H, Kt,
                                                   (int)cap, out, stream));
@@ -741,6 +795,17 @@ static moe_status_t check_mx_shape(int T, int H, int I, int Et, int Kt, int tile
     if (!mxfp4act_tile_supported(tile_m) || !mxfp4act_shape_supported(H, I))
         return MOE_ERR_UNSUPPORTED_SHAPE;
     return check_ffn_shape(T, H, I, Et, Kt, tile_m, &p);
+}
+
+moe_status_t moe_split_e4m3x2(const uint16_t* x, int rows, int cols, uint8_t* q_hi, uint8_t* q_lo,
+                              uint8_t* s_hi, uint8_t* s_lo, cudaStream_t stream) {
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (cols % 32 || (int64_t)rows * cols >= ((int64_t)1 << 40) || rows >= (1 << 30))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!ptrs_ok({x, q_hi, q_lo}, 16) || !s_hi || !s_lo) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_split_rows(x, cols, rows, nullptr, nullptr, 0, 1, 0, 0, q_hi, q_lo, s_hi,
+                                         s_lo, stream));
 }
 
 moe_status_t moe_quantize_mxfp4(const uint16_t* x, int rows, int cols, uint8_t* codes,

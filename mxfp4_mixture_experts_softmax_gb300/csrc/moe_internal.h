@@ -268,6 +268,25 @@ cudaError_t launch_mxfp4act_gate_up(const GroupedGemm& g, cudaStream_t s);
 cudaError_t launch_mxfp4act_down(const GroupedGemm& g, cudaStream_t s);
 cudaError_t read_device_error_mxfp4act(int* flag, int clear);
 
+// bf16 activations as two E4M3 terms on the block-scaled tensor cores
+// (tcgen05 kind::mxf8f6f4, ffn_fp8x2.cu).  B rows of a tile of N positions:
+// N high-term rows, then N low-term rows (act [max_tiles * 2N][K] bytes, E8M0
+// scales act_scales [max_tiles * 2N][K/32]); gate_up writes h in the same form
+// (hq_codes [max_tiles * 2N][I], hq_scales [max_tiles * 2N][I/32]).
+bool fp8x2_tile_supported(int tile_m);
+bool fp8x2_shape_supported(int H, int I);
+cudaError_t launch_fp8x2_gate_up(const GroupedGemm& g, cudaStream_t s);
+cudaError_t launch_fp8x2_down(const GroupedGemm& g, cudaStream_t s);
+// The two terms of bf16 rows [rows][cols]: with sorted_pairs, the token rows
+// of the used positions p (zeros for padding) land in row
+// (p / tile_n) * 2 tile_n + p % tile_n of q_hi / s_hi and q_lo / s_lo (the
+// caller passes them tile_n rows apart); without, row p lands in row p.
+cudaError_t launch_split_rows(const uint16_t* x, int cols, int rows, const int32_t* sorted_pairs,
+                              const int32_t* num_tiles, int tile_n, int Kt, int cap, int num_pairs,
+                              uint8_t* q_hi, uint8_t* q_lo, uint8_t* s_hi, uint8_t* s_lo,
+                              cudaStream_t s);
+cudaError_t read_device_error_fp8x2(int* flag, int clear);
+
 // grouping of one dense expert over T tokens (Kt = 1); ones[T] = 1 if given
 cudaError_t launch_identity_perm(int T, int tile_m, int cap, int max_tiles, int32_t* sorted_pairs,
                                  int32_t* tile_expert, int32_t* num_tiles, float* ones,

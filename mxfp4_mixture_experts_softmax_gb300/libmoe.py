@@ -23,6 +23,7 @@ MOE_ERR_INTERNAL = 5
 MOE_PATH_AUTO = 0
 MOE_PATH_DECODE = 1
 MOE_PATH_PREFILL = 2
+MOE_PATH_PREFILL_FP8X2 = 3
 
 EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_route_ex", "moe_permute_capacity",
            "moe_permute_max_tiles", "moe_permute", "moe_route_permute", "moe_ffn_workspace_size",
@@ -33,7 +34,7 @@ EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_route_ex", "moe
            "moe_selftest_wait_timeout", "moe_selftest_wait_split", "moe_set_gemm_events",
            "moe_quantize_mxfp4", "moe_ffn_mxfp4act_workspace_size",
            "moe_ffn_mxfp4act", "moe_ffn_mxfp4act_gate_up", "moe_ffn_mxfp4act_down",
-           "moe_ffn_mxfp4act_h_offsets", "moe_ffn_down_combine")
+           "moe_ffn_mxfp4act_h_offsets", "moe_ffn_down_combine", "moe_split_e4m3x2")
 
 # bytes of the fixed device scratch behind moe_ffn_noalloc (include/moe.h)
 MOE_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -118,6 +119,8 @@ def load(build: bool = True):
         L.moe_ffn_down_combine.restype = ci
         L.moe_quantize_mxfp4.argtypes = [vp, ci, ci, vp, vp, vp]
         L.moe_quantize_mxfp4.restype = ci
+        L.moe_split_e4m3x2.argtypes = [vp, ci, ci, vp, vp, vp, vp, vp]
+        L.moe_split_e4m3x2.restype = ci
         L.moe_ffn_mxfp4act_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci]
         L.moe_ffn_mxfp4act_workspace_size.restype = sz
         L.moe_ffn_mxfp4act.argtypes = ffn_args + [vp]
@@ -445,6 +448,22 @@ def moe_ffn_dense_shared(x, w13, s13, w2, s2, topk_w, perm: dict, w13s, s13s, w2
 
 
 # ------------------------------------------------ MXFP4-quantised activations
+
+def moe_split_e4m3x2(x, stream=None):
+    """bf16 [rows, cols] -> (q_hi, q_lo uint8 [rows, cols], s_hi, s_lo uint8
+    [rows, cols/32]): the two-term E4M3 encoding of MOE_PATH_PREFILL_FP8X2
+    (include/moe.h)."""
+    import torch
+    _dev(x, "x")
+    rows, cols = x.shape
+    q_hi = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    q_lo = torch.empty_like(q_hi)
+    s_hi = torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device)
+    s_lo = torch.empty_like(s_hi)
+    _check(load().moe_split_e4m3x2(_ptr(x), rows, cols, _ptr(q_hi), _ptr(q_lo), _ptr(s_hi), _ptr(s_lo),
+                                   _stream(stream)), "moe_split_e4m3x2")
+    return q_hi, q_lo, s_hi, s_lo
+
 
 def moe_quantize_mxfp4(x, codes=None, scales=None, stream=None):
     """bf16 [rows, cols] -> (codes uint8 [rows, cols/2], scales uint8 [rows, cols/32]),

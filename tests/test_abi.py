@@ -113,6 +113,41 @@ def test_mxfp4act_host_validation_and_layout(lib):
     assert lib.moe_ffn_mxfp4act_h_offsets(4, 256, 128, 8, 2, 32, None, None) == m.MOE_ERR_INVALID_ARG
 
 
+def test_fp8x2_path_host_validation(lib):
+    """MOE_PATH_PREFILL_FP8X2: widths multiples of 512 (whole 16-byte scale
+    boxes), tile heights 32/64/128, weights 32-byte aligned; the split call's
+    checks; all before any launch."""
+    from mxfp4_mixture_experts_softmax_gb300 import libmoe as m
+    nul = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x1000)
+    P = m.MOE_PATH_PREFILL_FP8X2
+
+    def ffn(T=64, H=512, I=512, Et=8, Kt=2, tile_m=64, ws=1 << 30, w=fake, path=P):
+        return lib.moe_ffn_path(fake, w, fake, w, fake, fake, fake, fake, fake, fake, fake,
+                                T, H, I, Et, Kt, tile_m, fake, fake, ws, path, nul)
+    assert ffn(H=256) == m.MOE_ERR_UNSUPPORTED_SHAPE      # H % 512
+    assert ffn(I=1536 + 256) == m.MOE_ERR_UNSUPPORTED_SHAPE  # I % 512
+    for tm in (8, 16, 256):
+        assert ffn(tile_m=tm) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert ffn(ws=64) == m.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert ffn(w=ctypes.c_void_p(0x1010)) == m.MOE_ERR_INVALID_ARG  # 16- but not 32-byte aligned
+    assert ffn(T=0) == m.MOE_OK
+    assert lib.moe_split_e4m3x2(fake, 4, 48, fake, fake, fake, fake, nul) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_split_e4m3x2(fake, -1, 64, fake, fake, fake, fake, nul) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_split_e4m3x2(fake, 4, 64, fake, fake, nul, fake, nul) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_split_e4m3x2(nul, 0, 64, nul, nul, nul, nul, nul) == m.MOE_OK
+    # the workspace holds h's two terms (2 tile_m rows per tile) in the h
+    # area, x's in the tile-ordered copy's area and h's scale bytes at its end
+    H, I, Et, Kt = 4096, 1024, 513, 11
+    for T, tm in ((288, 32), (1536, 64), (8192, 128)):
+        cap = m.moe_permute_capacity(T, Kt, Et, tm)
+        tiles = m.moe_permute_max_tiles(T, Kt, Et, tm)
+        assert tiles * 2 * tm * I <= m.moe_ffn_y_offset(T, I, Et, Kt, tm)
+        assert m.moe_ffn_workspace_size(T, H, I, Et, Kt, tm) >= (
+            m.moe_ffn_y_offset(T, I, Et, Kt, tm) + max(T * Kt * H * 4, cap * H * 2) + T * H * 2
+            + cap * H * 2 + (T + 2 * cap) * 4 + tiles * 2 * tm * (I // 32))
+
+
 def test_bf16_workspace_holds_staged_y_for_prefill_tiles(lib):
     """moe_ffn_down_combine's prefill path writes y as f16 rows over cap
     positions: the workspace reserves that much for prefill tile heights."""
