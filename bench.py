@@ -326,8 +326,8 @@ class Layer:
         self.path = {"auto": libmoe.MOE_PATH_AUTO, "decode": libmoe.MOE_PATH_DECODE,
                      "prefill": libmoe.MOE_PATH_PREFILL,
                      "prefill_fp8x2": libmoe.MOE_PATH_PREFILL_FP8X2}[path_arg]
-        resolved = (libmoe.moe_ffn_auto_path(w.T, w.Kt, w.Et, tm) if self.path == libmoe.MOE_PATH_AUTO
-                    else self.path)
+        resolved = (libmoe.moe_ffn_auto_path_shape(w.T, w.H, w.I, w.Et, w.Kt, tm)
+                    if self.path == libmoe.MOE_PATH_AUTO else self.path)
         if self.mx:
             self.path_name = "mxfp4act"
         else:

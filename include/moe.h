@@ -525,8 +525,17 @@ moe_status_t moe_ffn_mxfp4act_down(const uint8_t* w2, const uint8_t* s2, const f
 moe_status_t moe_ffn_mxfp4act_h_offsets(int T, int H, int I, int Et, int Kt, int tile_m,
                                         size_t* codes_offset, size_t* scales_offset);
 
-/* The path MOE_PATH_AUTO picks for these sizes [VL, small-M vs large-M]. */
+/* The regime MOE_PATH_AUTO picks for these sizes [VL, small-M vs large-M]:
+ * MOE_PATH_DECODE or MOE_PATH_PREFILL (the large-M regime, whichever of its
+ * two paths moe_ffn_auto_path_shape names). */
 moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m);
+
+/* The path MOE_PATH_AUTO runs for these sizes: in the large-M regime
+ * MOE_PATH_PREFILL_FP8X2 where its widths and tile heights allow (it is the
+ * faster of the two there), else MOE_PATH_PREFILL; the MOE_FORCE_PATH
+ * environment override (decode, prefill, prefill_fp8x2) applies as it does
+ * to the FFN calls.  Returns MOE_PATH_AUTO for sizes no path supports. */
+moe_path_t moe_ffn_auto_path_shape(int T, int H, int I, int Et, int Kt, int tile_m);
 
 #ifdef __cplusplus
 }

@@ -79,6 +79,7 @@ constexpr int kBK = 128;                 // k per stage: one 128-byte shared-mem
 constexpr int kRowBytes = 128;
 constexpr int kABytes = 128 * kRowBytes;  // 16 KB weight stage (unpacked codes)
 constexpr int kABox = 64;                 // weight rows per TMA box
+constexpr int kSfGroupMax = 8;           // stages whose scale bytes one load brings
 constexpr int kPrefetch = 16;             // weight stages prefetched into L2 ahead, across items
 constexpr int kSmemLimit = 232448;
 
@@ -87,16 +88,19 @@ struct X2Layout {
     static constexpr int kBRows = 2 * N;               // high-term rows, then low-term rows
     static constexpr int kBRowsCta = PAIR ? N : kBRows;  // a pair's CTA loads one term's rows
     static constexpr int kBBytes = kBRowsCta * kRowBytes;
-    static constexpr int kSfBytes = (128 + kBRows) * 16;  // one 16-byte scale box row per operand row
+    // scale bytes of a group of up to 8 stages (4 per stage and row): the
+    // weight rows, then all 2N B rows; two slots
+    static constexpr int kSfRows = 128 + kBRows;
+    static constexpr int kSfSlotBytes = kSfRows * 4 * kSfGroupMax;
     static constexpr int kStage = kABytes + kBBytes;
-    static_assert(kStage % 1024 == 0 && kSfBytes % 128 == 0, "alignment");
+    static_assert(kStage % 1024 == 0 && kSfSlotBytes % 128 == 0, "alignment");
     static constexpr int kStgRow = 132;
     static constexpr int kStgBytes = MODE == 0 ? 32 * kStgRow * 4 : 0;
-    static constexpr int kFit = (kSmemLimit - 1024 - 512 - kStgBytes) / (kStage + kSfBytes);
+    static constexpr int kFit = (kSmemLimit - 1024 - 512 - kStgBytes - 2 * kSfSlotBytes) / kStage;
     static constexpr int kStages = kFit > 8 ? 8 : kFit;
     static_assert(kStages >= 3, "ring depth");
     static constexpr int kSf = kStages * kStage;
-    static constexpr int kStg = kSf + kStages * kSfBytes;
+    static constexpr int kStg = kSf + 2 * kSfSlotBytes;
     static constexpr int kBar = kStg + kStgBytes;
     static constexpr int kTotal = kBar + 512 + 1024;  // + barriers, alignment slack
     static_assert(kTotal <= kSmemLimit, "shared memory");
@@ -308,13 +312,15 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
     uint64_t* tma_full = reinterpret_cast<uint64_t*>(smem + L::kBar);  // per stage, this CTA's loads
     uint64_t* sf_full = tma_full + kStages;       // scale factors in tensor memory (even CTA: both)
     uint64_t* stage_free = sf_full + kStages;     // the stage's MMAs completed
-    uint64_t* acc_full = stage_free + kStages;    // [2]
+    uint64_t* sf_loaded = stage_free + kStages;   // [2] a scale group's bytes landed
+    uint64_t* sf_done = sf_loaded + 2;            // [2] the scale warps read the group
+    uint64_t* acc_full = sf_done + 2;             // [2]
     uint64_t* acc_free = acc_full + 2;            // [2] drained (even CTA: by both)
     uint64_t* drain = acc_free + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     auto stage_a = [&](int s) { return smem + s * L::kStage; };
     auto stage_b = [&](int s) { return smem + s * L::kStage + kABytes; };
-    auto sf_slot = [&](int s) { return smem + L::kSf + s * L::kSfBytes; };
+    auto sf_slot = [&](int k) { return smem + L::kSf + k * L::kSfSlotBytes; };
     auto arrive0 = [&](uint64_t* bar) {  // on the barrier the even CTA waits on
         if (PAIR)
             mbar_arrive_remote(bar, 0);
@@ -327,6 +333,10 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
     const int cta0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // first item
     const int cstep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;   // item stride
     const int nk = g.K / kBK;  // K % 512 == 0
+    // stages per scale group: 8 (32-byte rows) when the item's stages split
+    // into whole groups of 8, else 4 (16-byte rows); the launcher's scale
+    // maps use the same width
+    const int sfg = nk % 8 == 0 ? 8 : 4;
     const int row_blocks = MODE == 0 ? g.I / 64 : g.rows / 128;
     const int row_groups = PAIR ? row_blocks / 2 : row_blocks;  // even for pairs (K % 512 widths)
     const int items = checked_tiles(g) * row_groups;
@@ -338,6 +348,10 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
             mbar_init(&tma_full[s], 1);
             mbar_init(&sf_full[s], 4 * kCtas);
             mbar_init(&stage_free[s], 1);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&sf_loaded[k], 1);
+            mbar_init(&sf_done[k], 4);
         }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -389,7 +403,7 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
                 }
             };
             for (int i = 0; i < kPrefetch; ++i) prefetch_next();
-            uint32_t gs = 0;
+            uint32_t gs = 0, gc = 0;  // stages and scale groups issued
             bool ok = true;
             for (int item = cta0; item < items && ok; item += cstep) {
                 const int tile = item / row_groups, block = block_of(item);
@@ -401,6 +415,20 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
                 for (int st = 0; st < nk; ++st, ++gs) {
                     const int s = gs % kStages;
                     prefetch_next();
+                    if (st % sfg == 0) {  // the scale bytes of stages st .. st + sfg - 1, one load per row
+                        const int k = gc & 1;
+                        if (gc >= 2 && !mbar_wait(&sf_done[k], ((gc >> 1) - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        const int w = 4 * sfg;  // bytes per row
+                        mbar_arrive_expect_tx(&sf_loaded[k], (uint32_t)(L::kSfRows * w));
+                        const uint32_t sfd = smem_u32(sf_slot(k));
+                        tma_load_2d(sfd, &sfa_map, 4 * st, ar0, &sf_loaded[k]);
+                        tma_load_2d(sfd + kABox * w, &sfa_map, 4 * st, ar1, &sf_loaded[k]);
+                        tma_load_2d(sfd + 128 * w, &sfb_map, 4 * st, br, &sf_loaded[k]);
+                        ++gc;
+                    }
                     if (gs >= (uint32_t)kStages && !mbar_wait(&stage_free[s], ((gs / kStages) - 1) & 1)) {
                         ok = false;
                         break;
@@ -408,15 +436,11 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
                     // the unpacking loads write 8 bytes per 16 codes (the gaps
                     // between them are not written): the weight stage counts
                     // its packed size
-                    mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kABytes / 2 + L::kBBytes + L::kSfBytes));
-                    const uint32_t a = smem_u32(stage_a(s)), sfd = smem_u32(sf_slot(s));
+                    mbar_arrive_expect_tx(&tma_full[s], (uint32_t)(kABytes / 2 + L::kBBytes));
+                    const uint32_t a = smem_u32(stage_a(s));
                     tma_load_2d(a, &a_map, st * kBK, ar0, &tma_full[s]);
                     tma_load_2d(a + kABox * kRowBytes, &a_map, st * kBK, ar1, &tma_full[s]);
                     tma_load_2d(smem_u32(stage_b(s)), &b_map, st * kRowBytes, br + rank * N, &tma_full[s]);
-                    const int kx = (st >> 2) * 16;  // the 16 scale groups of stages 4 (st/4) ..
-                    tma_load_2d(sfd, &sfa_map, kx, ar0, &tma_full[s]);
-                    tma_load_2d(sfd + kABox * 16, &sfa_map, kx, ar1, &tma_full[s]);
-                    tma_load_2d(sfd + 128 * 16, &sfb_map, kx, br, &tma_full[s]);
                 }
             }
             // wait (bounded) until the last loads landed before the CTA can exit
@@ -491,29 +515,42 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
         const int quad = warp & 3;
         const int rho = 32 * quad + lane;  // weight row of the stage = accumulator lane
         const uint32_t lane_base = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)L::kSfCol0;
-        uint32_t gs = 0;
+        const int w = 4 * sfg;  // scale bytes per row in a group slot
+        uint32_t gs = 0, gc = 0;
         bool ok = true;
         for (int item = cta0; item < items && ok; item += cstep) {
             if (checked_expert(g, item / row_groups, false) < 0) continue;
             for (int st = 0; st < nk; ++st, ++gs) {
-                const int s = gs % kStages;
-                // the stage's slot is filled once the producer saw the MMAs
-                // that last read these tensor-memory columns complete
-                if (!mbar_wait_warp(&tma_full[s], (gs / kStages) & 1)) {
+                const int s = gs % kStages, k = gc & 1;
+                // the stage's scale factors go into tensor memory as soon as
+                // the group's bytes are here and the MMAs that last read those
+                // columns have completed, ahead of the stage's operands
+                if ((st % sfg == 0 && !mbar_wait_warp(&sf_loaded[k], (gc >> 1) & 1)) ||
+                    (gs >= (uint32_t)kStages && !mbar_wait_warp(&stage_free[s], ((gs / kStages) - 1) & 1))) {
                     ok = false;
                     break;
                 }
-                const uint8_t* sf = sf_slot(s) + 4 * (st & 3);
+                const uint8_t* sf = sf_slot(k) + 4 * (st % sfg);
                 uint32_t av[1], bv[L::kBJst];
-                av[0] = lds32(sf + rho * 16);
+                av[0] = lds32(sf + rho * w);
 #pragma unroll
                 for (int j = 0; j < L::kBJst; ++j)
-                    bv[j] = j < L::kBJ ? lds32(sf + (128 + 32 * j + lane) * 16) : 0u;
+                    bv[j] = j < L::kBJ ? lds32(sf + (128 + 32 * j + lane) * w) : 0u;
                 tc_fence_after();
                 const uint32_t col = lane_base + (uint32_t)(s * L::kSfCols);
                 tmem_st_x<1>(col + (uint32_t)quad, av);
                 tmem_st_x<L::kBJst>(col + 8u, bv);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                if (st % sfg == sfg - 1) {  // this warp's reads of the group are done
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sf_done[k]);
+                    ++gc;
+                }
+                // then this CTA's operands of the stage
+                if (!mbar_wait_warp(&tma_full[s], (gs / kStages) & 1)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) arrive0(&sf_full[s]);
@@ -650,11 +687,13 @@ cudaError_t launch_n(const GroupedGemm& g, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     err = encode_codes_map(&b_map, g.act, g.K, (uint64_t)g.act_rows, kRowBytes, L::kBRowsCta);
     if (err != cudaSuccess) return err;
+    // scale rows of K/32 bytes, boxes of one scale group (the kernel's width)
+    const int sfw = 4 * ((g.K / kBK) % 8 == 0 ? 8 : 4);
     err = encode_2d_map(&sfa_map, g.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K / 32, wrows,
-                        (uint64_t)(g.K / 32), 16, kABox, CU_TENSOR_MAP_SWIZZLE_NONE);
+                        (uint64_t)(g.K / 32), sfw, kABox, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
     err = encode_2d_map(&sfb_map, g.act_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K / 32,
-                        (uint64_t)g.act_rows, (uint64_t)(g.K / 32), 16, 2 * N, CU_TENSOR_MAP_SWIZZLE_NONE);
+                        (uint64_t)g.act_rows, (uint64_t)(g.K / 32), sfw, 2 * N, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
     const int row_blocks = MODE == 0 ? g.I / 64 : g.rows / 128;
     const long long max_items = (long long)g.max_tiles * (PAIR ? row_blocks / 2 : row_blocks);

@@ -402,7 +402,12 @@ static moe_status_t check_ffn_shape(int T, int H, int I, int Et, int Kt, int til
         if (f && !strcmp(f, "decode")) p = MOE_PATH_DECODE;
         else if (f && !strcmp(f, "prefill")) p = MOE_PATH_PREFILL;
         else if (f && !strcmp(f, "prefill_fp8x2")) p = MOE_PATH_PREFILL_FP8X2;
-        else p = moe_ffn_auto_path(T, Kt, Et, tile_m);
+        else {
+            p = moe_ffn_auto_path(T, Kt, Et, tile_m);
+            // the large-M regime: the block-scaled two-term path where it applies
+            if (p == MOE_PATH_PREFILL && fp8x2_tile_supported(tile_m) && fp8x2_shape_supported(H, I))
+                p = MOE_PATH_PREFILL_FP8X2;
+        }
     }
     if (p == MOE_PATH_DECODE && !decode_tile_supported(tile_m)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (p == MOE_PATH_PREFILL && (!prefill_tile_supported(tile_m) || !prefill_shape_supported(H, I)))
@@ -411,6 +416,11 @@ static moe_status_t check_ffn_shape(int T, int H, int I, int Et, int Kt, int til
         return MOE_ERR_UNSUPPORTED_SHAPE;
     *path = p;
     return MOE_OK;
+}
+
+moe_path_t moe_ffn_auto_path_shape(int T, int H, int I, int Et, int Kt, int tile_m) {
+    moe_path_t p = MOE_PATH_AUTO;
+    return check_ffn_shape(T, H, I, Et, Kt, tile_m, &p) == MOE_OK ? p : MOE_PATH_AUTO;
 }
 
 static bool ptrs_ok(std::initializer_list<const void*> ptrs, size_t align) {

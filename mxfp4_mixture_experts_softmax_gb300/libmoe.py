@@ -34,7 +34,7 @@ EXPORTS = ("moe_status_string", "moe_version", "moe_route", "moe_route_ex", "moe
            "moe_selftest_wait_timeout", "moe_selftest_wait_split", "moe_set_gemm_events",
            "moe_quantize_mxfp4", "moe_ffn_mxfp4act_workspace_size",
            "moe_ffn_mxfp4act", "moe_ffn_mxfp4act_gate_up", "moe_ffn_mxfp4act_down",
-           "moe_ffn_mxfp4act_h_offsets", "moe_ffn_down_combine", "moe_split_e4m3x2")
+           "moe_ffn_mxfp4act_h_offsets", "moe_ffn_down_combine", "moe_split_e4m3x2", "moe_ffn_auto_path_shape")
 
 # bytes of the fixed device scratch behind moe_ffn_noalloc (include/moe.h)
 MOE_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -92,6 +92,8 @@ def load(build: bool = True):
         L.moe_ffn_path.restype = ci
         L.moe_ffn_auto_path.argtypes = [ci, ci, ci, ci]
         L.moe_ffn_auto_path.restype = ci
+        L.moe_ffn_auto_path_shape.argtypes = [ci, ci, ci, ci, ci, ci]
+        L.moe_ffn_auto_path_shape.restype = ci
         L.moe_ffn_gate_up.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, sz, ci, vp]
         L.moe_ffn_gate_up.restype = ci
         L.moe_ffn_down.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, sz, ci, vp]
@@ -254,6 +256,10 @@ def moe_ffn_workspace_size(T: int, H: int, I: int, Et: int, Kt: int, tile_m: int
 
 def moe_ffn_auto_path(T: int, Kt: int, Et: int, tile_m: int) -> int:
     return int(load().moe_ffn_auto_path(T, Kt, Et, tile_m))
+
+
+def moe_ffn_auto_path_shape(T: int, H: int, I: int, Et: int, Kt: int, tile_m: int) -> int:
+    return int(load().moe_ffn_auto_path_shape(T, H, I, Et, Kt, tile_m))
 
 
 def alloc_workspace(T: int, H: int, I: int, Et: int, Kt: int, tile_m: int, device="cuda"):

@@ -45,6 +45,13 @@ def test_status_strings_and_sizes(lib):
     ws = m.moe_ffn_workspace_size(64, 4096, 1024, 513, 11, 8)
     assert ws >= cap * 1024 * 2 + 64 * 11 * 4096 * 4
     assert m.moe_ffn_auto_path(64, 11, 513, 8) == m.MOE_PATH_DECODE
+    # the large-M regime: the two-term path where widths and tile height allow it
+    assert m.moe_ffn_auto_path_shape(1536, 4096, 1024, 513, 11, 64) == m.MOE_PATH_PREFILL_FP8X2
+    assert m.moe_ffn_auto_path_shape(8192, 4096, 1024, 513, 11, 128) == m.MOE_PATH_PREFILL_FP8X2
+    assert m.moe_ffn_auto_path_shape(8192, 4096, 1024, 513, 11, 256) == m.MOE_PATH_PREFILL
+    assert m.moe_ffn_auto_path_shape(1536, 4096, 256, 513, 11, 64) == m.MOE_PATH_PREFILL
+    assert m.moe_ffn_auto_path_shape(64, 4096, 1024, 513, 11, 8) == m.MOE_PATH_DECODE
+    assert m.moe_ffn_auto_path_shape(64, 250, 1024, 513, 11, 8) == m.MOE_PATH_AUTO  # H % 32
 
 
 def test_host_validation_rejects_before_launch(lib):

@@ -64,8 +64,12 @@ def test_per_config_covers_every_full_size_workload():
     assert bench.DEFAULT_WORKLOAD in bench.PER_CONFIG
     for n in bench.PER_CONFIG:  # the bf16 tile height gives the path the pages' regime names
         w = synth.WORKLOADS[n]
-        path = libmoe.moe_ffn_auto_path(w.T, w.Kt, w.Et, bench.default_tile_m(w, "bf16"))
-        assert path == (libmoe.MOE_PATH_DECODE if w.T <= 288 else libmoe.MOE_PATH_PREFILL), n
+        tm = bench.default_tile_m(w, "bf16")
+        regime = libmoe.moe_ffn_auto_path(w.T, w.Kt, w.Et, tm)
+        assert regime == (libmoe.MOE_PATH_DECODE if w.T <= 288 else libmoe.MOE_PATH_PREFILL), n
+        # the large-M regime runs the two-term path at these widths (H, I multiples of 512)
+        path = libmoe.moe_ffn_auto_path_shape(w.T, w.H, w.I, w.Et, w.Kt, tm)
+        assert path == (libmoe.MOE_PATH_DECODE if w.T <= 288 else libmoe.MOE_PATH_PREFILL_FP8X2), n
 
 
 def test_launch_counts_per_path():
@@ -78,6 +82,8 @@ def test_launch_counts_per_path():
     # 16,896 and 90,112 pairs: the four-launch multi-block sort
     assert bench.launches_per_step(W["prefill1536"], "prefill") == 11
     assert bench.launches_per_step(W["skewed_prefill8192"], "prefill") == 11
+    # split of x into tile order, gate_up | position weights, down, combine
+    assert bench.launches_per_step(W["skewed_prefill8192"], "prefill_fp8x2") == 10
     assert bench.launches_per_step(W["skewed_prefill8192"], "mxfp4act") == 11
 
 

@@ -46,10 +46,12 @@ def test_noalloc_matches_moe_ffn_on_two_calls_in_a_row():
                       with_shared=True, seed=31), 8, libmoe.MOE_PATH_DECODE),
         (synth.scaled(synth.WORKLOADS["tiny16"], T=200, H=512, I=256, E=16, K=4,
                       with_shared=True, seed=33), 64, libmoe.MOE_PATH_PREFILL),
+        (synth.scaled(synth.WORKLOADS["tiny16"], T=200, H=512, I=512, E=16, K=4,
+                      with_shared=True, seed=35), 64, libmoe.MOE_PATH_PREFILL_FP8X2),
         (synth.WORKLOADS["decode64"], 8, libmoe.MOE_PATH_DECODE),
     ]
     for w, tile_m, want_path in cases:
-        assert libmoe.moe_ffn_auto_path(w.T, w.Kt, w.Et, tile_m) == want_path
+        assert libmoe.moe_ffn_auto_path_shape(w.T, w.H, w.I, w.Et, w.Kt, tile_m) == want_path
         d = synth.make_inputs(w)
         ids, wt = oracle.route(d["logits"], w.K, w.with_shared)
         dev_w = gc.upload_weights(d)
