@@ -68,11 +68,11 @@ constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kScaleWarp0 = 2;   // 2..5: warp % 4 covers every lane quadrant
 constexpr int kEpiWarp0 = 6;
-constexpr int kEpiThreads = 128;  // gate_up's epilogue warps, which meet at named barrier 1
-// down: two warps per lane quadrant, warp h of a quadrant draining the
-// 32-column chunks h, h + 2, ...
+constexpr int kEpiThreads = 128;  // one epilogue group (4 warps); gate_up's meet at named barrier 1 + group
+// two groups of four warps (one per lane quadrant); group h drains the
+// 32-column chunks h and h + 2 of the accumulator
 template <int MODE>
-__host__ __device__ constexpr int x2_epi_warps() { return MODE == 1 ? 8 : 4; }
+__host__ __device__ constexpr int x2_epi_warps() { return 8; }
 template <int MODE>
 __host__ __device__ constexpr int x2_threads() { return (kEpiWarp0 + x2_epi_warps<MODE>()) * 32; }
 constexpr int kBK = 128;                 // k per stage: one 128-byte shared-memory row per operand row
@@ -95,7 +95,7 @@ struct X2Layout {
     static constexpr int kStage = kABytes + kBBytes;
     static_assert(kStage % 1024 == 0 && kSfSlotBytes % 128 == 0, "alignment");
     static constexpr int kStgRow = 132;
-    static constexpr int kStgBytes = MODE == 0 ? 32 * kStgRow * 4 : 0;
+    static constexpr int kStgBytes = MODE == 0 ? 2 * 32 * kStgRow * 4 : 0;  // one per epilogue group
     static constexpr int kFit = (kSmemLimit - 1024 - 512 - kStgBytes - 2 * kSfSlotBytes) / kStage;
     static constexpr int kStages = kFit > 8 ? 8 : kFit;
     static_assert(kStages >= 3, "ring depth");
@@ -558,33 +558,41 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
         }
     } else {
         // -------------------------------------------------------- epilogue
-        const int quad = warp & 3;                        // lanes 32 quad .. 32 quad + 31
-        const int et = (warp - kEpiWarp0) * 32 + lane;    // gate_up: 0..127
-        constexpr int kPerQuad = x2_epi_warps<MODE>() / 4;
-        const int half = MODE == 1 ? (warp - kEpiWarp0) >> 2 : 0;
-        constexpr int kCStep = 32 * kPerQuad;
+        // Each warp copies its (at most two) chunks of D_hi + D_lo out of
+        // tensor memory, releases the accumulator, and only then computes
+        // and stores: the next item's MMAs wait for the copies alone.
+        static_assert(N <= 128, "two chunks per epilogue warp");
+        constexpr int kChunks = (N + 63) / 64;  // per warp
+        const int quad = warp & 3;                              // lanes 32 quad .. 32 quad + 31
+        const int grp = (warp - kEpiWarp0) >> 2;                // chunks 32 grp, 32 grp + 64
+        const int et = ((warp - kEpiWarp0) & 3) * 32 + lane;    // gate_up: 0..127 within the group
+        float* stg_g = stg + grp * 32 * L::kStgRow;
         uint32_t it = 0;
         for (int item = cta0; item < items; item += cstep) {
             const int tile = item / row_groups, block = block_of(item);
             if (checked_expert(g, tile, false) < 0) continue;
             const uint32_t b = it % kAccBufs;
-            // down: the pair of this lane's position in the warp's first chunk
-            int q = MODE == 1 && 32 * half < N ? checked_pair(g, tile * N + 32 * half + lane) : -1;
-            // one outcome for the warp, and in gate_up for all four epilogue
-            // warps, which meet at named barrier 1 below: none may go on to
+            // down: the pair of this lane's position in each of the warp's chunks
+            int q[kChunks];
+#pragma unroll
+            for (int j = 0; j < kChunks; ++j) q[j] = -1;
+            if (MODE == 1) {
+#pragma unroll
+                for (int j = 0; j < kChunks; ++j)
+                    if (32 * grp + 64 * j < N) q[j] = checked_pair(g, tile * N + 32 * grp + 64 * j + lane);
+            }
+            // one outcome for the warp, and in gate_up for the group's four
+            // warps, which meet at a named barrier below: none may go on to
             // that barrier while another stopped
             bool acc_ok = mbar_wait_warp(&acc_full[b], (it / kAccBufs) & 1);
-            if (MODE == 0) acc_ok = all_at_barrier(acc_ok, 1, kEpiThreads);
+            if (MODE == 0) acc_ok = all_at_barrier(acc_ok, 1 + grp, kEpiThreads);
             if (!acc_ok) break;
             tc_fence_after();
-            if (32 * half >= N) {  // no chunk for this warp (narrow tiles)
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) arrive0(&acc_free[b]);
-            }
-#pragma unroll 1
-            for (int c0 = 32 * half; c0 < N; c0 += kCStep) {
-                uint32_t v[32];
+            uint32_t v[kChunks][32];
+#pragma unroll
+            for (int j = 0; j < kChunks; ++j) {
+                const int c0 = 32 * grp + 64 * j;
+                if (c0 >= N) continue;
                 const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + b * kAccCols + (uint32_t)c0;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {  // D_hi + D_lo, 16 columns at a time
@@ -594,38 +602,40 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        v[16 * hf + i] = __float_as_uint(__uint_as_float(dh[i]) + __uint_as_float(dl[i]));
+                        v[j][16 * hf + i] = __float_as_uint(__uint_as_float(dh[i]) + __uint_as_float(dl[i]));
                 }
-                if (c0 + kCStep >= N) {  // this warp's part is drained: the next item may use it
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) arrive0(&acc_free[b]);
-                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive0(&acc_free[b]);  // this warp's part is drained: the next item may use it
+#pragma unroll
+            for (int j = 0; j < kChunks; ++j) {
+                const int c0 = 32 * grp + 64 * j;
+                if (c0 >= N) continue;
                 if (MODE == 1) {
-                    if (c0 != 32 * half) q = checked_pair(g, tile * N + c0 + lane);
-                    const int nc = __popc(__ballot_sync(0xFFFFFFFFu, q >= 0));  // pairs form a prefix
+                    const int nc = __popc(__ballot_sync(0xFFFFFFFFu, q[j] >= 0));  // pairs form a prefix
                     const int row = block * 128 + 32 * quad + lane;
                     if (g.y_blocked) {
-                        store_y16_chunk(g, v, 1.0f, block, quad, lane, tile * N + c0, nc, row < g.rows);
+                        store_y16_chunk(g, v[j], 1.0f, block, quad, lane, tile * N + c0, nc, row < g.rows);
                     } else {  // y by pair, times the routing weight
-                        const float wq = q >= 0 ? __ldg(g.topk_w + q) : 0.0f;
+                        const float wq = q[j] >= 0 ? __ldg(g.topk_w + q[j]) : 0.0f;
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            const int qi = __shfl_sync(0xFFFFFFFFu, q, i);
+                            const int qi = __shfl_sync(0xFFFFFFFFu, q[j], i);
                             const float wi = __shfl_sync(0xFFFFFFFFu, wq, i);
                             if (qi >= 0 && row < g.rows)
-                                g.y_out[(size_t)qi * g.rows + row] = __uint_as_float(v[i]) * wi;
+                                g.y_out[(size_t)qi * g.rows + row] = __uint_as_float(v[j][i]) * wi;
                         }
                     }
                 } else {
                     // transpose through shared memory: stg[column][accumulator row]
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) stg[i * L::kStgRow + 32 * quad + lane] = __uint_as_float(v[i]);
-                    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+                    for (int i = 0; i < 32; ++i) stg_g[i * L::kStgRow + 32 * quad + lane] = __uint_as_float(v[j][i]);
+                    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kEpiThreads) : "memory");
                     // thread -> (column, 32-block of i, half): rows 0..63 are the
                     // gate rows of i = block * 64 + row, rows 64..127 the up rows
                     const int hh = et & 1, col = (et >> 1) & 31, blk = et >> 6;
-                    const float* gp = stg + col * L::kStgRow + 32 * blk + 16 * hh;
+                    const float* gp = stg_g + col * L::kStgRow + 32 * blk + 16 * hh;
                     float a[16];
                     float amax = 0.0f;
 #pragma unroll
@@ -634,11 +644,11 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
                         const float4 uv = *reinterpret_cast<const float4*>(gp + 64 + 4 * k4);
                         const float gg[4] = {gv.x, gv.y, gv.z, gv.w}, uu[4] = {uv.x, uv.y, uv.z, uv.w};
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
+                        for (int k = 0; k < 4; ++k) {
                             // h = bf16(silu(g) * u), kept as its fp32 value
                             const float hv = __uint_as_float(
-                                (uint32_t)f32_to_bf16_bits(silu_fast(gg[j]) * uu[j]) << 16);
-                            a[4 * k4 + j] = hv;
+                                (uint32_t)f32_to_bf16_bits(silu_fast(gg[k]) * uu[k]) << 16);
+                            a[4 * k4 + k] = hv;
                             amax = fmaxf(amax, fabsf(hv));
                         }
                     }
@@ -651,7 +661,7 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
                     *reinterpret_cast<uint4*>(g.hq_codes + hrow * (size_t)g.I + i0) = hq;
                     *reinterpret_cast<uint4*>(g.hq_codes + (hrow + N) * (size_t)g.I + i0) = lq;
                     g.hq_scales[(hrow + (hh ? N : 0)) * (size_t)(g.I / 32) + i0 / 32] = (uint8_t)(hh ? sl : sh);
-                    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+                    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kEpiThreads) : "memory");
                 }
             }
             ++it;
