@@ -12,6 +12,7 @@ of every token against the prefill path.
 import numpy as np
 import pytest
 
+import e4m3
 import gpu_common as gc
 
 torch = pytest.importorskip("torch")
@@ -29,36 +30,8 @@ THREADS = synth.cpu_threads()
 P = libmoe.MOE_PATH_PREFILL_FP8X2
 
 
-def _e4m3_values() -> np.ndarray:
-    """Value of every E4M3 code (OCP 8-bit floating point, E4M3: sign,
-    4 exponent bits with bias 7, 3 mantissa bits; exponent 0 subnormal;
-    S.1111.111 NaN, no infinities)."""
-    v = np.empty(256)
-    for c in range(256):
-        s = -1.0 if c & 0x80 else 1.0
-        e, m = (c >> 3) & 0xF, c & 7
-        if e == 15 and m == 7:
-            v[c] = np.nan
-        elif e == 0:
-            v[c] = s * (m / 8.0) * 2.0 ** -6
-        else:
-            v[c] = s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
-    return v
-
-
-E4M3 = _e4m3_values()
-POS = E4M3[:127]  # codes 0..126: the non-negative finite values, ascending
-
-
-def _rne_e4m3(u: np.ndarray) -> np.ndarray:
-    """Nearest E4M3 value, ties to the even code (|u| <= 448 here)."""
-    a = np.abs(u)
-    assert np.all(a <= 448.0)
-    i = np.clip(np.searchsorted(POS, a), 1, 126)
-    lo, hi = POS[i - 1], POS[i]
-    dlo, dhi = a - lo, hi - a
-    pick_hi = (dhi < dlo) | ((dhi == dlo) & (i % 2 == 0))
-    return np.sign(u) * np.where(pick_hi, hi, lo)
+E4M3 = e4m3.VALUES
+_rne_e4m3 = e4m3.rne
 
 
 def _bf16_rows(rng, rows, cols):
