@@ -378,10 +378,11 @@ size_t moe_ffn_workspace_size(int T, int H, int I, int Et, int Kt, int tile_m) {
 moe_path_t moe_ffn_auto_path(int T, int Kt, int Et, int tile_m) {
     // mean rows per expert; the decode path wins while most experts see only
     // a few rows, so the weight stream, not the MMA, bounds the time
+    // (the large-M regime's tile heights: the f16 prefill path's and the two-term path's 96)
     const double rows_per_expert = Et > 0 ? (double)T * Kt / Et : 0.0;
-    if (rows_per_expert >= 16.0 && prefill_tile_supported(tile_m)) return MOE_PATH_PREFILL;
+    if (rows_per_expert >= 16.0 && staged_tile(tile_m)) return MOE_PATH_PREFILL;
     if (decode_tile_supported(tile_m)) return MOE_PATH_DECODE;
-    return prefill_tile_supported(tile_m) ? MOE_PATH_PREFILL : MOE_PATH_DECODE;
+    return staged_tile(tile_m) ? MOE_PATH_PREFILL : MOE_PATH_DECODE;
 }
 
 // Shape/path checks shared by the FFN calls.  Resolves AUTO (and the

@@ -52,6 +52,9 @@ def test_status_strings_and_sizes(lib):
     assert m.moe_ffn_auto_path_shape(1536, 4096, 256, 513, 11, 64) == m.MOE_PATH_PREFILL
     assert m.moe_ffn_auto_path_shape(64, 4096, 1024, 513, 11, 8) == m.MOE_PATH_DECODE
     assert m.moe_ffn_auto_path_shape(64, 250, 1024, 513, 11, 8) == m.MOE_PATH_AUTO  # H % 32
+    # 96-row tiles: only the two-term path has them
+    assert m.moe_ffn_auto_path_shape(8192, 4096, 1024, 513, 11, 96) == m.MOE_PATH_PREFILL_FP8X2
+    assert m.moe_ffn_auto_path_shape(8192, 4096, 256, 513, 11, 96) == m.MOE_PATH_AUTO
 
 
 def test_host_validation_rejects_before_launch(lib):
