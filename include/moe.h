@@ -252,7 +252,12 @@ moe_status_t moe_ffn_path(const uint16_t* x, const uint8_t* w13, const uint8_t* 
  * moe_ffn_gate_up: h[p, n] = bf16(silu(g) * u) for every sorted position p
  *   that holds a pair (pads are not written), then each such row re-encoded
  *   in place as f16 times a power of two per row (the row factors after the
- *   activation area), the form the down GEMMs read.
+ *   activation area), the form the down GEMMs read.  On
+ *   MOE_PATH_PREFILL_FP8X2 h is written instead as its two E4M3 terms (see
+ *   moe_ffn): the h area holds 2 tile_m rows of I bytes per tile (the tile's
+ *   high terms, then its low terms) and their scale bytes follow the shifts
+ *   of the staged y; x's terms are written in the same form into the area of
+ *   the tile-ordered copy, their scale bytes into the y area.
  * moe_ffn_down:    y[q, m] = topk_w[q] * (W2[e] h_p)[m] for every pair q at
  *   position p (the routing-weighted expert outputs).
  * moe_combine:     out[t, m] = bf16(sum over j = 0..Kt-1, ascending, of
@@ -273,7 +278,7 @@ moe_status_t moe_combine(const float* y, int T, int H, int Kt, uint16_t* out, cu
 /*
  * moe_ffn_down_combine -- moe_ffn_down followed by moe_combine, in one call
  * (moe_ffn runs gate_up and then this).  The decode path gives the same
- * results bit for bit.  The prefill path writes y by sorted position
+ * results bit for bit.  The prefill and two-term paths write y by sorted position
  * ([cap][H rounded up to 128]) as f16 times a power of two per (8 output
  * rows, 32 sorted positions), with the shift bytes after the position
  * weights; the combine undoes the shift exactly, multiplies by the routing
