@@ -80,6 +80,7 @@ constexpr int kRowBytes = 128;
 constexpr int kABytes = 128 * kRowBytes;  // 16 KB weight stage (unpacked codes)
 constexpr int kABox = 64;                 // weight rows per TMA box
 constexpr int kSfGroupMax = 8;           // stages whose scale bytes one load brings
+constexpr int kItemTab = 512;            // work items whose expert a CTA tabulates at its start
 constexpr int kPrefetch = 16;             // weight stages prefetched into L2 ahead, across items
 constexpr int kSmemLimit = 232448;
 
@@ -96,12 +97,14 @@ struct X2Layout {
     static_assert(kStage % 1024 == 0 && kSfSlotBytes % 128 == 0, "alignment");
     static constexpr int kStgRow = 132;
     static constexpr int kStgBytes = MODE == 0 ? 2 * 32 * kStgRow * 4 : 0;  // one per epilogue group
-    static constexpr int kFit = (kSmemLimit - 1024 - 512 - kStgBytes - 2 * kSfSlotBytes) / kStage;
+    static constexpr int kFit =
+        (kSmemLimit - 1024 - 512 - kStgBytes - 2 * kSfSlotBytes - kItemTab * 4) / kStage;
     static constexpr int kStages = kFit > 8 ? 8 : kFit;
     static_assert(kStages >= 3, "ring depth");
     static constexpr int kSf = kStages * kStage;
     static constexpr int kStg = kSf + 2 * kSfSlotBytes;
-    static constexpr int kBar = kStg + kStgBytes;
+    static constexpr int kItems = kStg + kStgBytes;  // the CTA's item -> expert table
+    static constexpr int kBar = kItems + kItemTab * 4;
     static constexpr int kTotal = kBar + 512 + 1024;  // + barriers, alignment slack
     static_assert(kTotal <= kSmemLimit, "shared memory");
     static constexpr int kBJ = kBRows / 32;             // B scale columns
@@ -343,6 +346,21 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
     auto block_of = [&](int item) { return PAIR ? 2 * (item % row_groups) + rank : item % row_groups; };
     constexpr uint32_t kTmemCols = 512;
 
+    // The expert of each of the CTA's first kItemTab work items (item cta0 +
+    // k cstep at k), read once here by all threads together, so that no role
+    // waits on a global load at the start of an item; later items read it
+    // when they start.  -1: an expert out of range (flagged), skipped by
+    // every role.
+    int32_t* item_e = reinterpret_cast<int32_t*>(smem + L::kItems);
+    for (int k = tid; k < kItemTab && cta0 + k * cstep < items; k += blockDim.x) {
+        const int item = cta0 + k * cstep;
+        item_e[k] = checked_expert(g, item / row_groups, block_of(item) == 0);
+    }
+    auto expert_of = [&](int item) {
+        const int k = (item - cta0) / cstep;
+        return k < kItemTab ? item_e[k] : checked_expert(g, item / row_groups, false);
+    };
+
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&tma_full[s], 1);
@@ -378,7 +396,7 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
             // two 64-row halves (down); -1 for an item every role skips
             auto item_rows = [&](int item, int& r0, int& r1) {
                 const int block = block_of(item);
-                const int e = checked_expert(g, item / row_groups, false);
+                const int e = expert_of(item);
                 r0 = e < 0 ? -1 : e * g.rows + (MODE == 0 ? block * 64 : block * 128);
                 r1 = MODE == 0 ? e * g.rows + g.I + block * 64 : r0 + kABox;
             };
@@ -407,7 +425,8 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
             bool ok = true;
             for (int item = cta0; item < items && ok; item += cstep) {
                 const int tile = item / row_groups, block = block_of(item);
-                const int e = checked_expert(g, tile, block == 0);
+                const int e = (item - cta0) / cstep < kItemTab ? expert_of(item)
+                                                               : checked_expert(g, tile, block == 0);
                 if (e < 0) continue;  // skipped by every role (of both CTAs)
                 const int ar0 = e * g.rows + (MODE == 0 ? block * 64 : block * 128);
                 const int ar1 = MODE == 0 ? e * g.rows + g.I + block * 64 : ar0 + kABox;
@@ -458,7 +477,7 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
             uint32_t gs = 0, it = 0;
             bool ok = true;
             for (int item = cta0; item < items && ok; item += cstep) {
-                if (checked_expert(g, item / row_groups, false) < 0) continue;
+                if (expert_of(item) < 0) continue;
                 const uint32_t b = it % kAccBufs;
                 if (it >= (uint32_t)kAccBufs && !mbar_wait(&acc_free[b], ((it / kAccBufs) - 1) & 1)) break;
                 tc_fence_after();
@@ -519,7 +538,7 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
         uint32_t gs = 0, gc = 0;
         bool ok = true;
         for (int item = cta0; item < items && ok; item += cstep) {
-            if (checked_expert(g, item / row_groups, false) < 0) continue;
+            if (expert_of(item) < 0) continue;
             for (int st = 0; st < nk; ++st, ++gs) {
                 const int s = gs % kStages, k = gc & 1;
                 // the stage's scale factors go into tensor memory as soon as
@@ -570,7 +589,7 @@ __global__ void __launch_bounds__(x2_threads<MODE>(), 1)
         uint32_t it = 0;
         for (int item = cta0; item < items; item += cstep) {
             const int tile = item / row_groups, block = block_of(item);
-            if (checked_expert(g, tile, false) < 0) continue;
+            if (expert_of(item) < 0) continue;
             const uint32_t b = it % kAccBufs;
             // down: the pair of this lane's position in each of the warp's chunks
             int q[kChunks];
