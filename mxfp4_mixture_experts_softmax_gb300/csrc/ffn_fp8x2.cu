@@ -29,28 +29,35 @@
 //
 // GEMM work item = one tile of N token rows of one expert x one block of 128
 // weight rows (64 gate + 64 up rows for gate_up; 128 rows of W2 for down).
-// Persistent CTAs (one per SM); warp roles:
+// Persistent CTAs (one per SM, or CTA pairs from 96-row tiles: see
+// fp8x2_gemm_kernel); each CTA first tabulates its items' experts in shared
+// memory.  Warp roles:
 //   * producer warp: 2D TMA loads per 128-k stage: the block's codes, which
 //     the TMA unpacks into the 16-byte-per-16-codes layout the MMA reads
-//     (data type 16U4_ALIGN16B, 128-byte swizzle), the tile's 2N activation
-//     rows (E4M3 bytes, 128-byte swizzle), and the 16-byte scale boxes (four
-//     stages' worth; the scale warps pick the stage's 4 bytes) of every weight
-//     row and activation row; weights prefetched into L2 ahead of the ring;
-//   * MMA warp: one thread issues the stage's four K = 32 MMAs (M = 128,
-//     N = 2 tile rows, scale id = k step) and commits them to the stage's
+//     (data type 16U4_ALIGN16B, 128-byte swizzle), and the tile's activation
+//     rows (E4M3 bytes, 128-byte swizzle); once per group of 8 stages (4 when
+//     the item's stages do not split into 8s) the group's scale bytes of every
+//     weight row and activation row, one 32-byte (16-byte) box row each, into a
+//     two-slot ring; an L2 prefetch cursor runs 16 stages ahead, across items;
+//   * MMA warp: one thread issues the stage's four K = 32 MMAs (M = 128 or
+//     256, N = 2 tile rows, scale id = k step) and commits them to the stage's
 //     barrier, which frees the stage;
-//   * 4 scale warps, one per tensor-memory lane quadrant: copy the stage's
-//     scale bytes into tensor memory (tcgen05.st).  The MMA reads weight row
-//     r's scale at lane r, column base + r / 32, and B column n's at lane
-//     32 q + n % 32, column base + 8 + n / 32 in every quadrant q; byte j of a
-//     32-bit cell is k group j of the stage;
-//   * epilogue warps: D_hi + D_lo; gate_up (4 warps) passes each 32-column
-//     slice through shared memory (transposed) so each thread holds 16
-//     consecutive i of one token: SwiGLU in fp32, h rounded to bf16 (the
-//     oracle's rounding), then split into the two E4M3 terms of the down
-//     GEMM's B rows; down stages y as f16 rows by sorted position
-//     (store_y16_chunk) for the combine, or writes y by pair times the routing
-//     weight.
+//   * 4 scale warps, one per tensor-memory lane quadrant: copy each stage's
+//     scale bytes into tensor memory (tcgen05.st) as soon as the group has
+//     landed and the columns are free, then wait for the stage's operands and
+//     arrive on the MMA's barrier.  The MMA reads weight row r's scale at lane
+//     r, column base + r / 32, and B column n's at lane 32 q + n % 32, column
+//     base + 8 + n / 32 in every quadrant q; byte j of a 32-bit cell is k group
+//     j of the stage;
+//   * 8 epilogue warps in two groups of four, group h draining the 32-column
+//     chunks h and h + 2 of D_hi + D_lo: each warp copies its chunks out of
+//     tensor memory and releases the accumulator before computing.  gate_up
+//     passes each chunk through its group's shared-memory buffer (transposed)
+//     so each thread holds 16 consecutive i of one token: SwiGLU in fp32, h
+//     rounded to bf16 (the oracle's rounding), then split into the two E4M3
+//     terms of the down GEMM's B rows; down stages y as f16 rows by sorted
+//     position (store_y16_chunk) for the combine, or writes y by pair times the
+//     routing weight.
 // Every wait is bounded (see mbar_wait); after a timeout each role stops, the
 // MMA thread drains its own MMAs (bounded), and tensor memory is freed.
 #include <cuda_fp16.h>
