@@ -105,6 +105,23 @@ def test_out_of_range_indices_are_flagged_not_followed(corrupt, path, tile_m):
 
 
 @pytest.mark.parametrize("corrupt", [_bad_expert, _bad_pair, _bad_tile_count])
+@pytest.mark.parametrize("tile_m", [32, 128])
+def test_fp8x2_out_of_range_indices_are_flagged_not_followed(corrupt, tile_m):
+    """The two-term path (one CTA per weight block at 32-row tiles, CTA pairs at 128): the
+    split, both GEMMs and the position weights skip out-of-range work and flag it."""
+    w = synth.scaled(synth.WORKLOADS["tiny16"], **dict(CASE, I=512))
+    d = synth.make_inputs(w)
+    ids, wt = oracle.route(d["logits"], w.K, w.with_shared)
+    ref = gc.bits_to_f64(oracle.ffn(d["x"], d["w13"], d["s13"], d["w2"], d["s2"], ids, wt))
+    P = libmoe.MOE_PATH_PREFILL_FP8X2
+    assert libmoe.moe_device_error(clear=True) in (0, 1, 2, 3)
+    _run(w, d, ids, wt, tile_m, P, corrupt)  # outputs of the skipped work are unspecified
+    assert libmoe.moe_device_error(clear=True) & 2
+    gc.ffn_parity(_run(w, d, ids, wt, tile_m, P), ref, "after the index error")
+    assert libmoe.moe_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("corrupt", [_bad_expert, _bad_pair, _bad_tile_count])
 @pytest.mark.parametrize("tile_m", [32, 64])
 def test_mxfp4act_out_of_range_indices_are_flagged_not_followed(corrupt, tile_m):
     """The MXFP4-activation path (gather, both GEMMs with their scale warps,
